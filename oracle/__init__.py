@@ -1,0 +1,325 @@
+"""CPU oracle of the DSpark sequential Markov draft-sampling loop.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The library under
+``dspark_markov_draft_anchor_gb300`` never imports this package, and this
+package imports nothing from it.
+
+The arithmetic lives in ``dspark_oracle.c`` (plain C, one IEEE operation per
+expression, ``-ffp-contract=off``); this module only compiles it with gcc and
+marshals numpy arrays through ctypes.  Every function names the page and the
+section it follows in the C source.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dspark_oracle.c")
+_HDR = os.path.join(_HERE, "dspark_oracle.h")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libdspark_oracle.so")
+_lib = None
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread", "-std=c11"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into ``oracle/_build`` (atomic rename)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= max(
+        os.path.getmtime(_SRC), os.path.getmtime(_HDR)
+    )
+    if fresh and not force:
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD)
+    os.close(fd)
+    cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class LoopArgs(ctypes.Structure):
+    _fields_ = [
+        ("vocab", ctypes.c_int64),
+        ("rank", ctypes.c_int32),
+        ("w1_rows", ctypes.c_int64),
+        ("w1", ctypes.c_void_p),
+        ("w2", ctypes.c_void_p),
+        ("rows", ctypes.c_int32),
+        ("steps", ctypes.c_int32),
+        ("base", ctypes.c_void_p),
+        ("base_s0", ctypes.c_int64),
+        ("base_s1", ctypes.c_int64),
+        ("cache", ctypes.c_void_p),
+        ("cache_s0", ctypes.c_int64),
+        ("cache_s1", ctypes.c_int64),
+        ("input_ids", ctypes.c_void_p),
+        ("anchor_idx", ctypes.c_void_p),
+        ("req_idx", ctypes.c_void_p),
+        ("req_s0", ctypes.c_int64),
+        ("sample_pos", ctypes.c_void_p),
+        ("pos_s0", ctypes.c_int64),
+        ("num_req", ctypes.c_int64),
+        ("seeds", ctypes.c_void_p),
+        ("temperature", ctypes.c_void_p),
+        ("mult", ctypes.c_float),
+        ("cap", ctypes.c_float),
+        ("salt", ctypes.c_uint32),
+        ("fed_bias", ctypes.c_void_p),
+        ("tokens", ctypes.c_void_p),
+        ("tokens_s0", ctypes.c_int64),
+        ("bias_out", ctypes.c_void_p),
+        ("keys_out", ctypes.c_void_p),
+        ("nthreads", ctypes.c_int),
+    ]
+
+
+def lib():
+    """The loaded oracle library (built on first use)."""
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        P, i64, i32, u32, f32, u16 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                      ctypes.c_uint32, ctypes.c_float, ctypes.c_uint16)
+        sigs = {
+            "oracle_bf16_to_f32": (f32, [u16]),
+            "oracle_f32_to_bf16": (u16, [f32]),
+            "oracle_logf": (f32, [f32]),
+            "oracle_tanhf": (f32, [f32]),
+            "oracle_murmur_block": (u32, [u32, u32]),
+            "oracle_murmur_fmix": (u32, [u32]),
+            "oracle_noise_hash": (u32, [i64, i32, i64, u32, u32]),
+            "oracle_uniform": (f32, [u32]),
+            "oracle_log1m": (f32, [f32]),
+            "oracle_noise_L": (f32, [u32]),
+            "oracle_key": (f32, [f32, f32, u32]),
+            "oracle_argmax": (i64, [P, i64]),
+            "oracle_combine_first_wins": (ctypes.c_int, [f32, i64, f32, i64]),
+            "oracle_dot_bf16": (u16, [P, P, ctypes.c_int]),
+            "oracle_markov_loop": (ctypes.c_int, [ctypes.POINTER(LoopArgs)]),
+            "oracle_build_verify_tokens": (None, [P, P, P, i32, i32, i32]),
+            "oracle_greedy_accept": (ctypes.c_int, [P, P, P, P, P, i32, i32, i32, i64]),
+            "oracle_noise_L_array": (None, [P, P, i64]),
+            "oracle_uniform_array": (None, [P, P, i64]),
+            "oracle_log1m_array": (None, [P, P, i64]),
+            "oracle_logf_array": (None, [P, P, i64]),
+            "oracle_tanhf_array": (None, [P, P, i64]),
+            "oracle_logit_array": (None, [P, P, P, P, i64, f32, f32]),
+            "oracle_noise_hash_array": (None, [i64, i32, i64, u32, P, P, i64]),
+            "oracle_dot_bf16_rows": (None, [P, P, P, i64, ctypes.c_int]),
+            "oracle_f32_to_bf16_array": (None, [P, P, i64]),
+            "oracle_key_array": (None, [P, f32, P, P, i64]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --------------------------------------------------------------------------
+# Scalar / array wrappers used by the pins
+# --------------------------------------------------------------------------
+
+def logf(x):
+    x = _c(x, np.float32)
+    out = np.empty_like(x)
+    lib().oracle_logf_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def tanhf(x):
+    x = _c(x, np.float32)
+    out = np.empty_like(x)
+    lib().oracle_tanhf_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def uniform(h):
+    h = _c(h, np.uint32)
+    out = np.empty(h.shape, np.float32)
+    lib().oracle_uniform_array(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def log1m(u):
+    u = _c(u, np.float32)
+    out = np.empty_like(u)
+    lib().oracle_log1m_array(_ptr(u), _ptr(out), u.size)
+    return out
+
+
+def noise_L(h):
+    h = _c(h, np.uint32)
+    out = np.empty(h.shape, np.float32)
+    lib().oracle_noise_L_array(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def noise_hash(seed, step, sample_pos, salt, vocab_ids):
+    v = _c(vocab_ids, np.uint32)
+    out = np.empty(v.shape, np.uint32)
+    lib().oracle_noise_hash_array(int(seed), int(step), int(sample_pos), int(salt) & 0xFFFFFFFF,
+                                  _ptr(v), _ptr(out), v.size)
+    return out
+
+
+def key(l, temp, h):
+    l = _c(l, np.float32)
+    h = _c(h, np.uint32)
+    out = np.empty_like(l)
+    lib().oracle_key_array(_ptr(l), float(temp), _ptr(h), _ptr(out), l.size)
+    return out
+
+
+def logit(base, bias, mult=1.0, cap=0.0):
+    """(cache BF16 bits, FP32 logit) of BF16 base and bias bit arrays."""
+    base = _c(base, np.uint16)
+    bias = _c(np.broadcast_to(bias, base.shape), np.uint16)
+    c = np.empty(base.shape, np.uint16)
+    l = np.empty(base.shape, np.float32)
+    lib().oracle_logit_array(_ptr(base), _ptr(bias), _ptr(c), _ptr(l), base.size, float(mult), float(cap))
+    return c, l
+
+
+def dot_bf16(a, b):
+    """Exactly rounded dot products of the rows of two BF16 bit arrays."""
+    a = _c(a, np.uint16)
+    b = _c(b, np.uint16)
+    if a.ndim == 1:
+        a, b = a[None], b[None]
+    out = np.empty(a.shape[0], np.uint16)
+    lib().oracle_dot_bf16_rows(_ptr(a), _ptr(b), _ptr(out), a.shape[0], a.shape[1])
+    return out
+
+
+def f32_to_bf16(x):
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().oracle_f32_to_bf16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def argmax(keys):
+    keys = _c(keys, np.float32)
+    return int(lib().oracle_argmax(_ptr(keys), keys.size))
+
+
+def combine_first_wins(v1, i1, v2, i2):
+    return bool(lib().oracle_combine_first_wins(float(v1), int(i1), float(v2), int(i2)))
+
+
+def murmur_block(h, k):
+    return int(lib().oracle_murmur_block(h & 0xFFFFFFFF, k & 0xFFFFFFFF))
+
+
+def murmur_fmix(h):
+    return int(lib().oracle_murmur_fmix(h & 0xFFFFFFFF))
+
+
+# --------------------------------------------------------------------------
+# The loop and the verify side
+# --------------------------------------------------------------------------
+
+def markov_loop(*, w1, w2, base, input_ids, anchor_idx, sample_pos, seeds, temperature,
+                req_idx=None, num_req=None, mult=1.0, cap=0.0, salt=1 << 30, fed_bias=None,
+                cache=None, want_bias=False, want_keys=False, rows=None, nthreads=None):
+    """Run the oracle loop.
+
+    ``base`` is a BF16 bit array ``[rows, steps, V]`` (any strides with last
+    stride 1); ``cache`` (optional) is updated in place, ``[num_req, steps, V]``.
+    Returns ``dict(tokens=[rows, steps] int64, bias=..., keys=...)``.
+    ``rows`` restricts the call to the first ``rows`` rows.
+    """
+    w1 = _c(w1, np.uint16)
+    w2 = _c(w2, np.uint16)
+    assert base.dtype == np.uint16 and base.strides[-1] == 2
+    R = base.shape[0] if rows is None else rows
+    K = base.shape[1]
+    V = base.shape[2]
+    assert w2.shape[0] == V
+    input_ids = _c(input_ids, np.int32)
+    anchor_idx = _c(anchor_idx, np.int64)
+    sample_pos = np.asarray(sample_pos, dtype=np.int64)
+    assert sample_pos.strides[1] == 8
+    seeds = _c(seeds, np.int64)
+    temperature = _c(temperature, np.float32)
+    if num_req is None:
+        num_req = seeds.shape[0]
+    if req_idx is not None:
+        req_idx = np.asarray(req_idx, dtype=np.int64)
+        assert req_idx.strides[1] == 8
+    tokens = np.full((R, K), -7, np.int64)
+    bias_out = np.empty((R, K, V), np.uint16) if want_bias else None
+    keys_out = np.empty((R, K, V), np.float32) if want_keys else None
+    if fed_bias is not None:
+        fed_bias = _c(fed_bias, np.uint16)
+        assert fed_bias.shape[0] >= R and fed_bias.shape[1:] == (K, V)
+    if cache is not None:
+        assert cache.dtype == np.uint16 and cache.strides[-1] == 2
+    a = LoopArgs()
+    a.vocab, a.rank, a.w1_rows = V, w2.shape[1], w1.shape[0]
+    a.w1, a.w2 = _ptr(w1), _ptr(w2)
+    a.rows, a.steps = R, K
+    a.base, a.base_s0, a.base_s1 = base.ctypes.data, base.strides[0] // 2, base.strides[1] // 2
+    if cache is not None:
+        a.cache, a.cache_s0, a.cache_s1 = cache.ctypes.data, cache.strides[0] // 2, cache.strides[1] // 2
+    a.input_ids, a.anchor_idx = _ptr(input_ids), _ptr(anchor_idx)
+    if req_idx is not None:
+        a.req_idx, a.req_s0 = req_idx.ctypes.data, req_idx.strides[0] // 8
+    a.sample_pos, a.pos_s0 = sample_pos.ctypes.data, sample_pos.strides[0] // 8
+    a.num_req = int(num_req)
+    a.seeds, a.temperature = _ptr(seeds), _ptr(temperature)
+    a.mult, a.cap, a.salt = float(mult), float(cap), int(salt) & 0xFFFFFFFF
+    a.fed_bias = _ptr(fed_bias)
+    a.tokens, a.tokens_s0 = _ptr(tokens), K
+    a.bias_out, a.keys_out = _ptr(bias_out), _ptr(keys_out)
+    a.nthreads = int(nthreads or os.cpu_count() or 1)
+    rc = lib().oracle_markov_loop(ctypes.byref(a))
+    if rc != 0:
+        raise RuntimeError(f"oracle_markov_loop failed: {rc}")
+    return {"tokens": tokens, "bias": bias_out, "keys": keys_out}
+
+
+def build_verify_tokens(last, draft, P):
+    last = _c(last, np.int64)
+    draft = np.asarray(draft, dtype=np.int64)
+    assert draft.strides[1] == 8
+    B = last.shape[0]
+    out = np.empty((B, P + 1), np.int64)
+    lib().oracle_build_verify_tokens(_ptr(last), draft.ctypes.data, _ptr(out), B,
+                                     draft.strides[0] // 8, P)
+    return out
+
+
+def greedy_accept(logits, draft, proposal_len, P):
+    """``logits`` BF16 bits ``[B, P+1, V]``; returns (accepted [B, P+1], accept_len [B])."""
+    logits = _c(logits, np.uint16)
+    draft = np.asarray(draft, dtype=np.int64)
+    assert draft.strides[1] == 8
+    proposal_len = _c(proposal_len, np.int32)
+    B, P1, V = logits.shape
+    assert P1 == P + 1
+    accepted = np.empty((B, P + 1), np.int64)
+    accept_len = np.empty(B, np.int32)
+    rc = lib().oracle_greedy_accept(_ptr(logits), draft.ctypes.data, _ptr(proposal_len),
+                                    _ptr(accepted), _ptr(accept_len), B, draft.strides[0] // 8, P, V)
+    if rc != 0:
+        raise RuntimeError(f"oracle_greedy_accept failed: {rc}")
+    return accepted, accept_len

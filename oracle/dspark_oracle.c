@@ -1,0 +1,646 @@
+/*
+ * dspark_oracle.c -- plain, slow, CPU reference of the DSpark sequential
+ * Markov draft-sampling loop and its verify side.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library path links, loads or
+ * calls this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or constant with the
+ * CUDA sources.
+ *
+ * Every function follows the definition on the pages it cites, written out
+ * element by element with no blocking, fusion or reordering:
+ *
+ *   [P1] "Dspark Kernels" (TensorRT Edge-LLM C++ API, dsparkKernels.html):
+ *        dsparkBuildVerifyTokens, dsparkGreedyAccept.
+ *   [P2] vllm.models.kimi_k3.nvidia.specialized_decode.drafter.markov:
+ *        module docstring (exactness paragraph), _gumbel_key, _loop_rest.
+ *   [P3] vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.draft.markov:
+ *        module docstring, _StepKernel.kernel, _logit, _gumbel,
+ *        _murmur_prefix, _combine, _w1_row, _nonzero_f32, anchor_embed.
+ *   [P4] vllm.models.deepseek_v41.amd.ops.fused_markov: module docstring.
+ *
+ * Floating point: compile with -O2 -ffp-contract=off and no fast-math, so
+ * that every float expression below is one IEEE binary32 operation rounded
+ * to nearest even, and fmaf() is the fused multiply-add.
+ *
+ * Readings of points the pages leave open (each also listed in the design doc):
+ *   - the MurmurHash3 block step (_MURMUR_MIX, not printed) is the published
+ *     MurmurHash3_x86_32 block mix; the printed tail fixes the finaliser;
+ *   - logf/tanhf are the library's own functions (below), because the pages'
+ *     logf and tanhf are a vendor math library's; division is IEEE;
+ *   - the bias is the exactly rounded dot product (any FP32 order is allowed
+ *     by [P2]/[P4]; the exact value is the one order-free definition);
+ *   - a request index outside [0, num_req) marks the row invalid, like a
+ *     negative one ([P3] _StepKernel.kernel: valid = req >= 0).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "dspark_oracle.h"
+
+/* ------------------------------------------------------------------------ */
+/* BF16 <-> FP32                                                            */
+/* ------------------------------------------------------------------------ */
+
+float oracle_bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* Round-to-nearest-even FP32 -> BF16; every NaN becomes the canonical
+ * 0x7FFF (the value a cvt.rn.bf16.f32 of [P3] _logit produces). */
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if (isnan(f)) return 0x7FFF;
+  uint32_t upper = u >> 16, lower = u & 0xFFFFu;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+  return (uint16_t)upper;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Own natural logarithm (replaces the pages' vendor logf).                */
+/* For positive normal finite x:                                            */
+/*   x = 2^e * m with m in [sqrt(1/2), sqrt(2)),  f = m - 1 (exact),        */
+/*   log(1 + f) = 2 atanh(s),  s = f / (2 + f),                             */
+/*   2 atanh(s) = 2s + s*R,  R = sum_{n>=1} 2 z^n / (2n+1),  z = s^2,       */
+/*   and since 2s = f - s*f = f - (hfsq - s*hfsq) with hfsq = f^2 / 2:      */
+/*   log(1 + f) = f - (hfsq - s * (hfsq + R)),                              */
+/*   log x = e * ln2 + log m, ln2 split as LN2_HI + LN2_LO (Cody-Waite), so */
+/*   that e * LN2_HI is exact.                                              */
+/* Coefficients 2/(2n+1) are the Taylor coefficients of 2 atanh, each       */
+/* rounded once to binary32 (the compiler rounds the double quotient; none  */
+/* of these quotients lies on a binary32 rounding boundary).                */
+/* ------------------------------------------------------------------------ */
+
+static const float LOG_C3 = (float)(2.0 / 3.0);
+static const float LOG_C5 = (float)(2.0 / 5.0);
+static const float LOG_C7 = (float)(2.0 / 7.0);
+static const float LOG_C9 = (float)(2.0 / 9.0);
+static const float LOG_C11 = (float)(2.0 / 11.0);
+/* ln 2 with its last 8 significand bits cleared: e * LN2_HI is exact for
+ * |e| < 2^8.  LN2_LO is the rest, rounded once. */
+static const float LN2_HI = 0.693145751953125f;
+#define ORACLE_LN2_DOUBLE 0.69314718055994530941723212145818
+static const float LN2_LO = (float)(ORACLE_LN2_DOUBLE - 0.693145751953125);
+
+float oracle_logf(float x) {
+  uint32_t bits;
+  memcpy(&bits, &x, 4);
+  int e = (int)(bits >> 23) - 127;
+  uint32_t mbits = (bits & 0x007FFFFFu) | 0x3F800000u; /* m in [1, 2) */
+  if (mbits > 0x3FB504F3u) {                           /* m > RN(sqrt 2) */
+    mbits -= 0x00800000u;                              /* m / 2 */
+    e += 1;
+  }
+  float m;
+  memcpy(&m, &mbits, 4);
+  float f = m - 1.0f;
+  float s = f / (2.0f + f);
+  float z = s * s;
+  float p = fmaf(z, LOG_C11, LOG_C9);
+  p = fmaf(z, p, LOG_C7);
+  p = fmaf(z, p, LOG_C5);
+  p = fmaf(z, p, LOG_C3);
+  float R = z * p;
+  float hfsq = (0.5f * f) * f;
+  float t = hfsq + R;
+  float corr = fmaf(-s, t, hfsq);
+  float logm = f - corr;
+  float fe = (float)e;
+  return fmaf(fe, LN2_HI, fmaf(fe, LN2_LO, logm));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Own hyperbolic tangent (replaces the pages' vendor tanhf, [P3] _logit). */
+/*   tanh|z| = E / (E + 2),  E = expm1(2|z|),  sign restored at the end;    */
+/*   |z| > 9.1: tanh rounds to 1 in binary32;  NaN propagates.              */
+/*   expm1(x), x >= 0:  k = nearest integer to x / ln2,                     */
+/*   r = x - k ln2 (Cody-Waite, |r| <= ln2/2 + tiny),                       */
+/*   expm1(r) = r + r^2 (1/2! + r/3! + ... + r^7/9!)  (Taylor),             */
+/*   expm1(x) = 2^k expm1(r) + (2^k - 1).                                   */
+/* ------------------------------------------------------------------------ */
+
+static const float INV_LN2 = (float)(1.0 / ORACLE_LN2_DOUBLE);
+static const float EXP_C2 = (float)(1.0 / 2.0);
+static const float EXP_C3 = (float)(1.0 / 6.0);
+static const float EXP_C4 = (float)(1.0 / 24.0);
+static const float EXP_C5 = (float)(1.0 / 120.0);
+static const float EXP_C6 = (float)(1.0 / 720.0);
+static const float EXP_C7 = (float)(1.0 / 5040.0);
+static const float EXP_C8 = (float)(1.0 / 40320.0);
+static const float EXP_C9 = (float)(1.0 / 362880.0);
+
+static float own_expm1f_nonneg(float x) {
+  float kf = rintf(x * INV_LN2);
+  float r = fmaf(-kf, LN2_HI, x);
+  r = fmaf(-kf, LN2_LO, r);
+  float p = fmaf(r, EXP_C9, EXP_C8);
+  p = fmaf(r, p, EXP_C7);
+  p = fmaf(r, p, EXP_C6);
+  p = fmaf(r, p, EXP_C5);
+  p = fmaf(r, p, EXP_C4);
+  p = fmaf(r, p, EXP_C3);
+  p = fmaf(r, p, EXP_C2);
+  float em1 = fmaf(r * r, p, r);
+  int k = (int)kf;
+  if (k == 0) return em1;
+  float two_k = ldexpf(1.0f, k);
+  return fmaf(two_k, em1, two_k - 1.0f);
+}
+
+float oracle_tanhf(float z) {
+  if (isnan(z)) return z;
+  float a = fabsf(z);
+  float t;
+  if (a > 9.1f) {
+    t = 1.0f;
+  } else {
+    float E = own_expm1f_nonneg(2.0f * a);
+    t = E / (E + 2.0f);
+  }
+  return copysignf(t, z);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Output transform ([P3] _logit; [P2] module docstring "the add is one    */
+/* FP32 add rounded to the logits dtype"):                                  */
+/*   hx = RN_bf16(f32(base) + f32(bias))          (add.bf16)                */
+/*   y  = RN(mult * f32(hx))                                                */
+/*   w  = has_cap ? RN(cap * tanh(RN(inv_cap * y))) : y                     */
+/*   c  = RN_bf16(w), the cached (pre-temperature) logit; l = f32(c).       */
+/* ------------------------------------------------------------------------ */
+
+uint16_t oracle_logit(uint16_t base, uint16_t bias, float mult, int has_cap,
+                      float inv_cap, float cap, float *l_out) {
+  float sum = oracle_bf16_to_f32(base) + oracle_bf16_to_f32(bias);
+  float x = oracle_bf16_to_f32(oracle_f32_to_bf16(sum));
+  float y = mult * x;
+  float w = y;
+  if (has_cap) {
+    float z = inv_cap * y;
+    w = cap * oracle_tanhf(z);
+  }
+  uint16_t c = oracle_f32_to_bf16(w);
+  if (l_out) *l_out = oracle_bf16_to_f32(c);
+  return c;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Noise hash ([P3] _StepKernel.kernel, _murmur_prefix, _gumbel):          */
+/* MurmurHash3_x86_32 with seed 0 over the four little-endian words         */
+/*   lo32(step_seed), hi32(step_seed), lo32(pos - 1 + salt), vocab id,      */
+/* step_seed = seed XOR (step << 32).                                       */
+/* ------------------------------------------------------------------------ */
+
+static uint32_t rotl32(uint32_t x, int r) { return (x << r) | (x >> (32 - r)); }
+
+uint32_t oracle_murmur_block(uint32_t h, uint32_t k) {
+  k *= 0xcc9e2d51u;
+  k = rotl32(k, 15);
+  k *= 0x1b873593u;
+  h ^= k;
+  h = rotl32(h, 13);
+  h = h * 5u + 0xe6546b64u;
+  return h;
+}
+
+uint32_t oracle_murmur_fmix(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
+}
+
+uint32_t oracle_noise_hash(int64_t seed, int32_t step, int64_t sample_pos,
+                           uint32_t salt, uint32_t vocab_id) {
+  uint64_t step_seed = (uint64_t)seed ^ ((uint64_t)(uint32_t)step << 32);
+  uint64_t salted = (uint64_t)sample_pos - 1u + (uint64_t)salt;
+  uint32_t h = 0;
+  h = oracle_murmur_block(h, (uint32_t)(step_seed & 0xFFFFFFFFu));
+  h = oracle_murmur_block(h, (uint32_t)(step_seed >> 32));
+  h = oracle_murmur_block(h, (uint32_t)(salted & 0xFFFFFFFFu));
+  h = oracle_murmur_block(h, vocab_id);
+  h ^= 16u; /* key length in bytes */
+  return oracle_murmur_fmix(h);
+}
+
+/* u = RN_f32((h + 0.5) / 2^32): [P3] _gumbel builds it as
+ * fma(f32(h >> 16), 2^-16, (f32(h & 0xffff) + 0.5) * 2^-32), a single
+ * rounding of the same exact value. */
+float oracle_uniform(uint32_t h) {
+  return (float)(((double)h + 0.5) * 0x1p-32);
+}
+
+/* log(1 - u) as [P3] _gumbel (and [P2] _log1p_neg_stable) computes it:
+ * below 0.25 the Taylor series -u * (1 + u/2 + ... + u^7/8) in Horner form
+ * with coefficients RN_f32(1/n); else log(max(RN(1 - u), 2^-24)). */
+float oracle_log1m(float u) {
+  if (u < 0.25f) {
+    float poly = fmaf(u, (float)(1.0 / 8.0), (float)(1.0 / 7.0));
+    poly = fmaf(u, poly, (float)(1.0 / 6.0));
+    poly = fmaf(u, poly, (float)(1.0 / 5.0));
+    poly = fmaf(u, poly, (float)(1.0 / 4.0));
+    poly = fmaf(u, poly, (float)(1.0 / 3.0));
+    poly = fmaf(u, poly, (float)(1.0 / 2.0));
+    poly = fmaf(u, poly, 1.0f);
+    return poly * (-u);
+  }
+  float om = 1.0f - u;
+  float xa = om > 0x1p-24f ? om : 0x1p-24f;
+  return oracle_logf(xa);
+}
+
+/* L(h) = log(-log(1 - u(h))); the Gumbel noise is -L ([P2] _gumbel_key,
+ * _gumbel_log_arg32: the kernel takes the outer log itself). */
+float oracle_noise_L(uint32_t h) {
+  float u = oracle_uniform(h);
+  float sel = oracle_log1m(u);
+  return oracle_logf(-sel);
+}
+
+/* [P3] _nonzero_f32: temp != 0.0 as an ordered compare (NaN counts as
+ * nonzero).  [P2] _gumbel_key: key = l / temp + g, g = -L, else l. */
+float oracle_key(float l, float temp, uint32_t h) {
+  if (temp == 0.0f) return l;
+  float q = l / temp;
+  return q - oracle_noise_L(h);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Total-order argmax ([P3] module docstring, _combine): the first NaN,    */
+/* else the lowest index of the maximum (+0 == -0).                         */
+/* ------------------------------------------------------------------------ */
+
+int64_t oracle_argmax(const float *keys, int64_t n) {
+  if (n <= 0) return -1;
+  int64_t bi = 0;
+  float best = keys[0];
+  for (int64_t v = 1; v < n; v++) {
+    if (isnan(best)) break;
+    if (isnan(keys[v]) || keys[v] > best) {
+      best = keys[v];
+      bi = v;
+    }
+  }
+  return bi;
+}
+
+/* [P3] _combine, written from its description: the first pair if v1 > v2,
+ * or v1 == v2 and i1 < i2, or v1 is NaN and (v2 is not NaN or i1 < i2). */
+int oracle_combine_first_wins(float v1, int64_t i1, float v2, int64_t i2) {
+  if (isnan(v1)) return !isnan(v2) || i1 < i2;
+  if (isnan(v2)) return 0;
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exactly rounded BF16 dot product ([P2] module docstring: "the FP32 dot  */
+/* product of the embedding and the markov_w2 row rounded once"; any FP32   */
+/* summation order is allowed, the exact sum is the order-free value).      */
+/* Each BF16 value is sig * 2^exp with an integer sig < 256.  Products are  */
+/* integers < 2^16 scaled by 2^(exp1+exp2), exp1 + exp2 >= -266; the sum   */
+/* is kept exactly in two unsigned 640-bit integers (positive and negative  */
+/* parts, bit 0 = 2^-266) and rounded once, to nearest even, to BF16.       */
+/* ------------------------------------------------------------------------ */
+
+#define ACC_LIMBS 10
+#define ACC_OFFSET 266
+
+typedef struct {
+  uint64_t w[ACC_LIMBS];
+} wide_t;
+
+static void wide_add_shifted(wide_t *a, uint64_t mag, int pos) {
+  int limb = pos / 64, sh = pos % 64;
+  uint64_t lo = mag << sh;
+  uint64_t hi = sh ? (mag >> (64 - sh)) : 0;
+  uint64_t carry = 0;
+  for (int i = limb; i < ACC_LIMBS; i++) {
+    uint64_t add = (i == limb) ? lo : (i == limb + 1 ? hi : 0);
+    uint64_t s = a->w[i] + add;
+    uint64_t c1 = s < add;
+    uint64_t s2 = s + carry;
+    uint64_t c2 = s2 < carry;
+    a->w[i] = s2;
+    carry = c1 + c2;
+    if (i > limb + 1 && carry == 0) break;
+  }
+}
+
+static int wide_cmp(const wide_t *a, const wide_t *b) {
+  for (int i = ACC_LIMBS - 1; i >= 0; i--) {
+    if (a->w[i] != b->w[i]) return a->w[i] > b->w[i] ? 1 : -1;
+  }
+  return 0;
+}
+
+static void wide_sub(wide_t *r, const wide_t *a, const wide_t *b) { /* a >= b */
+  uint64_t borrow = 0;
+  for (int i = 0; i < ACC_LIMBS; i++) {
+    uint64_t d = a->w[i] - b->w[i];
+    uint64_t b1 = a->w[i] < b->w[i];
+    uint64_t d2 = d - borrow;
+    uint64_t b2 = d < borrow;
+    r->w[i] = d2;
+    borrow = b1 + b2;
+  }
+}
+
+static int wide_bit(const wide_t *a, int pos) {
+  if (pos < 0) return 0;
+  return (int)((a->w[pos / 64] >> (pos % 64)) & 1u);
+}
+
+static int wide_any_below(const wide_t *a, int pos) { /* bits [0, pos) */
+  for (int i = 0; i < pos; i++)
+    if (wide_bit(a, i)) return 1;
+  return 0;
+}
+
+static int wide_top(const wide_t *a) {
+  for (int i = ACC_LIMBS - 1; i >= 0; i--) {
+    if (a->w[i]) {
+      for (int b = 63; b >= 0; b--)
+        if ((a->w[i] >> b) & 1u) return i * 64 + b;
+    }
+  }
+  return -1;
+}
+
+/* BF16 fields -> (sig, exp) with value = sig * 2^exp; 0 for zero. */
+static void bf16_parts(uint16_t b, uint32_t *sig, int *exp) {
+  int E = (b >> 7) & 0xFF;
+  uint32_t M = b & 0x7F;
+  if (E == 0) {
+    *sig = M;
+    *exp = 1 - 134;
+  } else {
+    *sig = 128u + M;
+    *exp = E - 134;
+  }
+}
+
+/* Round sign * mag * 2^-ACC_OFFSET to BF16, nearest even. */
+static uint16_t wide_to_bf16(const wide_t *mag, int negative) {
+  uint16_t sign = negative ? 0x8000 : 0;
+  int t = wide_top(mag);
+  if (t < 0) return sign;
+  /* lowest kept bit: 8 significant bits, but never below the BF16
+   * subnormal quantum 2^-133 (accumulator bit 133). */
+  int q = t - 7;
+  if (q < 133) q = 133;
+  uint32_t kept = 0;
+  for (int b = t; b >= q; b--) kept = (kept << 1) | (uint32_t)wide_bit(mag, b);
+  int rbit = wide_bit(mag, q - 1);
+  int sticky = wide_any_below(mag, q - 1);
+  if (rbit && (sticky || (kept & 1u))) kept += 1u;
+  if (kept == 0) return sign;
+  if (q == 133 && kept < 128u) return (uint16_t)(sign | kept); /* subnormal */
+  if (kept >= 256u) {
+    kept >>= 1;
+    q += 1;
+  }
+  int E = q - 132;
+  if (E >= 255) return (uint16_t)(sign | 0x7F80);
+  return (uint16_t)(sign | ((uint32_t)E << 7) | (kept - 128u));
+}
+
+uint16_t oracle_dot_bf16(const uint16_t *a, const uint16_t *b, int n) {
+  int has_nan = 0, has_pinf = 0, has_ninf = 0, all_negzero = 1;
+  wide_t pos, neg;
+  memset(&pos, 0, sizeof(pos));
+  memset(&neg, 0, sizeof(neg));
+  for (int j = 0; j < n; j++) {
+    uint16_t x = a[j], y = b[j];
+    int x_nan = ((x & 0x7F80) == 0x7F80) && (x & 0x7F);
+    int y_nan = ((y & 0x7F80) == 0x7F80) && (y & 0x7F);
+    int x_inf = (x & 0x7FFF) == 0x7F80, y_inf = (y & 0x7FFF) == 0x7F80;
+    int x_zero = (x & 0x7FFF) == 0, y_zero = (y & 0x7FFF) == 0;
+    int negative = ((x ^ y) & 0x8000) != 0;
+    if (x_nan || y_nan) {
+      has_nan = 1;
+      continue;
+    }
+    if (x_inf || y_inf) {
+      if (x_zero || y_zero) has_nan = 1; /* inf * 0 */
+      else if (negative) has_ninf = 1;
+      else has_pinf = 1;
+      continue;
+    }
+    if (x_zero || y_zero) {
+      if (!negative) all_negzero = 0;
+      continue;
+    }
+    all_negzero = 0;
+    uint32_t sx, sy;
+    int ex, ey;
+    bf16_parts(x, &sx, &ex);
+    bf16_parts(y, &sy, &ey);
+    uint64_t mag = (uint64_t)sx * (uint64_t)sy;
+    int at = ex + ey + ACC_OFFSET;
+    wide_add_shifted(negative ? &neg : &pos, mag, at);
+  }
+  if (has_nan || (has_pinf && has_ninf)) return 0x7FFF;
+  if (has_pinf) return 0x7F80;
+  if (has_ninf) return 0xFF80;
+  int c = wide_cmp(&pos, &neg);
+  if (c == 0) return (n > 0 && all_negzero) ? 0x8000 : 0x0000;
+  wide_t mag;
+  if (c > 0) wide_sub(&mag, &pos, &neg);
+  else wide_sub(&mag, &neg, &pos);
+  return wide_to_bf16(&mag, c < 0);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The loop ([P2] _loop_rest; [P3] module docstring, _StepKernel.kernel,   */
+/* anchor_embed, _w1_row).  For each step s and row r:                     */
+/*   prev(0)   = sext32(input_ids[anchor_idx[r]])                           */
+/*   e         = w1[min(u64(prev), w1_rows - 1)]                            */
+/*   bias[v]   = RN_bf16(exact dot(e, w2[v]))   (or the fed bias)           */
+/*   (c, l)    = transform(base[r, s, v], bias[v])                          */
+/*   cache[req, s, v] = c when the row is valid                             */
+/*   key[v]    = temp != 0 ? RN(RN(l / temp) - L(h(r, s, v))) : l           */
+/*   token     = total-order argmax of key; tokens[r, s] = token; prev = it */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const oracle_loop_args *a;
+  int32_t r, s;
+  const uint16_t *e;
+  int64_t req;
+  int valid;
+  float temp;
+  int64_t seed;
+  int64_t pos;
+  int has_cap;
+  float inv_cap;
+  float *keys;
+  int64_t v0, v1;
+} row_step_job;
+
+static void *row_step_range(void *arg) {
+  row_step_job *j = (row_step_job *)arg;
+  const oracle_loop_args *a = j->a;
+  const int64_t V = a->vocab;
+  const uint16_t *base_row = a->base + (int64_t)j->r * a->base_s0 + (int64_t)j->s * a->base_s1;
+  for (int64_t v = j->v0; v < j->v1; v++) {
+    uint16_t b;
+    if (a->fed_bias)
+      b = a->fed_bias[((int64_t)j->r * a->steps + j->s) * V + v];
+    else
+      b = oracle_dot_bf16(j->e, a->w2 + v * a->rank, a->rank);
+    if (a->bias_out) a->bias_out[((int64_t)j->r * a->steps + j->s) * V + v] = b;
+    float l;
+    uint16_t c = oracle_logit(base_row[v], b, a->mult, j->has_cap, j->inv_cap, a->cap, &l);
+    if (j->valid && a->cache) a->cache[j->req * a->cache_s0 + (int64_t)j->s * a->cache_s1 + v] = c;
+    uint32_t h = oracle_noise_hash(j->seed, j->s, j->pos, a->salt, (uint32_t)v);
+    j->keys[v] = oracle_key(l, j->temp, h);
+  }
+  return NULL;
+}
+
+int oracle_markov_loop(const oracle_loop_args *a) {
+  if (!a || a->vocab <= 0 || a->rank <= 0 || a->w1_rows <= 0 || a->rows < 0 || a->steps < 0)
+    return -1;
+  const int64_t V = a->vocab;
+  int nthreads = a->nthreads > 0 ? a->nthreads : 1;
+  if (nthreads > 256) nthreads = 256;
+  float *keys = (float *)malloc(sizeof(float) * (size_t)V);
+  if (!keys) return -2;
+  int has_cap = a->cap != 0.0f;
+  float inv_cap = has_cap ? 1.0f / a->cap : 0.0f;
+  pthread_t th[256];
+  row_step_job jobs[256];
+  for (int32_t r = 0; r < a->rows; r++) {
+    int64_t prev = (int64_t)a->input_ids[a->anchor_idx[r]]; /* int32, sign-extended */
+    for (int32_t s = 0; s < a->steps; s++) {
+      uint64_t last = (uint64_t)(a->w1_rows - 1);
+      uint64_t row = (uint64_t)prev < last ? (uint64_t)prev : last;
+      const uint16_t *e = a->w1 + (int64_t)row * a->rank;
+      int64_t req = a->req_idx ? a->req_idx[(int64_t)r * a->req_s0 + s] : r;
+      int valid = req >= 0 && req < a->num_req;
+      float temp = valid ? a->temperature[req] : 0.0f;
+      int64_t seed = valid ? a->seeds[req] : 0;
+      int64_t pos = a->sample_pos[(int64_t)r * a->pos_s0 + s];
+      int64_t chunk = (V + nthreads - 1) / nthreads;
+      int launched[256];
+      int njobs = 0;
+      for (int t = 0; t < nthreads; t++) {
+        int64_t v0 = (int64_t)t * chunk, v1 = v0 + chunk;
+        if (v0 >= V) break;
+        if (v1 > V) v1 = V;
+        row_step_job jb = {a, r, s, e, req, valid, temp, seed, pos, has_cap, inv_cap, keys, v0, v1};
+        jobs[t] = jb;
+        launched[t] = nthreads > 1 && pthread_create(&th[t], NULL, row_step_range, &jobs[t]) == 0;
+        if (!launched[t]) row_step_range(&jobs[t]);
+        njobs++;
+      }
+      for (int t = 0; t < njobs; t++)
+        if (launched[t]) pthread_join(th[t], NULL);
+      int64_t tok = oracle_argmax(keys, V);
+      a->tokens[(int64_t)r * a->tokens_s0 + s] = tok;
+      if (a->keys_out) memcpy(a->keys_out + ((int64_t)r * a->steps + s) * V, keys, sizeof(float) * (size_t)V);
+      prev = tok;
+    }
+  }
+  free(keys);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [P1] dsparkBuildVerifyTokens:                                            */
+/*   verify[b, 0] = last[b];  verify[b, j + 1] = draft[b, j], j < P.        */
+/* ------------------------------------------------------------------------ */
+
+void oracle_build_verify_tokens(const int64_t *last, const int64_t *draft, int64_t *verify,
+                                int32_t batch, int32_t draft_stride, int32_t P) {
+  for (int32_t b = 0; b < batch; b++) {
+    verify[(int64_t)b * (P + 1)] = last[b];
+    for (int32_t j = 0; j < P; j++)
+      verify[(int64_t)b * (P + 1) + j + 1] = draft[(int64_t)b * draft_stride + j];
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* [P1] dsparkGreedyAccept: a_j = argmax(logits[b, j, :]) (total order);    */
+/* accept draft[b, j] while it equals a_j, j < min(proposal_len[b], P);    */
+/* then append the bonus a_n.  accepted[b] = a_0 .. a_n, then -1;           */
+/* accept_len[b] = n + 1 (the accepted drafts plus the bonus token).        */
+/* ------------------------------------------------------------------------ */
+
+static int64_t argmax_bf16_row(const uint16_t *row, int64_t n, float *scratch) {
+  for (int64_t v = 0; v < n; v++) scratch[v] = oracle_bf16_to_f32(row[v]);
+  return oracle_argmax(scratch, n);
+}
+
+int oracle_greedy_accept(const uint16_t *logits, const int64_t *draft, const int32_t *proposal_len,
+                         int64_t *accepted, int32_t *accept_len, int32_t batch, int32_t draft_stride,
+                         int32_t P, int64_t vocab) {
+  float *scratch = (float *)malloc(sizeof(float) * (size_t)(vocab > 0 ? vocab : 1));
+  if (!scratch) return -2;
+  for (int32_t b = 0; b < batch; b++) {
+    int32_t pl = proposal_len[b];
+    if (pl < 0) pl = 0;
+    if (pl > P) pl = P;
+    const uint16_t *rows = logits + (int64_t)b * (P + 1) * vocab;
+    int32_t n = 0;
+    int64_t a = argmax_bf16_row(rows, vocab, scratch);
+    while (n < pl && draft[(int64_t)b * draft_stride + n] == a) {
+      accepted[(int64_t)b * (P + 1) + n] = a;
+      n++;
+      a = argmax_bf16_row(rows + (int64_t)n * vocab, vocab, scratch);
+    }
+    accepted[(int64_t)b * (P + 1) + n] = a;
+    for (int32_t j = n + 1; j <= P; j++) accepted[(int64_t)b * (P + 1) + j] = -1;
+    accept_len[b] = n + 1;
+  }
+  free(scratch);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Array helpers for the tests (plain loops over the scalar functions).    */
+/* ------------------------------------------------------------------------ */
+
+void oracle_noise_L_array(const uint32_t *h, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_noise_L(h[i]);
+}
+void oracle_uniform_array(const uint32_t *h, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_uniform(h[i]);
+}
+void oracle_log1m_array(const float *u, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_log1m(u[i]);
+}
+void oracle_logf_array(const float *x, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_logf(x[i]);
+}
+void oracle_tanhf_array(const float *x, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_tanhf(x[i]);
+}
+void oracle_logit_array(const uint16_t *base, const uint16_t *bias, uint16_t *c, float *l,
+                        int64_t n, float mult, float cap) {
+  int has_cap = cap != 0.0f;
+  float inv_cap = has_cap ? 1.0f / cap : 0.0f;
+  for (int64_t i = 0; i < n; i++) c[i] = oracle_logit(base[i], bias[i], mult, has_cap, inv_cap, cap, &l[i]);
+}
+void oracle_noise_hash_array(int64_t seed, int32_t step, int64_t sample_pos, uint32_t salt,
+                             const uint32_t *vocab_ids, uint32_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_noise_hash(seed, step, sample_pos, salt, vocab_ids[i]);
+}
+void oracle_dot_bf16_rows(const uint16_t *a, const uint16_t *b, uint16_t *out, int64_t rows, int n) {
+  for (int64_t r = 0; r < rows; r++) out[r] = oracle_dot_bf16(a + r * n, b + r * n, n);
+}
+void oracle_f32_to_bf16_array(const float *x, uint16_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_f32_to_bf16(x[i]);
+}
+void oracle_key_array(const float *l, float temp, const uint32_t *h, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_key(l[i], temp, h[i]);
+}
