@@ -1,0 +1,414 @@
+"""Benchmark of the GB300 DSpark Markov draft-sampling loop.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Workload: ``large16`` -- V = 163840, Markov rank 256, 16 request rows, k = 5
+draft steps, synthetic seeded inputs (workloads.py).  One timed "step" is one
+whole loop (anchor + 5 fused Markov steps) replayed from a CUDA graph with
+inputs resident in HBM; L2 is flushed (a 512 MB write) before each timed loop.
+Prints one JSON line (rank 0).
+
+Metric: µs per 5-step loop (lower is better) and achieved HBM GB/s of the
+step kernel against the measured copy bandwidth.  Algorithmic bytes per step
+launch: w2 (V * 256 * 2) + base read (R * V * 2) + cache write (R * V * 2).
+
+With N > 1 (torchrun), every rank runs its own 16-row loop on its own seeded
+rows over replicated tables (request rows are independent): weak scaling,
+no collective on the data path; the barrier and the max over ranks are the
+timing contract's.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "large16"
+METRIC = "µs per 5-step DSpark Markov loop and achieved HBM GB/s vs GB300 peak"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (also exercised by the gloo tests)
+# --------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend: str):
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend, rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, value: float, device=None) -> float:
+        if not self.pg:
+            return value
+        import torch
+        t = torch.tensor([value], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, value: float, device=None) -> float:
+        if not self.pg:
+            return value
+        import torch
+        t = torch.tensor([value], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def rank_seed_salt(rank: int) -> int:
+    """Each rank draws its own request rows (same shapes and distributions)."""
+    return 1000 + rank
+
+
+def algorithmic_bytes_per_step(vocab: int, rows: int, rank: int = 256) -> int:
+    return vocab * rank * 2 + 2 * rows * vocab * 2
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "dspark_markov_draft_anchor_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per step launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("source_digest") != source_digest() or d.get("workload") != WORKLOAD:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample_us_per_loop(wl, rows_sampled: int, nthreads: int, steps_sampled: int | None = None):
+    """Run the oracle on the first `rows_sampled` rows and `steps_sampled`
+    steps of the workload and scale to µs per full loop (rows are independent
+    and every step does the same work).  Returns (µs per full loop, wall s)."""
+    import oracle
+    K = wl.steps if steps_sampled is None else steps_sampled
+    cache = np.zeros((wl.num_req, K, wl.vocab), np.uint16)
+    t0 = time.perf_counter()
+    oracle.markov_loop(w1=wl.w1, w2=wl.w2, base=wl.base[:, :K], input_ids=wl.input_ids, anchor_idx=wl.anchor_idx,
+                       sample_pos=wl.sample_pos[:, :K], seeds=wl.seeds, temperature=wl.temperature,
+                       req_idx=wl.req_idx[:, :K], mult=wl.mult, cap=wl.cap, salt=wl.salt, cache=cache,
+                       rows=rows_sampled, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt * 1e6 * (wl.rows / rows_sampled) * (wl.steps / K), dt
+
+
+def run_reference(args, d: Dist):
+    """The reference arm: the CPU oracle, as it stands, on the host cores.
+    Each timed step is one row of the workload for as many of its draft steps
+    as keep the whole run near two minutes, scaled to a full loop."""
+    from dspark_markov_draft_anchor_gb300 import workloads
+    if d.rank != 0:
+        return 0
+    wl = workloads.make(WORKLOAD, seed_salt=rank_seed_salt(0))
+    nthreads = os.cpu_count() or 1
+    _, one = oracle_sample_us_per_loop(wl, 1, nthreads, 1)  # calibration: one row-step
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    k = int(max(1, min(wl.steps, budget // max(one, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_us_per_loop(wl, 1, nthreads, k)
+    times = []
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        us, _ = oracle_sample_us_per_loop(wl, 1, nthreads, k)
+        times.append(us)
+    wall = time.perf_counter() - t_start
+    value = statistics.mean(times)
+    sample = (f"1 of {wl.rows} rows x {k} of {wl.steps} steps of {WORKLOAD} per timed step, "
+              f"scaled x{wl.rows * wl.steps / k:g} to a full loop")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "us", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: V=163840, rank 256, 16 rows, k=5", "model": "DSpark Markov head (random-init)",
+                   "global_batch": wl.rows, "seq_len": wl.steps, "parallelism": "cpu oracle"},
+        "cpu_baseline": {"value": value, "unit": "us", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_native(args, d: Dist):
+    import torch
+    from dspark_markov_draft_anchor_gb300 import binding, workloads
+
+    torch.cuda.set_device(d.local_rank)
+    dev = torch.device("cuda", d.local_rank)
+    d.init("nccl")
+    wl = workloads.make(WORKLOAD, seed_salt=rank_seed_salt(d.rank))
+    R, K, V = wl.rows, wl.steps, wl.vocab
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    w1, w2 = bf16(wl.w1), bf16(wl.w2)
+    base, ids, anc, pos, req = bf16(wl.base), t(wl.input_ids), t(wl.anchor_idx), t(wl.sample_pos), t(wl.req_idx)
+    seeds, temp = t(wl.seeds), t(wl.temperature)
+    cache = torch.zeros((wl.num_req, K, V), dtype=torch.int16, device=dev)
+    tokens = torch.zeros((R, K), dtype=torch.int64, device=dev)
+    ctx = binding.MarkovContext(w1, w2, max_rows=R, max_steps=K, flags=binding.FLAG_PDL)
+    a = binding.loop_args(base=base, cache=cache, input_ids=ids, anchor_idx=anc, sample_pos=pos, seeds=seeds,
+                          temperature=temp, tokens=tokens, req_idx=req, mult=wl.mult, cap=wl.cap, salt=wl.salt)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    # capture anchor + k steps once
+    with torch.cuda.stream(stream):
+        ctx.loop(a, stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        ctx.loop(a, stream)
+    torch.cuda.synchronize()
+
+    def timed_loops(n, per_kernel=False):
+        """n loops, each after an L2 flush; CUDA events on the launch stream."""
+        ev = []
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                flush.fill_(1)
+                if per_kernel:
+                    marks = [torch.cuda.Event(enable_timing=True) for _ in range(K + 2)]
+                    marks[0].record(stream)
+                    ctx.anchor(a, stream)
+                    marks[1].record(stream)
+                    for s in range(K):
+                        ctx.step(a, s, stream)
+                        marks[s + 2].record(stream)
+                    ev.append(marks)
+                else:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                    ev.append((e0, e1))
+        return ev
+
+    for _ in range(max(args.warmup, 3)):
+        timed_loops(1)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(d.local_rank)
+    if d.rank == 0:
+        clocks.start()
+    d.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    ev = timed_loops(args.steps)
+    torch.cuda.synchronize()
+    d.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clock_info = clocks.stop() if d.rank == 0 else None
+    loop_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    mean_us = statistics.mean(loop_ms) * 1e3
+    mean_us = d.max(mean_us, dev)
+
+    # per-kernel durations of the step kernel (same launches, eager, events
+    # between kernels) for the roofline
+    for _ in range(2):
+        timed_loops(1, per_kernel=True)
+    evk = timed_loops(max(10, min(args.steps, 50)), per_kernel=True)
+    torch.cuda.synchronize()
+    step_ms = [m[s + 2 - 1].elapsed_time(m[s + 2]) for m in evk for s in range(K)]
+    step_us = statistics.mean(step_ms) * 1e3
+    eager_loop_us = statistics.mean([m[0].elapsed_time(m[K + 1]) for m in evk]) * 1e3
+
+    # end to end through the C ABI from pinned host buffers
+    hb = {k: v.cpu().pin_memory() for k, v in dict(base=base, ids=ids, anc=anc, pos=pos, req=req, seeds=seeds,
+                                                   temp=temp).items()}
+    h_tokens = torch.empty_like(tokens, device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hb.values())
+    d2h = h_tokens.numel() * h_tokens.element_size()
+    dev_bufs = dict(base=base, ids=ids, anc=anc, pos=pos, req=req, seeds=seeds, temp=temp)
+
+    def e2e_loops(n):
+        out = []
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for k_, v in hb.items():
+                    dev_bufs[k_].copy_(v, non_blocking=True)
+                ctx.loop(a, stream)
+                h_tokens.copy_(tokens, non_blocking=True)
+                e1.record(stream)
+                out.append((e0, e1))
+        return out
+
+    e2e_loops(3)
+    torch.cuda.synchronize()
+    e2e_ev = e2e_loops(max(10, min(args.steps, 200)))
+    torch.cuda.synchronize()
+    e2e_us = statistics.mean([e0.elapsed_time(e1) for e0, e1 in e2e_ev]) * 1e3
+    e2e_us = d.max(e2e_us, dev)
+
+    result = None
+    if d.rank == 0:
+        peak, peak_kind = measured_peaks()
+        algo = algorithmic_bytes_per_step(V, R)
+        achieved = algo / (step_us * 1e-6) / 1e9
+        cpu_us, cpu_s = (None, None)
+        cores = os.cpu_count() or 1
+        if args.cpu_baseline and d.world == 1:
+            cpu_us, cpu_s = oracle_sample_us_per_loop(wl, args.cpu_rows, cores)
+        qs = np.percentile(loop_ms, [10, 50, 90]) * 1e3
+        result = {
+            "metric": METRIC, "value": mean_us, "unit": "us", "n_gpus": d.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init Markov tables)",
+            "config": {"workload": f"{WORKLOAD}: V=163840, rank 256, 16 rows, k=5, t=1, Zipf spikes",
+                       "model": "DSpark Markov head (random-init w1/w2 BF16)", "global_batch": R * d.world,
+                       "seq_len": K, "parallelism": f"replicas x{d.world} (rows sharded, no collective)",
+                       "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed loop",
+                       "graph": True, "pdl": True, "bias_path": ["fma", "tcgen05"][ctx.bias_path(R)]},
+            "loop_us": {"mean": mean_us, "p10": qs[0], "p50": qs[1], "p90": qs[2], "eager_with_events": eager_loop_us},
+            "gbs_loop": algo * K / (mean_us * 1e-6) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": recorded_traffic(), "peak_kind": f"{peak_kind} hbm_gbs",
+                         "kernel": "markov_step", "kernel_us": step_us, "algorithmic_bytes": algo},
+            "cpu_baseline": None if cpu_us is None else {
+                "value": cpu_us, "unit": "us", "cores": cores, "kind": "oracle",
+                "sample": f"rows 0..{args.cpu_rows - 1} of {R} x {K} steps ({cpu_s:.1f} s wall), scaled x{R / args.cpu_rows:g}"},
+            "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * (1 + K),
+            "clocks": clock_info,
+            "wall_timed_s": t_wall,
+        }
+    ctx.close()
+    d.close()
+    if result is not None:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--cpu-rows", type=int, default=4)
+    p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = p.parse_args(argv)
+    d = Dist()
+    if args.impl == "reference":
+        return run_reference(args, d)
+    return run_native(args, d)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,204 @@
+// api.cu -- the C ABI of libdspark_markov.so (declared in include/dspark_markov.h):
+// argument validation, the context's scratch, and the launch sequence of the
+// Markov loop ([P2] FusedMarkov.run; [P3] anchor_embed + markov_step).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "dspark_markov.h"
+#include "kernels.h"
+
+struct dspark_markov_ctx {
+  int device;
+  int sm_count;
+  dspark_markov_config cfg;
+  const uint16_t* w1;
+  const uint16_t* w2;
+  unsigned long long* slots;  // [(max_steps + 1) * max_rows] packed argmax slots
+  unsigned int* counters;     // [max_steps] arrival counters
+  int* status;                // device status word
+  int grid_simple;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_args(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
+  if (!ctx || !a) return DSPARK_ERR_INVALID_ARG;
+  if (a->rows < 1 || a->steps < 1) return DSPARK_ERR_INVALID_ARG;
+  if (a->rows > ctx->cfg.max_rows || a->steps > ctx->cfg.max_steps) return DSPARK_ERR_TOO_MANY_ROWS;
+  if (!a->base || !a->input_ids || !a->anchor_idx || !a->sample_pos || !a->tokens) return DSPARK_ERR_INVALID_ARG;
+  if (a->num_req < 0 || (a->num_req > 0 && (!a->seeds || !a->temperature))) return DSPARK_ERR_INVALID_ARG;
+  if (!isfinite(a->mult) || !isfinite(a->cap)) return DSPARK_ERR_INVALID_ARG;
+  if (a->base_s0 < 0 || a->base_s1 < 0 || a->tokens_s0 < a->steps || a->pos_s0 < a->steps)
+    return DSPARK_ERR_INVALID_ARG;
+  if (a->req_idx && a->req_s0 < a->steps) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(a->base) || (a->base_s0 % 8) || (a->base_s1 % 8)) return DSPARK_ERR_MISALIGNED;
+  if (a->cache) {
+    if (a->cache_s0 < 0 || a->cache_s1 < 0) return DSPARK_ERR_INVALID_ARG;
+    if (!aligned16(a->cache) || (a->cache_s0 % 8) || (a->cache_s1 % 8)) return DSPARK_ERR_MISALIGNED;
+  }
+  return DSPARK_OK;
+}
+
+dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int step) {
+  dspark::StepParams p;
+  p.w1 = ctx->w1;
+  p.w2 = ctx->w2;
+  p.base = static_cast<const uint16_t*>(a->base) + static_cast<int64_t>(step) * a->base_s1;
+  p.base_s0 = a->base_s0;
+  p.cache = a->cache ? static_cast<uint16_t*>(a->cache) + static_cast<int64_t>(step) * a->cache_s1 : nullptr;
+  p.cache_s0 = a->cache_s0;
+  p.req_idx = a->req_idx;
+  p.req_s0 = a->req_s0;
+  p.sample_pos = a->sample_pos;
+  p.pos_s0 = a->pos_s0;
+  p.num_req = a->num_req;
+  p.seeds = a->seeds;
+  p.temperature = a->temperature;
+  p.tokens = a->tokens;
+  p.tokens_s0 = a->tokens_s0;
+  p.bias_out = static_cast<uint16_t*>(a->bias_out);
+  const int64_t mr = ctx->cfg.max_rows;
+  p.slots_prev = ctx->slots + static_cast<int64_t>(step) * mr;
+  p.slots_out = ctx->slots + static_cast<int64_t>(step + 1) * mr;
+  p.counter = ctx->counters + step;
+  p.status = ctx->status;
+  p.vocab = ctx->cfg.vocab;
+  p.w1_rows = ctx->cfg.w1_rows;
+  p.rows = a->rows;
+  p.steps = a->steps;
+  p.step = step;
+  p.mult = a->mult;
+  p.cap = a->cap;
+  p.inv_cap = a->cap != 0.0f ? 1.0f / a->cap : 0.0f;
+  p.salt = a->salt;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dspark_strerror(int code) {
+  switch (code) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_ERR_INVALID_ARG: return "invalid argument";
+    case DSPARK_ERR_UNSUPPORTED_RANK: return "unsupported Markov rank (256 only)";
+    case DSPARK_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case DSPARK_ERR_TOO_MANY_ROWS: return "rows or steps above the context's maximum";
+    case DSPARK_ERR_CAPTURING: return "stream is capturing (init allocates)";
+    case DSPARK_ERR_CUDA: return "CUDA error";
+    case DSPARK_ERR_DEVICE_TIMEOUT: return "a bounded device wait gave up";
+    case DSPARK_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (GB300)";
+    default: return "unknown error";
+  }
+}
+
+int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg, const void* w1_bf16,
+                       const void* w2_bf16, cudaStream_t stream) {
+  if (!out || !cfg || !w1_bf16 || !w2_bf16) return DSPARK_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg->rank != dspark::kRank) return DSPARK_ERR_UNSUPPORTED_RANK;
+  if (cfg->vocab < 1 || cfg->w1_rows < 1) return DSPARK_ERR_INVALID_ARG;
+  if (cfg->max_rows < 1 || cfg->max_rows > dspark::kMaxRows) return DSPARK_ERR_TOO_MANY_ROWS;
+  if (cfg->max_steps < 1 || cfg->max_steps > dspark::kMaxSteps) return DSPARK_ERR_TOO_MANY_ROWS;
+  if (!aligned16(w1_bf16) || !aligned16(w2_bf16)) return DSPARK_ERR_MISALIGNED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return DSPARK_ERR_CAPTURING;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (major != 10 || minor != 3) return DSPARK_ERR_UNSUPPORTED_DEVICE;
+  if (dspark::setup_step_simple() != cudaSuccess) return DSPARK_ERR_CUDA;
+
+  dspark_markov_ctx* ctx = static_cast<dspark_markov_ctx*>(calloc(1, sizeof(dspark_markov_ctx)));
+  if (!ctx) return DSPARK_ERR_INVALID_ARG;
+  ctx->device = dev;
+  ctx->sm_count = sms;
+  ctx->cfg = *cfg;
+  ctx->w1 = static_cast<const uint16_t*>(w1_bf16);
+  ctx->w2 = static_cast<const uint16_t*>(w2_bf16);
+  const size_t nslots = static_cast<size_t>(cfg->max_steps + 1) * cfg->max_rows;
+  if (cudaMalloc(&ctx->slots, nslots * sizeof(unsigned long long)) != cudaSuccess ||
+      cudaMalloc(&ctx->counters, cfg->max_steps * sizeof(unsigned int)) != cudaSuccess ||
+      cudaMalloc(&ctx->status, sizeof(int)) != cudaSuccess) {
+    dspark_markov_destroy(ctx);
+    return DSPARK_ERR_CUDA;
+  }
+  if (cudaMemsetAsync(ctx->slots, 0, nslots * sizeof(unsigned long long), stream) != cudaSuccess ||
+      cudaMemsetAsync(ctx->counters, 0, cfg->max_steps * sizeof(unsigned int), stream) != cudaSuccess ||
+      cudaMemsetAsync(ctx->status, 0, sizeof(int), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    dspark_markov_destroy(ctx);
+    return DSPARK_ERR_CUDA;
+  }
+  ctx->grid_simple = dspark::simple_step_grid(cfg->vocab);
+  *out = ctx;
+  return DSPARK_OK;
+}
+
+void dspark_markov_destroy(dspark_markov_ctx* ctx) {
+  if (!ctx) return;
+  if (ctx->slots) cudaFree(ctx->slots);
+  if (ctx->counters) cudaFree(ctx->counters);
+  if (ctx->status) cudaFree(ctx->status);
+  free(ctx);
+}
+
+int32_t dspark_markov_partial_count(const dspark_markov_ctx* ctx) { return ctx ? ctx->grid_simple : 0; }
+
+int32_t dspark_markov_bias_path(const dspark_markov_ctx* ctx, int32_t rows) {
+  (void)ctx;
+  (void)rows;
+  return 0;
+}
+
+int dspark_markov_anchor(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
+  int rc = check_args(ctx, a);
+  if (rc != DSPARK_OK) return rc;
+  if (dspark::launch_anchor(a->input_ids, a->anchor_idx, ctx->slots, ctx->counters, a->rows, a->steps,
+                            ctx->cfg.max_rows, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+int dspark_markov_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_t step,
+                       cudaStream_t stream) {
+  int rc = check_args(ctx, a);
+  if (rc != DSPARK_OK) return rc;
+  if (step < 0 || step >= a->steps) return DSPARK_ERR_INVALID_ARG;
+  const dspark::StepParams p = make_params(ctx, a, step);
+  const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
+  if (dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
+  int rc = dspark_markov_anchor(ctx, a, stream);
+  if (rc != DSPARK_OK) return rc;
+  for (int s = 0; s < a->steps; ++s) {
+    rc = dspark_markov_step(ctx, a, s, stream);
+    if (rc != DSPARK_OK) return rc;
+  }
+  return DSPARK_OK;
+}
+
+int dspark_markov_get_status(dspark_markov_ctx* ctx, cudaStream_t stream, int32_t* device_status) {
+  if (!ctx || !device_status) return DSPARK_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaMemcpy(&v, ctx->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaMemset(ctx->status, 0, sizeof(int)) != cudaSuccess) return DSPARK_ERR_CUDA;
+  *device_status = v;
+  return DSPARK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,21 @@
+// kernels.h -- host-side launchers of the library's kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "step_common.cuh"
+
+namespace dspark {
+
+// Anchor: slots_prev row 0 <- the anchor tokens, later step slots and the
+// arrival counters cleared ([P3] anchor_embed, _AnchorKernel).
+cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, unsigned long long* slots,
+                          unsigned int* counters, int rows, int steps, int max_rows, cudaStream_t stream);
+
+// Simple fused step: one CTA per 128-entry vocabulary tile, FP32 FMA bias.
+int simple_step_grid(int64_t vocab);
+cudaError_t setup_step_simple();
+cudaError_t launch_step_simple(const StepParams& p, bool has_cap, bool pdl, cudaStream_t stream);
+
+}  // namespace dspark

@@ -1,0 +1,91 @@
+// step_common.cuh -- parameters and small device helpers shared by the
+// anchor and step kernels of the Markov loop.
+#pragma once
+
+#include <stdint.h>
+
+#include "markov_math.cuh"
+
+namespace dspark {
+
+constexpr int kRank = 256;           // Markov rank supported by the kernels
+constexpr int kMaxRows = 256;        // rows per loop call
+constexpr int kMaxSteps = 64;        // draft steps per loop call
+
+// Device status codes (mirrors of the DSPARK_ERR_* values).
+constexpr int kStatusTimeout = -7;
+
+// Everything one step launch needs.  Strides are in elements.
+struct StepParams {
+  const uint16_t* w1;   // [w1_rows, 256] BF16
+  const uint16_t* w2;   // [V, 256] BF16
+  const uint16_t* base; // base logits, step column already applied: base + step*base_s1
+  int64_t base_s0;
+  uint16_t* cache;      // cache, step column already applied: cache + step*cache_s1 (or null)
+  int64_t cache_s0;
+  const int64_t* req_idx;  // [rows, steps] or null
+  int64_t req_s0;
+  const int64_t* sample_pos;
+  int64_t pos_s0;
+  int64_t num_req;
+  const int64_t* seeds;
+  const float* temperature;
+  int64_t* tokens;
+  int64_t tokens_s0;
+  uint16_t* bias_out;   // [rows, steps, V] or null; step applied by the kernel
+  const unsigned long long* slots_prev;  // [rows] previous token (packed)
+  unsigned long long* slots_out;         // [rows] this step's packed argmax
+  unsigned int* counter;                 // this step's arrival counter
+  int* status;
+  int64_t vocab;
+  int64_t w1_rows;
+  int32_t rows;
+  int32_t steps;
+  int32_t step;
+  float mult;
+  float inv_cap;
+  float cap;
+  uint32_t salt;
+};
+
+// PTX griddepcontrol (programmatic dependent launch): wait for the grids this
+// one depends on to complete and flush; a no-op without a dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Per-row, per-step sampling state ([P3] _StepKernel.kernel): request,
+// validity, temperature, seed and the Murmur3 prefix.
+struct RowInfo {
+  uint32_t prefix;
+  float temp;
+  int32_t valid;
+  int32_t pad;
+  int64_t cache_off;  // req * cache_s0 (valid rows)
+};
+
+__device__ __forceinline__ RowInfo row_info(const StepParams& p, int r) {
+  RowInfo ri;
+  const int64_t req = p.req_idx ? p.req_idx[static_cast<int64_t>(r) * p.req_s0 + p.step] : r;
+  const bool valid = req >= 0 && req < p.num_req;
+  const float temp = valid ? p.temperature[req] : 0.0f;
+  const uint64_t seed = valid ? static_cast<uint64_t>(p.seeds[req]) : 0ull;
+  const int64_t pos = p.sample_pos[static_cast<int64_t>(r) * p.pos_s0 + p.step];
+  ri.prefix = murmur_prefix(seed, p.step, pos, p.salt);
+  ri.temp = temp;
+  ri.valid = valid && p.cache != nullptr;
+  ri.pad = 0;
+  ri.cache_off = valid ? req * p.cache_s0 : 0;
+  return ri;
+}
+
+}  // namespace dspark

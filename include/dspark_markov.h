@@ -1,0 +1,193 @@
+/*
+ * dspark_markov.h -- C ABI of the GB300 (sm_103a) DSpark Markov draft-sampling
+ * library, libdspark_markov.so.
+ *
+ * The operations follow these pages (cited as "page, section"):
+ *   [P1] TensorRT Edge-LLM C++ API, "Dspark Kernels": dsparkMarkovPartialCount,
+ *        dsparkBuildVerifyTokens, dsparkGreedyAccept.
+ *   [P2] vLLM models.kimi_k3.nvidia.specialized_decode.drafter.markov: module
+ *        docstring (exactness paragraph), FusedMarkov, _gumbel_key, _loop_rest.
+ *   [P3] vLLM models.muse_spark.nvidia.specialized_decode.cutedsl.draft.markov:
+ *        module docstring, anchor_embed, markov_step (_StepKernel.kernel,
+ *        _finish, _logit, _gumbel, _murmur_prefix, _combine, _w1_row).
+ *   [P4] vLLM models.deepseek_v41.amd.ops.fused_markov: module docstring.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to device memory of the
+ *     current CUDA device; the caller owns them.  The library owns only the
+ *     context's scratch.  Strides are in elements.
+ *   - Return 0 (DSPARK_OK) or a negative DSPARK_ERR_* code; nothing throws.
+ *     Launch-type entry points do not synchronise the host; they enqueue on
+ *     `stream` and are safe to capture in a CUDA graph (fixed pointers, no
+ *     allocation).  dspark_markov_init and dspark_markov_get_status are not.
+ *   - BF16 tensors are passed as raw 16-bit storage (`const void *`).
+ */
+#ifndef DSPARK_MARKOV_H
+#define DSPARK_MARKOV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes ------------------------------------------------------- */
+#define DSPARK_OK 0
+#define DSPARK_ERR_INVALID_ARG (-1)      /* null pointer, bad size, bad stride */
+#define DSPARK_ERR_UNSUPPORTED_RANK (-2) /* Markov rank other than 256 */
+#define DSPARK_ERR_MISALIGNED (-3)       /* a pointer or stride breaks 16-byte alignment */
+#define DSPARK_ERR_TOO_MANY_ROWS (-4)    /* rows > max_rows or steps > max_steps */
+#define DSPARK_ERR_CAPTURING (-5)        /* init called while `stream` is capturing */
+#define DSPARK_ERR_CUDA (-6)             /* a CUDA runtime call or launch failed */
+#define DSPARK_ERR_DEVICE_TIMEOUT (-7)   /* a bounded device wait gave up (status word) */
+#define DSPARK_ERR_UNSUPPORTED_DEVICE (-8) /* not a compute capability 10.3 device */
+
+/* ---- config flags ------------------------------------------------------ */
+#define DSPARK_FLAG_PDL 0x1        /* launch steps with programmatic dependent launch */
+#define DSPARK_FLAG_FORCE_FMA 0x2  /* bias on CUDA-core FMA for every row count */
+#define DSPARK_FLAG_FORCE_MMA 0x4  /* bias on tcgen05 tensor cores for every row count */
+
+/* Opaque context: the Markov tables, the tensor maps over them and the
+ * scratch of one loop (per-step argmax slots and arrival counters), sized
+ * once for max_rows x max_steps so that captured graphs keep its addresses
+ * ([P2] FusedMarkov: "scratch sized for its largest batch, allocated once"). */
+typedef struct dspark_markov_ctx dspark_markov_ctx;
+
+typedef struct {
+  int32_t vocab;     /* V: rows of w2 and width of a logits row (>= 1) */
+  int32_t rank;      /* Markov rank R of w1 and w2; must be 256 */
+  int32_t w1_rows;   /* rows of w1 (>= 1); ids are clamped to w1_rows - 1 */
+  int32_t max_rows;  /* largest `rows` a loop call may pass (1..256) */
+  int32_t max_steps; /* largest `steps` a loop call may pass (1..64) */
+  int32_t flags;     /* DSPARK_FLAG_* */
+} dspark_markov_config;
+
+/*
+ * dspark_markov_init -- validate the tables and allocate the context
+ * ([P2] FusedMarkov.__init__, why_not; [P3] MarkovKernels).
+ *   w1_bf16: device, [w1_rows, rank] BF16, row-major, 16-byte aligned.
+ *   w2_bf16: device, [vocab, rank] BF16, row-major, 16-byte aligned.
+ * The tables are not copied: they must stay valid and unchanged while the
+ * context is used.  Allocates with cudaMalloc, so it must not run while
+ * `stream` is being captured (DSPARK_ERR_CAPTURING).  On success *out owns
+ * the context; free it with dspark_markov_destroy.
+ */
+DSPARK_API int dspark_markov_init(dspark_markov_ctx **out, const dspark_markov_config *cfg, const void *w1_bf16,
+                       const void *w2_bf16, cudaStream_t stream);
+
+/* Arguments of one loop call (all device pointers unless stated). */
+typedef struct {
+  int32_t rows;  /* request rows of this call, 1..max_rows */
+  int32_t steps; /* draft steps k, 1..max_steps */
+  /* Base logits [rows, steps, V] BF16: base[r, s, v] = base[r*base_s0 + s*base_s1 + v].
+   * 16-byte aligned, strides multiples of 8 elements. */
+  const void *base;
+  int64_t base_s0, base_s1;
+  /* Draft-logits cache [num_req, steps, V] BF16 (pre-temperature logits),
+   * written at [req, s, v] for valid rows ([P3] _StepKernel.kernel).
+   * 16-byte aligned, strides multiples of 8 elements; must not overlap base. */
+  void *cache;
+  int64_t cache_s0, cache_s1;
+  /* Step 0's previous token: sext(input_ids[anchor_idx[r]]) ([P3] anchor_embed). */
+  const int32_t *input_ids;  /* int32 token ids */
+  const int64_t *anchor_idx; /* [rows] int64 indices into input_ids */
+  /* Request of (row, step): req_idx[r*req_s0 + s] (int64); NULL means req = r.
+   * A request outside [0, num_req) marks the row invalid for that step: no
+   * cache store, temperature and seed read as 0 (greedy). */
+  const int64_t *req_idx;
+  int64_t req_s0;
+  const int64_t *sample_pos; /* [rows, steps] int64 at sample_pos[r*pos_s0 + s] */
+  int64_t pos_s0;
+  int64_t num_req;           /* length of seeds / temperature, rows of cache */
+  const int64_t *seeds;      /* [num_req] int64 (a uint64 bit pattern) */
+  const float *temperature;  /* [num_req] f32; 0 = greedy */
+  float mult;                /* logit multiplier ([P3] _logit), finite */
+  float cap;                 /* soft cap, finite; 0 = none */
+  uint32_t salt;             /* draft noise salt; the pages use 1u << 30 */
+  int64_t *tokens;           /* out: [rows, steps] int64 at tokens[r*tokens_s0 + s] */
+  int64_t tokens_s0;
+  /* Optional: the BF16 bias the kernel used, [rows, steps, V] contiguous;
+   * NULL in production (a checking aid, costs one extra write per element). */
+  void *bias_out;
+} dspark_markov_loop_args;
+
+/*
+ * dspark_markov_loop -- the whole k-step loop ([P2] FusedMarkov.run,
+ * _loop_rest; [P3] anchor_embed + markov_step per step): for each step s and
+ * row r, embed the previous token (w1 row clamped to the last row), bias
+ * GEMV against w2 in FP32 rounded once to BF16, BF16 add to the base logits,
+ * multiplier and optional soft cap, cache store, Gumbel-max with
+ * MurmurHash3 noise of (seed, step, position + salt, vocab id), and a
+ * total-order argmax (first NaN, else lowest id of the maximum).  The
+ * winner is tokens[r, s] and the next step's previous token.
+ * Enqueues 1 + steps kernels on `stream`; no host synchronisation.
+ */
+DSPARK_API int dspark_markov_loop(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args,
+                       cudaStream_t stream);
+
+/* dspark_markov_anchor / dspark_markov_step -- the loop's kernels one at a
+ * time ([P3] anchor_embed, markov_step): anchor first, then step 0 .. steps-1
+ * in order, with the same args.  dspark_markov_loop is exactly this sequence. */
+DSPARK_API int dspark_markov_anchor(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args,
+                         cudaStream_t stream);
+DSPARK_API int dspark_markov_step(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args, int32_t step,
+                       cudaStream_t stream);
+
+/* [P1] dsparkMarkovPartialCount: the number of vocabulary blocks the step
+ * kernel partitions the vocabulary into (its grid size). */
+DSPARK_API int32_t dspark_markov_partial_count(const dspark_markov_ctx *ctx);
+
+/* Which bias path a call with `rows` rows takes: 0 = FMA, 1 = tcgen05. */
+DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t rows);
+
+/* Synchronise `stream`, then read and clear the device status word: 0, or a
+ * DSPARK_ERR_* a kernel recorded (a bounded wait that gave up).  Returns
+ * DSPARK_OK or DSPARK_ERR_CUDA. */
+DSPARK_API int dspark_markov_get_status(dspark_markov_ctx *ctx, cudaStream_t stream, int32_t *device_status);
+
+DSPARK_API void dspark_markov_destroy(dspark_markov_ctx *ctx);
+
+/*
+ * dspark_build_verify_tokens -- [P1] dsparkBuildVerifyTokens:
+ *   verify[b, 0] = last[b];  verify[b, j + 1] = draft[b * draft_stride + j], j < P.
+ * last [batch] int64, draft [batch, draft_stride] int64, verify [batch, P + 1]
+ * int64 contiguous (device).  batch >= 0, 0 <= P <= draft_stride.
+ */
+DSPARK_API int dspark_build_verify_tokens(const int64_t *last, const int64_t *draft, int64_t *verify,
+                               int32_t batch, int32_t draft_stride, int32_t P, cudaStream_t stream);
+
+/*
+ * dspark_greedy_accept -- [P1] dsparkGreedyAccept: a_j = total-order argmax
+ * of logits[b, j, :]; accept draft[b, j] while it equals a_j for
+ * j < clamp(proposal_len[b], 0, P); then append the bonus a_n.
+ *   logits: device BF16 [batch, P + 1, vocab], contiguous, 16-byte aligned,
+ *           vocab a multiple of 8.
+ *   draft [batch, draft_stride] int64; proposal_len [batch] int32.
+ *   accepted: out [batch, P + 1] int64: a_0 .. a_n, then -1.
+ *   accept_len: out [batch] int32 = n + 1 (drafts accepted plus the bonus).
+ *   scratch: device, >= dspark_greedy_accept_scratch_bytes(batch, P, vocab)
+ *            bytes, 16-byte aligned; its contents on entry do not matter.
+ * Positions after the last one the acceptance can reach are not scanned.
+ */
+DSPARK_API size_t dspark_greedy_accept_scratch_bytes(int32_t batch, int32_t P, int32_t vocab);
+DSPARK_API int dspark_greedy_accept(const void *logits, const int64_t *draft, const int32_t *proposal_len,
+                         int64_t *accepted, int32_t *accept_len, void *scratch, size_t scratch_bytes,
+                         int32_t batch, int32_t draft_stride, int32_t P, int32_t vocab,
+                         cudaStream_t stream);
+
+/* A short English description of a DSPARK_* code (static storage). */
+DSPARK_API const char *dspark_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_MARKOV_H */

@@ -1,0 +1,47 @@
+/*
+ * dspark_markov_check.h -- checking aids of libdspark_markov.so.
+ *
+ * Each entry point runs, element by element on the GPU, one of the device
+ * functions the Markov step kernel inlines, so that tests can compare them
+ * bit for bit with an independent implementation over exhaustive input
+ * ranges.  They are not part of the sampling path.
+ *
+ * All pointers are device pointers; n >= 0; each call enqueues one kernel on
+ * `stream` and returns DSPARK_OK or a DSPARK_ERR_* code (dspark_markov.h).
+ */
+#ifndef DSPARK_MARKOV_CHECK_H
+#define DSPARK_MARKOV_CHECK_H
+
+#include "dspark_markov.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* L[i] = log(-log(1 - u(h0 + i))), u(h) = RN((h + 0.5) / 2^32): the noise of
+ * [P3] _gumbel with this library's own logarithm; h0 + i wraps modulo 2^32. */
+DSPARK_API int dspark_check_noise_range(uint32_t h0, float *L, int64_t n, cudaStream_t stream);
+
+/* Murmur3 noise hash of [P3] _StepKernel.kernel for ids[i]:
+ * out[i] = MurmurHash3_x86_32(seed 0; lo(s'), hi(s'), lo(pos - 1 + salt), ids[i]),
+ * s' = seed XOR (step << 32). */
+DSPARK_API int dspark_check_hash(int64_t seed, int32_t step, int64_t pos, uint32_t salt, const uint32_t *ids,
+                                 uint32_t *out, int64_t n, cudaStream_t stream);
+
+/* Output transform of [P3] _logit: c[i] = cached BF16 of (base[i], bias[i]),
+ * l[i] its FP32 value; cap = 0 means no soft cap. */
+DSPARK_API int dspark_check_logit(const uint16_t *base, const uint16_t *bias, uint16_t *c, float *l, int64_t n,
+                                  float mult, float cap, cudaStream_t stream);
+
+/* key[i] = RN(RN(l[i] / temp) - L(h[i])) for temp != 0, else l[i] ([P2] _gumbel_key). */
+DSPARK_API int dspark_check_key(const float *l, float temp, const uint32_t *h, float *key, int64_t n,
+                                cudaStream_t stream);
+
+/* own log and tanh of the library, elementwise. */
+DSPARK_API int dspark_check_logf(const float *x, float *y, int64_t n, cudaStream_t stream);
+DSPARK_API int dspark_check_tanhf(const float *x, float *y, int64_t n, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
