@@ -35,10 +35,10 @@ int check_args(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
   if (a->base_s0 < 0 || a->base_s1 < 0 || a->tokens_s0 < a->steps || a->pos_s0 < a->steps)
     return DSPARK_ERR_INVALID_ARG;
   if (a->req_idx && a->req_s0 < a->steps) return DSPARK_ERR_INVALID_ARG;
-  if (!aligned16(a->base) || (a->base_s0 % 8) || (a->base_s1 % 8)) return DSPARK_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(a->base) & 1u) return DSPARK_ERR_MISALIGNED;
   if (a->cache) {
     if (a->cache_s0 < 0 || a->cache_s1 < 0) return DSPARK_ERR_INVALID_ARG;
-    if (!aligned16(a->cache) || (a->cache_s0 % 8) || (a->cache_s1 % 8)) return DSPARK_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(a->cache) & 1u) return DSPARK_ERR_MISALIGNED;
   }
   return DSPARK_OK;
 }

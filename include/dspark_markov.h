@@ -44,7 +44,7 @@ extern "C" {
 #define DSPARK_OK 0
 #define DSPARK_ERR_INVALID_ARG (-1)      /* null pointer, bad size, bad stride */
 #define DSPARK_ERR_UNSUPPORTED_RANK (-2) /* Markov rank other than 256 */
-#define DSPARK_ERR_MISALIGNED (-3)       /* a pointer or stride breaks 16-byte alignment */
+#define DSPARK_ERR_MISALIGNED (-3)       /* a pointer breaks its required alignment */
 #define DSPARK_ERR_TOO_MANY_ROWS (-4)    /* rows > max_rows or steps > max_steps */
 #define DSPARK_ERR_CAPTURING (-5)        /* init called while `stream` is capturing */
 #define DSPARK_ERR_CUDA (-6)             /* a CUDA runtime call or launch failed */
@@ -89,12 +89,14 @@ typedef struct {
   int32_t rows;  /* request rows of this call, 1..max_rows */
   int32_t steps; /* draft steps k, 1..max_steps */
   /* Base logits [rows, steps, V] BF16: base[r, s, v] = base[r*base_s0 + s*base_s1 + v].
-   * 16-byte aligned, strides multiples of 8 elements. */
+   * Any non-negative strides; the TMA-fed step kernel is used when the
+   * pointer is 16-byte aligned and the strides are multiples of 8 elements
+   * (the values are the same either way, [P3] vectorized). */
   const void *base;
   int64_t base_s0, base_s1;
   /* Draft-logits cache [num_req, steps, V] BF16 (pre-temperature logits),
-   * written at [req, s, v] for valid rows ([P3] _StepKernel.kernel).
-   * 16-byte aligned, strides multiples of 8 elements; must not overlap base. */
+   * written at [req, s, v] for valid rows ([P3] _StepKernel.kernel); NULL
+   * stores nothing.  Must not overlap base. */
   void *cache;
   int64_t cache_s0, cache_s1;
   /* Step 0's previous token: sext(input_ids[anchor_idx[r]]) ([P3] anchor_embed). */

@@ -191,7 +191,7 @@ def test_argument_errors_are_reported_not_launched():
         g.ctx.loop(a)
     assert e.value.code == -4
     a = g.args(cache, tokens)
-    a.base += 2  # one element off: not 16-byte aligned
+    a.base += 1  # half an element off
     with pytest.raises(binding.DsparkError) as e:
         g.ctx.loop(a)
     assert e.value.code == -3
