@@ -19,11 +19,22 @@ struct dspark_markov_ctx {
   unsigned int* counters;     // [max_steps] arrival counters
   int* status;                // device status word
   int grid_simple;
+  int grid_tc;
+  bool tc_ok;                 // tensor-core step available (tensor map encoded)
+  CUtensorMap w2_map;         // TMA map over w2: boxes of 32 rows x 64 K, 128-byte swizzle
 };
 
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Rows up to which the CUDA-core kernel forms the bias; above, tensor cores.
+constexpr int kFmaMaxRows = 4;
+
+// The TMA-fed kernel reads base rows as tensor tiles: 16-byte aligned rows.
+bool tma_base_ok(const dspark_markov_loop_args* a) {
+  return aligned16(a->base) && (a->base_s0 % 8) == 0 && (a->base_s1 % 8) == 0;
+}
 
 int check_args(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
   if (!ctx || !a) return DSPARK_ERR_INVALID_ARG;
@@ -118,6 +129,8 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
     return DSPARK_ERR_CUDA;
   if (major != 10 || minor != 3) return DSPARK_ERR_UNSUPPORTED_DEVICE;
   if (dspark::setup_step_simple() != cudaSuccess) return DSPARK_ERR_CUDA;
+  const bool tc_setup = dspark::setup_step_tc() == cudaSuccess;
+  (void)cudaGetLastError();
 
   dspark_markov_ctx* ctx = static_cast<dspark_markov_ctx*>(calloc(1, sizeof(dspark_markov_ctx)));
   if (!ctx) return DSPARK_ERR_INVALID_ARG;
@@ -141,6 +154,8 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
     return DSPARK_ERR_CUDA;
   }
   ctx->grid_simple = dspark::simple_step_grid(cfg->vocab);
+  ctx->grid_tc = dspark::tc_step_grid(cfg->vocab, sms);
+  ctx->tc_ok = tc_setup && dspark::encode_w2_map(&ctx->w2_map, w2_bf16, cfg->vocab);
   *out = ctx;
   return DSPARK_OK;
 }
@@ -153,12 +168,15 @@ void dspark_markov_destroy(dspark_markov_ctx* ctx) {
   free(ctx);
 }
 
-int32_t dspark_markov_partial_count(const dspark_markov_ctx* ctx) { return ctx ? ctx->grid_simple : 0; }
-
 int32_t dspark_markov_bias_path(const dspark_markov_ctx* ctx, int32_t rows) {
-  (void)ctx;
-  (void)rows;
-  return 0;
+  if (!ctx || !ctx->tc_ok || (ctx->cfg.flags & DSPARK_FLAG_FORCE_FMA)) return 0;
+  if (ctx->cfg.flags & DSPARK_FLAG_FORCE_MMA) return 1;
+  return rows > kFmaMaxRows ? 1 : 0;
+}
+
+int32_t dspark_markov_partial_count(const dspark_markov_ctx* ctx) {
+  if (!ctx) return 0;
+  return dspark_markov_bias_path(ctx, ctx->cfg.max_rows) ? ctx->grid_tc : ctx->grid_simple;
 }
 
 int dspark_markov_anchor(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
@@ -177,8 +195,12 @@ int dspark_markov_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
   if (step < 0 || step >= a->steps) return DSPARK_ERR_INVALID_ARG;
   const dspark::StepParams p = make_params(ctx, a, step);
   const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
-  if (dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream) != cudaSuccess) return DSPARK_ERR_CUDA;
-  return DSPARK_OK;
+  cudaError_t e;
+  if (dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a))
+    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->grid_tc, pdl, stream);
+  else
+    e = dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream);
+  return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
 int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {

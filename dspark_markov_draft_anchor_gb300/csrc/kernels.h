@@ -1,6 +1,7 @@
 // kernels.h -- host-side launchers of the library's kernels (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,5 +18,13 @@ cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, u
 int simple_step_grid(int64_t vocab);
 cudaError_t setup_step_simple();
 cudaError_t launch_step_simple(const StepParams& p, bool has_cap, bool pdl, cudaStream_t stream);
+
+// Tensor-core fused step: persistent CTAs over vocabulary ranges, TMA-fed w2
+// and base, tcgen05 bias into TMEM.
+cudaError_t setup_step_tc();
+int tc_step_grid(int64_t vocab, int sm_count);
+int tc_smem_bytes(int rows);
+bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab);
+cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int grid, bool pdl, cudaStream_t stream);
 
 }  // namespace dspark

@@ -1,0 +1,530 @@
+// step_tc.cu -- the fused Markov step on Blackwell tensor cores (sm_103a).
+//
+// One persistent CTA per SM owns a contiguous vocabulary range (whole
+// 32-entry units, the ranges differing by at most one unit) and every request
+// row.  Per 128-entry vocabulary tile:
+//   * warp 0 streams the tile's w2 rows with TMA into a ring of 16 KB
+//     stages (128 rows x 64 K, 128-byte swizzle), 4 stages per tile;
+//   * warp 2 streams the tile's base logits with TMA, 8 rows x 128 entries
+//     per 2 KB chunk, into a second ring;
+//   * warp 1 issues tcgen05.mma (M = 128 vocab rows, N = rows padded to 16,
+//     K = 256 in 16 steps of 16) into one of two TMEM accumulators;
+//   * warps 4..11 (two warpgroups, each warp reading its TMEM lane quarter)
+//     load the FP32 dots with tcgen05.ld and run the per-element epilogue of
+//     [P3] _StepKernel.kernel: bias rounded once to BF16, BF16 add,
+//     multiplier, soft cap, cache store, Gumbel key ([P3] _logit, _gumbel).
+// The row maxima live in shared memory as packed (orderable key, ~id) words,
+// so any update order gives the total-order winner ([P3] module docstring);
+// one global atomicMax per row and CTA publishes them, and the CTA that
+// arrives last writes the step's tokens ([P3] _finish).
+//
+// The Gumbel key of an element is only evaluated when it can win: the
+// noise -L(h) never exceeds (clz(h) + 1) ln 2 (u >= 2^(31 - clz(h) - 32) and
+// -log(1 - u) >= u), so an element whose upper bound l/t + (clz(h)+1) ln 2
+// (with margins for rounding) is below the row's current maximum cannot be
+// the argmax and is skipped.  Skipping never changes the result.
+//
+// The bias is the previous step's token's w1 row (clamped to the last row)
+// times w2 in FP32, the summation order being the tensor core's; the pages
+// allow any order ([P2] module docstring, [P4] module docstring).
+//
+// Programmatic dependent launch: the TMA producers read only inputs written
+// before the loop (w2, base) and start before griddepcontrol.wait; every
+// other warp waits first.  All mbarrier waits are bounded; a wait that gives
+// up records DSPARK_ERR_DEVICE_TIMEOUT in the status word and the CTA leaves
+// its loops, waits (bounded) for its copies in flight and frees its TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kTileV = 128;
+constexpr int kUnit = 32;              // vocabulary rows per partition unit / TMA box
+constexpr int kKBlock = 64;            // K per w2 stage (one 128-byte swizzle row)
+constexpr int kKBlocks = kRank / kKBlock;
+constexpr int kW2StageBytes = kTileV * kKBlock * 2;  // 16 KB
+constexpr int kChunkRows = 8;          // base rows per chunk
+constexpr int kChunkBytes = kChunkRows * kTileV * 2;  // 2 KB
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiThreads = 256;
+constexpr uint32_t kWaitLimit = 1u << 20;
+
+struct TcLayout {
+  int n;         // MMA N: rows padded to 16
+  int stages;    // w2 ring stages
+  int nbase;     // base ring slots
+  int tmem_cols;
+  int smem;      // dynamic shared memory bytes
+  int emb_off, w2_off, base_off, bar_off, best_off, info_off;
+};
+
+__host__ __device__ inline int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+TcLayout tc_layout(int rows) {
+  TcLayout L;
+  L.n = ((rows + 15) / 16) * 16;
+  L.tmem_cols = pow2_at_least(2 * L.n);
+  const int emb = L.n * kRank * 2;
+  L.stages = L.n > 128 ? 4 : 8;
+  L.nbase = L.n > 128 ? 8 : 16;
+  int off = 0;
+  L.emb_off = off;
+  off += emb;
+  L.w2_off = off;
+  off += L.stages * kW2StageBytes;
+  L.base_off = off;
+  off += L.nbase * kChunkBytes;
+  L.bar_off = off;
+  off += 8 * (2 * L.stages + 2 * L.nbase + 4 + 2);
+  off = (off + 15) & ~15;
+  L.best_off = off;
+  off += kMaxRows * 8;
+  L.info_off = off;
+  off += kMaxRows * static_cast<int>(sizeof(RowInfo)) + kMaxRows * 4;
+  L.smem = off + 1024;  // room to align the base to 1024 bytes
+  return L;
+}
+
+struct TcParams {
+  StepParams p;
+  int32_t n;
+  int32_t stages;
+  int32_t nbase;
+  int32_t tmem_cols;
+  int32_t emb_off, w2_off, base_off, bar_off, best_off, info_off;
+  int32_t num_units;  // ceil(V / 32)
+};
+
+__device__ __forceinline__ float decode_best(unsigned long long packed) {
+  const uint32_t o = static_cast<uint32_t>(packed >> 32);
+  const uint32_t bits = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(bits);
+}
+
+struct Shared {
+  unsigned char* emb;
+  unsigned char* w2;
+  unsigned char* base;
+  uint64_t* full_w2;
+  uint64_t* empty_w2;
+  uint64_t* full_base;
+  uint64_t* empty_base;
+  uint64_t* tmem_full;   // [2]
+  uint64_t* tmem_empty;  // [2]
+  uint64_t* emb_ready;
+  uint64_t* spare;
+  unsigned long long* best;
+  RowInfo* info;
+  float* rinv;
+};
+
+template <bool kHasCap, bool kMultOne>
+__global__ void __launch_bounds__(kThreads, 1)
+step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_base,
+               const TcParams tp) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_last;
+
+  const StepParams& p = tp.p;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = tp.n;
+  const int S = tp.stages;
+  const int NB = tp.nbase;
+
+  Shared sh;
+  sh.emb = smem + tp.emb_off;
+  sh.w2 = smem + tp.w2_off;
+  sh.base = smem + tp.base_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tp.bar_off);
+  sh.full_w2 = bars;
+  sh.empty_w2 = bars + S;
+  sh.full_base = bars + 2 * S;
+  sh.empty_base = bars + 2 * S + NB;
+  sh.tmem_full = bars + 2 * S + 2 * NB;
+  sh.tmem_empty = sh.tmem_full + 2;
+  sh.emb_ready = sh.tmem_full + 4;
+  sh.spare = sh.tmem_full + 5;
+  sh.best = reinterpret_cast<unsigned long long*>(smem + tp.best_off);
+  sh.info = reinterpret_cast<RowInfo*>(smem + tp.info_off);
+  sh.rinv = reinterpret_cast<float*>(sh.info + kMaxRows);
+
+  // This CTA's vocabulary range.
+  const int G = gridDim.x;
+  const int64_t u0 = static_cast<int64_t>(blockIdx.x) * tp.num_units / G;
+  const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * tp.num_units / G;
+  const int64_t v_begin = u0 * kUnit;
+  const int64_t v_end = min(u1 * kUnit, p.vocab);
+  const int n_tiles = static_cast<int>((v_end - v_begin + kTileV - 1) / kTileV);
+  const int chunks = (p.rows + kChunkRows - 1) / kChunkRows;
+
+  pdl_launch_dependents();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(&sh.full_w2[i], 1);
+      ptx::mbar_init(&sh.empty_w2[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) {
+      ptx::mbar_init(&sh.full_base[i], 1);
+      ptx::mbar_init(&sh.empty_base[i], 4);  // the four warps of the consuming warpgroup
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&sh.tmem_full[i], 1);
+      ptx::mbar_init(&sh.tmem_empty[i], 8);  // the eight epilogue warps
+    }
+    ptx::mbar_init(sh.emb_ready, 1);
+    ptx::mbar_init(sh.spare, 1);
+    s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&s_tmem_base, static_cast<uint32_t>(tp.tmem_cols));
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  volatile int* abort_flag = &s_abort;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    atomicExch(p.status, kStatusTimeout);
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((i & 63) == 63 && *abort_flag) return false;
+    }
+    give_up();
+    return false;
+  };
+
+  if (warp == 0) {
+    // ---------------- w2 producer ----------------
+    if (lane == 0 && n_tiles > 0) {
+      ptx::prefetch_tmap(&tmap_w2);
+      int issued = 0;
+      for (int i = 0; i < n_tiles && !*abort_flag; ++i) {
+        const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
+        const int rows_i = static_cast<int>(v_end - t0 < kTileV ? v_end - t0 : kTileV);
+        const int boxes = (rows_i + kUnit - 1) / kUnit;
+        for (int kb = 0; kb < kKBlocks; ++kb) {
+          const int j = i * kKBlocks + kb;
+          const int s = j % S;
+          if (!wait(&sh.empty_w2[s], ((j / S) & 1) ^ 1)) break;
+          ptx::mbar_arrive_expect_tx(&sh.full_w2[s], static_cast<uint32_t>(boxes * kUnit * kKBlock * 2));
+          for (int b = 0; b < boxes; ++b)
+            ptx::tma_load_2d(sh.w2 + s * kW2StageBytes + b * kUnit * 128, &tmap_w2, &sh.full_w2[s],
+                             kb * kKBlock, static_cast<int32_t>(t0 + b * kUnit));
+          issued = j + 1;
+        }
+      }
+      if (*abort_flag) {  // let copies in flight land before the CTA exits
+        for (int j = max(0, issued - S); j < issued; ++j) ptx::mbar_wait(&sh.full_w2[j % S], (j / S) & 1, kWaitLimit);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- base producer ----------------
+    if (lane == 0 && n_tiles > 0) {
+      ptx::prefetch_tmap(&tmap_base);
+      int issued = 0;
+      for (int i = 0; i < n_tiles && !*abort_flag; ++i) {
+        const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
+        for (int c = 0; c < chunks; ++c) {
+          const int j = i * chunks + c;
+          const int s = j % NB;
+          if (!wait(&sh.empty_base[s], ((j / NB) & 1) ^ 1)) break;
+          ptx::mbar_arrive_expect_tx(&sh.full_base[s], kChunkBytes);
+          ptx::tma_load_2d(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], static_cast<int32_t>(t0),
+                           c * kChunkRows);
+          issued = j + 1;
+        }
+      }
+      if (*abort_flag) {
+        for (int j = max(0, issued - NB); j < issued; ++j)
+          ptx::mbar_wait(&sh.full_base[j % NB], (j / NB) & 1, kWaitLimit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && n_tiles > 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, static_cast<uint32_t>(N));
+      const uint32_t emb_addr = ptx::smem_addr(sh.emb);
+      const uint32_t w2_addr = ptx::smem_addr(sh.w2);
+      bool ok = wait(sh.emb_ready, 0);
+      ptx::tc_fence_after();
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const int b = i & 1;
+        if (!(ok = wait(&sh.tmem_empty[b], ((i >> 1) & 1) ^ 1))) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(b * N);
+        for (int kb = 0; kb < kKBlocks && ok; ++kb) {
+          const int j = i * kKBlocks + kb;
+          const int s = j % S;
+          if (!(ok = wait(&sh.full_w2[s], (j / S) & 1))) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kKBlock / 16; ++kk) {
+            const uint64_t a = ptx::sw128_desc(w2_addr + s * kW2StageBytes + kk * 32, 1024);
+            const uint64_t bdesc = ptx::sw128_desc(emb_addr + kb * N * 128 + kk * 32, 1024);
+            ptx::mma_bf16(d, a, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&sh.empty_w2[s]);
+        }
+        if (ok) ptx::mma_commit(&sh.tmem_full[b]);
+      }
+      // every MMA this thread issued has completed before TMEM is freed
+      ptx::mma_commit(sh.spare);
+      ptx::mbar_wait(sh.spare, 0, kWaitLimit);
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ---------------- epilogue ----------------
+    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
+    const int wg = (warp - kEpiWarp0) >> 2;       // 0 or 1
+    const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    pdl_wait();
+
+    // Markov embeddings of the previous tokens, in the MMA's B layout:
+    // 4 K-blocks of [N rows x 128 bytes], 128-byte swizzle.
+    const uint64_t last_row = static_cast<uint64_t>(p.w1_rows - 1);
+    for (int idx = et; idx < N * 32; idx += kEpiThreads) {
+      const int r = idx >> 5, ch = idx & 31;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (r < p.rows) {
+        const int64_t tok = slot_token(__ldcg(p.slots_prev + r));
+        const uint64_t row = static_cast<uint64_t>(tok) < last_row ? static_cast<uint64_t>(tok) : last_row;
+        val = ldg_nc_v4(p.w1 + row * kRank + ch * 8);
+      }
+      const int kb = ch >> 3, c = ch & 7;
+      *reinterpret_cast<uint4*>(sh.emb + kb * N * 128 + r * 128 + ((c ^ (r & 7)) << 4)) = val;
+    }
+    for (int r = et; r < p.rows; r += kEpiThreads) {
+      const RowInfo ri = row_info(p, r);
+      sh.info[r] = ri;
+      sh.rinv[r] = ri.temp != 0.0f ? __frcp_rn(ri.temp) : 0.0f;
+      sh.best[r] = 0ull;
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(1, kEpiThreads);
+    if (et == 0) ptx::mbar_arrive(sh.emb_ready);
+
+    bool ok = true;
+    for (int i = 0; i < n_tiles && ok; ++i) {
+      const int b = i & 1;
+      ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (i >> 1) & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
+      const int vr = quarter * 32 + lane;
+      const int64_t v = t0 + vr;
+      const bool in = v < v_end;
+      for (int c = wg; c < chunks && ok; c += 2) {
+        const int j = i * chunks + c;
+        const int s = j % NB;
+        ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (j / NB) & 1));
+        if (!ok) break;
+        uint32_t acc[8];
+        ptx::tmem_ld8(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                          static_cast<uint32_t>(b * N + c * kChunkRows),
+                      acc);
+        const uint16_t* bs = reinterpret_cast<const uint16_t*>(sh.base + s * kChunkBytes);
+        uint32_t bb[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) bb[rr] = bs[rr * kTileV + vr];
+        ptx::tmem_ld_wait();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sh.empty_base[s]);
+        if (in) {
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            const int r = c * kChunkRows + rr;
+            if (r < p.rows) {
+              const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
+              if (p.bias_out)
+                p.bias_out[(static_cast<int64_t>(r) * p.steps + p.step) * p.vocab + v] = __bfloat16_as_ushort(b16);
+              const RowInfo& ri = sh.info[r];
+              float l;
+              uint16_t cbits;
+              if (kMultOne && !kHasCap) {
+                const __nv_bfloat16 hx = __float2bfloat16_rn(__fadd_rn(bf16_bits_to_float(bb[rr]), __bfloat162float(b16)));
+                cbits = __bfloat16_as_ushort(hx);
+                // x * 1 then round: the same BF16, NaN canonicalised as cvt does
+                if (__hisnan(hx)) cbits = 0x7FFFu;
+                l = __bfloat162float(hx);
+              } else {
+                cbits = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult, p.inv_cap,
+                                                 p.cap, &l);
+              }
+              if (ri.valid) p.cache[ri.cache_off + v] = cbits;
+              unsigned long long* best = sh.best + r;
+              float key = l;
+              bool eval = true;
+              if (ri.temp != 0.0f) {
+                const uint32_t h = murmur_finish(ri.prefix, static_cast<uint32_t>(v));
+                const float qa = __fmul_rn(l, sh.rinv[r]);
+                const float g = __fmaf_rn(__int2float_rn(__clz(h) + 1), 0.6931472f, 1e-4f);
+                const float bound = __fadd_rn(__fadd_rn(qa, __fmul_rn(fabsf(qa), 0x1p-20f)), g);
+                if (bound < decode_best(*reinterpret_cast<volatile unsigned long long*>(best))) eval = false;
+                else key = noised_key(l, ri.temp, h);
+              }
+              if (eval) {
+                const unsigned long long cand = pack_key(key, static_cast<uint32_t>(v));
+                if (cand > *reinterpret_cast<volatile unsigned long long*>(best)) atomicMax(best, cand);
+              }
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sh.tmem_empty[b]);
+    }
+
+    // Publish this CTA's row maxima; the last CTA writes the tokens.
+    ptx::named_bar_sync(1, kEpiThreads);
+    if (n_tiles > 0 && !*abort_flag)
+      for (int r = et; r < p.rows; r += kEpiThreads) atomicMax(p.slots_out + r, sh.best[r]);
+    __threadfence();
+    ptx::named_bar_sync(1, kEpiThreads);
+    if (et == 0) s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
+    ptx::named_bar_sync(1, kEpiThreads);
+    if (s_last) {
+      __threadfence();
+      for (int r = et; r < p.rows; r += kEpiThreads) {
+        const unsigned long long sv = atomicAdd(p.slots_out + r, 0ull);
+        p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + p.step] = slot_token(sv);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, static_cast<uint32_t>(tp.tmem_cols));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+template <bool C, bool M>
+cudaError_t set_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(step_tc_kernel<C, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       tc_layout(kMaxRows).smem);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t setup_step_tc() {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  cudaError_t e;
+  if ((e = set_attrs<false, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<false, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<true, false>()) != cudaSuccess) return e;
+  return set_attrs<true, true>();
+}
+
+int tc_smem_bytes(int rows) { return tc_layout(rows).smem; }
+
+bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRank), static_cast<cuuint64_t>(vocab)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRank * 2)};
+  const cuuint32_t box[2] = {kKBlock, kUnit};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w2), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_base_map(CUtensorMap* map, const void* base_step, int64_t vocab, int rows, int64_t base_s0) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(vocab), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(base_s0 * 2)};
+  const cuuint32_t box[2] = {kTileV, kChunkRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base_step), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int tc_step_grid(int64_t vocab, int sm_count) {
+  const int64_t units = (vocab + kUnit - 1) / kUnit;
+  return static_cast<int>(units < sm_count ? units : sm_count);
+}
+
+cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int grid, bool pdl,
+                           cudaStream_t stream) {
+  CUtensorMap base_map;
+  if (!encode_base_map(&base_map, p.base, p.vocab, p.rows, p.base_s0)) return cudaErrorInvalidValue;
+  const TcLayout L = tc_layout(p.rows);
+  TcParams tp;
+  tp.p = p;
+  tp.n = L.n;
+  tp.stages = L.stages;
+  tp.nbase = L.nbase;
+  tp.tmem_cols = L.tmem_cols;
+  tp.emb_off = L.emb_off;
+  tp.w2_off = L.w2_off;
+  tp.base_off = L.base_off;
+  tp.bar_off = L.bar_off;
+  tp.best_off = L.best_off;
+  tp.info_off = L.info_off;
+  tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const bool cap = p.cap != 0.0f;
+  const bool one = p.mult == 1.0f;
+  if (cap && one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, true>, w2_map, base_map, tp);
+  if (cap) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, false>, w2_map, base_map, tp);
+  if (one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, true>, w2_map, base_map, tp);
+  return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, false>, w2_map, base_map, tp);
+}
+
+}  // namespace dspark
