@@ -26,6 +26,7 @@ FLAG_FORCE_MMA = 0x4
 EXPORTED = (
     "dspark_markov_init", "dspark_markov_loop", "dspark_markov_anchor", "dspark_markov_step",
     "dspark_markov_partial_count", "dspark_markov_bias_path", "dspark_markov_get_status",
+    "dspark_markov_get_status_detail",
     "dspark_markov_destroy", "dspark_build_verify_tokens", "dspark_greedy_accept_scratch_bytes",
     "dspark_greedy_accept", "dspark_strerror",
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
@@ -86,6 +87,7 @@ def load(build_if_missing: bool = False):
         "dspark_markov_partial_count": (i32, [P]),
         "dspark_markov_bias_path": (i32, [P, i32]),
         "dspark_markov_get_status": (ctypes.c_int, [P, P, ctypes.POINTER(i32)]),
+        "dspark_markov_get_status_detail": (ctypes.c_int, [P, P, ctypes.POINTER(i32)]),
         "dspark_markov_destroy": (None, [P]),
         "dspark_build_verify_tokens": (ctypes.c_int, [P, P, P, i32, i32, i32, P]),
         "dspark_greedy_accept_scratch_bytes": (sz, [i32, i32, i32]),
@@ -174,6 +176,12 @@ def dspark_markov_get_status(ctx, stream=None) -> int:
     st = ctypes.c_int32(0)
     _check(load().dspark_markov_get_status(ctx, _stream(stream), ctypes.byref(st)), "dspark_markov_get_status")
     return int(st.value)
+
+
+def dspark_markov_get_status_detail(ctx, stream=None) -> list:
+    d = (ctypes.c_int32 * 4)()
+    _check(load().dspark_markov_get_status_detail(ctx, _stream(stream), d), "dspark_markov_get_status_detail")
+    return list(d)
 
 
 def dspark_build_verify_tokens(last, draft, verify, batch, draft_stride, P, stream=None):
@@ -270,6 +278,9 @@ class MarkovContext:
 
     def status(self, stream=None) -> int:
         return dspark_markov_get_status(self.ctx, stream)
+
+    def status_detail(self, stream=None) -> list:
+        return dspark_markov_get_status_detail(self.ctx, stream)
 
     def close(self):
         if self.ctx:

@@ -142,13 +142,13 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   const size_t nslots = static_cast<size_t>(cfg->max_steps + 1) * cfg->max_rows;
   if (cudaMalloc(&ctx->slots, nslots * sizeof(unsigned long long)) != cudaSuccess ||
       cudaMalloc(&ctx->counters, cfg->max_steps * sizeof(unsigned int)) != cudaSuccess ||
-      cudaMalloc(&ctx->status, sizeof(int)) != cudaSuccess) {
+      cudaMalloc(&ctx->status, 4 * sizeof(int)) != cudaSuccess) {
     dspark_markov_destroy(ctx);
     return DSPARK_ERR_CUDA;
   }
   if (cudaMemsetAsync(ctx->slots, 0, nslots * sizeof(unsigned long long), stream) != cudaSuccess ||
       cudaMemsetAsync(ctx->counters, 0, cfg->max_steps * sizeof(unsigned int), stream) != cudaSuccess ||
-      cudaMemsetAsync(ctx->status, 0, sizeof(int), stream) != cudaSuccess ||
+      cudaMemsetAsync(ctx->status, 0, 4 * sizeof(int), stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess) {
     dspark_markov_destroy(ctx);
     return DSPARK_ERR_CUDA;
@@ -213,14 +213,22 @@ int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
   return DSPARK_OK;
 }
 
-int dspark_markov_get_status(dspark_markov_ctx* ctx, cudaStream_t stream, int32_t* device_status) {
-  if (!ctx || !device_status) return DSPARK_ERR_INVALID_ARG;
-  int v = 0;
+int dspark_markov_get_status_detail(dspark_markov_ctx* ctx, cudaStream_t stream, int32_t* detail) {
+  if (!ctx || !detail) return DSPARK_ERR_INVALID_ARG;
+  int v[4] = {0, 0, 0, 0};
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (cudaMemcpy(&v, ctx->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (cudaMemset(ctx->status, 0, sizeof(int)) != cudaSuccess) return DSPARK_ERR_CUDA;
-  *device_status = v;
+  if (cudaMemcpy(v, ctx->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaMemset(ctx->status, 0, sizeof(v)) != cudaSuccess) return DSPARK_ERR_CUDA;
+  for (int i = 0; i < 4; ++i) detail[i] = v[i];
   return DSPARK_OK;
+}
+
+int dspark_markov_get_status(dspark_markov_ctx* ctx, cudaStream_t stream, int32_t* device_status) {
+  if (!device_status) return DSPARK_ERR_INVALID_ARG;
+  int32_t d[4];
+  const int rc = dspark_markov_get_status_detail(ctx, stream, d);
+  if (rc == DSPARK_OK) *device_status = d[0];
+  return rc;
 }
 
 }  // extern "C"

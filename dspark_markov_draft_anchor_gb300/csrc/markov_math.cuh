@@ -143,14 +143,28 @@ __device__ __forceinline__ uint32_t murmur_prefix(uint64_t seed, int32_t step, i
   return murmur_round(h, salted);
 }
 
-__device__ __forceinline__ uint32_t murmur_finish(uint32_t prefix, uint32_t vocab_id) {
-  uint32_t h = murmur_round(prefix, vocab_id) ^ 16u;
+// The block step split in its key half (which depends only on the vocab id,
+// so it is shared by every row) and its state half.
+__device__ __forceinline__ uint32_t murmur_kmix(uint32_t k) {
+  k *= 0xcc9e2d51u;
+  k = __funnelshift_l(k, k, 15);
+  return k * 0x1b873593u;
+}
+
+__device__ __forceinline__ uint32_t murmur_finish_mixed(uint32_t prefix, uint32_t kmixed) {
+  uint32_t h = prefix ^ kmixed;
+  h = __funnelshift_l(h, h, 13);
+  h = (h * 5u + 0xe6546b64u) ^ 16u;
   h ^= h >> 16;
   h *= 0x85ebca6bu;
   h ^= h >> 13;
   h *= 0xc2b2ae35u;
   h ^= h >> 16;
   return h;
+}
+
+__device__ __forceinline__ uint32_t murmur_finish(uint32_t prefix, uint32_t vocab_id) {
+  return murmur_finish_mixed(prefix, murmur_kmix(vocab_id));
 }
 
 // ---------------------------------------------------------------------------

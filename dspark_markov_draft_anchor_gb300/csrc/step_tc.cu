@@ -53,15 +53,17 @@ constexpr int kChunkRows = 8;          // base rows per chunk
 constexpr int kChunkBytes = kChunkRows * kTileV * 2;  // 2 KB
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiThreads = 256;
-constexpr uint32_t kWaitLimit = 1u << 20;
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kQCap = 64;  // entries of a warp's key-evaluation queue
 
 struct TcLayout {
   int n;         // MMA N: rows padded to 16
+  int nacc;      // TMEM accumulators (tiles the MMA may run ahead)
   int stages;    // w2 ring stages
-  int nbase;     // base ring slots
+  int nbase;     // base ring slots (two rings, one per epilogue warpgroup)
   int tmem_cols;
   int smem;      // dynamic shared memory bytes
-  int emb_off, w2_off, base_off, bar_off, best_off, info_off;
+  int emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, queue_off;
 };
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -70,27 +72,44 @@ __host__ __device__ inline int pow2_at_least(int x) {
   return p;
 }
 
+// Per-row constants of a step, 16 bytes (one broadcast shared load).
+struct RowConst {
+  uint32_t prefix;  // Murmur3 state after seed and position words
+  float temp;
+  float rinv;       // RN(1 / temp), for the key bound
+  uint32_t valid;   // the row stores into the cache
+};
+
+constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared variables
+
 TcLayout tc_layout(int rows) {
   TcLayout L;
   L.n = ((rows + 15) / 16) * 16;
-  L.tmem_cols = pow2_at_least(2 * L.n);
-  const int emb = L.n * kRank * 2;
-  L.stages = L.n > 128 ? 4 : 8;
+  L.nacc = 4 * L.n <= 512 ? 4 : 2;  // even: each accumulator belongs to one warpgroup
+  L.tmem_cols = pow2_at_least(L.nacc * L.n);
   L.nbase = L.n > 128 ? 8 : 16;
+  const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 4 + 2) + 16 +
+                    kMaxRows * (8 + static_cast<int>(sizeof(RowConst)) + 8) + 8 * kQCap * 16 + 1024 + 64;
+  L.stages = (kSmemBudget - fixed) / kW2StageBytes;
+  if (L.stages > 12) L.stages = 12;
   int off = 0;
   L.emb_off = off;
-  off += emb;
+  off += L.n * kRank * 2;
   L.w2_off = off;
   off += L.stages * kW2StageBytes;
   L.base_off = off;
   off += L.nbase * kChunkBytes;
   L.bar_off = off;
-  off += 8 * (2 * L.stages + 2 * L.nbase + 4 + 2);
+  off += 8 * (2 * L.stages + 2 * L.nbase + 2 * L.nacc + 2);
   off = (off + 15) & ~15;
   L.best_off = off;
   off += kMaxRows * 8;
   L.info_off = off;
-  off += kMaxRows * static_cast<int>(sizeof(RowInfo)) + kMaxRows * 4;
+  off += kMaxRows * static_cast<int>(sizeof(RowConst));
+  L.coff_off = off;
+  off += kMaxRows * 8;
+  L.queue_off = off;
+  off += 8 * kQCap * 16;
   L.smem = off + 1024;  // room to align the base to 1024 bytes
   return L;
 }
@@ -98,10 +117,11 @@ TcLayout tc_layout(int rows) {
 struct TcParams {
   StepParams p;
   int32_t n;
+  int32_t nacc;
   int32_t stages;
   int32_t nbase;
   int32_t tmem_cols;
-  int32_t emb_off, w2_off, base_off, bar_off, best_off, info_off;
+  int32_t emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, queue_off;
   int32_t num_units;  // ceil(V / 32)
 };
 
@@ -111,6 +131,32 @@ __device__ __forceinline__ float decode_best(unsigned long long packed) {
   return __uint_as_float(bits);
 }
 
+// A warp's queue of elements whose Gumbel key must be evaluated (their exact
+// bound reaches the row's current maximum).  Evaluating them 32 at a time,
+// one per lane, keeps rare survivors from costing the warp a full pass each.
+struct Cand {
+  uint32_t v;
+  float l;
+  uint32_t h;
+  uint32_t r;
+};
+struct Shared;
+
+struct WarpQueue {
+  Cand* q;
+  uint32_t head = 0, count = 0;  // warp-uniform
+
+  __device__ __forceinline__ void push(bool take, int lane, uint32_t v, float l, uint32_t h, int r) {
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+    if (take) {
+      const uint32_t pos = (head + count + __popc(m & ((1u << lane) - 1u))) & (kQCap - 1);
+      q[pos] = Cand{v, l, h, static_cast<uint32_t>(r)};
+    }
+    count += __popc(m);
+  }
+  __device__ __forceinline__ void flush(uint32_t min_count, const Shared& sh);
+};
+
 struct Shared {
   unsigned char* emb;
   unsigned char* w2;
@@ -119,14 +165,37 @@ struct Shared {
   uint64_t* empty_w2;
   uint64_t* full_base;
   uint64_t* empty_base;
-  uint64_t* tmem_full;   // [2]
-  uint64_t* tmem_empty;  // [2]
+  uint64_t* tmem_full;   // [nacc]
+  uint64_t* tmem_empty;  // [nacc]
   uint64_t* emb_ready;
   uint64_t* spare;
   unsigned long long* best;
-  RowInfo* info;
-  float* rinv;
+  RowConst* info;
+  int64_t* cache_off;
+  Cand* queues;
 };
+
+// The Gumbel key of one element, out of line: it is evaluated for few
+// elements, and one copy keeps the kernel's code small.
+__device__ __noinline__ float eval_key(float l, float temp, uint32_t h) { return noised_key(l, temp, h); }
+
+__device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Shared& sh) {
+  const int lane = threadIdx.x & 31;
+  while (count >= min_count && count > 0) {
+    __syncwarp();
+    const uint32_t n = count < 32u ? count : 32u;
+    if (static_cast<uint32_t>(lane) < n) {
+      const Cand e = q[(head + lane) & (kQCap - 1)];
+      const float key = eval_key(e.l, sh.info[e.r].temp, e.h);
+      const unsigned long long cand = pack_key(key, e.v);
+      unsigned long long* best = sh.best + e.r;
+      if (cand > *reinterpret_cast<volatile unsigned long long*>(best)) atomicMax(best, cand);
+    }
+    head = (head + n) & (kQCap - 1);
+    count -= n;
+  }
+  __syncwarp();
+}
 
 template <bool kHasCap, bool kMultOne>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -145,6 +214,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   const int N = tp.n;
   const int S = tp.stages;
   const int NB = tp.nbase;
+  const int NBG = NB / 2;  // slots of each warpgroup's base ring
+  const int NACC = tp.nacc;
 
   Shared sh;
   sh.emb = smem + tp.emb_off;
@@ -156,12 +227,13 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.full_base = bars + 2 * S;
   sh.empty_base = bars + 2 * S + NB;
   sh.tmem_full = bars + 2 * S + 2 * NB;
-  sh.tmem_empty = sh.tmem_full + 2;
-  sh.emb_ready = sh.tmem_full + 4;
-  sh.spare = sh.tmem_full + 5;
+  sh.tmem_empty = sh.tmem_full + NACC;
+  sh.emb_ready = sh.tmem_full + 2 * NACC;
+  sh.spare = sh.emb_ready + 1;
   sh.best = reinterpret_cast<unsigned long long*>(smem + tp.best_off);
-  sh.info = reinterpret_cast<RowInfo*>(smem + tp.info_off);
-  sh.rinv = reinterpret_cast<float*>(sh.info + kMaxRows);
+  sh.info = reinterpret_cast<RowConst*>(smem + tp.info_off);
+  sh.cache_off = reinterpret_cast<int64_t*>(smem + tp.coff_off);
+  sh.queues = reinterpret_cast<Cand*>(smem + tp.queue_off);
 
   // This CTA's vocabulary range.
   const int G = gridDim.x;
@@ -183,9 +255,9 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       ptx::mbar_init(&sh.full_base[i], 1);
       ptx::mbar_init(&sh.empty_base[i], 4);  // the four warps of the consuming warpgroup
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NACC; ++i) {
       ptx::mbar_init(&sh.tmem_full[i], 1);
-      ptx::mbar_init(&sh.tmem_empty[i], 8);  // the eight epilogue warps
+      ptx::mbar_init(&sh.tmem_empty[i], 4);  // the four warps of the consuming warpgroup
     }
     ptx::mbar_init(sh.emb_ready, 1);
     ptx::mbar_init(sh.spare, 1);
@@ -202,16 +274,22 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   const uint32_t tmem_base = s_tmem_base;
   volatile int* abort_flag = &s_abort;
 
-  auto give_up = [&]() {
+  // A wait that gives up records where: status[1] = wait site,
+  // status[2] = block, status[3] = tile << 16 | sequence number.
+  auto give_up = [&](int site, int detail) {
     *abort_flag = 1;
-    atomicExch(p.status, kStatusTimeout);
-  };
-  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
-      if (ptx::mbar_try_wait(bar, parity)) return true;
-      if ((i & 63) == 63 && *abort_flag) return false;
+    if (atomicCAS(p.status, 0, kStatusTimeout) == 0) {
+      p.status[1] = site;
+      p.status[2] = static_cast<int>(blockIdx.x);
+      p.status[3] = detail;
     }
-    give_up();
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity, int site, int detail) -> bool {
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((it & 63) == 63 && *abort_flag) return false;
+    }
+    give_up(site, detail);
     return false;
   };
 
@@ -227,7 +305,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         for (int kb = 0; kb < kKBlocks; ++kb) {
           const int j = i * kKBlocks + kb;
           const int s = j % S;
-          if (!wait(&sh.empty_w2[s], ((j / S) & 1) ^ 1)) break;
+          if (!wait(&sh.empty_w2[s], ((j / S) & 1) ^ 1, 1, (i << 16) | j)) break;
           ptx::mbar_arrive_expect_tx(&sh.full_w2[s], static_cast<uint32_t>(boxes * kUnit * kKBlock * 2));
           for (int b = 0; b < boxes; ++b)
             ptx::tma_load_2d(sh.w2 + s * kW2StageBytes + b * kUnit * 128, &tmap_w2, &sh.full_w2[s],
@@ -241,24 +319,33 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     }
   } else if (warp == 2) {
     // ---------------- base producer ----------------
+    // Tile i's chunks go to warpgroup (i % 2)'s ring, so that every ring has
+    // one consumer that takes its slots in order (an mbarrier's parity only
+    // tells adjacent phases apart).
     if (lane == 0 && n_tiles > 0) {
       ptx::prefetch_tmap(&tmap_base);
-      int issued = 0;
-      for (int i = 0; i < n_tiles && !*abort_flag; ++i) {
+      int issued[2] = {0, 0};
+      bool stop = false;
+      for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
+        const int g = i & 1;
         const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
         for (int c = 0; c < chunks; ++c) {
-          const int j = i * chunks + c;
-          const int s = j % NB;
-          if (!wait(&sh.empty_base[s], ((j / NB) & 1) ^ 1)) break;
+          const int k = issued[g];
+          const int s = g * NBG + k % NBG;
+          if (!wait(&sh.empty_base[s], ((k / NBG) & 1) ^ 1, 2, (i << 16) | k)) {
+            stop = true;
+            break;
+          }
           ptx::mbar_arrive_expect_tx(&sh.full_base[s], kChunkBytes);
           ptx::tma_load_2d(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], static_cast<int32_t>(t0),
                            c * kChunkRows);
-          issued = j + 1;
+          issued[g] = k + 1;
         }
       }
       if (*abort_flag) {
-        for (int j = max(0, issued - NB); j < issued; ++j)
-          ptx::mbar_wait(&sh.full_base[j % NB], (j / NB) & 1, kWaitLimit);
+        for (int g = 0; g < 2; ++g)
+          for (int k = max(0, issued[g] - NBG); k < issued[g]; ++k)
+            ptx::mbar_wait(&sh.full_base[g * NBG + k % NBG], (k / NBG) & 1, kWaitLimit);
       }
     }
   } else if (warp == 1) {
@@ -267,17 +354,17 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, static_cast<uint32_t>(N));
       const uint32_t emb_addr = ptx::smem_addr(sh.emb);
       const uint32_t w2_addr = ptx::smem_addr(sh.w2);
-      bool ok = wait(sh.emb_ready, 0);
+      bool ok = wait(sh.emb_ready, 0, 3, 0);
       ptx::tc_fence_after();
       for (int i = 0; i < n_tiles && ok; ++i) {
-        const int b = i & 1;
-        if (!(ok = wait(&sh.tmem_empty[b], ((i >> 1) & 1) ^ 1))) break;
+        const int b = i % NACC;
+        if (!(ok = wait(&sh.tmem_empty[b], ((i / NACC) & 1) ^ 1, 4, i << 16))) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(b * N);
         for (int kb = 0; kb < kKBlocks && ok; ++kb) {
           const int j = i * kKBlocks + kb;
           const int s = j % S;
-          if (!(ok = wait(&sh.full_w2[s], (j / S) & 1))) break;
+          if (!(ok = wait(&sh.full_w2[s], (j / S) & 1, 5, (i << 16) | j))) break;
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kKBlock / 16; ++kk) {
@@ -296,7 +383,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue ----------------
     const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
-    const int wg = (warp - kEpiWarp0) >> 2;       // 0 or 1
+    const int wg = (warp - kEpiWarp0) >> 2;       // warpgroup: takes tiles i = wg, wg + 2, ...
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     pdl_wait();
 
@@ -316,28 +403,37 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     }
     for (int r = et; r < p.rows; r += kEpiThreads) {
       const RowInfo ri = row_info(p, r);
-      sh.info[r] = ri;
-      sh.rinv[r] = ri.temp != 0.0f ? __frcp_rn(ri.temp) : 0.0f;
+      RowConst rc;
+      rc.prefix = ri.prefix;
+      rc.temp = ri.temp;
+      rc.rinv = ri.temp != 0.0f ? __frcp_rn(ri.temp) : 0.0f;
+      rc.valid = ri.valid ? 1u : 0u;
+      sh.info[r] = rc;
+      sh.cache_off[r] = ri.cache_off;
       sh.best[r] = 0ull;
     }
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(1, kEpiThreads);
     if (et == 0) ptx::mbar_arrive(sh.emb_ready);
 
+    WarpQueue q;
+    q.q = sh.queues + (warp - kEpiWarp0) * kQCap;
+    int taken = 0;  // chunks this warpgroup has taken from its base ring
+    const int vr = quarter * 32 + lane;  // this thread's vocabulary row of a tile
     bool ok = true;
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      const int b = i & 1;
-      ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (i >> 1) & 1));
+    for (int i = wg; i < n_tiles && ok; i += 2) {
+      const int b = i % NACC;
+      ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (i / NACC) & 1, 6, i << 16));
       if (!ok) break;
       ptx::tc_fence_after();
-      const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
-      const int vr = quarter * 32 + lane;
-      const int64_t v = t0 + vr;
+      const int64_t v = v_begin + static_cast<int64_t>(i) * kTileV + vr;
       const bool in = v < v_end;
-      for (int c = wg; c < chunks && ok; c += 2) {
-        const int j = i * chunks + c;
-        const int s = j % NB;
-        ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (j / NB) & 1));
+      const uint32_t kv = murmur_kmix(static_cast<uint32_t>(v));
+      const bool first = i == wg;
+      for (int c = 0; c < chunks && ok; ++c) {
+        const int k = taken++;
+        const int s = wg * NBG + k % NBG;
+        ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (k / NBG) & 1, 7, (i << 16) | k));
         if (!ok) break;
         uint32_t acc[8];
         ptx::tmem_ld8(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
@@ -350,42 +446,82 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         ptx::tmem_ld_wait();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh.empty_base[s]);
-        if (in) {
+
+        // (a) bias, transform, cache store and hash of the chunk's 8 rows
+        float lv[8];
+        uint32_t hv[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const int r = c * kChunkRows + rr;
+          lv[rr] = 0.0f;
+          hv[rr] = 0u;
+          if (r < p.rows) {
+            const RowConst rc = sh.info[r];
+            if (in) {
+              const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
+              if (p.bias_out)
+                p.bias_out[(static_cast<int64_t>(r) * p.steps + p.step) * p.vocab + v] = __bfloat16_as_ushort(b16);
+              float l;
+              uint16_t cbits;
+              if (kMultOne && !kHasCap) {
+                // x * 1 rounds to the same BF16 (cvt gives NaNs as 0x7FFF)
+                const __nv_bfloat16 hx =
+                    __float2bfloat16_rn(__fadd_rn(bf16_bits_to_float(bb[rr]), __bfloat162float(b16)));
+                cbits = __bfloat16_as_ushort(hx);
+                l = __bfloat162float(hx);
+              } else {
+                cbits = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult,
+                                                 p.inv_cap, p.cap, &l);
+              }
+              if (rc.valid) p.cache[sh.cache_off[r] + v] = cbits;
+              lv[rr] = l;
+              hv[rr] = murmur_finish_mixed(rc.prefix, kv);
+            }
+          }
+        }
+
+        // (b) the warpgroup's first tile: seed each row's maximum with the
+        // key of the warp's largest l / t (one evaluation per row)
+        if (first) {
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             const int r = c * kChunkRows + rr;
             if (r < p.rows) {
-              const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
-              if (p.bias_out)
-                p.bias_out[(static_cast<int64_t>(r) * p.steps + p.step) * p.vocab + v] = __bfloat16_as_ushort(b16);
-              const RowInfo& ri = sh.info[r];
-              float l;
-              uint16_t cbits;
-              if (kMultOne && !kHasCap) {
-                const __nv_bfloat16 hx = __float2bfloat16_rn(__fadd_rn(bf16_bits_to_float(bb[rr]), __bfloat162float(b16)));
-                cbits = __bfloat16_as_ushort(hx);
-                // x * 1 then round: the same BF16, NaN canonicalised as cvt does
-                if (__hisnan(hx)) cbits = 0x7FFFu;
-                l = __bfloat162float(hx);
-              } else {
-                cbits = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult, p.inv_cap,
-                                                 p.cap, &l);
+              const RowConst rc = sh.info[r];
+              if (rc.temp != 0.0f) {
+                const uint32_t o = in ? orderable(__fmul_rn(lv[rr], rc.rinv)) : 0u;
+                const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
+                const uint32_t who = __ffs(__ballot_sync(0xFFFFFFFFu, o == top)) - 1;
+                q.push(lane == static_cast<int>(who) && in, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r);
               }
-              if (ri.valid) p.cache[ri.cache_off + v] = cbits;
-              unsigned long long* best = sh.best + r;
-              float key = l;
-              bool eval = true;
-              if (ri.temp != 0.0f) {
-                const uint32_t h = murmur_finish(ri.prefix, static_cast<uint32_t>(v));
-                const float qa = __fmul_rn(l, sh.rinv[r]);
-                const float g = __fmaf_rn(__int2float_rn(__clz(h) + 1), 0.6931472f, 1e-4f);
-                const float bound = __fadd_rn(__fadd_rn(qa, __fmul_rn(fabsf(qa), 0x1p-20f)), g);
-                if (bound < decode_best(*reinterpret_cast<volatile unsigned long long*>(best))) eval = false;
-                else key = noised_key(l, ri.temp, h);
-              }
-              if (eval) {
-                const unsigned long long cand = pack_key(key, static_cast<uint32_t>(v));
+            }
+          }
+          q.flush(1, sh);
+        }
+
+        // (c) keys: greedy rows directly; noised rows through the exact
+        // bound, survivors queued and evaluated 32 at a time
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const int r = c * kChunkRows + rr;
+          if (r < p.rows) {
+            const RowConst rc = sh.info[r];
+            unsigned long long* best = sh.best + r;
+            const float bestv = decode_best(*reinterpret_cast<volatile unsigned long long*>(best));
+            if (rc.temp == 0.0f) {
+              const float l = lv[rr];
+              if (in && !(l < bestv)) {
+                const unsigned long long cand = pack_key(l, static_cast<uint32_t>(v));
                 if (cand > *reinterpret_cast<volatile unsigned long long*>(best)) atomicMax(best, cand);
+              }
+            } else {
+              const float qa = __fmul_rn(lv[rr], rc.rinv);
+              const float g = __fmaf_rn(__int2float_rn(__clz(hv[rr]) + 1), 0.6931472f, 1e-4f);
+              const float bound = __fadd_rn(__fadd_rn(qa, __fmul_rn(fabsf(qa), 0x1p-20f)), g);
+              const bool take = in && !(bound < bestv);
+              if (__any_sync(0xFFFFFFFFu, take)) {
+                q.push(take, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r);
+                q.flush(32, sh);
               }
             }
           }
@@ -395,6 +531,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sh.tmem_empty[b]);
     }
+    q.flush(1, sh);
 
     // Publish this CTA's row maxima; the last CTA writes the tokens.
     ptx::named_bar_sync(1, kEpiThreads);
@@ -442,11 +579,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+int max_tc_smem() {
+  int m = 0;
+  for (int r = 1; r <= kMaxRows; ++r) m = tc_layout(r).smem > m ? tc_layout(r).smem : m;
+  return m;
+}
+
 template <bool C, bool M>
 cudaError_t set_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(step_tc_kernel<C, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       tc_layout(kMaxRows).smem);
-  return e;
+  return cudaFuncSetAttribute(step_tc_kernel<C, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_tc_smem());
 }
 
 }  // namespace
@@ -499,6 +640,7 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int g
   TcParams tp;
   tp.p = p;
   tp.n = L.n;
+  tp.nacc = L.nacc;
   tp.stages = L.stages;
   tp.nbase = L.nbase;
   tp.tmem_cols = L.tmem_cols;
@@ -508,6 +650,8 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int g
   tp.bar_off = L.bar_off;
   tp.best_off = L.best_off;
   tp.info_off = L.info_off;
+  tp.coff_off = L.coff_off;
+  tp.queue_off = L.queue_off;
   tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -156,6 +156,13 @@ DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t
  * DSPARK_OK or DSPARK_ERR_CUDA. */
 DSPARK_API int dspark_markov_get_status(dspark_markov_ctx *ctx, cudaStream_t stream, int32_t *device_status);
 
+/* As dspark_markov_get_status, with where a bounded wait gave up:
+ * detail[0] = status, detail[1] = wait site (1 w2 slot free, 2 base slot free,
+ * 3 embeddings ready, 4 accumulator free, 5 w2 tile landed, 6 accumulator
+ * ready, 7 base chunk landed), detail[2] = block, detail[3] = tile << 16 |
+ * sequence number.  Reading clears the record. */
+DSPARK_API int dspark_markov_get_status_detail(dspark_markov_ctx *ctx, cudaStream_t stream, int32_t *detail);
+
 DSPARK_API void dspark_markov_destroy(dspark_markov_ctx *ctx);
 
 /*

@@ -49,6 +49,11 @@ CASES = [
     ("stress256", 2048 + 1, 256, 2),
     ("tiny", 128, 3, 2),
     ("tiny", 1, 2, 2),
+    # several vocabulary tiles per CTA at row counts whose base chunks and
+    # accumulators cycle through the rings in different patterns
+    ("large16", 60000, 24, 2),
+    ("tc64", 40000 + 16, 128, 2),
+    ("stress256", 40000 + 8, 256, 2),
 ]
 
 
