@@ -22,13 +22,14 @@ ERRORS = {
 FLAG_PDL = 0x1
 FLAG_FORCE_FMA = 0x2
 FLAG_FORCE_MMA = 0x4
+NOALLOC_MAX_VERIFY_ROWS = 8192  # DSPARK_NOALLOC_MAX_VERIFY_ROWS
 
 EXPORTED = (
     "dspark_markov_init", "dspark_markov_loop", "dspark_markov_anchor", "dspark_markov_step",
     "dspark_markov_partial_count", "dspark_markov_bias_path", "dspark_markov_get_status",
     "dspark_markov_get_status_detail",
     "dspark_markov_destroy", "dspark_build_verify_tokens", "dspark_greedy_accept_scratch_bytes",
-    "dspark_greedy_accept", "dspark_strerror",
+    "dspark_greedy_accept", "dspark_greedy_accept_noalloc", "dspark_strerror",
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
     "dspark_check_logf", "dspark_check_tanhf",
 )
@@ -92,6 +93,7 @@ def load(build_if_missing: bool = False):
         "dspark_build_verify_tokens": (ctypes.c_int, [P, P, P, i32, i32, i32, P]),
         "dspark_greedy_accept_scratch_bytes": (sz, [i32, i32, i32]),
         "dspark_greedy_accept": (ctypes.c_int, [P, P, P, P, P, P, sz, i32, i32, i32, i32, P]),
+        "dspark_greedy_accept_noalloc": (ctypes.c_int, [P, P, P, P, P, i32, i32, i32, i32, P]),
         "dspark_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "dspark_check_noise_range": (ctypes.c_int, [ctypes.c_uint32, P, i64, P]),
         "dspark_check_hash": (ctypes.c_int, [i64, i32, i64, ctypes.c_uint32, P, P, i64, P]),
@@ -198,6 +200,16 @@ def dspark_greedy_accept(logits, draft, proposal_len, accepted, accept_len, scra
     _check(load().dspark_greedy_accept(_ptr(logits), _ptr(draft), _ptr(proposal_len), _ptr(accepted),
                                        _ptr(accept_len), _ptr(scratch), scratch_bytes, batch, draft_stride, P,
                                        vocab, _stream(stream)), "dspark_greedy_accept")
+
+
+def dspark_greedy_accept_noalloc(logits, draft, proposal_len, accepted, accept_len, batch, draft_stride, P, vocab,
+                                 stream=None):
+    """dspark_greedy_accept on the library's fixed scratch array (no device
+    allocation by the library or by this wrapper); batch * (P + 1) must not
+    exceed NOALLOC_MAX_VERIFY_ROWS.  Calls must not overlap on the GPU."""
+    _check(load().dspark_greedy_accept_noalloc(_ptr(logits), _ptr(draft), _ptr(proposal_len), _ptr(accepted),
+                                               _ptr(accept_len), batch, draft_stride, P, vocab, _stream(stream)),
+           "dspark_greedy_accept_noalloc")
 
 
 def dspark_check_noise_range(h0, L, n, stream=None):

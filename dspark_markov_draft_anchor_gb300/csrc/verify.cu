@@ -10,9 +10,20 @@
 // caller's scratch needs no initialisation.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "dspark_markov.h"
 #include "markov_math.cuh"
 #include "step_common.cuh"
+
+// Scratch of dspark_greedy_accept_noalloc: one argmax slot per verify row
+// plus the arrival counter, in a fixed array of the module, so that the entry
+// point needs no allocation.  Every device that loads the library keeps it
+// (64 KB + 16 bytes) until the process exits.  Host code must not pass
+// `g_accept_noalloc_scratch` itself to a kernel: on the host the name denotes
+// a stand-in, not the device address; that comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned long long g_accept_noalloc_scratch[DSPARK_NOALLOC_MAX_VERIFY_ROWS + 2];
 
 namespace dspark {
 namespace {
@@ -114,6 +125,27 @@ accept_scan_kernel(const uint16_t* __restrict__ logits, const int64_t* __restric
   }
 }
 
+constexpr int kNoAllocMaxDevices = 64;
+
+std::atomic<void*> g_noalloc_addr[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// The device address of the array on the current device, looked up once per
+// device; nullptr if the lookup failed.
+void* noalloc_scratch_address(int device) {
+  void* p = g_noalloc_addr[device].load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  p = g_noalloc_addr[device].load(std::memory_order_relaxed);
+  if (p) return p;
+  if (cudaGetSymbolAddress(&p, ::g_accept_noalloc_scratch) != cudaSuccess || !p) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  g_noalloc_addr[device].store(p, std::memory_order_release);
+  return p;
+}
+
 }  // namespace
 }  // namespace dspark
 
@@ -160,6 +192,27 @@ int dspark_greedy_accept(const void* logits, const int64_t* draft, const int32_t
       static_cast<const uint16_t*>(logits), draft, proposal_len, accepted, accept_len, slots, counter, batch,
       draft_stride, P, vocab);
   return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+int dspark_greedy_accept_noalloc(const void* logits, const int64_t* draft, const int32_t* proposal_len,
+                                 int64_t* accepted, int32_t* accept_len, int32_t batch, int32_t draft_stride,
+                                 int32_t P, int32_t vocab, cudaStream_t stream) {
+  if (batch < 0 || P < 0 || vocab < 1 || draft_stride < P) return DSPARK_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * (P + 1) > DSPARK_NOALLOC_MAX_VERIFY_ROWS) return DSPARK_ERR_TOO_MANY_ROWS;
+  if (batch == 0) return DSPARK_OK;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= dspark::kNoAllocMaxDevices) {
+    (void)cudaGetLastError();
+    return DSPARK_ERR_CUDA;
+  }
+  void* scratch = dspark::noalloc_scratch_address(device);
+  if (!scratch) return DSPARK_ERR_CUDA;
+  // The slots and the counter are cleared by the first kernel of every call
+  // (dspark_greedy_accept's own sequence), so whatever the previous call left
+  // in the array does not matter.
+  return dspark_greedy_accept(logits, draft, proposal_len, accepted, accept_len, scratch,
+                              static_cast<size_t>(DSPARK_NOALLOC_MAX_VERIFY_ROWS + 2) * sizeof(unsigned long long),
+                              batch, draft_stride, P, vocab, stream);
 }
 
 }  // extern "C"

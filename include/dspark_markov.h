@@ -193,6 +193,43 @@ DSPARK_API int dspark_greedy_accept(const void *logits, const int64_t *draft, co
                          int32_t batch, int32_t draft_stride, int32_t P, int32_t vocab,
                          cudaStream_t stream);
 
+/*
+ * dspark_greedy_accept_noalloc -- dspark_greedy_accept with library-owned
+ * scratch, for callers that cannot allocate device memory.  The pages have
+ * no counterpart of this entry point; it exists for this library's users.
+ *
+ * Who needs it: a caller whose device memory belongs to someone else (an
+ * inference engine that reserves nearly all of HBM at start-up for its KV
+ * cache and gives a plugin no workspace), or a caller on a latency-critical
+ * path where cudaMalloc/cudaFree must not run (cudaFree synchronises the
+ * whole device, and a new allocation can stall as well).  Such a caller
+ * still owns every input and output; only the scratch moves into the
+ * library.
+ *
+ * Arguments, results and error codes are those of dspark_greedy_accept, less
+ * `scratch` and `scratch_bytes`.  The scratch is a fixed device array of
+ * DSPARK_NOALLOC_MAX_VERIFY_ROWS + 2 eight-byte words (64 KB + 16 bytes)
+ * that every device which loads the library holds until the process exits.
+ *   - batch * (P + 1) > DSPARK_NOALLOC_MAX_VERIFY_ROWS is rejected with
+ *     DSPARK_ERR_TOO_MANY_ROWS before anything is launched; use
+ *     dspark_greedy_accept with caller scratch for larger batches.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *     first call before any stream capture.  If the lookup fails the call
+ *     returns DSPARK_ERR_CUDA and the next call tries again.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - Every call shares the one array, which keeps the last call's contents.
+ *     The slots and the arrival counter, which must start at zero, are
+ *     cleared by the call's first kernel, so stale contents do no harm.  Two
+ *     calls whose kernels overlap on the GPU (different streams without an
+ *     ordering between them) race on the array and may give wrong results:
+ *     order them on one stream or with events.
+ */
+#define DSPARK_NOALLOC_MAX_VERIFY_ROWS 8192
+DSPARK_API int dspark_greedy_accept_noalloc(const void *logits, const int64_t *draft, const int32_t *proposal_len,
+                                 int64_t *accepted, int32_t *accept_len, int32_t batch,
+                                 int32_t draft_stride, int32_t P, int32_t vocab, cudaStream_t stream);
+
 /* A short English description of a DSPARK_* code (static storage). */
 DSPARK_API const char *dspark_strerror(int code);
 
