@@ -113,6 +113,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The same with the accumulate flag fixed at compile time (no predicate
+// register to set up per instruction).
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_bf16_c(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(kAccumulate ? 1 : 0)
+      : "memory");
+}
+
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -121,16 +133,19 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// 32 lanes x 32 bits, 8 consecutive columns: thread t of the warp gets lane
-// (base lane + t), columns col .. col + 7.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+// 32 lanes x 32 bits, 8 consecutive columns (thread t of the warp gets lane
+// base + t), loaded and waited for in one statement: tcgen05.ld writes its
+// destination registers asynchronously and they are defined only after
+// tcgen05.wait::ld, so the compiler must not see them (to read, copy or
+// reuse) before the wait.
+__device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&v)[8]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
       : "r"(taddr)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of tcgen05.mma for a K-major operand in the
 // 128-byte swizzle layout: 8-row x 128-byte atoms, stride between 8-row
@@ -153,6 +168,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
          | (1u << 10)         // B: BF16
          | ((n >> 3) << 17)   // N / 8
          | ((m >> 4) << 24);  // M / 16
+}
+
+// Packed BF16 arithmetic: two FP32 values rounded to nearest into one BF16x2
+// word (`lo` in bits 0..15), and the round-to-nearest sum of two BF16x2 words.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {

@@ -315,6 +315,12 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
         for (int j = max(0, issued - S); j < issued; ++j) ptx::mbar_wait(&sh.full_w2[j % S], (j / S) & 1, kWaitLimit);
+      } else {
+        // Producer tail: observe the MMA's release of every stage in flight,
+        // so that no tensor-core arrival on this CTA's barriers is still
+        // pending when the CTA exits.
+        for (int j = issued; j < issued + S; ++j)
+          if (!wait(&sh.empty_w2[j % S], ((j / S) & 1) ^ 1, 8, j)) break;
       }
     }
   } else if (warp == 2) {
@@ -352,8 +358,11 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     // ---------------- MMA issuer ----------------
     if (lane == 0 && n_tiles > 0) {
       const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, static_cast<uint32_t>(N));
-      const uint32_t emb_addr = ptx::smem_addr(sh.emb);
-      const uint32_t w2_addr = ptx::smem_addr(sh.w2);
+      // descriptors of stage 0 / K-block 0; a stage is 16 KB (1024 in the
+      // descriptor's 16-byte units), a K step of 16 is 32 bytes (2 units)
+      const uint64_t a0 = ptx::sw128_desc(ptx::smem_addr(sh.w2), 1024);
+      const uint64_t b0 = ptx::sw128_desc(ptx::smem_addr(sh.emb), 1024);
+      const uint64_t b_kstep = static_cast<uint64_t>((N * 128) >> 4);
       bool ok = wait(sh.emb_ready, 0, 3, 0);
       ptx::tc_fence_after();
       for (int i = 0; i < n_tiles && ok; ++i) {
@@ -366,12 +375,15 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           const int s = j % S;
           if (!(ok = wait(&sh.full_w2[s], (j / S) & 1, 5, (i << 16) | j))) break;
           ptx::tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kKBlock / 16; ++kk) {
-            const uint64_t a = ptx::sw128_desc(w2_addr + s * kW2StageBytes + kk * 32, 1024);
-            const uint64_t bdesc = ptx::sw128_desc(emb_addr + kb * N * 128 + kk * 32, 1024);
-            ptx::mma_bf16(d, a, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+          const uint64_t a = a0 + static_cast<uint64_t>(s * (kW2StageBytes >> 4));
+          const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
+          if (kb == 0)
+            ptx::mma_bf16_c<false>(d, a, bd, idesc);
+          else
+            ptx::mma_bf16_c<true>(d, a, bd, idesc);
+          ptx::mma_bf16_c<true>(d, a + 2, bd + 2, idesc);
+          ptx::mma_bf16_c<true>(d, a + 4, bd + 4, idesc);
+          ptx::mma_bf16_c<true>(d, a + 6, bd + 6, idesc);
           ptx::mma_commit(&sh.empty_w2[s]);
         }
         if (ok) ptx::mma_commit(&sh.tmem_full[b]);
@@ -435,15 +447,14 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         const int s = wg * NBG + k % NBG;
         ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (k / NBG) & 1, 7, (i << 16) | k));
         if (!ok) break;
-        uint32_t acc[8];
-        ptx::tmem_ld8(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                          static_cast<uint32_t>(b * N + c * kChunkRows),
-                      acc);
         const uint16_t* bs = reinterpret_cast<const uint16_t*>(sh.base + s * kChunkBytes);
         uint32_t bb[8];
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) bb[rr] = bs[rr * kTileV + vr];
-        ptx::tmem_ld_wait();
+        uint32_t acc[8];
+        ptx::tmem_ld8_sync(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(b * N + c * kChunkRows),
+                           acc);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh.empty_base[s]);
 
