@@ -55,6 +55,7 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kQCap = 64;  // entries of a warp's key-evaluation queue
+constexpr int kGTab = 48;  // noise-bound table entries (clz 0..32, padded)
 
 struct TcLayout {
   int n;         // MMA N: rows padded to 16
@@ -63,7 +64,7 @@ struct TcLayout {
   int nbase;     // base ring slots (two rings, one per epilogue warpgroup)
   int tmem_cols;
   int smem;      // dynamic shared memory bytes
-  int emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, queue_off;
+  int emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, thr_off, gtab_off, queue_off;
 };
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -89,7 +90,7 @@ TcLayout tc_layout(int rows) {
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
   L.nbase = L.n > 128 ? 8 : 16;
   const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 4 + 2) + 16 +
-                    kMaxRows * (8 + static_cast<int>(sizeof(RowConst)) + 8) + 8 * kQCap * 16 + 1024 + 64;
+                    kMaxRows * (8 + static_cast<int>(sizeof(RowConst)) + 8 + 4) + 4 * kGTab + 8 * kQCap * 16 + 1024 + 64;
   L.stages = (kSmemBudget - fixed) / kW2StageBytes;
   if (L.stages > 12) L.stages = 12;
   int off = 0;
@@ -108,6 +109,10 @@ TcLayout tc_layout(int rows) {
   off += kMaxRows * static_cast<int>(sizeof(RowConst));
   L.coff_off = off;
   off += kMaxRows * 8;
+  L.thr_off = off;
+  off += kMaxRows * 4;
+  L.gtab_off = off;
+  off += 4 * kGTab;
   L.queue_off = off;
   off += 8 * kQCap * 16;
   L.smem = off + 1024;  // room to align the base to 1024 bytes
@@ -121,15 +126,9 @@ struct TcParams {
   int32_t stages;
   int32_t nbase;
   int32_t tmem_cols;
-  int32_t emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, queue_off;
+  int32_t emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, thr_off, gtab_off, queue_off;
   int32_t num_units;  // ceil(V / 32)
 };
-
-__device__ __forceinline__ float decode_best(unsigned long long packed) {
-  const uint32_t o = static_cast<uint32_t>(packed >> 32);
-  const uint32_t bits = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
-  return __uint_as_float(bits);
-}
 
 // A warp's queue of elements whose Gumbel key must be evaluated (their exact
 // bound reaches the row's current maximum).  Evaluating them 32 at a time,
@@ -172,12 +171,37 @@ struct Shared {
   unsigned long long* best;
   RowConst* info;
   int64_t* cache_off;
+  float* thr;   // per-row pruning threshold: never above the row's maximum key
+  float* gtab;  // (clz + 1) ln 2 + 1e-4 by clz
   Cand* queues;
 };
 
 // The Gumbel key of one element, out of line: it is evaluated for few
 // elements, and one copy keeps the kernel's code small.
 __device__ __noinline__ float eval_key(float l, float temp, uint32_t h) { return noised_key(l, temp, h); }
+
+// Murmur3 of the row prefix and the pre-mixed vocabulary word, without the
+// finaliser's last xor-shift h ^= h >> 16, which leaves the top 16 bits and
+// hence clz(h) unchanged.
+__device__ __forceinline__ uint32_t murmur_pre(uint32_t prefix, uint32_t kmixed) {
+  uint32_t h = prefix ^ kmixed;
+  h = __funnelshift_l(h, h, 13);
+  h = (h * 5u + 0xe6546b64u) ^ 16u;
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  return h;
+}
+
+// Four floats of shared memory that other warps update (never cached).
+__device__ __forceinline__ float4 ld_volatile_f4(const float* ptr) {
+  float4 r;
+  asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "r"(ptx::smem_addr(ptr)));
+  return r;
+}
 
 __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Shared& sh) {
   const int lane = threadIdx.x & 31;
@@ -186,10 +210,12 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
     const uint32_t n = count < 32u ? count : 32u;
     if (static_cast<uint32_t>(lane) < n) {
       const Cand e = q[(head + lane) & (kQCap - 1)];
-      const float key = eval_key(e.l, sh.info[e.r].temp, e.h);
+      const float t = sh.info[e.r].temp;
+      // the queue holds the hash before its last xor-shift
+      const float key = t != 0.0f ? eval_key(e.l, t, e.h ^ (e.h >> 16)) : e.l;
       const unsigned long long cand = pack_key(key, e.v);
-      unsigned long long* best = sh.best + e.r;
-      if (cand > *reinterpret_cast<volatile unsigned long long*>(best)) atomicMax(best, cand);
+      const unsigned long long old = atomicMax(sh.best + e.r, cand);
+      if (cand > old) sh.thr[e.r] = key != key ? INFINITY : key;
     }
     head = (head + n) & (kQCap - 1);
     count -= n;
@@ -233,6 +259,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.best = reinterpret_cast<unsigned long long*>(smem + tp.best_off);
   sh.info = reinterpret_cast<RowConst*>(smem + tp.info_off);
   sh.cache_off = reinterpret_cast<int64_t*>(smem + tp.coff_off);
+  sh.thr = reinterpret_cast<float*>(smem + tp.thr_off);
+  sh.gtab = reinterpret_cast<float*>(smem + tp.gtab_off);
   sh.queues = reinterpret_cast<Cand*>(smem + tp.queue_off);
 
   // This CTA's vocabulary range.
@@ -422,8 +450,12 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       rc.valid = ri.valid ? 1u : 0u;
       sh.info[r] = rc;
       sh.cache_off[r] = ri.cache_off;
-      sh.best[r] = 0ull;
     }
+    // every row slot: empty maximum; live rows start unpruned, padding rows
+    // are never taken (one thread per slot, kEpiThreads == kMaxRows)
+    sh.best[et] = 0ull;
+    sh.thr[et] = et < p.rows ? -INFINITY : INFINITY;
+    if (et < 33) sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(1, kEpiThreads);
     if (et == 0) ptx::mbar_arrive(sh.emb_ready);
@@ -458,82 +490,93 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh.empty_base[s]);
 
-        // (a) bias, transform, cache store and hash of the chunk's 8 rows
-        float lv[8];
+        // (a) bias rounded to BF16 and the transform, for all 8 rows; with
+        // multiplier 1 and no cap on packed BF16 pairs (x * 1 rounds to the
+        // same BF16, and the BF16 add is the FP32 add rounded once)
+        uint32_t cb[8], biasb[8];
+        float lx[8];
+        if (kMultOne && !kHasCap) {
+#pragma unroll
+          for (int pr = 0; pr < 4; ++pr) {
+            const uint32_t bias2 = ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
+            const uint32_t c2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
+            biasb[2 * pr] = bias2 & 0xFFFFu;
+            biasb[2 * pr + 1] = bias2 >> 16;
+            cb[2 * pr] = c2 & 0xFFFFu;
+            cb[2 * pr + 1] = c2 >> 16;
+            lx[2 * pr] = __uint_as_float(c2 << 16);
+            lx[2 * pr + 1] = __uint_as_float(c2 & 0xFFFF0000u);
+          }
+        } else {
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
+            biasb[rr] = __bfloat16_as_ushort(b16);
+            cb[rr] = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult, p.inv_cap,
+                                              p.cap, &lx[rr]);
+          }
+        }
+        // cache store, hash and the exact upper bound of each key:
+        // key <= l/t + (clz(h) + 1) ln 2 (with rounding margins); a greedy
+        // row's key is l itself
+        float lv[8], bnd[8];
         uint32_t hv[8];
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
           const int r = c * kChunkRows + rr;
           lv[rr] = 0.0f;
           hv[rr] = 0u;
+          bnd[rr] = -INFINITY;
           if (r < p.rows) {
             const RowConst rc = sh.info[r];
             if (in) {
-              const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
               if (p.bias_out)
-                p.bias_out[(static_cast<int64_t>(r) * p.steps + p.step) * p.vocab + v] = __bfloat16_as_ushort(b16);
-              float l;
-              uint16_t cbits;
-              if (kMultOne && !kHasCap) {
-                // x * 1 rounds to the same BF16 (cvt gives NaNs as 0x7FFF)
-                const __nv_bfloat16 hx =
-                    __float2bfloat16_rn(__fadd_rn(bf16_bits_to_float(bb[rr]), __bfloat162float(b16)));
-                cbits = __bfloat16_as_ushort(hx);
-                l = __bfloat162float(hx);
+                p.bias_out[(static_cast<int64_t>(r) * p.steps + p.step) * p.vocab + v] =
+                    static_cast<uint16_t>(biasb[rr]);
+              if (rc.valid) p.cache[sh.cache_off[r] + v] = static_cast<uint16_t>(cb[rr]);
+              lv[rr] = lx[rr];
+              hv[rr] = murmur_pre(rc.prefix, kv);
+              if (rc.temp != 0.0f) {
+                const float qa = __fmul_rn(lx[rr], rc.rinv);
+                bnd[rr] = __fadd_rn(__fmaf_rn(fabsf(qa), 0x1p-20f, qa), sh.gtab[__clz(hv[rr])]);
               } else {
-                cbits = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult,
-                                                 p.inv_cap, p.cap, &l);
+                bnd[rr] = lx[rr];
               }
-              if (rc.valid) p.cache[sh.cache_off[r] + v] = cbits;
-              lv[rr] = l;
-              hv[rr] = murmur_finish_mixed(rc.prefix, kv);
             }
           }
         }
 
         // (b) the warpgroup's first tile: seed each row's maximum with the
-        // key of the warp's largest l / t (one evaluation per row)
+        // key of the warp's element of largest bound (one evaluation per row)
         if (first) {
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             const int r = c * kChunkRows + rr;
             if (r < p.rows) {
-              const RowConst rc = sh.info[r];
-              if (rc.temp != 0.0f) {
-                const uint32_t o = in ? orderable(__fmul_rn(lv[rr], rc.rinv)) : 0u;
-                const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
-                const uint32_t who = __ffs(__ballot_sync(0xFFFFFFFFu, o == top)) - 1;
-                q.push(lane == static_cast<int>(who) && in, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r);
-              }
+              const uint32_t o = in ? orderable(bnd[rr]) : 0u;
+              const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
+              const uint32_t who = __ballot_sync(0xFFFFFFFFu, in && o == top);
+              q.push(who != 0u && lane == __ffs(who) - 1, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r);
             }
           }
           q.flush(1, sh);
         }
 
-        // (c) keys: greedy rows directly; noised rows through the exact
-        // bound, survivors queued and evaluated 32 at a time
+        // (c) an element whose bound is below its row's threshold cannot be
+        // the argmax; the rest are queued and evaluated 32 at a time
+        const float4 th0 = ld_volatile_f4(sh.thr + c * kChunkRows);
+        const float4 th1 = ld_volatile_f4(sh.thr + c * kChunkRows + 4);
+        const float th[8] = {th0.x, th0.y, th0.z, th0.w, th1.x, th1.y, th1.z, th1.w};
+        uint32_t take = 0;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          const int r = c * kChunkRows + rr;
-          if (r < p.rows) {
-            const RowConst rc = sh.info[r];
-            unsigned long long* best = sh.best + r;
-            const float bestv = decode_best(*reinterpret_cast<volatile unsigned long long*>(best));
-            if (rc.temp == 0.0f) {
-              const float l = lv[rr];
-              if (in && !(l < bestv)) {
-                const unsigned long long cand = pack_key(l, static_cast<uint32_t>(v));
-                if (cand > *reinterpret_cast<volatile unsigned long long*>(best)) atomicMax(best, cand);
-              }
-            } else {
-              const float qa = __fmul_rn(lv[rr], rc.rinv);
-              const float g = __fmaf_rn(__int2float_rn(__clz(hv[rr]) + 1), 0.6931472f, 1e-4f);
-              const float bound = __fadd_rn(__fadd_rn(qa, __fmul_rn(fabsf(qa), 0x1p-20f)), g);
-              const bool take = in && !(bound < bestv);
-              if (__any_sync(0xFFFFFFFFu, take)) {
-                q.push(take, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r);
-                q.flush(32, sh);
-              }
+        for (int rr = 0; rr < 8; ++rr) take |= (in && !(bnd[rr] < th[rr]) ? 1u : 0u) << rr;
+        if (__any_sync(0xFFFFFFFFu, take != 0u)) {
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            const bool t = (take >> rr) & 1u;
+            if (__any_sync(0xFFFFFFFFu, t)) {
+              q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], c * kChunkRows + rr);
+              q.flush(32, sh);
             }
           }
         }
@@ -662,6 +705,8 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int g
   tp.best_off = L.best_off;
   tp.info_off = L.info_off;
   tp.coff_off = L.coff_off;
+  tp.thr_off = L.thr_off;
+  tp.gtab_off = L.gtab_off;
   tp.queue_off = L.queue_off;
   tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
   cudaLaunchConfig_t cfg = {};
