@@ -64,7 +64,7 @@ struct TcLayout {
   int nbase;     // base ring slots (two rings, one per epilogue warpgroup)
   int tmem_cols;
   int smem;      // dynamic shared memory bytes
-  int emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, thr_off, gtab_off, queue_off;
+  int emb_off, w2_off, base_off, bar_off, row_off, queue_off;
 };
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -73,13 +73,18 @@ __host__ __device__ inline int pow2_at_least(int x) {
   return p;
 }
 
-// Per-row constants of a step, 16 bytes (one broadcast shared load).
-struct RowConst {
-  uint32_t prefix;  // Murmur3 state after seed and position words
-  float temp;
-  float rinv;       // RN(1 / temp), for the key bound
-  uint32_t valid;   // the row stores into the cache
-};
+// Per-row arrays in shared memory (structure of arrays, kMaxRows entries
+// each) and their byte offsets inside the row region.
+constexpr int kRowBest = 0;                            // u64 packed maxima
+constexpr int kRowCoff = kRowBest + 8 * kMaxRows;      // i64 cache offsets
+constexpr int kRowPrefix = kRowCoff + 8 * kMaxRows;    // u32 Murmur3 prefixes
+constexpr int kRowRinv = kRowPrefix + 4 * kMaxRows;    // f32 RN(1/t) (1 for greedy rows)
+constexpr int kRowNs = kRowRinv + 4 * kMaxRows;        // f32 noise scale (0 greedy, 1 else)
+constexpr int kRowTemp = kRowNs + 4 * kMaxRows;        // f32 temperature
+constexpr int kRowThr = kRowTemp + 4 * kMaxRows;       // f32 pruning threshold
+constexpr int kRowGmask = kRowThr + 4 * kMaxRows;      // u32 per 8-row chunk: store bits 0..7, live bits 8..15
+constexpr int kRowGtab = kRowGmask + 4 * (kMaxRows / kChunkRows);  // f32 noise bound by clz
+constexpr int kRowBytes = kRowGtab + 4 * kGTab;
 
 constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared variables
 
@@ -90,7 +95,7 @@ TcLayout tc_layout(int rows) {
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
   L.nbase = L.n > 128 ? 8 : 16;
   const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 4 + 2) + 16 +
-                    kMaxRows * (8 + static_cast<int>(sizeof(RowConst)) + 8 + 4) + 4 * kGTab + 8 * kQCap * 16 + 1024 + 64;
+                    kRowBytes + 8 * kQCap * 16 + 1024 + 64;
   L.stages = (kSmemBudget - fixed) / kW2StageBytes;
   if (L.stages > 12) L.stages = 12;
   int off = 0;
@@ -103,16 +108,9 @@ TcLayout tc_layout(int rows) {
   L.bar_off = off;
   off += 8 * (2 * L.stages + 2 * L.nbase + 2 * L.nacc + 2);
   off = (off + 15) & ~15;
-  L.best_off = off;
-  off += kMaxRows * 8;
-  L.info_off = off;
-  off += kMaxRows * static_cast<int>(sizeof(RowConst));
-  L.coff_off = off;
-  off += kMaxRows * 8;
-  L.thr_off = off;
-  off += kMaxRows * 4;
-  L.gtab_off = off;
-  off += 4 * kGTab;
+  L.row_off = off;
+  off += kRowBytes;
+  off = (off + 15) & ~15;
   L.queue_off = off;
   off += 8 * kQCap * 16;
   L.smem = off + 1024;  // room to align the base to 1024 bytes
@@ -126,7 +124,7 @@ struct TcParams {
   int32_t stages;
   int32_t nbase;
   int32_t tmem_cols;
-  int32_t emb_off, w2_off, base_off, bar_off, best_off, info_off, coff_off, thr_off, gtab_off, queue_off;
+  int32_t emb_off, w2_off, base_off, bar_off, row_off, queue_off;
   int32_t num_units;  // ceil(V / 32)
 };
 
@@ -169,10 +167,14 @@ struct Shared {
   uint64_t* emb_ready;
   uint64_t* spare;
   unsigned long long* best;
-  RowConst* info;
   int64_t* cache_off;
-  float* thr;   // per-row pruning threshold: never above the row's maximum key
-  float* gtab;  // (clz + 1) ln 2 + 1e-4 by clz
+  uint32_t* prefix;
+  float* rinv;
+  float* ns;
+  float* temp;
+  float* thr;       // per-row pruning threshold: never above the row's maximum key
+  uint32_t* gmask;  // per 8-row chunk: rows that store (bits 0..7), rows that exist (8..15)
+  float* gtab;      // (clz + 1) ln 2 + 1e-4 by clz
   Cand* queues;
 };
 
@@ -194,6 +196,26 @@ __device__ __forceinline__ uint32_t murmur_pre(uint32_t prefix, uint32_t kmixed)
   return h;
 }
 
+// Explicit shared-space loads of per-row data, by the runtime shared address
+// (the compiler need not order them against the epilogue's global stores).
+__device__ __forceinline__ uint4 lds_u4(const void* ptr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(ptx::smem_addr(ptr)));
+  return r;
+}
+__device__ __forceinline__ longlong2 lds_ll2(const void* ptr) {
+  longlong2 r;
+  asm volatile("ld.shared.v2.s64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "r"(ptx::smem_addr(ptr)));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds_u32(const void* ptr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(ptx::smem_addr(ptr)));
+  return r;
+}
+
 // Four floats of shared memory that other warps update (never cached).
 __device__ __forceinline__ float4 ld_volatile_f4(const float* ptr) {
   float4 r;
@@ -210,7 +232,7 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
     const uint32_t n = count < 32u ? count : 32u;
     if (static_cast<uint32_t>(lane) < n) {
       const Cand e = q[(head + lane) & (kQCap - 1)];
-      const float t = sh.info[e.r].temp;
+      const float t = sh.temp[e.r];
       // the queue holds the hash before its last xor-shift
       const float key = t != 0.0f ? eval_key(e.l, t, e.h ^ (e.h >> 16)) : e.l;
       const unsigned long long cand = pack_key(key, e.v);
@@ -228,6 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_base,
                const TcParams tp) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // The 1024-byte alignment is taken from the runtime address of the array.
+  // (A build that instead offset the array by a pad computed from its shared
+  // address faulted on the GPU; shared-space loads below convert runtime
+  // addresses explicitly.)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ uint32_t s_tmem_base;
@@ -256,11 +282,16 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.tmem_empty = sh.tmem_full + NACC;
   sh.emb_ready = sh.tmem_full + 2 * NACC;
   sh.spare = sh.emb_ready + 1;
-  sh.best = reinterpret_cast<unsigned long long*>(smem + tp.best_off);
-  sh.info = reinterpret_cast<RowConst*>(smem + tp.info_off);
-  sh.cache_off = reinterpret_cast<int64_t*>(smem + tp.coff_off);
-  sh.thr = reinterpret_cast<float*>(smem + tp.thr_off);
-  sh.gtab = reinterpret_cast<float*>(smem + tp.gtab_off);
+  unsigned char* rowreg = smem + tp.row_off;
+  sh.best = reinterpret_cast<unsigned long long*>(rowreg + kRowBest);
+  sh.cache_off = reinterpret_cast<int64_t*>(rowreg + kRowCoff);
+  sh.prefix = reinterpret_cast<uint32_t*>(rowreg + kRowPrefix);
+  sh.rinv = reinterpret_cast<float*>(rowreg + kRowRinv);
+  sh.ns = reinterpret_cast<float*>(rowreg + kRowNs);
+  sh.temp = reinterpret_cast<float*>(rowreg + kRowTemp);
+  sh.thr = reinterpret_cast<float*>(rowreg + kRowThr);
+  sh.gmask = reinterpret_cast<uint32_t*>(rowreg + kRowGmask);
+  sh.gtab = reinterpret_cast<float*>(rowreg + kRowGtab);
   sh.queues = reinterpret_cast<Cand*>(smem + tp.queue_off);
 
   // This CTA's vocabulary range.
@@ -441,21 +472,36 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       const int kb = ch >> 3, c = ch & 7;
       *reinterpret_cast<uint4*>(sh.emb + kb * N * 128 + r * 128 + ((c ^ (r & 7)) << 4)) = val;
     }
-    for (int r = et; r < p.rows; r += kEpiThreads) {
-      const RowInfo ri = row_info(p, r);
-      RowConst rc;
-      rc.prefix = ri.prefix;
-      rc.temp = ri.temp;
-      rc.rinv = ri.temp != 0.0f ? __frcp_rn(ri.temp) : 0.0f;
-      rc.valid = ri.valid ? 1u : 0u;
-      sh.info[r] = rc;
-      sh.cache_off[r] = ri.cache_off;
+    // Per-row sampling constants, one thread per row slot (kEpiThreads ==
+    // kMaxRows); slots beyond the rows are never taken.
+    {
+      const int r = et;
+      float thr = INFINITY, rinv = 1.0f, ns = 0.0f, temp = 0.0f;
+      uint32_t prefix = 0;
+      int64_t coff = 0;
+      bool store = false;
+      if (r < p.rows) {
+        const RowInfo ri = row_info(p, r);
+        temp = ri.temp;
+        const bool noisy = ri.temp != 0.0f;
+        rinv = noisy ? __frcp_rn(ri.temp) : 1.0f;
+        ns = noisy ? 1.0f : 0.0f;
+        prefix = ri.prefix;
+        coff = ri.cache_off;
+        store = ri.valid != 0;
+        thr = -INFINITY;
+      }
+      sh.best[r] = 0ull;
+      sh.cache_off[r] = coff;
+      sh.prefix[r] = prefix;
+      sh.rinv[r] = rinv;
+      sh.ns[r] = ns;
+      sh.temp[r] = temp;
+      sh.thr[r] = thr;
+      const uint32_t sb = __ballot_sync(0xFFFFFFFFu, store), lb = __ballot_sync(0xFFFFFFFFu, r < p.rows);
+      if ((lane & 7) == 0) sh.gmask[r >> 3] = ((sb >> lane) & 0xFFu) | (((lb >> lane) & 0xFFu) << 8);
+      if (et < 33) sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
     }
-    // every row slot: empty maximum; live rows start unpruned, padding rows
-    // are never taken (one thread per slot, kEpiThreads == kMaxRows)
-    sh.best[et] = 0ull;
-    sh.thr[et] = et < p.rows ? -INFINITY : INFINITY;
-    if (et < 33) sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(1, kEpiThreads);
     if (et == 0) ptx::mbar_arrive(sh.emb_ready);
@@ -516,34 +562,29 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
                                               p.cap, &lx[rr]);
           }
         }
-        // cache store, hash and the exact upper bound of each key:
-        // key <= l/t + (clz(h) + 1) ln 2 (with rounding margins); a greedy
-        // row's key is l itself
+        // the chunk's per-row constants, all loaded before any global store
+        const int r0 = c * kChunkRows;
+        const uint4 pf0 = lds_u4(sh.prefix + r0), pf1 = lds_u4(sh.prefix + r0 + 4);
+        const uint4 ri0 = lds_u4(sh.rinv + r0), ri1 = lds_u4(sh.rinv + r0 + 4);
+        const uint4 ns0 = lds_u4(sh.ns + r0), ns1 = lds_u4(sh.ns + r0 + 4);
+        const uint32_t gm = lds_u32(sh.gmask + c);
+        const uint32_t pf[8] = {pf0.x, pf0.y, pf0.z, pf0.w, pf1.x, pf1.y, pf1.z, pf1.w};
+        const uint32_t ri[8] = {ri0.x, ri0.y, ri0.z, ri0.w, ri1.x, ri1.y, ri1.z, ri1.w};
+        const uint32_t nsb[8] = {ns0.x, ns0.y, ns0.z, ns0.w, ns1.x, ns1.y, ns1.z, ns1.w};
+        const uint32_t live = in ? (gm >> 8) & 0xFFu : 0u;  // rows of this chunk that exist, in range
+
+        // hash and the exact upper bound of each key: key <= l/t + (clz(h) +
+        // 1) ln 2 with rounding margins; a greedy row's bound is l (plus a
+        // margin), its key l itself
         float lv[8], bnd[8];
         uint32_t hv[8];
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
-          const int r = c * kChunkRows + rr;
-          lv[rr] = 0.0f;
-          hv[rr] = 0u;
-          bnd[rr] = -INFINITY;
-          if (r < p.rows) {
-            const RowConst rc = sh.info[r];
-            if (in) {
-              if (p.bias_out)
-                p.bias_out[(static_cast<int64_t>(r) * p.steps + p.step) * p.vocab + v] =
-                    static_cast<uint16_t>(biasb[rr]);
-              if (rc.valid) p.cache[sh.cache_off[r] + v] = static_cast<uint16_t>(cb[rr]);
-              lv[rr] = lx[rr];
-              hv[rr] = murmur_pre(rc.prefix, kv);
-              if (rc.temp != 0.0f) {
-                const float qa = __fmul_rn(lx[rr], rc.rinv);
-                bnd[rr] = __fadd_rn(__fmaf_rn(fabsf(qa), 0x1p-20f, qa), sh.gtab[__clz(hv[rr])]);
-              } else {
-                bnd[rr] = lx[rr];
-              }
-            }
-          }
+          lv[rr] = lx[rr];
+          hv[rr] = murmur_pre(pf[rr], kv);
+          const float qa = __fmul_rn(lx[rr], __uint_as_float(ri[rr]));
+          const float g = __uint_as_float(lds_u32(sh.gtab + __clz(hv[rr])));
+          bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa), 0x1p-20f, qa));
         }
 
         // (b) the warpgroup's first tile: seed each row's maximum with the
@@ -551,12 +592,12 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         if (first) {
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
-            const int r = c * kChunkRows + rr;
-            if (r < p.rows) {
-              const uint32_t o = in ? orderable(bnd[rr]) : 0u;
+            if (gm & (0x100u << rr)) {
+              const bool mine = (live >> rr) & 1u;
+              const uint32_t o = mine ? orderable(bnd[rr]) : 0u;
               const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
-              const uint32_t who = __ballot_sync(0xFFFFFFFFu, in && o == top);
-              q.push(who != 0u && lane == __ffs(who) - 1, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r);
+              const uint32_t who = __ballot_sync(0xFFFFFFFFu, mine && o == top);
+              q.push(who != 0u && lane == __ffs(who) - 1, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
             }
           }
           q.flush(1, sh);
@@ -564,20 +605,38 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
 
         // (c) an element whose bound is below its row's threshold cannot be
         // the argmax; the rest are queued and evaluated 32 at a time
-        const float4 th0 = ld_volatile_f4(sh.thr + c * kChunkRows);
-        const float4 th1 = ld_volatile_f4(sh.thr + c * kChunkRows + 4);
+        const float4 th0 = ld_volatile_f4(sh.thr + r0);
+        const float4 th1 = ld_volatile_f4(sh.thr + r0 + 4);
         const float th[8] = {th0.x, th0.y, th0.z, th0.w, th1.x, th1.y, th1.z, th1.w};
         uint32_t take = 0;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) take |= (in && !(bnd[rr] < th[rr]) ? 1u : 0u) << rr;
+        for (int rr = 0; rr < 8; ++rr) take |= (bnd[rr] < th[rr] ? 0u : 1u) << rr;
+        take &= live;
         if (__any_sync(0xFFFFFFFFu, take != 0u)) {
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             const bool t = (take >> rr) & 1u;
             if (__any_sync(0xFFFFFFFFu, t)) {
-              q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], c * kChunkRows + rr);
+              q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
               q.flush(32, sh);
             }
+          }
+        }
+
+        // (d) cache and bias stores of the chunk
+        if (in) {
+          const longlong2 co0 = lds_ll2(sh.cache_off + r0), co1 = lds_ll2(sh.cache_off + r0 + 2);
+          const longlong2 co2 = lds_ll2(sh.cache_off + r0 + 4), co3 = lds_ll2(sh.cache_off + r0 + 6);
+          const int64_t co[8] = {co0.x, co0.y, co1.x, co1.y, co2.x, co2.y, co3.x, co3.y};
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr)
+            if (gm & (1u << rr)) p.cache[co[rr] + v] = static_cast<uint16_t>(cb[rr]);
+          if (p.bias_out) {
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr)
+              if (gm & (0x100u << rr))
+                p.bias_out[(static_cast<int64_t>(r0 + rr) * p.steps + p.step) * p.vocab + v] =
+                    static_cast<uint16_t>(biasb[rr]);
           }
         }
       }
@@ -702,11 +761,7 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int g
   tp.w2_off = L.w2_off;
   tp.base_off = L.base_off;
   tp.bar_off = L.bar_off;
-  tp.best_off = L.best_off;
-  tp.info_off = L.info_off;
-  tp.coff_off = L.coff_off;
-  tp.thr_off = L.thr_off;
-  tp.gtab_off = L.gtab_off;
+  tp.row_off = L.row_off;
   tp.queue_off = L.queue_off;
   tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
   cudaLaunchConfig_t cfg = {};
