@@ -86,6 +86,8 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.cap = a->cap;
   p.inv_cap = a->cap != 0.0f ? 1.0f / a->cap : 0.0f;
   p.salt = a->salt;
+  p.finish = 1;
+  p.write_prev = 0;
   return p;
 }
 
@@ -188,26 +190,43 @@ int dspark_markov_anchor(dspark_markov_ctx* ctx, const dspark_markov_loop_args* 
   return DSPARK_OK;
 }
 
+namespace {
+
+// One step launch.  In a loop on the tensor-core path a step leaves its
+// tokens in the argmax slots and the next step's CTA 0 writes them, so that
+// no step but the last waits for a last-arriving CTA.
+int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_t step, bool in_loop,
+                cudaStream_t stream) {
+  dspark::StepParams p = make_params(ctx, a, step);
+  const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
+  cudaError_t e;
+  if (dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a)) {
+    if (in_loop) {
+      p.finish = step == a->steps - 1;
+      p.write_prev = step > 0;
+    }
+    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->grid_tc, pdl, stream);
+  } else {
+    e = dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream);
+  }
+  return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+}  // namespace
+
 int dspark_markov_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_t step,
                        cudaStream_t stream) {
   int rc = check_args(ctx, a);
   if (rc != DSPARK_OK) return rc;
   if (step < 0 || step >= a->steps) return DSPARK_ERR_INVALID_ARG;
-  const dspark::StepParams p = make_params(ctx, a, step);
-  const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
-  cudaError_t e;
-  if (dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a))
-    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->grid_tc, pdl, stream);
-  else
-    e = dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream);
-  return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+  return launch_step(ctx, a, step, false, stream);
 }
 
 int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
   int rc = dspark_markov_anchor(ctx, a, stream);
   if (rc != DSPARK_OK) return rc;
   for (int s = 0; s < a->steps; ++s) {
-    rc = dspark_markov_step(ctx, a, s, stream);
+    rc = launch_step(ctx, a, s, true, stream);
     if (rc != DSPARK_OK) return rc;
   }
   return DSPARK_OK;

@@ -46,6 +46,8 @@ struct StepParams {
   float inv_cap;
   float cap;
   uint32_t salt;
+  int32_t finish;      // this launch writes its own tokens (the last CTA to arrive)
+  int32_t write_prev;  // CTA 0 writes the previous step's tokens from slots_prev
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this

@@ -29,8 +29,11 @@
 // allow any order ([P2] module docstring, [P4] module docstring).
 //
 // Programmatic dependent launch: the TMA producers read only inputs written
-// before the loop (w2, base) and start before griddepcontrol.wait; every
-// other warp waits first.  All mbarrier waits are bounded; a wait that gives
+// before the loop (w2, base) and start before griddepcontrol.wait, and the
+// epilogue warps read the per-row sampling constants (also inputs) before it;
+// only the previous tokens wait.  Within a loop a step publishes its row
+// maxima and exits; the next step's CTA 0 writes its tokens, and only the
+// loop's last step lets its last-arriving CTA write them.  All mbarrier waits are bounded; a wait that gives
 // up records DSPARK_ERR_DEVICE_TIMEOUT in the status word and the CTA leaves
 // its loops, waits (bounded) for its copies in flight and frees its TMEM.
 #include <cuda.h>
@@ -456,24 +459,9 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
     const int wg = (warp - kEpiWarp0) >> 2;       // warpgroup: takes tiles i = wg, wg + 2, ...
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
-    pdl_wait();
-
-    // Markov embeddings of the previous tokens, in the MMA's B layout:
-    // 4 K-blocks of [N rows x 128 bytes], 128-byte swizzle.
-    const uint64_t last_row = static_cast<uint64_t>(p.w1_rows - 1);
-    for (int idx = et; idx < N * 32; idx += kEpiThreads) {
-      const int r = idx >> 5, ch = idx & 31;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (r < p.rows) {
-        const int64_t tok = slot_token(__ldcg(p.slots_prev + r));
-        const uint64_t row = static_cast<uint64_t>(tok) < last_row ? static_cast<uint64_t>(tok) : last_row;
-        val = ldg_nc_v4(p.w1 + row * kRank + ch * 8);
-      }
-      const int kb = ch >> 3, c = ch & 7;
-      *reinterpret_cast<uint4*>(sh.emb + kb * N * 128 + r * 128 + ((c ^ (r & 7)) << 4)) = val;
-    }
     // Per-row sampling constants, one thread per row slot (kEpiThreads ==
-    // kMaxRows); slots beyond the rows are never taken.
+    // kMaxRows); slots beyond the rows are never taken.  They are inputs of
+    // the loop, read before the grid dependency resolves.
     {
       const int r = et;
       float thr = INFINITY, rinv = 1.0f, ns = 0.0f, temp = 0.0f;
@@ -501,6 +489,25 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       const uint32_t sb = __ballot_sync(0xFFFFFFFFu, store), lb = __ballot_sync(0xFFFFFFFFu, r < p.rows);
       if ((lane & 7) == 0) sh.gmask[r >> 3] = ((sb >> lane) & 0xFFu) | (((lb >> lane) & 0xFFu) << 8);
       if (et < 33) sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
+    }
+
+    pdl_wait();
+
+    // Markov embeddings of the previous tokens, in the MMA's B layout:
+    // 4 K-blocks of [N rows x 128 bytes], 128-byte swizzle.
+    const uint64_t last_row = static_cast<uint64_t>(p.w1_rows - 1);
+    for (int idx = et; idx < N * 32; idx += kEpiThreads) {
+      const int r = idx >> 5, ch = idx & 31;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (r < p.rows) {
+        const int64_t tok = slot_token(__ldcg(p.slots_prev + r));
+        const uint64_t row = static_cast<uint64_t>(tok) < last_row ? static_cast<uint64_t>(tok) : last_row;
+        val = ldg_nc_v4(p.w1 + row * kRank + ch * 8);
+        if (p.write_prev && blockIdx.x == 0 && ch == 0)
+          p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + p.step - 1] = tok;
+      }
+      const int kb = ch >> 3, c = ch & 7;
+      *reinterpret_cast<uint4*>(sh.emb + kb * N * 128 + r * 128 + ((c ^ (r & 7)) << 4)) = val;
     }
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(1, kEpiThreads);
@@ -533,8 +540,13 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         ptx::tmem_ld8_sync(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(b * N + c * kChunkRows),
                            acc);
+        ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sh.empty_base[s]);
+        if (lane == 0) {
+          ptx::mbar_arrive(&sh.empty_base[s]);
+          // the tile's last chunk is in registers: the accumulator is free
+          if (c == chunks - 1) ptx::mbar_arrive(&sh.tmem_empty[b]);
+        }
 
         // (a) bias rounded to BF16 and the transform, for all 8 rows; with
         // multiplier 1 and no cap on packed BF16 pairs (x * 1 rounds to the
@@ -640,25 +652,26 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sh.tmem_empty[b]);
     }
     q.flush(1, sh);
 
-    // Publish this CTA's row maxima; the last CTA writes the tokens.
+    // Publish this CTA's row maxima.  The next step reads them once its grid
+    // dependency resolves; a step that finishes the loop (or runs alone)
+    // lets the CTA that arrives last write the tokens.
     ptx::named_bar_sync(1, kEpiThreads);
     if (n_tiles > 0 && !*abort_flag)
       for (int r = et; r < p.rows; r += kEpiThreads) atomicMax(p.slots_out + r, sh.best[r]);
-    __threadfence();
-    ptx::named_bar_sync(1, kEpiThreads);
-    if (et == 0) s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
-    ptx::named_bar_sync(1, kEpiThreads);
-    if (s_last) {
+    if (p.finish) {
       __threadfence();
-      for (int r = et; r < p.rows; r += kEpiThreads) {
-        const unsigned long long sv = atomicAdd(p.slots_out + r, 0ull);
-        p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + p.step] = slot_token(sv);
+      ptx::named_bar_sync(1, kEpiThreads);
+      if (et == 0) s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
+      ptx::named_bar_sync(1, kEpiThreads);
+      if (s_last) {
+        __threadfence();
+        for (int r = et; r < p.rows; r += kEpiThreads) {
+          const unsigned long long sv = atomicAdd(p.slots_out + r, 0ull);
+          p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + p.step] = slot_token(sv);
+        }
       }
     }
   }
