@@ -86,18 +86,20 @@ constexpr int kRowNs = kRowRinv + 4 * kMaxRows;        // f32 noise scale (0 gre
 constexpr int kRowTemp = kRowNs + 4 * kMaxRows;        // f32 temperature
 constexpr int kRowThr = kRowTemp + 4 * kMaxRows;       // f32 pruning threshold
 constexpr int kRowGmask = kRowThr + 4 * kMaxRows;      // u32 per 8-row chunk: store bits 0..7, live bits 8..15
-constexpr int kRowGtab = kRowGmask + 4 * (kMaxRows / kChunkRows);  // f32 noise bound by clz
-constexpr int kRowBytes = kRowGtab + 4 * kGTab;
+constexpr int kRowGtab = kRowGmask + 4 * (kMaxRows / kChunkRows);  // f32 noise upper bound by clz
+constexpr int kRowLtab = kRowGtab + 4 * kGTab;                     // f32 noise lower bound by clz
+constexpr int kRowBytes = kRowLtab + 4 * kGTab;
 
 constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared variables
 
 TcLayout tc_layout(int rows) {
   TcLayout L;
   L.n = ((rows + 15) / 16) * 16;
-  L.nacc = 4 * L.n <= 512 ? 4 : 2;  // even: each accumulator belongs to one warpgroup
+  // even: each accumulator belongs to one warpgroup
+  L.nacc = 8 * L.n <= 512 ? 8 : (4 * L.n <= 512 ? 4 : 2);
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
   L.nbase = L.n > 128 ? 8 : 16;
-  const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 4 + 2) + 16 +
+  const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 2) + 16 +
                     kRowBytes + 8 * kQCap * 16 + 1024 + 64;
   L.stages = (kSmemBudget - fixed) / kW2StageBytes;
   if (L.stages > 12) L.stages = 12;
@@ -129,6 +131,7 @@ struct TcParams {
   int32_t tmem_cols;
   int32_t emb_off, w2_off, base_off, bar_off, row_off, queue_off;
   int32_t num_units;  // ceil(V / 32)
+  float ltab[33];     // least noise by clz of the hash (host-computed)
 };
 
 // A warp's queue of elements whose Gumbel key must be evaluated (their exact
@@ -177,7 +180,8 @@ struct Shared {
   float* temp;
   float* thr;       // per-row pruning threshold: never above the row's maximum key
   uint32_t* gmask;  // per 8-row chunk: rows that store (bits 0..7), rows that exist (8..15)
-  float* gtab;      // (clz + 1) ln 2 + 1e-4 by clz
+  float* gtab;      // (clz + 1) ln 2 + 1e-4 by clz: the noise never exceeds it
+  float* ltab;      // by clz: the computed noise is never below it
   Cand* queues;
 };
 
@@ -295,6 +299,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.thr = reinterpret_cast<float*>(rowreg + kRowThr);
   sh.gmask = reinterpret_cast<uint32_t*>(rowreg + kRowGmask);
   sh.gtab = reinterpret_cast<float*>(rowreg + kRowGtab);
+  sh.ltab = reinterpret_cast<float*>(rowreg + kRowLtab);
   sh.queues = reinterpret_cast<Cand*>(smem + tp.queue_off);
 
   // This CTA's vocabulary range.
@@ -488,7 +493,10 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       sh.thr[r] = thr;
       const uint32_t sb = __ballot_sync(0xFFFFFFFFu, store), lb = __ballot_sync(0xFFFFFFFFu, r < p.rows);
       if ((lane & 7) == 0) sh.gmask[r >> 3] = ((sb >> lane) & 0xFFu) | (((lb >> lane) & 0xFFu) << 8);
-      if (et < 33) sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
+      if (et < 33) {
+        sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
+        sh.ltab[et] = tp.ltab[et];
+      }
     }
 
     pdl_wait();
@@ -599,20 +607,27 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa), 0x1p-20f, qa));
         }
 
-        // (b) the warpgroup's first tile: seed each row's maximum with the
-        // key of the warp's element of largest bound (one evaluation per row)
+        // (b) the warpgroup's first tile: raise each row's threshold to the
+        // warp's largest exact lower bound of a key, l/t + (least noise for
+        // clz(h)) with rounding margins; a threshold never above some key in
+        // this CTA's range never prunes the argmax
         if (first) {
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             if (gm & (0x100u << rr)) {
-              const bool mine = (live >> rr) & 1u;
-              const uint32_t o = mine ? orderable(bnd[rr]) : 0u;
+              const float qa = __fmul_rn(lx[rr], __uint_as_float(ri[rr]));
+              const float lb = __fmaf_rn(__uint_as_float(nsb[rr]), __uint_as_float(lds_u32(sh.ltab + __clz(hv[rr]))),
+                                         __fmaf_rn(-fabsf(qa), 0x1p-20f, qa));
+              const uint32_t o = ((live >> rr) & 1u) && lb == lb ? orderable(lb) : 0u;
               const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
-              const uint32_t who = __ballot_sync(0xFFFFFFFFu, mine && o == top);
-              q.push(who != 0u && lane == __ffs(who) - 1, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
+              if (lane == 0 && top != 0u) {
+                const float m = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
+                float* t = sh.thr + r0 + rr;
+                if (m > *reinterpret_cast<volatile float*>(t)) *t = m;
+              }
             }
           }
-          q.flush(1, sh);
+          __syncwarp();
         }
 
         // (c) an element whose bound is below its row's threshold cannot be
@@ -729,6 +744,23 @@ cudaError_t setup_step_tc() {
 
 int tc_smem_bytes(int rows) { return tc_layout(rows).smem; }
 
+// The least noise -L(h) over the hashes with clz(h) = c: -L(u) =
+// -log(-log(1 - u)) falls as u grows, and with clz(h) = c the noise's u is at
+// most 2^-c (c = 32: 2^-33; c = 0: 1 - 2^-33).  Less a margin far above the
+// rounding of its FP32 evaluation.
+const float* least_noise_table() {
+  static float t[33];
+  static bool done = false;
+  if (!done) {
+    for (int c = 0; c <= 32; ++c) {
+      const double um = c == 0 ? 1.0 - 0x1p-33 : (c == 32 ? 0x1p-33 : ldexp(1.0, -c));
+      t[c] = static_cast<float>(-log(-log1p(-um)) - 1e-3);
+    }
+    done = true;
+  }
+  return t;
+}
+
 bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -777,6 +809,8 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int g
   tp.row_off = L.row_off;
   tp.queue_off = L.queue_off;
   tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
+  const float* lt = least_noise_table();
+  for (int c = 0; c <= 32; ++c) tp.ltab[c] = lt[c];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
