@@ -147,6 +147,18 @@ __device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&v)[8]) 
       : "memory");
 }
 
+// The same for 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor of tcgen05.mma for a K-major operand in the
 // 128-byte swizzle layout: 8-row x 128-byte atoms, stride between 8-row
 // groups `sbo` bytes; `addr` is the operand's shared-memory byte address.

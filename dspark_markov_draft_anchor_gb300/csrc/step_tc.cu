@@ -52,8 +52,8 @@ constexpr int kUnit = 32;              // vocabulary rows per partition unit / T
 constexpr int kKBlock = 64;            // K per w2 stage (one 128-byte swizzle row)
 constexpr int kKBlocks = kRank / kKBlock;
 constexpr int kW2StageBytes = kTileV * kKBlock * 2;  // 16 KB
-constexpr int kChunkRows = 8;          // base rows per chunk
-constexpr int kChunkBytes = kChunkRows * kTileV * 2;  // 2 KB
+constexpr int kChunkRows = 16;         // base rows per chunk (one epilogue pass)
+constexpr int kChunkBytes = kChunkRows * kTileV * 2;  // 4 KB
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 24;
@@ -85,7 +85,7 @@ constexpr int kRowRinv = kRowPrefix + 4 * kMaxRows;    // f32 RN(1/t) (1 for gre
 constexpr int kRowNs = kRowRinv + 4 * kMaxRows;        // f32 noise scale (0 greedy, 1 else)
 constexpr int kRowTemp = kRowNs + 4 * kMaxRows;        // f32 temperature
 constexpr int kRowThr = kRowTemp + 4 * kMaxRows;       // f32 pruning threshold
-constexpr int kRowGmask = kRowThr + 4 * kMaxRows;      // u32 per 8-row chunk: store bits 0..7, live bits 8..15
+constexpr int kRowGmask = kRowThr + 4 * kMaxRows;      // u32 per 16-row chunk: store bits 0..15, live bits 16..31
 constexpr int kRowGtab = kRowGmask + 4 * (kMaxRows / kChunkRows);  // f32 noise upper bound by clz
 constexpr int kRowLtab = kRowGtab + 4 * kGTab;                     // f32 noise lower bound by clz
 constexpr int kRowBytes = kRowLtab + 4 * kGTab;
@@ -98,7 +98,7 @@ TcLayout tc_layout(int rows) {
   // even: each accumulator belongs to one warpgroup
   L.nacc = 8 * L.n <= 512 ? 8 : (4 * L.n <= 512 ? 4 : 2);
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
-  L.nbase = L.n > 128 ? 8 : 16;
+  L.nbase = 8;
   const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 2) + 16 +
                     kRowBytes + 8 * kQCap * 16 + 1024 + 64;
   L.stages = (kSmemBudget - fixed) / kW2StageBytes;
@@ -179,7 +179,7 @@ struct Shared {
   float* ns;
   float* temp;
   float* thr;       // per-row pruning threshold: never above the row's maximum key
-  uint32_t* gmask;  // per 8-row chunk: rows that store (bits 0..7), rows that exist (8..15)
+  uint32_t* gmask;  // per 16-row chunk: rows that store (bits 0..15), rows that exist (16..31)
   float* gtab;      // (clz + 1) ln 2 + 1e-4 by clz: the noise never exceeds it
   float* ltab;      // by clz: the computed noise is never below it
   Cand* queues;
@@ -492,7 +492,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       sh.temp[r] = temp;
       sh.thr[r] = thr;
       const uint32_t sb = __ballot_sync(0xFFFFFFFFu, store), lb = __ballot_sync(0xFFFFFFFFu, r < p.rows);
-      if ((lane & 7) == 0) sh.gmask[r >> 3] = ((sb >> lane) & 0xFFu) | (((lb >> lane) & 0xFFu) << 8);
+      if ((lane & 15) == 0) sh.gmask[r >> 4] = ((sb >> lane) & 0xFFFFu) | (((lb >> lane) & 0xFFFFu) << 16);
       if (et < 33) {
         sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
         sh.ltab[et] = tp.ltab[et];
@@ -541,13 +541,14 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (k / NBG) & 1, 7, (i << 16) | k));
         if (!ok) break;
         const uint16_t* bs = reinterpret_cast<const uint16_t*>(sh.base + s * kChunkBytes);
-        uint32_t bb[8];
+        constexpr int R = kChunkRows;
+        uint32_t bb[R];
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) bb[rr] = bs[rr * kTileV + vr];
-        uint32_t acc[8];
-        ptx::tmem_ld8_sync(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               static_cast<uint32_t>(b * N + c * kChunkRows),
-                           acc);
+        for (int rr = 0; rr < R; ++rr) bb[rr] = bs[rr * kTileV + vr];
+        uint32_t acc[R];
+        ptx::tmem_ld16_sync(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                static_cast<uint32_t>(b * N + c * kChunkRows),
+                            acc);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -556,68 +557,71 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           if (c == chunks - 1) ptx::mbar_arrive(&sh.tmem_empty[b]);
         }
 
-        // (a) bias rounded to BF16 and the transform, for all 8 rows; with
+        // (a) bias rounded to BF16 and the transform, for all rows; with
         // multiplier 1 and no cap on packed BF16 pairs (x * 1 rounds to the
         // same BF16, and the BF16 add is the FP32 add rounded once)
-        uint32_t cb[8], biasb[8];
-        float lx[8];
+        uint32_t cb[R], biasb[R];
+        float lv[R];
         if (kMultOne && !kHasCap) {
 #pragma unroll
-          for (int pr = 0; pr < 4; ++pr) {
+          for (int pr = 0; pr < R / 2; ++pr) {
             const uint32_t bias2 = ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
             const uint32_t c2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
             biasb[2 * pr] = bias2 & 0xFFFFu;
             biasb[2 * pr + 1] = bias2 >> 16;
             cb[2 * pr] = c2 & 0xFFFFu;
             cb[2 * pr + 1] = c2 >> 16;
-            lx[2 * pr] = __uint_as_float(c2 << 16);
-            lx[2 * pr + 1] = __uint_as_float(c2 & 0xFFFF0000u);
+            lv[2 * pr] = __uint_as_float(c2 << 16);
+            lv[2 * pr + 1] = __uint_as_float(c2 & 0xFFFF0000u);
           }
         } else {
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {
+          for (int rr = 0; rr < R; ++rr) {
             const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
             biasb[rr] = __bfloat16_as_ushort(b16);
             cb[rr] = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult, p.inv_cap,
-                                              p.cap, &lx[rr]);
+                                              p.cap, &lv[rr]);
           }
         }
+
         // the chunk's per-row constants, all loaded before any global store
         const int r0 = c * kChunkRows;
-        const uint4 pf0 = lds_u4(sh.prefix + r0), pf1 = lds_u4(sh.prefix + r0 + 4);
-        const uint4 ri0 = lds_u4(sh.rinv + r0), ri1 = lds_u4(sh.rinv + r0 + 4);
-        const uint4 ns0 = lds_u4(sh.ns + r0), ns1 = lds_u4(sh.ns + r0 + 4);
+        uint32_t pf[R], ri[R], nsb[R];
+#pragma unroll
+        for (int q4 = 0; q4 < R / 4; ++q4) {
+          const uint4 a = lds_u4(sh.prefix + r0 + 4 * q4);
+          const uint4 bq = lds_u4(sh.rinv + r0 + 4 * q4);
+          const uint4 cq = lds_u4(sh.ns + r0 + 4 * q4);
+          pf[4 * q4] = a.x; pf[4 * q4 + 1] = a.y; pf[4 * q4 + 2] = a.z; pf[4 * q4 + 3] = a.w;
+          ri[4 * q4] = bq.x; ri[4 * q4 + 1] = bq.y; ri[4 * q4 + 2] = bq.z; ri[4 * q4 + 3] = bq.w;
+          nsb[4 * q4] = cq.x; nsb[4 * q4 + 1] = cq.y; nsb[4 * q4 + 2] = cq.z; nsb[4 * q4 + 3] = cq.w;
+        }
         const uint32_t gm = lds_u32(sh.gmask + c);
-        const uint32_t pf[8] = {pf0.x, pf0.y, pf0.z, pf0.w, pf1.x, pf1.y, pf1.z, pf1.w};
-        const uint32_t ri[8] = {ri0.x, ri0.y, ri0.z, ri0.w, ri1.x, ri1.y, ri1.z, ri1.w};
-        const uint32_t nsb[8] = {ns0.x, ns0.y, ns0.z, ns0.w, ns1.x, ns1.y, ns1.z, ns1.w};
-        const uint32_t live = in ? (gm >> 8) & 0xFFu : 0u;  // rows of this chunk that exist, in range
+        const uint32_t live = in ? gm >> 16 : 0u;  // rows of this chunk that exist, this lane in range
 
         // hash and the exact upper bound of each key: key <= l/t + (clz(h) +
         // 1) ln 2 with rounding margins; a greedy row's bound is l (plus a
         // margin), its key l itself
-        float lv[8], bnd[8];
-        uint32_t hv[8];
+        float bnd[R], qa[R];
+        uint32_t hv[R];
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          lv[rr] = lx[rr];
+        for (int rr = 0; rr < R; ++rr) {
           hv[rr] = murmur_pre(pf[rr], kv);
-          const float qa = __fmul_rn(lx[rr], __uint_as_float(ri[rr]));
+          qa[rr] = __fmul_rn(lv[rr], __uint_as_float(ri[rr]));
           const float g = __uint_as_float(lds_u32(sh.gtab + __clz(hv[rr])));
-          bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa), 0x1p-20f, qa));
+          bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa[rr]), 0x1p-20f, qa[rr]));
         }
 
         // (b) the warpgroup's first tile: raise each row's threshold to the
         // warp's largest exact lower bound of a key, l/t + (least noise for
-        // clz(h)) with rounding margins; a threshold never above some key in
-        // this CTA's range never prunes the argmax
+        // clz(h)) with rounding margins; a threshold at or below some key of
+        // this CTA's range never prunes its argmax
         if (first) {
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {
-            if (gm & (0x100u << rr)) {
-              const float qa = __fmul_rn(lx[rr], __uint_as_float(ri[rr]));
+          for (int rr = 0; rr < R; ++rr) {
+            if (gm & (0x10000u << rr)) {
               const float lb = __fmaf_rn(__uint_as_float(nsb[rr]), __uint_as_float(lds_u32(sh.ltab + __clz(hv[rr]))),
-                                         __fmaf_rn(-fabsf(qa), 0x1p-20f, qa));
+                                         __fmaf_rn(-fabsf(qa[rr]), 0x1p-20f, qa[rr]));
               const uint32_t o = ((live >> rr) & 1u) && lb == lb ? orderable(lb) : 0u;
               const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
               if (lane == 0 && top != 0u) {
@@ -632,36 +636,60 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
 
         // (c) an element whose bound is below its row's threshold cannot be
         // the argmax; the rest are queued and evaluated 32 at a time
-        const float4 th0 = ld_volatile_f4(sh.thr + r0);
-        const float4 th1 = ld_volatile_f4(sh.thr + r0 + 4);
-        const float th[8] = {th0.x, th0.y, th0.z, th0.w, th1.x, th1.y, th1.z, th1.w};
         uint32_t take = 0;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) take |= (bnd[rr] < th[rr] ? 0u : 1u) << rr;
+        for (int q4 = 0; q4 < R / 4; ++q4) {
+          const float4 th = ld_volatile_f4(sh.thr + r0 + 4 * q4);
+          take |= (bnd[4 * q4] < th.x ? 0u : 1u) << (4 * q4);
+          take |= (bnd[4 * q4 + 1] < th.y ? 0u : 1u) << (4 * q4 + 1);
+          take |= (bnd[4 * q4 + 2] < th.z ? 0u : 1u) << (4 * q4 + 2);
+          take |= (bnd[4 * q4 + 3] < th.w ? 0u : 1u) << (4 * q4 + 3);
+        }
         take &= live;
         if (__any_sync(0xFFFFFFFFu, take != 0u)) {
+          // one warp scan places every survivor in the queue when they fit
+          const uint32_t nt = __popc(take);
+          uint32_t incl = nt;
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {
-            const bool t = (take >> rr) & 1u;
-            if (__any_sync(0xFFFFFFFFu, t)) {
-              q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
-              q.flush(32, sh);
+          for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += y;
+          }
+          const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+          if (q.count + total <= static_cast<uint32_t>(kQCap)) {
+            uint32_t pos = q.head + q.count + incl - nt;
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr)
+              if ((take >> rr) & 1u) {
+                q.q[pos & (kQCap - 1)] = Cand{static_cast<uint32_t>(v), lv[rr], hv[rr], static_cast<uint32_t>(r0 + rr)};
+                ++pos;
+              }
+            q.count += total;
+            q.flush(32, sh);
+          } else {
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+              const bool t = (take >> rr) & 1u;
+              if (__any_sync(0xFFFFFFFFu, t)) {
+                q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
+                q.flush(32, sh);
+              }
             }
           }
         }
 
         // (d) cache and bias stores of the chunk
         if (in) {
-          const longlong2 co0 = lds_ll2(sh.cache_off + r0), co1 = lds_ll2(sh.cache_off + r0 + 2);
-          const longlong2 co2 = lds_ll2(sh.cache_off + r0 + 4), co3 = lds_ll2(sh.cache_off + r0 + 6);
-          const int64_t co[8] = {co0.x, co0.y, co1.x, co1.y, co2.x, co2.y, co3.x, co3.y};
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr)
-            if (gm & (1u << rr)) p.cache[co[rr] + v] = static_cast<uint16_t>(cb[rr]);
+          for (int q2 = 0; q2 < R / 2; ++q2) {
+            const longlong2 co = lds_ll2(sh.cache_off + r0 + 2 * q2);
+            if (gm & (1u << (2 * q2))) p.cache[co.x + v] = static_cast<uint16_t>(cb[2 * q2]);
+            if (gm & (2u << (2 * q2))) p.cache[co.y + v] = static_cast<uint16_t>(cb[2 * q2 + 1]);
+          }
           if (p.bias_out) {
 #pragma unroll
-            for (int rr = 0; rr < 8; ++rr)
-              if (gm & (0x100u << rr))
+            for (int rr = 0; rr < R; ++rr)
+              if (gm & (0x10000u << rr))
                 p.bias_out[(static_cast<int64_t>(r0 + rr) * p.steps + p.step) * p.vocab + v] =
                     static_cast<uint16_t>(biasb[rr]);
           }
