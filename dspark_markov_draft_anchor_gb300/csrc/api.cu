@@ -22,6 +22,7 @@ struct dspark_markov_ctx {
   int grid_tc;
   bool tc_ok;                 // tensor-core step available (tensor map encoded)
   CUtensorMap w2_map;         // TMA map over w2: boxes of 32 rows x 64 K, 128-byte swizzle
+  CUtensorMap w2_tile_map;    // the same with boxes of 128 rows (whole vocabulary tiles)
 };
 
 namespace {
@@ -157,7 +158,8 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   }
   ctx->grid_simple = dspark::simple_step_grid(cfg->vocab);
   ctx->grid_tc = dspark::tc_step_grid(cfg->vocab, sms);
-  ctx->tc_ok = tc_setup && dspark::encode_w2_map(&ctx->w2_map, w2_bf16, cfg->vocab);
+  ctx->tc_ok = tc_setup && dspark::encode_w2_map(&ctx->w2_map, w2_bf16, cfg->vocab, 32) &&
+              dspark::encode_w2_map(&ctx->w2_tile_map, w2_bf16, cfg->vocab, 128);
   *out = ctx;
   return DSPARK_OK;
 }
@@ -205,7 +207,7 @@ int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_
       p.finish = step == a->steps - 1;
       p.write_prev = step > 0;
     }
-    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->grid_tc, pdl, stream);
+    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, stream);
   } else {
     e = dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream);
   }

@@ -24,7 +24,9 @@ cudaError_t launch_step_simple(const StepParams& p, bool has_cap, bool pdl, cuda
 cudaError_t setup_step_tc();
 int tc_step_grid(int64_t vocab, int sm_count);
 int tc_smem_bytes(int rows);
-bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab);
-cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int grid, bool pdl, cudaStream_t stream);
+// box_rows: 32 (any tile) or 128 (whole tiles, one copy per stage).
+bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab, int box_rows);
+cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
+                           bool pdl, cudaStream_t stream);
 
 }  // namespace dspark

@@ -98,11 +98,14 @@ TcLayout tc_layout(int rows) {
   // even: each accumulator belongs to one warpgroup
   L.nacc = 8 * L.n <= 512 ? 8 : (4 * L.n <= 512 ? 4 : 2);
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
-  L.nbase = 8;
-  const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 2) + 16 +
+  // 4 KB chunks, half per warpgroup ring; more slots only where a tile has
+  // several chunks and the w2 ring can spare the room
+  L.nbase = (L.n > kChunkRows && L.n < 128) ? 8 : 4;
+  const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 3) + 16 +
                     kRowBytes + 8 * kQCap * 16 + 1024 + 64;
   L.stages = (kSmemBudget - fixed) / kW2StageBytes;
   if (L.stages > 12) L.stages = 12;
+  L.stages &= ~1;  // two w2 rings of stages / 2, one per MMA warp
   int off = 0;
   L.emb_off = off;
   off += L.n * kRank * 2;
@@ -111,7 +114,7 @@ TcLayout tc_layout(int rows) {
   L.base_off = off;
   off += L.nbase * kChunkBytes;
   L.bar_off = off;
-  off += 8 * (2 * L.stages + 2 * L.nbase + 2 * L.nacc + 2);
+  off += 8 * (2 * L.stages + 2 * L.nbase + 2 * L.nacc + 3);
   off = (off + 15) & ~15;
   L.row_off = off;
   off += kRowBytes;
@@ -171,7 +174,7 @@ struct Shared {
   uint64_t* tmem_full;   // [nacc]
   uint64_t* tmem_empty;  // [nacc]
   uint64_t* emb_ready;
-  uint64_t* spare;
+  uint64_t* spare;       // [2], one per MMA warp
   unsigned long long* best;
   int64_t* cache_off;
   uint32_t* prefix;
@@ -254,8 +257,8 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
 
 template <bool kHasCap, bool kMultOne>
 __global__ void __launch_bounds__(kThreads, 1)
-step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_base,
-               const TcParams tp) {
+step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_w2_tile,
+               const __grid_constant__ CUtensorMap tmap_base, const TcParams tp) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // The 1024-byte alignment is taken from the runtime address of the array.
   // (A build that instead offset the array by a pad computed from its shared
@@ -328,6 +331,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     }
     ptx::mbar_init(sh.emb_ready, 1);
     ptx::mbar_init(sh.spare, 1);
+    ptx::mbar_init(sh.spare + 1, 1);
     s_abort = 0;
     ptx::fence_mbar_init();
   }
@@ -362,32 +366,51 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
 
   if (warp == 0) {
     // ---------------- w2 producer ----------------
+    // Tile i's stages go to ring (i % 2) of SG = S / 2 slots, consumed by MMA
+    // warp (i % 2): every ring has one consumer taking its slots in order.
     if (lane == 0 && n_tiles > 0) {
       ptx::prefetch_tmap(&tmap_w2);
-      int issued = 0;
-      for (int i = 0; i < n_tiles && !*abort_flag; ++i) {
+      ptx::prefetch_tmap(&tmap_w2_tile);
+      // every step reads the same w2: ask L2 to keep it
+      const uint64_t keep = ptx::make_policy_evict_last();
+      const int SG = S / 2;
+      int issued[2] = {0, 0};
+      bool stop = false;
+      for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
+        const int g = i & 1;
         const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
         const int rows_i = static_cast<int>(v_end - t0 < kTileV ? v_end - t0 : kTileV);
         const int boxes = (rows_i + kUnit - 1) / kUnit;
         for (int kb = 0; kb < kKBlocks; ++kb) {
-          const int j = i * kKBlocks + kb;
-          const int s = j % S;
-          if (!wait(&sh.empty_w2[s], ((j / S) & 1) ^ 1, 1, (i << 16) | j)) break;
+          const int k = issued[g];
+          const int s = g * SG + k % SG;
+          if (!wait(&sh.empty_w2[s], ((k / SG) & 1) ^ 1, 1, (i << 16) | k)) {
+            stop = true;
+            break;
+          }
           ptx::mbar_arrive_expect_tx(&sh.full_w2[s], static_cast<uint32_t>(boxes * kUnit * kKBlock * 2));
-          for (int b = 0; b < boxes; ++b)
-            ptx::tma_load_2d(sh.w2 + s * kW2StageBytes + b * kUnit * 128, &tmap_w2, &sh.full_w2[s],
-                             kb * kKBlock, static_cast<int32_t>(t0 + b * kUnit));
-          issued = j + 1;
+          if (boxes == kTileV / kUnit) {  // a whole tile: one 128-row copy
+            ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes, &tmap_w2_tile, &sh.full_w2[s], kb * kKBlock,
+                                  static_cast<int32_t>(t0), keep);
+          } else {
+            for (int b = 0; b < boxes; ++b)
+              ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes + b * kUnit * 128, &tmap_w2, &sh.full_w2[s],
+                                    kb * kKBlock, static_cast<int32_t>(t0 + b * kUnit), keep);
+          }
+          issued[g] = k + 1;
         }
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
-        for (int j = max(0, issued - S); j < issued; ++j) ptx::mbar_wait(&sh.full_w2[j % S], (j / S) & 1, kWaitLimit);
+        for (int g = 0; g < 2; ++g)
+          for (int k = max(0, issued[g] - SG); k < issued[g]; ++k)
+            ptx::mbar_wait(&sh.full_w2[g * SG + k % SG], (k / SG) & 1, kWaitLimit);
       } else {
         // Producer tail: observe the MMA's release of every stage in flight,
         // so that no tensor-core arrival on this CTA's barriers is still
         // pending when the CTA exits.
-        for (int j = issued; j < issued + S; ++j)
-          if (!wait(&sh.empty_w2[j % S], ((j / S) & 1) ^ 1, 8, j)) break;
+        for (int g = 0; g < 2; ++g)
+          for (int k = issued[g]; k < issued[g] + SG; ++k)
+            if (!wait(&sh.empty_w2[g * SG + k % SG], ((k / SG) & 1) ^ 1, 8, k)) break;
       }
     }
   } else if (warp == 2) {
@@ -397,6 +420,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     // tells adjacent phases apart).
     if (lane == 0 && n_tiles > 0) {
       ptx::prefetch_tmap(&tmap_base);
+      // each base logit is read once: let it leave L2 first
+      const uint64_t stream = ptx::make_policy_evict_first();
       int issued[2] = {0, 0};
       bool stop = false;
       for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
@@ -410,8 +435,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
             break;
           }
           ptx::mbar_arrive_expect_tx(&sh.full_base[s], kChunkBytes);
-          ptx::tma_load_2d(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], static_cast<int32_t>(t0),
-                           c * kChunkRows);
+          ptx::tma_load_2d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], static_cast<int32_t>(t0),
+                                c * kChunkRows, stream);
           issued[g] = k + 1;
         }
       }
@@ -421,9 +446,14 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
             ptx::mbar_wait(&sh.full_base[g * NBG + k % NBG], (k / NBG) & 1, kWaitLimit);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0 && n_tiles > 0) {
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- MMA issuers ----------------
+    // Two warps issue (one instruction stream alone cannot keep up with the
+    // w2 stream at N = 16): warp 1 takes the even tiles, warp 3 the odd ones,
+    // each with its own w2 ring and accumulators b = i % NACC (NACC even).
+    const int g = warp == 1 ? 0 : 1;
+    if (lane == 0 && n_tiles > g) {
+      const int SG = S / 2;
       const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, static_cast<uint32_t>(N));
       // descriptors of stage 0 / K-block 0; a stage is 16 KB (1024 in the
       // descriptor's 16-byte units), a K step of 16 is 32 bytes (2 units)
@@ -432,15 +462,15 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       const uint64_t b_kstep = static_cast<uint64_t>((N * 128) >> 4);
       bool ok = wait(sh.emb_ready, 0, 3, 0);
       ptx::tc_fence_after();
-      for (int i = 0; i < n_tiles && ok; ++i) {
+      int k = 0;  // stages this warp has taken from its ring
+      for (int i = g; i < n_tiles && ok; i += 2) {
         const int b = i % NACC;
         if (!(ok = wait(&sh.tmem_empty[b], ((i / NACC) & 1) ^ 1, 4, i << 16))) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(b * N);
-        for (int kb = 0; kb < kKBlocks && ok; ++kb) {
-          const int j = i * kKBlocks + kb;
-          const int s = j % S;
-          if (!(ok = wait(&sh.full_w2[s], (j / S) & 1, 5, (i << 16) | j))) break;
+        for (int kb = 0; kb < kKBlocks && ok; ++kb, ++k) {
+          const int s = g * SG + k % SG;
+          if (!(ok = wait(&sh.full_w2[s], (k / SG) & 1, 5, (i << 16) | k))) break;
           ptx::tc_fence_after();
           const uint64_t a = a0 + static_cast<uint64_t>(s * (kW2StageBytes >> 4));
           const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
@@ -456,8 +486,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         if (ok) ptx::mma_commit(&sh.tmem_full[b]);
       }
       // every MMA this thread issued has completed before TMEM is freed
-      ptx::mma_commit(sh.spare);
-      ptx::mbar_wait(sh.spare, 0, kWaitLimit);
+      ptx::mma_commit(sh.spare + g);
+      ptx::mbar_wait(sh.spare + g, 0, kWaitLimit);
     }
   } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue ----------------
@@ -683,8 +713,9 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
 #pragma unroll
           for (int q2 = 0; q2 < R / 2; ++q2) {
             const longlong2 co = lds_ll2(sh.cache_off + r0 + 2 * q2);
-            if (gm & (1u << (2 * q2))) p.cache[co.x + v] = static_cast<uint16_t>(cb[2 * q2]);
-            if (gm & (2u << (2 * q2))) p.cache[co.y + v] = static_cast<uint16_t>(cb[2 * q2 + 1]);
+            // streaming stores: the cache is not read back by the loop
+            if (gm & (1u << (2 * q2))) __stcs(p.cache + co.x + v, static_cast<unsigned short>(cb[2 * q2]));
+            if (gm & (2u << (2 * q2))) __stcs(p.cache + co.y + v, static_cast<unsigned short>(cb[2 * q2 + 1]));
           }
           if (p.bias_out) {
 #pragma unroll
@@ -789,12 +820,12 @@ const float* least_noise_table() {
   return t;
 }
 
-bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab) {
+bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRank), static_cast<cuuint64_t>(vocab)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRank * 2)};
-  const cuuint32_t box[2] = {kKBlock, kUnit};
+  const cuuint32_t box[2] = {kKBlock, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w2), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -818,8 +849,8 @@ int tc_step_grid(int64_t vocab, int sm_count) {
   return static_cast<int>(units < sm_count ? units : sm_count);
 }
 
-cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int grid, bool pdl,
-                           cudaStream_t stream) {
+cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
+                           bool pdl, cudaStream_t stream) {
   CUtensorMap base_map;
   if (!encode_base_map(&base_map, p.base, p.vocab, p.rows, p.base_s0)) return cudaErrorInvalidValue;
   const TcLayout L = tc_layout(p.rows);
@@ -851,10 +882,10 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, int g
   cfg.numAttrs = pdl ? 1 : 0;
   const bool cap = p.cap != 0.0f;
   const bool one = p.mult == 1.0f;
-  if (cap && one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, true>, w2_map, base_map, tp);
-  if (cap) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, false>, w2_map, base_map, tp);
-  if (one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, true>, w2_map, base_map, tp);
-  return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, false>, w2_map, base_map, tp);
+  if (cap && one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, true>, w2_map, w2_tile_map, base_map, tp);
+  if (cap) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, false>, w2_map, w2_tile_map, base_map, tp);
+  if (one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, true>, w2_map, w2_tile_map, base_map, tp);
+  return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, false>, w2_map, w2_tile_map, base_map, tp);
 }
 
 }  // namespace dspark
