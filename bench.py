@@ -35,7 +35,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "large16"
+WORKLOAD = "large16"  # the headline configuration; --workload picks another
 METRIC = "µs per 5-step DSpark Markov loop and achieved HBM GB/s vs GB300 peak"
 L2_FLUSH_BYTES = 512 << 20
 
@@ -109,17 +109,26 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def recorded_traffic():
+def recorded_traffic(workload: str):
     """DRAM bytes per step launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+    taken on the current kernel sources and this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("source_digest") != source_digest() or d.get("workload") != WORKLOAD:
+    entry = d.get(workload)
+    if not entry or entry.get("source_digest") != source_digest():
         return None
-    return d.get("dram_bytes_per_launch")
+    return entry.get("dram_bytes_per_launch")
+
+
+def describe(wl) -> str:
+    mc = f", mult {wl.mult:g}" if wl.mult != 1.0 else ""
+    cap = f", cap {wl.cap:g}" if wl.cap else ""
+    temps = sorted(set(float(t) for t in wl.temperature))
+    t = f", t={temps[0]:g}" if len(temps) == 1 else ""
+    return f"{wl.name}: V={wl.vocab}, rank 256, {wl.rows} rows, k={wl.steps}{t}{mc}{cap}"
 
 
 class ClockSampler:
@@ -203,7 +212,7 @@ def run_reference(args, d: Dist):
     from dspark_markov_draft_anchor_gb300 import workloads
     if d.rank != 0:
         return 0
-    wl = workloads.make(WORKLOAD, seed_salt=rank_seed_salt(0))
+    wl = workloads.make(args.workload, seed_salt=rank_seed_salt(0))
     nthreads = os.cpu_count() or 1
     _, one = oracle_sample_us_per_loop(wl, 1, nthreads, 1)  # calibration: one row-step
     budget = 120.0 / max(1, args.steps + args.warmup)
@@ -217,13 +226,13 @@ def run_reference(args, d: Dist):
         times.append(us)
     wall = time.perf_counter() - t_start
     value = statistics.mean(times)
-    sample = (f"1 of {wl.rows} rows x {k} of {wl.steps} steps of {WORKLOAD} per timed step, "
+    sample = (f"1 of {wl.rows} rows x {k} of {wl.steps} steps of {wl.name} per timed step, "
               f"scaled x{wl.rows * wl.steps / k:g} to a full loop")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "us", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: V=163840, rank 256, 16 rows, k=5", "model": "DSpark Markov head (random-init)",
+        "config": {"workload": describe(wl), "model": "DSpark Markov head (random-init)",
                    "global_batch": wl.rows, "seq_len": wl.steps, "parallelism": "cpu oracle"},
         "cpu_baseline": {"value": value, "unit": "us", "cores": nthreads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -244,7 +253,7 @@ def run_native(args, d: Dist):
     torch.cuda.set_device(d.local_rank)
     dev = torch.device("cuda", d.local_rank)
     d.init("nccl")
-    wl = workloads.make(WORKLOAD, seed_salt=rank_seed_salt(d.rank))
+    wl = workloads.make(args.workload, seed_salt=rank_seed_salt(d.rank))
     R, K, V = wl.rows, wl.steps, wl.vocab
 
     def bf16(a):
@@ -272,10 +281,16 @@ def run_native(args, d: Dist):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         ctx.loop(a, stream)
+    # the anchor alone, to take it out of the loop time for the per-step figure
+    anchor_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(anchor_graph, stream=stream):
+        ctx.anchor(a, stream)
     torch.cuda.synchronize()
 
-    def timed_loops(n, per_kernel=False):
-        """n loops, each after an L2 flush; CUDA events on the launch stream."""
+    def timed_loops(n, per_kernel=False, g=None):
+        """n loops (or replays of graph g), each after an L2 flush; CUDA
+        events on the launch stream."""
+        g = graph if g is None else g
         ev = []
         with torch.cuda.stream(stream):
             for _ in range(n):
@@ -292,7 +307,7 @@ def run_native(args, d: Dist):
                 else:
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
-                    graph.replay()
+                    g.replay()
                     e1.record(stream)
                     ev.append((e0, e1))
         return ev
@@ -316,14 +331,21 @@ def run_native(args, d: Dist):
     mean_us = statistics.mean(loop_ms) * 1e3
     mean_us = d.max(mean_us, dev)
 
-    # per-kernel durations of the step kernel (same launches, eager, events
-    # between kernels) for the roofline
+    # The step kernel's average launch duration inside the loop: the graphed
+    # loop less the graphed anchor, over k (CUDA events, L2 flushed before
+    # each replay).  Eager launches with events between kernels (no
+    # programmatic overlap) are kept for reference.
+    na = max(20, min(args.steps, 200))
+    timed_loops(3, g=anchor_graph)
+    eva = timed_loops(na, g=anchor_graph)
+    torch.cuda.synchronize()
+    anchor_us = statistics.mean([e0.elapsed_time(e1) for e0, e1 in eva]) * 1e3
+    step_us = (mean_us - anchor_us) / K
     for _ in range(2):
         timed_loops(1, per_kernel=True)
     evk = timed_loops(max(10, min(args.steps, 50)), per_kernel=True)
     torch.cuda.synchronize()
-    step_ms = [m[s + 2 - 1].elapsed_time(m[s + 2]) for m in evk for s in range(K)]
-    step_us = statistics.mean(step_ms) * 1e3
+    eager_step_us = statistics.mean([m[s + 2 - 1].elapsed_time(m[s + 2]) for m in evk for s in range(K)]) * 1e3
     eager_loop_us = statistics.mean([m[0].elapsed_time(m[K + 1]) for m in evk]) * 1e3
 
     # end to end through the C ABI from pinned host buffers
@@ -370,16 +392,19 @@ def run_native(args, d: Dist):
             "metric": METRIC, "value": mean_us, "unit": "us", "n_gpus": d.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_us / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init Markov tables)",
-            "config": {"workload": f"{WORKLOAD}: V=163840, rank 256, 16 rows, k=5, t=1, Zipf spikes",
+            "config": {"workload": describe(wl),
                        "model": "DSpark Markov head (random-init w1/w2 BF16)", "global_batch": R * d.world,
                        "seq_len": K, "parallelism": f"replicas x{d.world} (rows sharded, no collective)",
                        "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed loop",
                        "graph": True, "pdl": True, "bias_path": ["fma", "tcgen05"][ctx.bias_path(R)]},
-            "loop_us": {"mean": mean_us, "p10": qs[0], "p50": qs[1], "p90": qs[2], "eager_with_events": eager_loop_us},
+            "loop_us": {"mean": mean_us, "p10": qs[0], "p50": qs[1], "p90": qs[2], "anchor": anchor_us,
+                        "eager_with_events": eager_loop_us},
             "gbs_loop": algo * K / (mean_us * 1e-6) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": recorded_traffic(), "peak_kind": f"{peak_kind} hbm_gbs",
-                         "kernel": "markov_step", "kernel_us": step_us, "algorithmic_bytes": algo},
+                         "frac": achieved / peak, "traffic": recorded_traffic(wl.name), "peak_kind": f"{peak_kind} hbm_gbs",
+                         "kernel": "markov_step", "kernel_us": step_us, "kernel_us_eager": eager_step_us,
+                         "kernel_us_from": "(graphed loop - graphed anchor) / k, CUDA events, L2 flushed",
+                         "algorithmic_bytes": algo},
             "cpu_baseline": None if cpu_us is None else {
                 "value": cpu_us, "unit": "us", "cores": cores, "kind": "oracle",
                 "sample": f"rows 0..{args.cpu_rows - 1} of {R} x {K} steps ({cpu_s:.1f} s wall), scaled x{R / args.cpu_rows:g}"},
@@ -402,6 +427,8 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--cpu-rows", type=int, default=4)
+    p.add_argument("--workload", default=WORKLOAD,
+                   help="named synthetic workload (large16 is the headline; others for reports and profiles)")
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     args = p.parse_args(argv)
     d = Dist()

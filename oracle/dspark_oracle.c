@@ -23,7 +23,7 @@
  * that every float expression below is one IEEE binary32 operation rounded
  * to nearest even, and fmaf() is the fused multiply-add.
  *
- * Readings of points the pages leave open (each also listed in the design doc):
+ * Readings of points the pages leave open:
  *   - the MurmurHash3 block step (_MURMUR_MIX, not printed) is the published
  *     MurmurHash3_x86_32 block mix; the printed tail fixes the finaliser;
  *   - logf/tanhf are the library's own functions (below), because the pages'
