@@ -58,7 +58,8 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kQCap = 64;  // entries of a warp's key-evaluation queue
-constexpr int kGTab = 48;  // noise-bound table entries (clz 0..32, padded)
+constexpr int kUbT = 296;  // noise upper bounds: 256 by the hash's top byte, then 33 by clz (padded)
+constexpr int kLbT = 256;  // noise lower bounds by the hash's top byte
 
 struct TcLayout {
   int n;         // MMA N: rows padded to 16
@@ -87,8 +88,8 @@ constexpr int kRowTemp = kRowNs + 4 * kMaxRows;        // f32 temperature
 constexpr int kRowThr = kRowTemp + 4 * kMaxRows;       // f32 pruning threshold
 constexpr int kRowGmask = kRowThr + 4 * kMaxRows;      // u32 per 16-row chunk: store bits 0..15, live bits 16..31
 constexpr int kRowGtab = kRowGmask + 4 * (kMaxRows / kChunkRows);  // f32 noise upper bound by clz
-constexpr int kRowLtab = kRowGtab + 4 * kGTab;                     // f32 noise lower bound by clz
-constexpr int kRowBytes = kRowLtab + 4 * kGTab;
+constexpr int kRowLtab = kRowGtab + 4 * kUbT;                      // f32 noise lower bound by top byte
+constexpr int kRowBytes = kRowLtab + 4 * kLbT;
 
 constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared variables
 
@@ -134,7 +135,6 @@ struct TcParams {
   int32_t tmem_cols;
   int32_t emb_off, w2_off, base_off, bar_off, row_off, queue_off;
   int32_t num_units;  // ceil(V / 32)
-  float ltab[33];     // least noise by clz of the hash (host-computed)
 };
 
 // A warp's queue of elements whose Gumbel key must be evaluated (their exact
@@ -183,10 +183,24 @@ struct Shared {
   float* temp;
   float* thr;       // per-row pruning threshold: never above the row's maximum key
   uint32_t* gmask;  // per 16-row chunk: rows that store (bits 0..15), rows that exist (16..31)
-  float* gtab;      // (clz + 1) ln 2 + 1e-4 by clz: the noise never exceeds it
-  float* ltab;      // by clz: the computed noise is never below it
+  float* gtab;      // the computed noise never exceeds gtab[noise_ub_index(h)]
+  float* ltab;      // the computed noise is never below ltab[h >> 24]
   Cand* queues;
 };
+
+// Bounds of the noise -L(h) as a function of the hash's top bits (host-computed
+// in double, with margins far above the rounding of the FP32 evaluation):
+// -L(u) = -log(-log(1 - u)) falls as u = RN((h + 0.5) 2^-32) grows.
+//   c_noise_ub[b] for b = h >> 24 >= 1: -L(b / 256); c_noise_ub[256 + c] for
+//   h < 2^24 with c = clz(h): -L(2^-(c+1)) (c = 32: -L(2^-33)).
+//   c_noise_lb[b]: -L((b + 1) / 256), and for b = 255 -L(1 - 2^-33).
+__constant__ float c_noise_ub[kUbT];
+__constant__ float c_noise_lb[kLbT];
+
+__device__ __forceinline__ uint32_t noise_ub_index(uint32_t h) {
+  const uint32_t b = h >> 24;
+  return b != 0u ? b : 256u + static_cast<uint32_t>(__clz(h));
+}
 
 // The Gumbel key of one element, out of line: it is evaluated for few
 // elements, and one copy keeps the kernel's code small.
@@ -523,10 +537,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       sh.thr[r] = thr;
       const uint32_t sb = __ballot_sync(0xFFFFFFFFu, store), lb = __ballot_sync(0xFFFFFFFFu, r < p.rows);
       if ((lane & 15) == 0) sh.gmask[r >> 4] = ((sb >> lane) & 0xFFFFu) | (((lb >> lane) & 0xFFFFu) << 16);
-      if (et < 33) {
-        sh.gtab[et] = __fmaf_rn(__int2float_rn(et + 1), 0.6931472f, 1e-4f);
-        sh.ltab[et] = tp.ltab[et];
-      }
+      for (int t = et; t < kUbT; t += kEpiThreads) sh.gtab[t] = c_noise_ub[t];
+      sh.ltab[et] = c_noise_lb[et];  // kEpiThreads == kLbT
     }
 
     pdl_wait();
@@ -638,7 +650,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         for (int rr = 0; rr < R; ++rr) {
           hv[rr] = murmur_pre(pf[rr], kv);
           qa[rr] = __fmul_rn(lv[rr], __uint_as_float(ri[rr]));
-          const float g = __uint_as_float(lds_u32(sh.gtab + __clz(hv[rr])));
+          const float g = __uint_as_float(lds_u32(sh.gtab + noise_ub_index(hv[rr])));
           bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa[rr]), 0x1p-20f, qa[rr]));
         }
 
@@ -650,7 +662,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
 #pragma unroll
           for (int rr = 0; rr < R; ++rr) {
             if (gm & (0x10000u << rr)) {
-              const float lb = __fmaf_rn(__uint_as_float(nsb[rr]), __uint_as_float(lds_u32(sh.ltab + __clz(hv[rr]))),
+              const float lb = __fmaf_rn(__uint_as_float(nsb[rr]), __uint_as_float(lds_u32(sh.ltab + (hv[rr] >> 24))),
                                          __fmaf_rn(-fabsf(qa[rr]), 0x1p-20f, qa[rr]));
               const uint32_t o = ((live >> rr) & 1u) && lb == lb ? orderable(lb) : 0u;
               const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
@@ -790,11 +802,34 @@ cudaError_t set_attrs() {
   return cudaFuncSetAttribute(step_tc_kernel<C, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_tc_smem());
 }
 
+// -L(u) = -log(-log(1 - u)) in double.
+double neg_log_neg_log1m(double u) { return -log(-log1p(-u)); }
+
+// Fill the noise-bound tables (see c_noise_ub / c_noise_lb).
+cudaError_t upload_noise_tables() {
+  float ub[kUbT], lb[kLbT];
+  const double margin = 1e-3;
+  for (int i = 0; i < kUbT; ++i) ub[i] = 1e30f;  // unused entries
+  for (int b = 1; b < 256; ++b) ub[b] = static_cast<float>(neg_log_neg_log1m(b / 256.0) + margin);
+  for (int c = 8; c <= 32; ++c) {
+    const double u = c == 32 ? 0x1p-33 : ldexp(1.0, -(c + 1));
+    ub[256 + c] = static_cast<float>(neg_log_neg_log1m(u) + margin);
+  }
+  for (int b = 0; b < 256; ++b) {
+    const double u = b == 255 ? 1.0 - 0x1p-33 : (b + 1) / 256.0;
+    lb[b] = static_cast<float>(neg_log_neg_log1m(u) - margin);
+  }
+  cudaError_t e = cudaMemcpyToSymbol(c_noise_ub, ub, sizeof(ub));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(c_noise_lb, lb, sizeof(lb));
+}
+
 }  // namespace
 
 cudaError_t setup_step_tc() {
   if (!encode_fn()) return cudaErrorNotSupported;
-  cudaError_t e;
+  cudaError_t e = upload_noise_tables();
+  if (e != cudaSuccess) return e;
   if ((e = set_attrs<false, false>()) != cudaSuccess) return e;
   if ((e = set_attrs<false, true>()) != cudaSuccess) return e;
   if ((e = set_attrs<true, false>()) != cudaSuccess) return e;
@@ -802,23 +837,6 @@ cudaError_t setup_step_tc() {
 }
 
 int tc_smem_bytes(int rows) { return tc_layout(rows).smem; }
-
-// The least noise -L(h) over the hashes with clz(h) = c: -L(u) =
-// -log(-log(1 - u)) falls as u grows, and with clz(h) = c the noise's u is at
-// most 2^-c (c = 32: 2^-33; c = 0: 1 - 2^-33).  Less a margin far above the
-// rounding of its FP32 evaluation.
-const float* least_noise_table() {
-  static float t[33];
-  static bool done = false;
-  if (!done) {
-    for (int c = 0; c <= 32; ++c) {
-      const double um = c == 0 ? 1.0 - 0x1p-33 : (c == 32 ? 0x1p-33 : ldexp(1.0, -c));
-      t[c] = static_cast<float>(-log(-log1p(-um)) - 1e-3);
-    }
-    done = true;
-  }
-  return t;
-}
 
 bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab, int box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -868,8 +886,7 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
   tp.row_off = L.row_off;
   tp.queue_off = L.queue_off;
   tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
-  const float* lt = least_noise_table();
-  for (int c = 0; c <= 32; ++c) tp.ltab[c] = lt[c];
+
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
