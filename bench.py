@@ -409,7 +409,7 @@ def run_native(args, d: Dist):
                 "value": cpu_us, "unit": "us", "cores": cores, "kind": "oracle",
                 "sample": f"rows 0..{args.cpu_rows - 1} of {R} x {K} steps ({cpu_s:.1f} s wall), scaled x{R / args.cpu_rows:g}"},
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * (1 + K),
+            "gpu_launches": args.steps * ctx.loop_kernels(a),
             "clocks": clock_info,
             "wall_timed_s": t_wall,
         }

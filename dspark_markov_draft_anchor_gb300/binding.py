@@ -22,16 +22,17 @@ ERRORS = {
 FLAG_PDL = 0x1
 FLAG_FORCE_FMA = 0x2
 FLAG_FORCE_MMA = 0x4
+FLAG_PER_STEP = 0x8
 NOALLOC_MAX_VERIFY_ROWS = 8192  # DSPARK_NOALLOC_MAX_VERIFY_ROWS
 
 EXPORTED = (
     "dspark_markov_init", "dspark_markov_loop", "dspark_markov_anchor", "dspark_markov_step",
-    "dspark_markov_partial_count", "dspark_markov_bias_path", "dspark_markov_get_status",
+    "dspark_markov_partial_count", "dspark_markov_bias_path", "dspark_markov_loop_kernels", "dspark_markov_get_status",
     "dspark_markov_get_status_detail",
     "dspark_markov_destroy", "dspark_build_verify_tokens", "dspark_greedy_accept_scratch_bytes",
     "dspark_greedy_accept", "dspark_greedy_accept_noalloc", "dspark_strerror",
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
-    "dspark_check_logf", "dspark_check_tanhf",
+    "dspark_check_logf", "dspark_check_tanhf", "dspark_noise_bound_tables",
 )
 
 
@@ -87,6 +88,7 @@ def load(build_if_missing: bool = False):
         "dspark_markov_step": (ctypes.c_int, [P, ctypes.POINTER(LoopArgs), i32, P]),
         "dspark_markov_partial_count": (i32, [P]),
         "dspark_markov_bias_path": (i32, [P, i32]),
+        "dspark_markov_loop_kernels": (i32, [P, ctypes.POINTER(LoopArgs)]),
         "dspark_markov_get_status": (ctypes.c_int, [P, P, ctypes.POINTER(i32)]),
         "dspark_markov_get_status_detail": (ctypes.c_int, [P, P, ctypes.POINTER(i32)]),
         "dspark_markov_destroy": (None, [P]),
@@ -101,6 +103,7 @@ def load(build_if_missing: bool = False):
         "dspark_check_key": (ctypes.c_int, [P, ctypes.c_float, P, P, i64, P]),
         "dspark_check_logf": (ctypes.c_int, [P, P, i64, P]),
         "dspark_check_tanhf": (ctypes.c_int, [P, P, i64, P]),
+        "dspark_noise_bound_tables": (ctypes.c_int, [P, P, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -174,6 +177,10 @@ def dspark_markov_bias_path(ctx, rows: int) -> int:
     return int(load().dspark_markov_bias_path(ctx, rows))
 
 
+def dspark_markov_loop_kernels(ctx, args: LoopArgs) -> int:
+    return int(load().dspark_markov_loop_kernels(ctx, ctypes.byref(args)))
+
+
 def dspark_markov_get_status(ctx, stream=None) -> int:
     st = ctypes.c_int32(0)
     _check(load().dspark_markov_get_status(ctx, _stream(stream), ctypes.byref(st)), "dspark_markov_get_status")
@@ -238,6 +245,16 @@ def dspark_check_tanhf(x, y, n, stream=None):
     _check(load().dspark_check_tanhf(_ptr(x), _ptr(y), n, _stream(stream)), "dspark_check_tanhf")
 
 
+def dspark_noise_bound_tables(n: int = 528):
+    """The step kernel's noise bounds (host code): (ub, lb) float32 arrays."""
+    ub = (ctypes.c_float * n)()
+    lb = (ctypes.c_float * n)()
+    rc = load().dspark_noise_bound_tables(ub, lb, n)
+    if rc < 0:
+        _check(rc, "dspark_noise_bound_tables")
+    return list(ub)[:rc], list(lb)[:rc]
+
+
 # --------------------------------------------------------------------------
 # torch convenience: one context over device tables, loop args from tensors
 # --------------------------------------------------------------------------
@@ -287,6 +304,9 @@ class MarkovContext:
 
     def bias_path(self, rows: int) -> int:
         return dspark_markov_bias_path(self.ctx, rows)
+
+    def loop_kernels(self, args: LoopArgs) -> int:
+        return dspark_markov_loop_kernels(self.ctx, args)
 
     def status(self, stream=None) -> int:
         return dspark_markov_get_status(self.ctx, stream)

@@ -16,11 +16,12 @@ struct dspark_markov_ctx {
   const uint16_t* w1;
   const uint16_t* w2;
   unsigned long long* slots;  // [(max_steps + 1) * max_rows] packed argmax slots
-  unsigned int* counters;     // [max_steps] arrival counters
+  unsigned int* counters;     // [max_steps] arrival counters, then the loop's abort word
   int* status;                // device status word
   int grid_simple;
   int grid_tc;
   bool tc_ok;                 // tensor-core step available (tensor map encoded)
+  bool fused_ok;              // the tensor-core kernel may run several steps in one cooperative launch
   CUtensorMap w2_map;         // TMA map over w2: boxes of 32 rows x 64 K, 128-byte swizzle
   CUtensorMap w2_tile_map;    // the same with boxes of 128 rows (whole vocabulary tiles)
 };
@@ -89,6 +90,11 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.salt = a->salt;
   p.finish = 1;
   p.write_prev = 0;
+  p.step_end = step + 1;
+  p.base_s1 = a->base_s1;
+  p.cache_s1 = a->cache_s1;
+  p.slots_s = mr;
+  p.abort_word = ctx->counters + ctx->cfg.max_steps;
   return p;
 }
 
@@ -144,13 +150,13 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   ctx->w2 = static_cast<const uint16_t*>(w2_bf16);
   const size_t nslots = static_cast<size_t>(cfg->max_steps + 1) * cfg->max_rows;
   if (cudaMalloc(&ctx->slots, nslots * sizeof(unsigned long long)) != cudaSuccess ||
-      cudaMalloc(&ctx->counters, cfg->max_steps * sizeof(unsigned int)) != cudaSuccess ||
+      cudaMalloc(&ctx->counters, (cfg->max_steps + 1) * sizeof(unsigned int)) != cudaSuccess ||
       cudaMalloc(&ctx->status, 4 * sizeof(int)) != cudaSuccess) {
     dspark_markov_destroy(ctx);
     return DSPARK_ERR_CUDA;
   }
   if (cudaMemsetAsync(ctx->slots, 0, nslots * sizeof(unsigned long long), stream) != cudaSuccess ||
-      cudaMemsetAsync(ctx->counters, 0, cfg->max_steps * sizeof(unsigned int), stream) != cudaSuccess ||
+      cudaMemsetAsync(ctx->counters, 0, (cfg->max_steps + 1) * sizeof(unsigned int), stream) != cudaSuccess ||
       cudaMemsetAsync(ctx->status, 0, 4 * sizeof(int), stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess) {
     dspark_markov_destroy(ctx);
@@ -160,6 +166,7 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   ctx->grid_tc = dspark::tc_step_grid(cfg->vocab, sms);
   ctx->tc_ok = tc_setup && dspark::encode_w2_map(&ctx->w2_map, w2_bf16, cfg->vocab, 32) &&
               dspark::encode_w2_map(&ctx->w2_tile_map, w2_bf16, cfg->vocab, 128);
+  ctx->fused_ok = ctx->tc_ok && dspark::tc_cooperative_ok(ctx->grid_tc);
   *out = ctx;
   return DSPARK_OK;
 }
@@ -186,8 +193,9 @@ int32_t dspark_markov_partial_count(const dspark_markov_ctx* ctx) {
 int dspark_markov_anchor(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
   int rc = check_args(ctx, a);
   if (rc != DSPARK_OK) return rc;
-  if (dspark::launch_anchor(a->input_ids, a->anchor_idx, ctx->slots, ctx->counters, a->rows, a->steps,
-                            ctx->cfg.max_rows, stream) != cudaSuccess)
+  if (dspark::launch_anchor(a->input_ids, a->anchor_idx, ctx->slots, ctx->counters,
+                            ctx->counters + ctx->cfg.max_steps, a->rows, a->steps, ctx->cfg.max_rows,
+                            stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
@@ -207,11 +215,18 @@ int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_
       p.finish = step == a->steps - 1;
       p.write_prev = step > 0;
     }
-    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, stream);
+    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, false, stream);
   } else {
     e = dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream);
   }
   return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// The loop runs as one multi-step launch: tensor-core path, TMA-readable base,
+// several steps, a cooperative launch possible and not switched off.
+bool loop_fused(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
+  return ctx->fused_ok && !(ctx->cfg.flags & DSPARK_FLAG_PER_STEP) && a->steps > 1 &&
+         dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a);
 }
 
 }  // namespace
@@ -224,9 +239,25 @@ int dspark_markov_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
   return launch_step(ctx, a, step, false, stream);
 }
 
+int32_t dspark_markov_loop_kernels(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
+  if (check_args(ctx, a) != DSPARK_OK) return 0;
+  return 1 + (loop_fused(ctx, a) ? 1 : a->steps);
+}
+
 int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
   int rc = dspark_markov_anchor(ctx, a, stream);
   if (rc != DSPARK_OK) return rc;
+  if (loop_fused(ctx, a)) {
+    // every step in one cooperative launch; the last CTA to arrive at the
+    // last step writes its tokens
+    dspark::StepParams p = make_params(ctx, a, 0);
+    p.step_end = a->steps;
+    const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
+    const cudaError_t e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, true, stream);
+    if (e == cudaSuccess) return DSPARK_OK;
+    if (e != cudaErrorInvalidValue) return DSPARK_ERR_CUDA;
+    // the base strides do not form the multi-step tensor map: step by step
+  }
   for (int s = 0; s < a->steps; ++s) {
     rc = launch_step(ctx, a, s, true, stream);
     if (rc != DSPARK_OK) return rc;

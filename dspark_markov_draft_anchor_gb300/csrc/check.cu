@@ -4,6 +4,7 @@
 
 #include "dspark_markov.h"
 #include "dspark_markov_check.h"
+#include "kernels.h"
 #include "markov_math.cuh"
 
 namespace dspark {
@@ -109,6 +110,12 @@ int dspark_check_tanhf(const float* x, float* y, int64_t n, cudaStream_t stream)
   if (n == 0) return DSPARK_OK;
   dspark::tanhf_kernel<<<dspark::grid_for(n), dspark::kThreads, 0, stream>>>(x, y, n);
   return dspark::done();
+}
+
+int dspark_noise_bound_tables(float* ub, float* lb, int32_t n) {
+  if (!ub || !lb || n < dspark::kNoiseBuckets) return DSPARK_ERR_INVALID_ARG;
+  dspark::noise_bound_tables(ub, lb);
+  return dspark::kNoiseBuckets;
 }
 
 }  // extern "C"

@@ -12,7 +12,8 @@ namespace dspark {
 // Anchor: slots_prev row 0 <- the anchor tokens, later step slots and the
 // arrival counters cleared ([P3] anchor_embed, _AnchorKernel).
 cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, unsigned long long* slots,
-                          unsigned int* counters, int rows, int steps, int max_rows, cudaStream_t stream);
+                          unsigned int* counters, unsigned int* abort_word, int rows, int steps, int max_rows,
+                          cudaStream_t stream);
 
 // Simple fused step: one CTA per 128-entry vocabulary tile, FP32 FMA bias.
 int simple_step_grid(int64_t vocab);
@@ -26,7 +27,19 @@ int tc_step_grid(int64_t vocab, int sm_count);
 int tc_smem_bytes(int rows);
 // box_rows: 32 (any tile) or 128 (whole tiles, one copy per stage).
 bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab, int box_rows);
+// Steps p.step .. p.step_end - 1 in one launch; more than one step needs a
+// cooperative launch (its CTAs wait for one another between steps).  Returns
+// cudaErrorInvalidValue, launching nothing, when the base logits' strides
+// cannot form the kernel's tensor map.
 cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
-                           bool pdl, cudaStream_t stream);
+                           bool pdl, bool cooperative, cudaStream_t stream);
+// The grid's CTAs can all be resident at once (a cooperative launch is possible).
+bool tc_cooperative_ok(int grid);
+
+// Bounds of the Gumbel noise -L(h) used to skip elements that cannot win:
+// bucket (clz(h) << 4) | (the 4 bits after h's leading one), h = 0 in bucket
+// 512; ub[b] >= -L(h) >= lb[b] for every h of bucket b (host code, no GPU).
+constexpr int kNoiseBuckets = 33 * 16;
+void noise_bound_tables(float* ub, float* lb);
 
 }  // namespace dspark

@@ -48,6 +48,14 @@ struct StepParams {
   uint32_t salt;
   int32_t finish;      // this launch writes its own tokens (the last CTA to arrive)
   int32_t write_prev;  // CTA 0 writes the previous step's tokens from slots_prev
+  // Several steps in one launch (the tensor-core kernel only): steps
+  // step .. step_end - 1; step j's base, cache, slots and counter are those of
+  // `step` advanced by (j - step) times the strides below.
+  int32_t step_end;
+  int64_t base_s1;
+  int64_t cache_s1;
+  int64_t slots_s;            // elements between consecutive steps' argmax slots
+  unsigned int* abort_word;   // set by a CTA whose bounded wait gave up; cleared by the anchor
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this
@@ -75,19 +83,21 @@ struct RowInfo {
   int64_t cache_off;  // req * cache_s0 (valid rows)
 };
 
-__device__ __forceinline__ RowInfo row_info(const StepParams& p, int r) {
+__device__ __forceinline__ RowInfo row_info(const StepParams& p, int r, int step) {
   RowInfo ri;
-  const int64_t req = p.req_idx ? p.req_idx[static_cast<int64_t>(r) * p.req_s0 + p.step] : r;
+  const int64_t req = p.req_idx ? p.req_idx[static_cast<int64_t>(r) * p.req_s0 + step] : r;
   const bool valid = req >= 0 && req < p.num_req;
   const float temp = valid ? p.temperature[req] : 0.0f;
   const uint64_t seed = valid ? static_cast<uint64_t>(p.seeds[req]) : 0ull;
-  const int64_t pos = p.sample_pos[static_cast<int64_t>(r) * p.pos_s0 + p.step];
-  ri.prefix = murmur_prefix(seed, p.step, pos, p.salt);
+  const int64_t pos = p.sample_pos[static_cast<int64_t>(r) * p.pos_s0 + step];
+  ri.prefix = murmur_prefix(seed, step, pos, p.salt);
   ri.temp = temp;
   ri.valid = valid && p.cache != nullptr;
   ri.pad = 0;
   ri.cache_off = valid ? req * p.cache_s0 : 0;
   return ri;
 }
+
+__device__ __forceinline__ RowInfo row_info(const StepParams& p, int r) { return row_info(p, r, p.step); }
 
 }  // namespace dspark

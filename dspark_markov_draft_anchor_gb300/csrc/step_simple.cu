@@ -26,15 +26,17 @@ constexpr int kW2Pitch = 528;  // bytes per staged w2 row: 512 + 16 (no bank con
 
 __global__ void anchor_kernel(const int32_t* __restrict__ input_ids, const int64_t* __restrict__ anchor_idx,
                               unsigned long long* __restrict__ slots, unsigned int* __restrict__ counters,
-                              int rows, int steps, int max_rows) {
+                              unsigned int* __restrict__ abort_word, int rows, int steps, int max_rows) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < rows) {
     const int32_t token = input_ids[anchor_idx[r]];
     slots[r] = static_cast<unsigned long long>(~static_cast<uint32_t>(token));
     for (int s = 1; s <= steps; ++s) slots[static_cast<int64_t>(s) * max_rows + r] = 0ull;
   }
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
     for (int s = threadIdx.x; s < steps; s += blockDim.x) counters[s] = 0u;
+    if (threadIdx.x == 0) *abort_word = 0u;
+  }
 }
 
 __device__ __forceinline__ void unpack8(const uint4 w, float* f) {
@@ -167,9 +169,10 @@ size_t simple_smem_bytes() {
 }  // namespace
 
 cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, unsigned long long* slots,
-                          unsigned int* counters, int rows, int steps, int max_rows, cudaStream_t stream) {
-  anchor_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(input_ids, anchor_idx, slots, counters, rows, steps,
-                                                         max_rows);
+                          unsigned int* counters, unsigned int* abort_word, int rows, int steps, int max_rows,
+                          cudaStream_t stream) {
+  anchor_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(input_ids, anchor_idx, slots, counters, abort_word, rows,
+                                                         steps, max_rows);
   return cudaGetLastError();
 }
 

@@ -3,26 +3,37 @@
 // One persistent CTA per SM owns a contiguous vocabulary range (whole
 // 32-entry units, the ranges differing by at most one unit) and every request
 // row.  Per 128-entry vocabulary tile:
-//   * warp 0 streams the tile's w2 rows with TMA into a ring of 16 KB
+//   * warp 0 streams the tile's w2 rows with TMA into two rings of 16 KB
 //     stages (128 rows x 64 K, 128-byte swizzle), 4 stages per tile;
-//   * warp 2 streams the tile's base logits with TMA, 8 rows x 128 entries
-//     per 2 KB chunk, into a second ring;
-//   * warp 1 issues tcgen05.mma (M = 128 vocab rows, N = rows padded to 16,
-//     K = 256 in 16 steps of 16) into one of two TMEM accumulators;
-//   * warps 4..11 (two warpgroups, each warp reading its TMEM lane quarter)
-//     load the FP32 dots with tcgen05.ld and run the per-element epilogue of
-//     [P3] _StepKernel.kernel: bias rounded once to BF16, BF16 add,
-//     multiplier, soft cap, cache store, Gumbel key ([P3] _logit, _gumbel).
+//   * warp 2 streams the tile's base logits with TMA, 16 rows x 128 entries
+//     per 4 KB chunk, into two more rings;
+//   * warps 1 and 3 issue tcgen05.mma (M = 128 vocab rows, N = rows padded
+//     to 16, K = 256 in 16 steps of 16) for the even and the odd tiles into
+//     TMEM accumulators;
+//   * warps 4..11 (two warpgroups, even and odd tiles, each warp reading its
+//     TMEM lane quarter) load the FP32 dots with tcgen05.ld and run the
+//     per-element epilogue of [P3] _StepKernel.kernel: bias rounded once to
+//     BF16, BF16 add, multiplier, soft cap, cache store, Gumbel key ([P3]
+//     _logit, _gumbel).
 // The row maxima live in shared memory as packed (orderable key, ~id) words,
 // so any update order gives the total-order winner ([P3] module docstring);
-// one global atomicMax per row and CTA publishes them, and the CTA that
-// arrives last writes the step's tokens ([P3] _finish).
+// one global atomicMax per row and CTA publishes them ([P3] _finish).
 //
-// The Gumbel key of an element is only evaluated when it can win: the
-// noise -L(h) never exceeds (clz(h) + 1) ln 2 (u >= 2^(31 - clz(h) - 32) and
-// -log(1 - u) >= u), so an element whose upper bound l/t + (clz(h)+1) ln 2
-// (with margins for rounding) is below the row's current maximum cannot be
-// the argmax and is skipped.  Skipping never changes the result.
+// One launch runs one step or, as a cooperative launch whose CTAs are all
+// resident, every step of the loop: after a step each CTA publishes its
+// maxima and adds one to the step's arrival counter; once the counter
+// reaches the grid size every CTA reads the step's tokens, gathers their w1
+// rows and goes on.  The producers do not wait at that boundary: w2 (the same
+// range every step) and the next step's base logits keep streaming into the
+// rings.  CTA 0 writes each step's tokens during the next step's gather; the
+// last step's are written by the CTA that arrives last.
+//
+// The Gumbel key of an element is only evaluated when it can win: the noise
+// -L(h) falls as the hash h grows, so h's top byte bounds it above and below
+// (tables computed on the host in double precision, with margins far above
+// the FP32 rounding).  An element whose upper bound l/t + noise bound is below
+// its row's threshold cannot be the argmax and is skipped; a threshold is
+// never above the row's maximum key, so skipping never changes the result.
 //
 // The bias is the previous step's token's w1 row (clamped to the last row)
 // times w2 in FP32, the summation order being the tensor core's; the pages
@@ -31,11 +42,10 @@
 // Programmatic dependent launch: the TMA producers read only inputs written
 // before the loop (w2, base) and start before griddepcontrol.wait, and the
 // epilogue warps read the per-row sampling constants (also inputs) before it;
-// only the previous tokens wait.  Within a loop a step publishes its row
-// maxima and exits; the next step's CTA 0 writes its tokens, and only the
-// loop's last step lets its last-arriving CTA write them.  All mbarrier waits are bounded; a wait that gives
-// up records DSPARK_ERR_DEVICE_TIMEOUT in the status word and the CTA leaves
-// its loops, waits (bounded) for its copies in flight and frees its TMEM.
+// only the previous tokens wait.  All waits are bounded; a wait that gives up
+// records DSPARK_ERR_DEVICE_TIMEOUT in the status word and raises the loop's
+// abort word (which ends the other CTAs' waits), and the CTA leaves its
+// loops, waits (bounded) for its copies in flight and frees its TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -46,7 +56,7 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;
 constexpr int kTileV = 128;
 constexpr int kUnit = 32;              // vocabulary rows per partition unit / TMA box
 constexpr int kKBlock = 64;            // K per w2 stage (one 128-byte swizzle row)
@@ -55,11 +65,17 @@ constexpr int kW2StageBytes = kTileV * kKBlock * 2;  // 16 KB
 constexpr int kChunkRows = 16;         // base rows per chunk (one epilogue pass)
 constexpr int kChunkBytes = kChunkRows * kTileV * 2;  // 4 KB
 constexpr int kEpiWarp0 = 4;
-constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = 16;          // four quartets: tile parity x half of each chunk's rows
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kHalfRows = kChunkRows / 2;  // rows of a chunk one epilogue warp handles
 constexpr uint32_t kWaitLimit = 1u << 24;
-constexpr int kQCap = 64;  // entries of a warp's key-evaluation queue
-constexpr int kUbT = 296;  // noise upper bounds: 256 by the hash's top byte, then 33 by clz (padded)
-constexpr int kLbT = 256;  // noise lower bounds by the hash's top byte
+constexpr uint64_t kWaitNs = 2000000000ull;  // a role's wait gives up after 2 s
+constexpr uint32_t kSuspendNs = 20000;        // suspend-time hint of one poll
+constexpr uint32_t kGridWaitLimit = 1u << 22;  // polls of a step's arrival counter (about a second)
+// Entries of a warp's key-evaluation queue: a push adds at most 32 to fewer
+// than 32 left after a flush, so 64 never overflows.
+constexpr int kQCap = 64;
+constexpr int kNoiseT = kNoiseBuckets;
 
 struct TcLayout {
   int n;         // MMA N: rows padded to 16
@@ -88,8 +104,8 @@ constexpr int kRowTemp = kRowNs + 4 * kMaxRows;        // f32 temperature
 constexpr int kRowThr = kRowTemp + 4 * kMaxRows;       // f32 pruning threshold
 constexpr int kRowGmask = kRowThr + 4 * kMaxRows;      // u32 per 16-row chunk: store bits 0..15, live bits 16..31
 constexpr int kRowGtab = kRowGmask + 4 * (kMaxRows / kChunkRows);  // f32 noise upper bound by clz
-constexpr int kRowLtab = kRowGtab + 4 * kUbT;                      // f32 noise lower bound by top byte
-constexpr int kRowBytes = kRowLtab + 4 * kLbT;
+constexpr int kRowLtab = kRowGtab + 4 * kNoiseT;                   // f32 noise lower bound by bucket
+constexpr int kRowBytes = kRowLtab + 4 * kNoiseT;
 
 constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared variables
 
@@ -103,7 +119,7 @@ TcLayout tc_layout(int rows) {
   // several chunks and the w2 ring can spare the room
   L.nbase = (L.n > kChunkRows && L.n < 128) ? 8 : 4;
   const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 3) + 16 +
-                    kRowBytes + 8 * kQCap * 16 + 1024 + 64;
+                    kRowBytes + kEpiWarps * kQCap * 16 + 1024 + 64;
   L.stages = (kSmemBudget - fixed) / kW2StageBytes;
   if (L.stages > 12) L.stages = 12;
   L.stages &= ~1;  // two w2 rings of stages / 2, one per MMA warp
@@ -121,7 +137,7 @@ TcLayout tc_layout(int rows) {
   off += kRowBytes;
   off = (off + 15) & ~15;
   L.queue_off = off;
-  off += 8 * kQCap * 16;
+  off += kEpiWarps * kQCap * 16;
   L.smem = off + 1024;  // room to align the base to 1024 bytes
   return L;
 }
@@ -135,6 +151,7 @@ struct TcParams {
   int32_t tmem_cols;
   int32_t emb_off, w2_off, base_off, bar_off, row_off, queue_off;
   int32_t num_units;  // ceil(V / 32)
+  int32_t base_steps_mid;  // base tensor map dims are (vocab, step, row), else (vocab, row, step)
 };
 
 // A warp's queue of elements whose Gumbel key must be evaluated (their exact
@@ -183,42 +200,30 @@ struct Shared {
   float* temp;
   float* thr;       // per-row pruning threshold: never above the row's maximum key
   uint32_t* gmask;  // per 16-row chunk: rows that store (bits 0..15), rows that exist (16..31)
-  float* gtab;      // the computed noise never exceeds gtab[noise_ub_index(h)]
-  float* ltab;      // the computed noise is never below ltab[h >> 24]
+  float* gtab;      // the computed noise never exceeds gtab[noise_index(h)]
+  float* ltab;      // the computed noise is never below ltab[noise_index(h)]
   Cand* queues;
 };
 
-// Bounds of the noise -L(h) as a function of the hash's top bits (host-computed
-// in double, with margins far above the rounding of the FP32 evaluation):
-// -L(u) = -log(-log(1 - u)) falls as u = RN((h + 0.5) 2^-32) grows.
-//   c_noise_ub[b] for b = h >> 24 >= 1: -L(b / 256); c_noise_ub[256 + c] for
-//   h < 2^24 with c = clz(h): -L(2^-(c+1)) (c = 32: -L(2^-33)).
-//   c_noise_lb[b]: -L((b + 1) / 256), and for b = 255 -L(1 - 2^-33).
-__constant__ float c_noise_ub[kUbT];
-__constant__ float c_noise_lb[kLbT];
+// Bounds of the noise -L(h) by bucket of the hash h: h's leading-zero count
+// c and the 4 bits m after its leading one (h = 0 is bucket 512).  -L falls as
+// u = RN((h + 0.5) 2^-32) grows, so a bucket's bounds are the noise at the
+// float u of its smallest and of its largest h, computed on the host in
+// double with a margin (1e-3) far above the FP32 evaluation's error.  Where u
+// < 1/16 (the large noise values that can win) a bucket spans a factor of at
+// most 17/16 in u, so its noise range is about ln(17/16) = 0.06 wide.
+__constant__ float c_noise_ub[kNoiseT];
+__constant__ float c_noise_lb[kNoiseT];
 
-__device__ __forceinline__ uint32_t noise_ub_index(uint32_t h) {
-  const uint32_t b = h >> 24;
-  return b != 0u ? b : 256u + static_cast<uint32_t>(__clz(h));
+__device__ __forceinline__ uint32_t noise_index(uint32_t h) {
+  const uint32_t c = __clz(h);
+  const uint32_t n = h << (c & 31u);  // leading one at bit 31 (0 for h = 0)
+  return (c << 4) | ((n >> 27) & 15u);
 }
 
 // The Gumbel key of one element, out of line: it is evaluated for few
 // elements, and one copy keeps the kernel's code small.
 __device__ __noinline__ float eval_key(float l, float temp, uint32_t h) { return noised_key(l, temp, h); }
-
-// Murmur3 of the row prefix and the pre-mixed vocabulary word, without the
-// finaliser's last xor-shift h ^= h >> 16, which leaves the top 16 bits and
-// hence clz(h) unchanged.
-__device__ __forceinline__ uint32_t murmur_pre(uint32_t prefix, uint32_t kmixed) {
-  uint32_t h = prefix ^ kmixed;
-  h = __funnelshift_l(h, h, 13);
-  h = (h * 5u + 0xe6546b64u) ^ 16u;
-  h ^= h >> 16;
-  h *= 0x85ebca6bu;
-  h ^= h >> 13;
-  h *= 0xc2b2ae35u;
-  return h;
-}
 
 // Explicit shared-space loads of per-row data, by the runtime shared address
 // (the compiler need not order them against the epilogue's global stores).
@@ -257,8 +262,7 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
     if (static_cast<uint32_t>(lane) < n) {
       const Cand e = q[(head + lane) & (kQCap - 1)];
       const float t = sh.temp[e.r];
-      // the queue holds the hash before its last xor-shift
-      const float key = t != 0.0f ? eval_key(e.l, t, e.h ^ (e.h >> 16)) : e.l;
+      const float key = t != 0.0f ? eval_key(e.l, t, e.h) : e.l;
       const unsigned long long cand = pack_key(key, e.v);
       const unsigned long long old = atomicMax(sh.best + e.r, cand);
       if (cand > old) sh.thr[e.r] = key != key ? INFINITY : key;
@@ -292,6 +296,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   const int NB = tp.nbase;
   const int NBG = NB / 2;  // slots of each warpgroup's base ring
   const int NACC = tp.nacc;
+  const int NA = NACC / 2;  // accumulators of each MMA warp / epilogue warpgroup
+  const int n_steps = p.step_end - p.step;
 
   Shared sh;
   sh.emb = smem + tp.emb_off;
@@ -337,11 +343,11 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     }
     for (int i = 0; i < NB; ++i) {
       ptx::mbar_init(&sh.full_base[i], 1);
-      ptx::mbar_init(&sh.empty_base[i], 4);  // the four warps of the consuming warpgroup
+      ptx::mbar_init(&sh.empty_base[i], 8);  // the eight warps of the consuming quartets
     }
     for (int i = 0; i < NACC; ++i) {
       ptx::mbar_init(&sh.tmem_full[i], 1);
-      ptx::mbar_init(&sh.tmem_empty[i], 4);  // the four warps of the consuming warpgroup
+      ptx::mbar_init(&sh.tmem_empty[i], 8);  // the eight warps of the consuming quartets
     }
     ptx::mbar_init(sh.emb_ready, 1);
     ptx::mbar_init(sh.spare, 1);
@@ -360,28 +366,38 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   volatile int* abort_flag = &s_abort;
 
   // A wait that gives up records where: status[1] = wait site,
-  // status[2] = block, status[3] = tile << 16 | sequence number.
+  // status[2] = block, status[3] = detail (step, tile, sequence number); it
+  // also raises the loop's abort word, which ends the other CTAs' waits for
+  // this one.
   auto give_up = [&](int site, int detail) {
     *abort_flag = 1;
+    atomicExch(p.abort_word, 1u);
     if (atomicCAS(p.status, 0, kStatusTimeout) == 0) {
       p.status[1] = site;
       p.status[2] = static_cast<int>(blockIdx.x);
       p.status[3] = detail;
     }
   };
+  // A bounded wait: polls that may suspend the thread until the phase
+  // completes, up to kWaitNs of the global timer (and at most kWaitLimit
+  // polls); it leaves early once the CTA is aborting.
   auto wait = [&](uint64_t* bar, uint32_t parity, int site, int detail) -> bool {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 0; it < kWaitLimit; ++it) {
-      if (ptx::mbar_try_wait(bar, parity)) return true;
-      if ((it & 63) == 63 && *abort_flag) return false;
+      if (ptx::mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+      if ((it & 15) == 15 && (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitNs)) break;
     }
+    if (*abort_flag) return false;
     give_up(site, detail);
     return false;
   };
 
   if (warp == 0) {
     // ---------------- w2 producer ----------------
-    // Tile i's stages go to ring (i % 2) of SG = S / 2 slots, consumed by MMA
-    // warp (i % 2): every ring has one consumer taking its slots in order.
+    // Every step streams the same w2 range.  Tile i's stages go to ring
+    // (i % 2) of SG = S / 2 slots, consumed by MMA warp (i % 2): every ring has
+    // one consumer taking its slots in order, across steps.
     if (lane == 0 && n_tiles > 0) {
       ptx::prefetch_tmap(&tmap_w2);
       ptx::prefetch_tmap(&tmap_w2_tile);
@@ -390,29 +406,32 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       const int SG = S / 2;
       int issued[2] = {0, 0};
       bool stop = false;
-      for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
-        const int g = i & 1;
-        const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
-        const int rows_i = static_cast<int>(v_end - t0 < kTileV ? v_end - t0 : kTileV);
-        const int boxes = (rows_i + kUnit - 1) / kUnit;
-        for (int kb = 0; kb < kKBlocks; ++kb) {
-          const int k = issued[g];
-          const int s = g * SG + k % SG;
-          if (!wait(&sh.empty_w2[s], ((k / SG) & 1) ^ 1, 1, (i << 16) | k)) {
-            stop = true;
-            break;
+      for (int st = 0; st < n_steps && !stop; ++st) {
+        for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
+          const int g = i & 1;
+          const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
+          const int rows_i = static_cast<int>(v_end - t0 < kTileV ? v_end - t0 : kTileV);
+          const int boxes = (rows_i + kUnit - 1) / kUnit;
+          for (int kb = 0; kb < kKBlocks; ++kb) {
+            const int k = issued[g];
+            const int s = g * SG + k % SG;
+            if (!wait(&sh.empty_w2[s], ((k / SG) & 1) ^ 1, 1, (st << 24) | (i << 12) | (k & 0xFFF))) {
+              stop = true;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&sh.full_w2[s], static_cast<uint32_t>(boxes * kUnit * kKBlock * 2));
+            if (boxes == kTileV / kUnit) {  // a whole tile: one 128-row copy
+              ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes, &tmap_w2_tile, &sh.full_w2[s], kb * kKBlock,
+                                    static_cast<int32_t>(t0), keep);
+            } else {
+              for (int b = 0; b < boxes; ++b)
+                ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes + b * kUnit * 128, &tmap_w2, &sh.full_w2[s],
+                                      kb * kKBlock, static_cast<int32_t>(t0 + b * kUnit), keep);
+            }
+            issued[g] = k + 1;
           }
-          ptx::mbar_arrive_expect_tx(&sh.full_w2[s], static_cast<uint32_t>(boxes * kUnit * kKBlock * 2));
-          if (boxes == kTileV / kUnit) {  // a whole tile: one 128-row copy
-            ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes, &tmap_w2_tile, &sh.full_w2[s], kb * kKBlock,
-                                  static_cast<int32_t>(t0), keep);
-          } else {
-            for (int b = 0; b < boxes; ++b)
-              ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes + b * kUnit * 128, &tmap_w2, &sh.full_w2[s],
-                                    kb * kKBlock, static_cast<int32_t>(t0 + b * kUnit), keep);
-          }
-          issued[g] = k + 1;
         }
+        if (*abort_flag) stop = true;
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
         for (int g = 0; g < 2; ++g)
@@ -431,28 +450,35 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     // ---------------- base producer ----------------
     // Tile i's chunks go to warpgroup (i % 2)'s ring, so that every ring has
     // one consumer that takes its slots in order (an mbarrier's parity only
-    // tells adjacent phases apart).
+    // tells adjacent phases apart).  The tensor map spans the launch's steps.
     if (lane == 0 && n_tiles > 0) {
       ptx::prefetch_tmap(&tmap_base);
       // each base logit is read once: let it leave L2 first
       const uint64_t stream = ptx::make_policy_evict_first();
       int issued[2] = {0, 0};
       bool stop = false;
-      for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
-        const int g = i & 1;
-        const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
-        for (int c = 0; c < chunks; ++c) {
-          const int k = issued[g];
-          const int s = g * NBG + k % NBG;
-          if (!wait(&sh.empty_base[s], ((k / NBG) & 1) ^ 1, 2, (i << 16) | k)) {
-            stop = true;
-            break;
+      for (int st = 0; st < n_steps && !stop; ++st) {
+        for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
+          const int g = i & 1;
+          const int32_t t0 = static_cast<int32_t>(v_begin + static_cast<int64_t>(i) * kTileV);
+          for (int c = 0; c < chunks; ++c) {
+            const int k = issued[g];
+            const int s = g * NBG + k % NBG;
+            if (!wait(&sh.empty_base[s], ((k / NBG) & 1) ^ 1, 2, (st << 24) | (i << 12) | (k & 0xFFF))) {
+              stop = true;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&sh.full_base[s], kChunkBytes);
+            if (tp.base_steps_mid)  // dims (vocab, step, row)
+              ptx::tma_load_3d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], t0, st, c * kChunkRows,
+                                    stream);
+            else  // dims (vocab, row, step)
+              ptx::tma_load_3d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], t0, c * kChunkRows, st,
+                                    stream);
+            issued[g] = k + 1;
           }
-          ptx::mbar_arrive_expect_tx(&sh.full_base[s], kChunkBytes);
-          ptx::tma_load_2d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], static_cast<int32_t>(t0),
-                                c * kChunkRows, stream);
-          issued[g] = k + 1;
         }
+        if (*abort_flag) stop = true;
       }
       if (*abort_flag) {
         for (int g = 0; g < 2; ++g)
@@ -463,8 +489,10 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   } else if (warp == 1 || warp == 3) {
     // ---------------- MMA issuers ----------------
     // Two warps issue (one instruction stream alone cannot keep up with the
-    // w2 stream at N = 16): warp 1 takes the even tiles, warp 3 the odd ones,
-    // each with its own w2 ring and accumulators b = i % NACC (NACC even).
+    // w2 stream at N = 16): in every step warp 1 takes the even tiles, warp 3
+    // the odd ones, each with its own w2 ring and accumulators g, g + 2, ...
+    // (its j-th tile uses accumulator g + 2 (j % NA)).  A step's MMAs start
+    // once the epilogue has written that step's embeddings.
     const int g = warp == 1 ? 0 : 1;
     if (lane == 0 && n_tiles > g) {
       const int SG = S / 2;
@@ -474,30 +502,35 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       const uint64_t a0 = ptx::sw128_desc(ptx::smem_addr(sh.w2), 1024);
       const uint64_t b0 = ptx::sw128_desc(ptx::smem_addr(sh.emb), 1024);
       const uint64_t b_kstep = static_cast<uint64_t>((N * 128) >> 4);
-      bool ok = wait(sh.emb_ready, 0, 3, 0);
-      ptx::tc_fence_after();
+      bool ok = true;
       int k = 0;  // stages this warp has taken from its ring
-      for (int i = g; i < n_tiles && ok; i += 2) {
-        const int b = i % NACC;
-        if (!(ok = wait(&sh.tmem_empty[b], ((i / NACC) & 1) ^ 1, 4, i << 16))) break;
+      int j = 0;  // tiles this warp has issued
+      for (int st = 0; st < n_steps && ok; ++st) {
+        // every step's embeddings, in order (each phase of emb_ready is seen)
+        if (!(ok = wait(sh.emb_ready, st & 1, 3, st << 24))) break;
         ptx::tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(b * N);
-        for (int kb = 0; kb < kKBlocks && ok; ++kb, ++k) {
-          const int s = g * SG + k % SG;
-          if (!(ok = wait(&sh.full_w2[s], (k / SG) & 1, 5, (i << 16) | k))) break;
+        for (int i = g; i < n_tiles && ok; i += 2, ++j) {
+          const int b = g + 2 * (j % NA);
+          if (!(ok = wait(&sh.tmem_empty[b], ((j / NA) & 1) ^ 1, 4, (st << 24) | (i << 12)))) break;
           ptx::tc_fence_after();
-          const uint64_t a = a0 + static_cast<uint64_t>(s * (kW2StageBytes >> 4));
-          const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
-          if (kb == 0)
-            ptx::mma_bf16_c<false>(d, a, bd, idesc);
-          else
-            ptx::mma_bf16_c<true>(d, a, bd, idesc);
-          ptx::mma_bf16_c<true>(d, a + 2, bd + 2, idesc);
-          ptx::mma_bf16_c<true>(d, a + 4, bd + 4, idesc);
-          ptx::mma_bf16_c<true>(d, a + 6, bd + 6, idesc);
-          ptx::mma_commit(&sh.empty_w2[s]);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(b * N);
+          for (int kb = 0; kb < kKBlocks && ok; ++kb, ++k) {
+            const int s = g * SG + k % SG;
+            if (!(ok = wait(&sh.full_w2[s], (k / SG) & 1, 5, (st << 24) | (i << 12) | (k & 0xFFF)))) break;
+            ptx::tc_fence_after();
+            const uint64_t a = a0 + static_cast<uint64_t>(s * (kW2StageBytes >> 4));
+            const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
+            if (kb == 0)
+              ptx::mma_bf16_c<false>(d, a, bd, idesc);
+            else
+              ptx::mma_bf16_c<true>(d, a, bd, idesc);
+            ptx::mma_bf16_c<true>(d, a + 2, bd + 2, idesc);
+            ptx::mma_bf16_c<true>(d, a + 4, bd + 4, idesc);
+            ptx::mma_bf16_c<true>(d, a + 6, bd + 6, idesc);
+            ptx::mma_commit(&sh.empty_w2[s]);
+          }
+          if (ok) ptx::mma_commit(&sh.tmem_full[b]);
         }
-        if (ok) ptx::mma_commit(&sh.tmem_full[b]);
       }
       // every MMA this thread issued has completed before TMEM is freed
       ptx::mma_commit(sh.spare + g);
@@ -505,26 +538,30 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     }
   } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue ----------------
-    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
-    const int wg = (warp - kEpiWarp0) >> 2;       // warpgroup: takes tiles i = wg, wg + 2, ...
+    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..511
+    const int quartet = (warp - kEpiWarp0) >> 2;
+    const int wg = quartet & 1;                   // takes tiles i = wg, wg + 2, ... of every step
+    const int half = quartet >> 1;                // takes rows 8 half .. 8 half + 7 of every chunk
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
-    // Per-row sampling constants, one thread per row slot (kEpiThreads ==
-    // kMaxRows); slots beyond the rows are never taken.  They are inputs of
-    // the loop, read before the grid dependency resolves.
-    {
+
+    // Per-row sampling constants of relative step st, one thread per row
+    // slot (the first kMaxRows epilogue threads); slots beyond the rows are
+    // never taken.  They are inputs of the loop (no grid dependency).
+    auto row_init = [&](int st) {
+      if (et >= kMaxRows) return;  // whole warps
       const int r = et;
       float thr = INFINITY, rinv = 1.0f, ns = 0.0f, temp = 0.0f;
       uint32_t prefix = 0;
       int64_t coff = 0;
       bool store = false;
       if (r < p.rows) {
-        const RowInfo ri = row_info(p, r);
+        const RowInfo ri = row_info(p, r, p.step + st);
         temp = ri.temp;
         const bool noisy = ri.temp != 0.0f;
         rinv = noisy ? __frcp_rn(ri.temp) : 1.0f;
         ns = noisy ? 1.0f : 0.0f;
         prefix = ri.prefix;
-        coff = ri.cache_off;
+        coff = ri.cache_off + static_cast<int64_t>(st) * p.cache_s1;
         store = ri.valid != 0;
         thr = -INFINITY;
       }
@@ -537,228 +574,279 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       sh.thr[r] = thr;
       const uint32_t sb = __ballot_sync(0xFFFFFFFFu, store), lb = __ballot_sync(0xFFFFFFFFu, r < p.rows);
       if ((lane & 15) == 0) sh.gmask[r >> 4] = ((sb >> lane) & 0xFFFFu) | (((lb >> lane) & 0xFFFFu) << 16);
-      for (int t = et; t < kUbT; t += kEpiThreads) sh.gtab[t] = c_noise_ub[t];
-      sh.ltab[et] = c_noise_lb[et];  // kEpiThreads == kLbT
-    }
+    };
 
-    pdl_wait();
-
-    // Markov embeddings of the previous tokens, in the MMA's B layout:
-    // 4 K-blocks of [N rows x 128 bytes], 128-byte swizzle.
+    // Markov embeddings of relative step st's previous tokens, in the MMA's
+    // B layout: 4 K-blocks of [N rows x 128 bytes], 128-byte swizzle.  CTA 0
+    // writes those tokens as the previous step's output.  Every MMA of the
+    // step before has completed (the epilogue consumed all its tiles).
     const uint64_t last_row = static_cast<uint64_t>(p.w1_rows - 1);
-    for (int idx = et; idx < N * 32; idx += kEpiThreads) {
-      const int r = idx >> 5, ch = idx & 31;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (r < p.rows) {
-        const int64_t tok = slot_token(__ldcg(p.slots_prev + r));
-        const uint64_t row = static_cast<uint64_t>(tok) < last_row ? static_cast<uint64_t>(tok) : last_row;
-        val = ldg_nc_v4(p.w1 + row * kRank + ch * 8);
-        if (p.write_prev && blockIdx.x == 0 && ch == 0)
-          p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + p.step - 1] = tok;
+    auto gather = [&](int st) {
+      const unsigned long long* prev = p.slots_prev + static_cast<int64_t>(st) * p.slots_s;
+      const bool write_prev = blockIdx.x == 0 && (st > 0 || p.write_prev);
+      const int64_t prev_step = static_cast<int64_t>(p.step) + st - 1;
+      for (int idx = et; idx < N * 32; idx += kEpiThreads) {
+        const int r = idx >> 5, ch = idx & 31;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.rows) {
+          const int64_t tok = slot_token(__ldcg(prev + r));
+          const uint64_t row = static_cast<uint64_t>(tok) < last_row ? static_cast<uint64_t>(tok) : last_row;
+          val = ldg_nc_v4(p.w1 + row * kRank + ch * 8);
+          if (write_prev && ch == 0) p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + prev_step] = tok;
+        }
+        const int kb = ch >> 3, c = ch & 7;
+        *reinterpret_cast<uint4*>(sh.emb + kb * N * 128 + r * 128 + ((c ^ (r & 7)) << 4)) = val;
       }
-      const int kb = ch >> 3, c = ch & 7;
-      *reinterpret_cast<uint4*>(sh.emb + kb * N * 128 + r * 128 + ((c ^ (r & 7)) << 4)) = val;
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(1, kEpiThreads);
+      if (et == 0) ptx::mbar_arrive(sh.emb_ready);
+    };
+
+    // All CTAs have published relative step st's row maxima (its arrival
+    // counter reached the grid size).  Every CTA of the cooperative launch is
+    // resident, so the wait ends unless a CTA gave up; the loop's abort word
+    // then ends it early.
+    auto wait_grid = [&](int st) -> bool {
+      const unsigned int* ctr = p.counter + st;
+      for (uint32_t it = 0; it < kGridWaitLimit; ++it) {
+        if (ptx::ld_acquire_gpu(ctr) >= static_cast<uint32_t>(G)) return true;
+        if ((it & 15) == 15 && (*abort_flag || ptx::ld_volatile_global(p.abort_word) != 0u)) {
+          *abort_flag = 1;
+          return false;
+        }
+      }
+      give_up(9, st << 24);
+      return false;
+    };
+
+    row_init(0);
+    for (int t = et; t < kNoiseT; t += kEpiThreads) {
+      sh.gtab[t] = c_noise_ub[t];
+      sh.ltab[t] = c_noise_lb[t];
     }
-    ptx::fence_proxy_async_smem();
-    ptx::named_bar_sync(1, kEpiThreads);
-    if (et == 0) ptx::mbar_arrive(sh.emb_ready);
+    pdl_wait();
+    gather(0);
 
     WarpQueue q;
     q.q = sh.queues + (warp - kEpiWarp0) * kQCap;
-    int taken = 0;  // chunks this warpgroup has taken from its base ring
+    int taken = 0;  // chunks this warp's quartet has taken from its base ring
+    int j = 0;      // tiles this warp's quartet has taken
     const int vr = quarter * 32 + lane;  // this thread's vocabulary row of a tile
-    bool ok = true;
-    for (int i = wg; i < n_tiles && ok; i += 2) {
-      const int b = i % NACC;
-      ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (i / NACC) & 1, 6, i << 16));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const int64_t v = v_begin + static_cast<int64_t>(i) * kTileV + vr;
-      const bool in = v < v_end;
-      const uint32_t kv = murmur_kmix(static_cast<uint32_t>(v));
-      const bool first = i == wg;
-      for (int c = 0; c < chunks && ok; ++c) {
-        const int k = taken++;
-        const int s = wg * NBG + k % NBG;
-        ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (k / NBG) & 1, 7, (i << 16) | k));
+    for (int st = 0; st < n_steps; ++st) {
+      const int step = p.step + st;
+      bool ok = true;
+      for (int i = wg; i < n_tiles && ok; i += 2, ++j) {
+        const int b = wg + 2 * (j % NA);
+        ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (j / NA) & 1, 6, (st << 24) | (i << 12)));
         if (!ok) break;
-        const uint16_t* bs = reinterpret_cast<const uint16_t*>(sh.base + s * kChunkBytes);
-        constexpr int R = kChunkRows;
-        uint32_t bb[R];
+        ptx::tc_fence_after();
+        const int64_t v = v_begin + static_cast<int64_t>(i) * kTileV + vr;
+        const bool in = v < v_end;
+        const uint32_t kv = murmur_kmix(static_cast<uint32_t>(v));
+        const bool first = i == wg;
+        for (int c = 0; c < chunks && ok; ++c) {
+          const int k = taken++;
+          const int s = wg * NBG + k % NBG;
+          ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (k / NBG) & 1, 7, (st << 24) | (i << 12) | (k & 0xFFF)));
+          if (!ok) break;
+          constexpr int R = kHalfRows;
+          const int r0 = c * kChunkRows + half * R;  // this warp's first row of the chunk
+          const uint16_t* bs = reinterpret_cast<const uint16_t*>(sh.base + s * kChunkBytes) + half * R * kTileV;
+          uint32_t bb[R];
 #pragma unroll
-        for (int rr = 0; rr < R; ++rr) bb[rr] = bs[rr * kTileV + vr];
-        uint32_t acc[R];
-        ptx::tmem_ld16_sync(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                static_cast<uint32_t>(b * N + c * kChunkRows),
-                            acc);
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(&sh.empty_base[s]);
-          // the tile's last chunk is in registers: the accumulator is free
-          if (c == chunks - 1) ptx::mbar_arrive(&sh.tmem_empty[b]);
-        }
-
-        // (a) bias rounded to BF16 and the transform, for all rows; with
-        // multiplier 1 and no cap on packed BF16 pairs (x * 1 rounds to the
-        // same BF16, and the BF16 add is the FP32 add rounded once)
-        uint32_t cb[R], biasb[R];
-        float lv[R];
-        if (kMultOne && !kHasCap) {
-#pragma unroll
-          for (int pr = 0; pr < R / 2; ++pr) {
-            const uint32_t bias2 = ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
-            const uint32_t c2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
-            biasb[2 * pr] = bias2 & 0xFFFFu;
-            biasb[2 * pr + 1] = bias2 >> 16;
-            cb[2 * pr] = c2 & 0xFFFFu;
-            cb[2 * pr + 1] = c2 >> 16;
-            lv[2 * pr] = __uint_as_float(c2 << 16);
-            lv[2 * pr + 1] = __uint_as_float(c2 & 0xFFFF0000u);
-          }
-        } else {
-#pragma unroll
-          for (int rr = 0; rr < R; ++rr) {
-            const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
-            biasb[rr] = __bfloat16_as_ushort(b16);
-            cb[rr] = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult, p.inv_cap,
-                                              p.cap, &lv[rr]);
-          }
-        }
-
-        // the chunk's per-row constants, all loaded before any global store
-        const int r0 = c * kChunkRows;
-        uint32_t pf[R], ri[R], nsb[R];
-#pragma unroll
-        for (int q4 = 0; q4 < R / 4; ++q4) {
-          const uint4 a = lds_u4(sh.prefix + r0 + 4 * q4);
-          const uint4 bq = lds_u4(sh.rinv + r0 + 4 * q4);
-          const uint4 cq = lds_u4(sh.ns + r0 + 4 * q4);
-          pf[4 * q4] = a.x; pf[4 * q4 + 1] = a.y; pf[4 * q4 + 2] = a.z; pf[4 * q4 + 3] = a.w;
-          ri[4 * q4] = bq.x; ri[4 * q4 + 1] = bq.y; ri[4 * q4 + 2] = bq.z; ri[4 * q4 + 3] = bq.w;
-          nsb[4 * q4] = cq.x; nsb[4 * q4 + 1] = cq.y; nsb[4 * q4 + 2] = cq.z; nsb[4 * q4 + 3] = cq.w;
-        }
-        const uint32_t gm = lds_u32(sh.gmask + c);
-        const uint32_t live = in ? gm >> 16 : 0u;  // rows of this chunk that exist, this lane in range
-
-        // hash and the exact upper bound of each key: key <= l/t + (clz(h) +
-        // 1) ln 2 with rounding margins; a greedy row's bound is l (plus a
-        // margin), its key l itself
-        float bnd[R], qa[R];
-        uint32_t hv[R];
-#pragma unroll
-        for (int rr = 0; rr < R; ++rr) {
-          hv[rr] = murmur_pre(pf[rr], kv);
-          qa[rr] = __fmul_rn(lv[rr], __uint_as_float(ri[rr]));
-          const float g = __uint_as_float(lds_u32(sh.gtab + noise_ub_index(hv[rr])));
-          bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa[rr]), 0x1p-20f, qa[rr]));
-        }
-
-        // (b) the warpgroup's first tile: raise each row's threshold to the
-        // warp's largest exact lower bound of a key, l/t + (least noise for
-        // clz(h)) with rounding margins; a threshold at or below some key of
-        // this CTA's range never prunes its argmax
-        if (first) {
-#pragma unroll
-          for (int rr = 0; rr < R; ++rr) {
-            if (gm & (0x10000u << rr)) {
-              const float lb = __fmaf_rn(__uint_as_float(nsb[rr]), __uint_as_float(lds_u32(sh.ltab + (hv[rr] >> 24))),
-                                         __fmaf_rn(-fabsf(qa[rr]), 0x1p-20f, qa[rr]));
-              const uint32_t o = ((live >> rr) & 1u) && lb == lb ? orderable(lb) : 0u;
-              const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
-              if (lane == 0 && top != 0u) {
-                const float m = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
-                float* t = sh.thr + r0 + rr;
-                if (m > *reinterpret_cast<volatile float*>(t)) *t = m;
-              }
-            }
-          }
+          for (int rr = 0; rr < R; ++rr) bb[rr] = bs[rr * kTileV + vr];
+          uint32_t acc[R];
+          ptx::tmem_ld8_sync(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(b * N + r0),
+                             acc);
+          ptx::tc_fence_before();
           __syncwarp();
-        }
-
-        // (c) an element whose bound is below its row's threshold cannot be
-        // the argmax; the rest are queued and evaluated 32 at a time
-        uint32_t take = 0;
-#pragma unroll
-        for (int q4 = 0; q4 < R / 4; ++q4) {
-          const float4 th = ld_volatile_f4(sh.thr + r0 + 4 * q4);
-          take |= (bnd[4 * q4] < th.x ? 0u : 1u) << (4 * q4);
-          take |= (bnd[4 * q4 + 1] < th.y ? 0u : 1u) << (4 * q4 + 1);
-          take |= (bnd[4 * q4 + 2] < th.z ? 0u : 1u) << (4 * q4 + 2);
-          take |= (bnd[4 * q4 + 3] < th.w ? 0u : 1u) << (4 * q4 + 3);
-        }
-        take &= live;
-        if (__any_sync(0xFFFFFFFFu, take != 0u)) {
-          // one warp scan places every survivor in the queue when they fit
-          const uint32_t nt = __popc(take);
-          uint32_t incl = nt;
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-            if (lane >= off) incl += y;
+          if (lane == 0) {
+            ptx::mbar_arrive(&sh.empty_base[s]);
+            // the tile's last chunk is in registers: the accumulator is free
+            if (c == chunks - 1) ptx::mbar_arrive(&sh.tmem_empty[b]);
           }
-          const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-          if (q.count + total <= static_cast<uint32_t>(kQCap)) {
-            uint32_t pos = q.head + q.count + incl - nt;
+
+          // (a) bias rounded to BF16 and the transform, for all rows; with
+          // multiplier 1 and no cap on packed BF16 pairs (x * 1 rounds to the
+          // same BF16, and the BF16 add is the FP32 add rounded once)
+          uint32_t cb[R], biasb[R];
+          float lv[R];
+          if (kMultOne && !kHasCap) {
 #pragma unroll
-            for (int rr = 0; rr < R; ++rr)
-              if ((take >> rr) & 1u) {
-                q.q[pos & (kQCap - 1)] = Cand{static_cast<uint32_t>(v), lv[rr], hv[rr], static_cast<uint32_t>(r0 + rr)};
-                ++pos;
-              }
-            q.count += total;
-            q.flush(32, sh);
+            for (int pr = 0; pr < R / 2; ++pr) {
+              const uint32_t bias2 =
+                  ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
+              const uint32_t c2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
+              biasb[2 * pr] = bias2 & 0xFFFFu;
+              biasb[2 * pr + 1] = bias2 >> 16;
+              cb[2 * pr] = c2 & 0xFFFFu;
+              cb[2 * pr + 1] = c2 >> 16;
+              lv[2 * pr] = __uint_as_float(c2 << 16);
+              lv[2 * pr + 1] = __uint_as_float(c2 & 0xFFFF0000u);
+            }
           } else {
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) {
-              const bool t = (take >> rr) & 1u;
-              if (__any_sync(0xFFFFFFFFu, t)) {
-                q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
-                q.flush(32, sh);
+              const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
+              biasb[rr] = __bfloat16_as_ushort(b16);
+              cb[rr] = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult,
+                                                p.inv_cap, p.cap, &lv[rr]);
+            }
+          }
+
+          // the rows' constants, all loaded before any global store
+          uint32_t pf[R], ri[R], nsb[R];
+#pragma unroll
+          for (int q4 = 0; q4 < R / 4; ++q4) {
+            const uint4 a = lds_u4(sh.prefix + r0 + 4 * q4);
+            const uint4 bq = lds_u4(sh.rinv + r0 + 4 * q4);
+            const uint4 cq = lds_u4(sh.ns + r0 + 4 * q4);
+            pf[4 * q4] = a.x; pf[4 * q4 + 1] = a.y; pf[4 * q4 + 2] = a.z; pf[4 * q4 + 3] = a.w;
+            ri[4 * q4] = bq.x; ri[4 * q4 + 1] = bq.y; ri[4 * q4 + 2] = bq.z; ri[4 * q4 + 3] = bq.w;
+            nsb[4 * q4] = cq.x; nsb[4 * q4 + 1] = cq.y; nsb[4 * q4 + 2] = cq.z; nsb[4 * q4 + 3] = cq.w;
+          }
+          const uint32_t gm16 = lds_u32(sh.gmask + c) >> (half * R);
+          const uint32_t gm = (gm16 & 0xFFu) | (gm16 >> 16 & 0xFFu) << 16;  // store bits 0..7, live bits 16..23
+          const uint32_t live = in ? gm >> 16 : 0u;  // this warp's rows that exist, this lane in range
+
+          // hash and the exact upper bound of each key: key <= l/t + (the
+          // noise bound of h's bucket) with rounding margins; a greedy row's
+          // bound is l (plus a margin), its key l itself
+          float bnd[R], qa[R];
+          uint32_t hv[R];
+#pragma unroll
+          for (int rr = 0; rr < R; ++rr) {
+            hv[rr] = murmur_finish_mixed(pf[rr], kv);
+            qa[rr] = __fmul_rn(lv[rr], __uint_as_float(ri[rr]));
+            const float g = __uint_as_float(lds_u32(sh.gtab + noise_index(hv[rr])));
+            bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa[rr]), 0x1p-20f, qa[rr]));
+          }
+
+          // (b) the warpgroup's first tile of the step: raise each row's
+          // threshold to the warp's largest exact lower bound of a key, l/t +
+          // (least noise of h's bucket) with rounding margins; a threshold
+          // at or below some key of this CTA's range never prunes its argmax
+          if (first) {
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+              if (gm & (0x10000u << rr)) {
+                const float lb =
+                    __fmaf_rn(__uint_as_float(nsb[rr]), __uint_as_float(lds_u32(sh.ltab + noise_index(hv[rr]))),
+                              __fmaf_rn(-fabsf(qa[rr]), 0x1p-20f, qa[rr]));
+                const uint32_t o = ((live >> rr) & 1u) && lb == lb ? orderable(lb) : 0u;
+                const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, o);
+                if (lane == 0 && top != 0u) {
+                  const float m = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
+                  float* t = sh.thr + r0 + rr;
+                  if (m > *reinterpret_cast<volatile float*>(t)) *t = m;
+                }
+              }
+            }
+            __syncwarp();
+          }
+
+          // (c) an element whose bound is below its row's threshold cannot be
+          // the argmax; the rest are queued and evaluated 32 at a time
+          uint32_t take = 0;
+#pragma unroll
+          for (int q4 = 0; q4 < R / 4; ++q4) {
+            const float4 th = ld_volatile_f4(sh.thr + r0 + 4 * q4);
+            take |= (bnd[4 * q4] < th.x ? 0u : 1u) << (4 * q4);
+            take |= (bnd[4 * q4 + 1] < th.y ? 0u : 1u) << (4 * q4 + 1);
+            take |= (bnd[4 * q4 + 2] < th.z ? 0u : 1u) << (4 * q4 + 2);
+            take |= (bnd[4 * q4 + 3] < th.w ? 0u : 1u) << (4 * q4 + 3);
+          }
+          take &= live;
+          if (__any_sync(0xFFFFFFFFu, take != 0u)) {
+            // one warp scan places every survivor in the queue when they fit
+            const uint32_t nt = __popc(take);
+            uint32_t incl = nt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+              const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+              if (lane >= off) incl += y;
+            }
+            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            if (q.count + total <= static_cast<uint32_t>(kQCap)) {
+              uint32_t pos = q.head + q.count + incl - nt;
+#pragma unroll
+              for (int rr = 0; rr < R; ++rr)
+                if ((take >> rr) & 1u) {
+                  q.q[pos & (kQCap - 1)] =
+                      Cand{static_cast<uint32_t>(v), lv[rr], hv[rr], static_cast<uint32_t>(r0 + rr)};
+                  ++pos;
+                }
+              q.count += total;
+              q.flush(32, sh);
+            } else {
+#pragma unroll
+              for (int rr = 0; rr < R; ++rr) {
+                const bool t = (take >> rr) & 1u;
+                if (__any_sync(0xFFFFFFFFu, t)) {
+                  q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
+                  q.flush(32, sh);
+                }
               }
             }
           }
-        }
 
-        // (d) cache and bias stores of the chunk
-        if (in) {
+          // (d) cache and bias stores of the chunk
+          if (in) {
 #pragma unroll
-          for (int q2 = 0; q2 < R / 2; ++q2) {
-            const longlong2 co = lds_ll2(sh.cache_off + r0 + 2 * q2);
-            // streaming stores: the cache is not read back by the loop
-            if (gm & (1u << (2 * q2))) __stcs(p.cache + co.x + v, static_cast<unsigned short>(cb[2 * q2]));
-            if (gm & (2u << (2 * q2))) __stcs(p.cache + co.y + v, static_cast<unsigned short>(cb[2 * q2 + 1]));
-          }
-          if (p.bias_out) {
+            for (int q2 = 0; q2 < R / 2; ++q2) {
+              const longlong2 co = lds_ll2(sh.cache_off + r0 + 2 * q2);
+              // streaming stores: the cache is not read back by the loop
+              if (gm & (1u << (2 * q2))) __stcs(p.cache + co.x + v, static_cast<unsigned short>(cb[2 * q2]));
+              if (gm & (2u << (2 * q2))) __stcs(p.cache + co.y + v, static_cast<unsigned short>(cb[2 * q2 + 1]));
+            }
+            if (p.bias_out) {
 #pragma unroll
-            for (int rr = 0; rr < R; ++rr)
-              if (gm & (0x10000u << rr))
-                p.bias_out[(static_cast<int64_t>(r0 + rr) * p.steps + p.step) * p.vocab + v] =
-                    static_cast<uint16_t>(biasb[rr]);
+              for (int rr = 0; rr < R; ++rr)
+                if (gm & (0x10000u << rr))
+                  p.bias_out[(static_cast<int64_t>(r0 + rr) * p.steps + step) * p.vocab + v] =
+                      static_cast<uint16_t>(biasb[rr]);
+            }
           }
         }
       }
-    }
-    q.flush(1, sh);
+      q.flush(1, sh);
 
-    // Publish this CTA's row maxima.  The next step reads them once its grid
-    // dependency resolves; a step that finishes the loop (or runs alone)
-    // lets the CTA that arrives last write the tokens.
-    ptx::named_bar_sync(1, kEpiThreads);
-    if (n_tiles > 0 && !*abort_flag)
-      for (int r = et; r < p.rows; r += kEpiThreads) atomicMax(p.slots_out + r, sh.best[r]);
-    if (p.finish) {
-      __threadfence();
+      // Both warpgroups are done with the step (a wait that gave up anywhere
+      // in the CTA ends the loop here, the same way in every thread).
+      if (ptx::named_bar_or(1, kEpiThreads, *abort_flag != 0)) break;
+      // Publish this CTA's row maxima.  Within a launch the next step waits
+      // until every CTA has published; a launch's last step either leaves its
+      // tokens to the next launch's CTA 0 or (finish) lets the CTA that
+      // arrives last write them.
+      unsigned long long* out = p.slots_out + static_cast<int64_t>(st) * p.slots_s;
+      for (int r = et; r < p.rows; r += kEpiThreads) atomicMax(out + r, sh.best[r]);
+      const bool last = st == n_steps - 1;
+      if (last && !p.finish) break;
+      // the arrival is released after every thread's maxima (the barrier
+      // orders them before the one fence, which is cumulative)
       ptx::named_bar_sync(1, kEpiThreads);
-      if (et == 0) s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
-      ptx::named_bar_sync(1, kEpiThreads);
-      if (s_last) {
+      if (et == 0) {
         __threadfence();
-        for (int r = et; r < p.rows; r += kEpiThreads) {
-          const unsigned long long sv = atomicAdd(p.slots_out + r, 0ull);
-          p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + p.step] = slot_token(sv);
-        }
+        s_last = atomicAdd(p.counter + st, 1u) == static_cast<unsigned int>(G - 1);
       }
+      if (last) {
+        ptx::named_bar_sync(1, kEpiThreads);
+        if (s_last) {
+          __threadfence();
+          for (int r = et; r < p.rows; r += kEpiThreads) {
+            const unsigned long long sv = atomicAdd(out + r, 0ull);
+            p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + step] = slot_token(sv);
+          }
+        }
+        break;
+      }
+      // The next step's row constants (the rows' shared state is free: both
+      // warpgroups are past the barrier) while the other CTAs arrive.
+      row_init(st + 1);
+      const bool arrived = et != 0 || wait_grid(st);
+      if (ptx::named_bar_or(1, kEpiThreads, !arrived || *abort_flag != 0)) break;
+      gather(st + 1);
     }
   }
 
@@ -802,23 +890,49 @@ cudaError_t set_attrs() {
   return cudaFuncSetAttribute(step_tc_kernel<C, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_tc_smem());
 }
 
-// -L(u) = -log(-log(1 - u)) in double.
-double neg_log_neg_log1m(double u) { return -log(-log1p(-u)); }
+// u of hash h as the kernels form it (two FP32 roundings, one of them an fma).
+float noise_u(uint32_t h) {
+  const float lo = (static_cast<float>(h & 0xFFFFu) + 0.5f) * 0x1p-32f;
+  return fmaf(static_cast<float>(h >> 16), 0x1p-16f, lo);
+}
 
-// Fill the noise-bound tables (see c_noise_ub / c_noise_lb).
-cudaError_t upload_noise_tables() {
-  float ub[kUbT], lb[kLbT];
+// -L(u) = -log(-log(1 - u)) in double, with the kernels' clamp of 1 - u at 2^-24.
+double neg_noise_L(float u) {
+  const double om = 1.0 - static_cast<double>(u);
+  const double l1m = om < 0x1p-24 ? log(0x1p-24) : log1p(-static_cast<double>(u));
+  return -log(-l1m);
+}
+
+}  // namespace
+
+void noise_bound_tables(float* ub, float* lb) {
   const double margin = 1e-3;
-  for (int i = 0; i < kUbT; ++i) ub[i] = 1e30f;  // unused entries
-  for (int b = 1; b < 256; ++b) ub[b] = static_cast<float>(neg_log_neg_log1m(b / 256.0) + margin);
-  for (int c = 8; c <= 32; ++c) {
-    const double u = c == 32 ? 0x1p-33 : ldexp(1.0, -(c + 1));
-    ub[256 + c] = static_cast<float>(neg_log_neg_log1m(u) + margin);
+  for (int idx = 0; idx < kNoiseT; ++idx) {
+    const int c = idx >> 4, m = idx & 15;
+    int64_t lo = -1, hi = -1;  // the bucket's hashes [lo, hi]; none if lo < 0
+    if (c == 32) {
+      if (m == 0) lo = hi = 0;
+    } else if (c <= 27) {
+      lo = (int64_t{1} << (31 - c)) + (static_cast<int64_t>(m) << (27 - c));
+      hi = lo + (int64_t{1} << (27 - c)) - 1;
+    } else if (m % (1 << (c - 27)) == 0) {
+      lo = hi = (int64_t{1} << (31 - c)) + (m >> (c - 27));
+    }
+    if (lo < 0) {
+      ub[idx] = lb[idx] = 0.0f;  // never looked up
+      continue;
+    }
+    ub[idx] = static_cast<float>(neg_noise_L(noise_u(static_cast<uint32_t>(lo))) + margin);
+    lb[idx] = static_cast<float>(neg_noise_L(noise_u(static_cast<uint32_t>(hi))) - margin);
   }
-  for (int b = 0; b < 256; ++b) {
-    const double u = b == 255 ? 1.0 - 0x1p-33 : (b + 1) / 256.0;
-    lb[b] = static_cast<float>(neg_log_neg_log1m(u) - margin);
-  }
+}
+
+namespace {
+
+// Fill the kernel's noise-bound tables (see c_noise_ub / c_noise_lb).
+cudaError_t upload_noise_tables() {
+  float ub[kNoiseT], lb[kNoiseT];
+  noise_bound_tables(ub, lb);
   cudaError_t e = cudaMemcpyToSymbol(c_noise_ub, ub, sizeof(ub));
   if (e != cudaSuccess) return e;
   return cudaMemcpyToSymbol(c_noise_lb, lb, sizeof(lb));
@@ -850,14 +964,28 @@ bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab, int box_rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_base_map(CUtensorMap* map, const void* base_step, int64_t vocab, int rows, int64_t base_s0) {
+// Base logits of steps p.step .. p.step_end - 1 as one 3-D tensor: the
+// (vocab, row, step) or (vocab, step, row) order, whichever has increasing
+// strides; boxes of 128 vocabulary entries x 16 rows x 1 step.  A dimension of
+// extent 1 takes the placeholder stride (previous stride x previous extent).
+bool encode_base_map(CUtensorMap* map, const StepParams& p, bool* steps_mid) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(vocab), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(base_s0 * 2)};
-  const cuuint32_t box[2] = {kTileV, kChunkRows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base_step), dims, strides, box, estr,
+  const int64_t nsteps = p.step_end - p.step;
+  const bool mid = nsteps > 1 && p.base_s1 < p.base_s0;
+  const int64_t ext1 = mid ? nsteps : p.rows, ext2 = mid ? p.rows : nsteps;
+  const int64_t row0 = (p.vocab * 2 + 15) / 16 * 16;
+  const int64_t str1 = ext1 > 1 ? 2 * (mid ? p.base_s1 : p.base_s0) : row0;
+  const int64_t str2 = ext2 > 1 ? 2 * (mid ? p.base_s0 : p.base_s1) : str1 * ext1;
+  if (str1 <= 0 || str2 <= 0 || (str1 & 15) || (str2 & 15) || str2 >= (int64_t{1} << 40)) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.vocab), static_cast<cuuint64_t>(ext1),
+                              static_cast<cuuint64_t>(ext2)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(str1), static_cast<cuuint64_t>(str2)};
+  const cuuint32_t box[3] = {kTileV, mid ? 1u : static_cast<cuuint32_t>(kChunkRows),
+                             mid ? static_cast<cuuint32_t>(kChunkRows) : 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  *steps_mid = mid;
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -867,10 +995,30 @@ int tc_step_grid(int64_t vocab, int sm_count) {
   return static_cast<int>(units < sm_count ? units : sm_count);
 }
 
+bool tc_cooperative_ok(int grid) {
+  int dev = 0, coop = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_tc_kernel<false, true>, kThreads,
+                                                    max_tc_smem()) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return coop != 0 && per_sm >= 1 && grid <= per_sm * sms;
+}
+
+namespace {
+// Whether a cooperative launch may also carry programmatic stream
+// serialisation: unknown until the first such launch (1 yes, 0 no, -1 unknown).
+int g_coop_pdl = -1;
+}  // namespace
+
 cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
-                           bool pdl, cudaStream_t stream) {
+                           bool pdl, bool cooperative, cudaStream_t stream) {
   CUtensorMap base_map;
-  if (!encode_base_map(&base_map, p.base, p.vocab, p.rows, p.base_s0)) return cudaErrorInvalidValue;
+  bool steps_mid = false;
+  if (!encode_base_map(&base_map, p, &steps_mid)) return cudaErrorInvalidValue;
   const TcLayout L = tc_layout(p.rows);
   TcParams tp;
   tp.p = p;
@@ -886,23 +1034,45 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
   tp.row_off = L.row_off;
   tp.queue_off = L.queue_off;
   tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
+  tp.base_steps_mid = steps_mid ? 1 : 0;
 
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
   const bool cap = p.cap != 0.0f;
   const bool one = p.mult == 1.0f;
-  if (cap && one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, true>, w2_map, w2_tile_map, base_map, tp);
-  if (cap) return cudaLaunchKernelEx(&cfg, step_tc_kernel<true, false>, w2_map, w2_tile_map, base_map, tp);
-  if (one) return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, true>, w2_map, w2_tile_map, base_map, tp);
-  return cudaLaunchKernelEx(&cfg, step_tc_kernel<false, false>, w2_map, w2_tile_map, base_map, tp);
+  auto kernel = cap ? (one ? step_tc_kernel<true, true> : step_tc_kernel<true, false>)
+                    : (one ? step_tc_kernel<false, true> : step_tc_kernel<false, false>);
+  auto launch = [&](bool with_pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (with_pdl) {
+      attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[n].val.programmaticStreamSerializationAllowed = 1;
+      ++n;
+    }
+    if (cooperative) {
+      attr[n].id = cudaLaunchAttributeCooperative;
+      attr[n].val.cooperative = 1;
+      ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, w2_map, w2_tile_map, base_map, tp);
+  };
+  if (!cooperative || !pdl) return launch(pdl);
+  if (g_coop_pdl != 0) {
+    const cudaError_t e = launch(true);
+    if (e == cudaSuccess || g_coop_pdl == 1) {
+      if (e == cudaSuccess) g_coop_pdl = 1;
+      return e;
+    }
+    (void)cudaGetLastError();
+    g_coop_pdl = 0;
+  }
+  return launch(false);
 }
 
 }  // namespace dspark

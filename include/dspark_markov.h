@@ -55,6 +55,7 @@ extern "C" {
 #define DSPARK_FLAG_PDL 0x1        /* launch steps with programmatic dependent launch */
 #define DSPARK_FLAG_FORCE_FMA 0x2  /* bias on CUDA-core FMA for every row count */
 #define DSPARK_FLAG_FORCE_MMA 0x4  /* bias on tcgen05 tensor cores for every row count */
+#define DSPARK_FLAG_PER_STEP 0x8   /* loop: one launch per step even where one launch could run them all */
 
 /* Opaque context: the Markov tables, the tensor maps over them and the
  * scratch of one loop (per-step argmax slots and arrival counters), sized
@@ -131,14 +132,18 @@ typedef struct {
  * MurmurHash3 noise of (seed, step, position + salt, vocab id), and a
  * total-order argmax (first NaN, else lowest id of the maximum).  The
  * winner is tokens[r, s] and the next step's previous token.
- * Enqueues 1 + steps kernels on `stream`; no host synchronisation.
+ * Enqueues the anchor kernel, then either one launch for all steps (tensor-
+ * core path, steps > 1, TMA-readable base, a cooperative launch possible and
+ * DSPARK_FLAG_PER_STEP not set: its CTAs, all resident at once, wait for one
+ * another between steps with bounded waits) or one launch per step; see
+ * dspark_markov_loop_kernels.  No host synchronisation.
  */
 DSPARK_API int dspark_markov_loop(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args,
                        cudaStream_t stream);
 
 /* dspark_markov_anchor / dspark_markov_step -- the loop's kernels one at a
  * time ([P3] anchor_embed, markov_step): anchor first, then step 0 .. steps-1
- * in order, with the same args.  dspark_markov_loop is exactly this sequence. */
+ * in order, with the same args.  The results equal dspark_markov_loop's. */
 DSPARK_API int dspark_markov_anchor(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args,
                          cudaStream_t stream);
 DSPARK_API int dspark_markov_step(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args, int32_t step,
@@ -151,6 +156,11 @@ DSPARK_API int32_t dspark_markov_partial_count(const dspark_markov_ctx *ctx);
 /* Which bias path a call with `rows` rows takes: 0 = FMA, 1 = tcgen05. */
 DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t rows);
 
+/* The number of kernels dspark_markov_loop enqueues for `args` (2 when one
+ * launch runs every step, else 1 + steps); 0 if the arguments are invalid.
+ * No counterpart in the pages: it tells a caller what a captured loop holds. */
+DSPARK_API int32_t dspark_markov_loop_kernels(const dspark_markov_ctx *ctx, const dspark_markov_loop_args *args);
+
 /* Synchronise `stream`, then read and clear the device status word: 0, or a
  * DSPARK_ERR_* a kernel recorded (a bounded wait that gave up).  Returns
  * DSPARK_OK or DSPARK_ERR_CUDA. */
@@ -159,8 +169,9 @@ DSPARK_API int dspark_markov_get_status(dspark_markov_ctx *ctx, cudaStream_t str
 /* As dspark_markov_get_status, with where a bounded wait gave up:
  * detail[0] = status, detail[1] = wait site (1 w2 slot free, 2 base slot free,
  * 3 embeddings ready, 4 accumulator free, 5 w2 tile landed, 6 accumulator
- * ready, 7 base chunk landed), detail[2] = block, detail[3] = tile << 16 |
- * sequence number.  Reading clears the record. */
+ * ready, 7 base chunk landed, 9 other CTAs' step results), detail[2] = block,
+ * detail[3] = the step within the launch << 24 | tile << 12 | sequence number
+ * (low 12 bits).  Reading clears the record. */
 DSPARK_API int dspark_markov_get_status_detail(dspark_markov_ctx *ctx, cudaStream_t stream, int32_t *detail);
 
 DSPARK_API void dspark_markov_destroy(dspark_markov_ctx *ctx);

@@ -23,6 +23,7 @@ FLAG_SETS = {
     "fma": binding.FLAG_PDL | binding.FLAG_FORCE_FMA,
     "mma": binding.FLAG_PDL | binding.FLAG_FORCE_MMA,
     "nopdl": 0,
+    "mma_per_step": binding.FLAG_PDL | binding.FLAG_FORCE_MMA | binding.FLAG_PER_STEP,
 }
 
 
@@ -169,6 +170,43 @@ def test_graph_replay_matches_eager_and_is_repeatable():
         graph.replay()
         torch.cuda.synchronize()
         assert np.array_equal(tokens.cpu().numpy(), ref)
+
+
+def test_loop_launch_counts():
+    """One launch runs every step on the tensor-core path (cooperative,
+    several steps); the per-step flag, one step or the FMA path launch one
+    kernel per step."""
+    for flags, R, K, want in [(binding.FLAG_PDL, 16, 5, 2), (0, 16, 5, 2), (binding.FLAG_PDL, 16, 1, 2),
+                              (binding.FLAG_PDL | binding.FLAG_PER_STEP, 16, 5, 6),
+                              (binding.FLAG_PDL | binding.FLAG_FORCE_FMA, 16, 5, 6),
+                              (binding.FLAG_PDL | binding.FLAG_FORCE_MMA, 1, 3, 2)]:
+        wl = _small("large16", 4096, R, K, salt=24)
+        g = GpuLoop(wl, flags=flags)
+        cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
+        tokens = torch.zeros((wl.rows, wl.steps), dtype=torch.int64, device="cuda")
+        assert g.ctx.loop_kernels(g.args(cache, tokens)) == want, (flags, R, K)
+        g.ctx.close()
+
+
+def test_fused_loop_with_step_major_base_layout():
+    """Base logits stored [steps, rows, V] (the step stride above the row
+    stride) take the other tensor-map order of the multi-step launch."""
+    wl = _small("large16", 3000 + 24, 24, 3, salt=25)
+    g = GpuLoop(wl, flags=binding.FLAG_PDL | binding.FLAG_FORCE_MMA)
+    base_t = torch.from_numpy(np.ascontiguousarray(wl.base.transpose(1, 0, 2)).view(np.int16)).cuda()
+    cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
+    tokens = torch.full((wl.rows, wl.steps), -9, dtype=torch.int64, device="cuda")
+    bias = torch.empty((wl.rows, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
+    a = g.args(cache, tokens, bias)
+    a.base = base_t.data_ptr()
+    a.base_s0, a.base_s1 = wl.vocab, wl.rows * wl.vocab
+    assert g.ctx.loop_kernels(a) == 2
+    g.ctx.loop(a)
+    torch.cuda.synchronize()
+    assert g.ctx.status() == 0
+    gpu = {"tokens": tokens.cpu().numpy(), "cache": cache.cpu().numpy().view(np.uint16),
+           "bias": bias.cpu().numpy().view(np.uint16)}
+    _fed_parity(wl, gpu)
 
 
 def test_step_by_step_entry_points_equal_loop():
