@@ -3,18 +3,18 @@
 // One persistent CTA per SM owns a contiguous vocabulary range (whole
 // 32-entry units, the ranges differing by at most one unit) and every request
 // row.  Per 128-entry vocabulary tile:
-//   * warp 0 streams the tile's w2 rows with TMA into two rings of 16 KB
-//     stages (128 rows x 64 K, 128-byte swizzle), 4 stages per tile;
-//   * warp 2 streams the tile's base logits with TMA, 16 rows x 128 entries
-//     per 4 KB chunk, into two more rings;
+//   * warps 0 and 2 (even and odd tiles) stream the tile's w2 rows with TMA
+//     into rings of 16 KB stages (128 rows x 64 K, 128-byte swizzle), 4
+//     stages per tile, and then its base logits, 16 rows x 128 entries per
+//     4 KB chunk, into rings of their own;
 //   * warps 1 and 3 issue tcgen05.mma (M = 128 vocab rows, N = rows padded
 //     to 16, K = 256 in 16 steps of 16) for the even and the odd tiles into
 //     TMEM accumulators;
-//   * warps 4..11 (two warpgroups, even and odd tiles, each warp reading its
-//     TMEM lane quarter) load the FP32 dots with tcgen05.ld and run the
-//     per-element epilogue of [P3] _StepKernel.kernel: bias rounded once to
-//     BF16, BF16 add, multiplier, soft cap, cache store, Gumbel key ([P3]
-//     _logit, _gumbel).
+//   * warps 4..19 (four quartets: tile parity x half of each 16-row chunk,
+//     each warp reading its TMEM lane quarter) load the FP32 dots with
+//     tcgen05.ld and run the per-element epilogue of [P3]
+//     _StepKernel.kernel: bias rounded once to BF16, BF16 add, multiplier,
+//     soft cap, cache store, Gumbel key ([P3] _logit, _gumbel).
 // The row maxima live in shared memory as packed (orderable key, ~id) words,
 // so any update order gives the total-order winner ([P3] module docstring);
 // one global atomicMax per row and CTA publishes them ([P3] _finish).
@@ -393,27 +393,35 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     return false;
   };
 
-  if (warp == 0) {
-    // ---------------- w2 producer ----------------
-    // Every step streams the same w2 range.  Tile i's stages go to ring
-    // (i % 2) of SG = S / 2 slots, consumed by MMA warp (i % 2): every ring has
-    // one consumer taking its slots in order, across steps.
-    if (lane == 0 && n_tiles > 0) {
+  if (warp == 0 || warp == 2) {
+    // ---------------- producers ----------------
+    // Warp 0 fills the rings of the even tiles, warp 2 those of the odd ones:
+    // per tile its four w2 stages (ring g of SG = S / 2 slots, consumed by MMA
+    // warp g) and then its base chunks (ring g of NBG slots, consumed by
+    // quartets of parity g).  Every ring has one producer and one consumer
+    // taking its slots in order, across steps (an mbarrier's parity only
+    // tells adjacent phases apart), and neither parity waits for the other.
+    // Every step streams the same w2 range; the tensor map of the base logits
+    // spans the launch's steps.
+    const int g = warp == 0 ? 0 : 1;
+    if (lane == 0 && n_tiles > g) {
       ptx::prefetch_tmap(&tmap_w2);
       ptx::prefetch_tmap(&tmap_w2_tile);
-      // every step reads the same w2: ask L2 to keep it
+      ptx::prefetch_tmap(&tmap_base);
+      // every step reads the same w2: ask L2 to keep it; each base logit is
+      // read once: let it leave L2 first
       const uint64_t keep = ptx::make_policy_evict_last();
+      const uint64_t stream = ptx::make_policy_evict_first();
       const int SG = S / 2;
-      int issued[2] = {0, 0};
+      int issued = 0, issued_b = 0;
       bool stop = false;
       for (int st = 0; st < n_steps && !stop; ++st) {
-        for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
-          const int g = i & 1;
+        for (int i = g; i < n_tiles && !stop && !*abort_flag; i += 2) {
           const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
           const int rows_i = static_cast<int>(v_end - t0 < kTileV ? v_end - t0 : kTileV);
           const int boxes = (rows_i + kUnit - 1) / kUnit;
           for (int kb = 0; kb < kKBlocks; ++kb) {
-            const int k = issued[g];
+            const int k = issued;
             const int s = g * SG + k % SG;
             if (!wait(&sh.empty_w2[s], ((k / SG) & 1) ^ 1, 1, (st << 24) | (i << 12) | (k & 0xFFF))) {
               stop = true;
@@ -424,45 +432,14 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
               ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes, &tmap_w2_tile, &sh.full_w2[s], kb * kKBlock,
                                     static_cast<int32_t>(t0), keep);
             } else {
-              for (int b = 0; b < boxes; ++b)
-                ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes + b * kUnit * 128, &tmap_w2, &sh.full_w2[s],
-                                      kb * kKBlock, static_cast<int32_t>(t0 + b * kUnit), keep);
+              for (int bx = 0; bx < boxes; ++bx)
+                ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes + bx * kUnit * 128, &tmap_w2, &sh.full_w2[s],
+                                      kb * kKBlock, static_cast<int32_t>(t0 + bx * kUnit), keep);
             }
-            issued[g] = k + 1;
+            issued = k + 1;
           }
-        }
-        if (*abort_flag) stop = true;
-      }
-      if (*abort_flag) {  // let copies in flight land before the CTA exits
-        for (int g = 0; g < 2; ++g)
-          for (int k = max(0, issued[g] - SG); k < issued[g]; ++k)
-            ptx::mbar_wait(&sh.full_w2[g * SG + k % SG], (k / SG) & 1, kWaitLimit);
-      } else {
-        // Producer tail: observe the MMA's release of every stage in flight,
-        // so that no tensor-core arrival on this CTA's barriers is still
-        // pending when the CTA exits.
-        for (int g = 0; g < 2; ++g)
-          for (int k = issued[g]; k < issued[g] + SG; ++k)
-            if (!wait(&sh.empty_w2[g * SG + k % SG], ((k / SG) & 1) ^ 1, 8, k)) break;
-      }
-    }
-  } else if (warp == 2) {
-    // ---------------- base producer ----------------
-    // Tile i's chunks go to warpgroup (i % 2)'s ring, so that every ring has
-    // one consumer that takes its slots in order (an mbarrier's parity only
-    // tells adjacent phases apart).  The tensor map spans the launch's steps.
-    if (lane == 0 && n_tiles > 0) {
-      ptx::prefetch_tmap(&tmap_base);
-      // each base logit is read once: let it leave L2 first
-      const uint64_t stream = ptx::make_policy_evict_first();
-      int issued[2] = {0, 0};
-      bool stop = false;
-      for (int st = 0; st < n_steps && !stop; ++st) {
-        for (int i = 0; i < n_tiles && !stop && !*abort_flag; ++i) {
-          const int g = i & 1;
-          const int32_t t0 = static_cast<int32_t>(v_begin + static_cast<int64_t>(i) * kTileV);
-          for (int c = 0; c < chunks; ++c) {
-            const int k = issued[g];
+          for (int c = 0; c < chunks && !stop; ++c) {
+            const int k = issued_b;
             const int s = g * NBG + k % NBG;
             if (!wait(&sh.empty_base[s], ((k / NBG) & 1) ^ 1, 2, (st << 24) | (i << 12) | (k & 0xFFF))) {
               stop = true;
@@ -470,20 +447,27 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
             }
             ptx::mbar_arrive_expect_tx(&sh.full_base[s], kChunkBytes);
             if (tp.base_steps_mid)  // dims (vocab, step, row)
-              ptx::tma_load_3d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], t0, st, c * kChunkRows,
-                                    stream);
+              ptx::tma_load_3d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s],
+                                    static_cast<int32_t>(t0), st, c * kChunkRows, stream);
             else  // dims (vocab, row, step)
-              ptx::tma_load_3d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s], t0, c * kChunkRows, st,
-                                    stream);
-            issued[g] = k + 1;
+              ptx::tma_load_3d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s],
+                                    static_cast<int32_t>(t0), c * kChunkRows, st, stream);
+            issued_b = k + 1;
           }
         }
         if (*abort_flag) stop = true;
       }
-      if (*abort_flag) {
-        for (int g = 0; g < 2; ++g)
-          for (int k = max(0, issued[g] - NBG); k < issued[g]; ++k)
-            ptx::mbar_wait(&sh.full_base[g * NBG + k % NBG], (k / NBG) & 1, kWaitLimit);
+      if (*abort_flag) {  // let copies in flight land before the CTA exits
+        for (int k = max(0, issued - SG); k < issued; ++k)
+          ptx::mbar_wait(&sh.full_w2[g * SG + k % SG], (k / SG) & 1, kWaitLimit);
+        for (int k = max(0, issued_b - NBG); k < issued_b; ++k)
+          ptx::mbar_wait(&sh.full_base[g * NBG + k % NBG], (k / NBG) & 1, kWaitLimit);
+      } else {
+        // Producer tail: observe the MMA's release of every w2 stage in
+        // flight, so that no tensor-core arrival on this CTA's barriers is
+        // still pending when the CTA exits.
+        for (int k = issued; k < issued + SG; ++k)
+          if (!wait(&sh.empty_w2[g * SG + k % SG], ((k / SG) & 1) ^ 1, 8, k)) break;
       }
     }
   } else if (warp == 1 || warp == 3) {
