@@ -267,7 +267,8 @@ def run_native(args, d: Dist):
     seeds, temp = t(wl.seeds), t(wl.temperature)
     cache = torch.zeros((wl.num_req, K, V), dtype=torch.int16, device=dev)
     tokens = torch.zeros((R, K), dtype=torch.int64, device=dev)
-    ctx = binding.MarkovContext(w1, w2, max_rows=R, max_steps=K, flags=binding.FLAG_PDL)
+    flags = binding.FLAG_PDL | {"auto": 0, "fma": binding.FLAG_FORCE_FMA, "mma": binding.FLAG_FORCE_MMA}[args.bias_path]
+    ctx = binding.MarkovContext(w1, w2, max_rows=R, max_steps=K, flags=flags)
     a = binding.loop_args(base=base, cache=cache, input_ids=ids, anchor_idx=anc, sample_pos=pos, seeds=seeds,
                           temperature=temp, tokens=tokens, req_idx=req, mult=wl.mult, cap=wl.cap, salt=wl.salt)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -430,6 +431,8 @@ def main(argv=None):
     p.add_argument("--workload", default=WORKLOAD,
                    help="named synthetic workload (large16 is the headline; others for reports and profiles)")
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    p.add_argument("--bias-path", choices=["auto", "fma", "mma"], default="auto",
+                   help="bias contraction: the library's choice by row count, or forced")
     args = p.parse_args(argv)
     d = Dist()
     if args.impl == "reference":

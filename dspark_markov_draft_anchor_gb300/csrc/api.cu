@@ -30,8 +30,11 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Rows up to which the CUDA-core kernel forms the bias; above, tensor cores.
-constexpr int kFmaMaxRows = 4;
+// Rows up to which the CUDA-core kernel forms the bias by default; above,
+// tensor cores.  Zero: the tensor-core loop is faster at every row count on
+// sm_103a (its MMA pipe idles most of a step, so padding the rows to N = 16
+// costs nothing, and it streams w2 through a pipelined persistent launch).
+constexpr int kFmaMaxRows = 0;
 
 // The TMA-fed kernel reads base rows as tensor tiles: 16-byte aligned rows.
 bool tma_base_ok(const dspark_markov_loop_args* a) {

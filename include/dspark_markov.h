@@ -53,7 +53,7 @@ extern "C" {
 
 /* ---- config flags ------------------------------------------------------ */
 #define DSPARK_FLAG_PDL 0x1        /* launch steps with programmatic dependent launch */
-#define DSPARK_FLAG_FORCE_FMA 0x2  /* bias on CUDA-core FMA for every row count */
+#define DSPARK_FLAG_FORCE_FMA 0x2  /* bias on CUDA-core FMA (one launch per step) for every row count */
 #define DSPARK_FLAG_FORCE_MMA 0x4  /* bias on tcgen05 tensor cores for every row count */
 #define DSPARK_FLAG_PER_STEP 0x8   /* loop: one launch per step even where one launch could run them all */
 
