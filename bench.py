@@ -9,8 +9,9 @@ inputs resident in HBM; L2 is flushed (a 512 MB write) before each timed loop.
 Prints one JSON line (rank 0).
 
 Metric: µs per 5-step loop (lower is better) and achieved HBM GB/s of the
-step kernel against the measured copy bandwidth.  Algorithmic bytes per step
-launch: w2 (V * 256 * 2) + base read (R * V * 2) + cache write (R * V * 2).
+loop kernel against the measured copy bandwidth.  Algorithmic bytes per step:
+w2 (V * 256 * 2) + base read (R * V * 2) + cache write (R * V * 2); one launch
+of the tensor-core loop kernel runs all k steps (else one launch per step).
 
 With N > 1 (torchrun), every rank runs its own 16-row loop on its own seeded
 rows over replicated tables (request rows are independent): weak scaling,
@@ -110,8 +111,9 @@ def measured_peaks():
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per step launch from the committed ncu summary, if it was
-    taken on the current kernel sources and this workload (else None)."""
+    """DRAM bytes per launch of the loop kernel from the committed ncu
+    summary, if it was taken on the current kernel sources and this workload
+    (else None)."""
     path = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
     if not os.path.exists(path):
         return None
@@ -332,16 +334,19 @@ def run_native(args, d: Dist):
     mean_us = statistics.mean(loop_ms) * 1e3
     mean_us = d.max(mean_us, dev)
 
-    # The step kernel's average launch duration inside the loop: the graphed
-    # loop less the graphed anchor, over k (CUDA events, L2 flushed before
-    # each replay).  Eager launches with events between kernels (no
-    # programmatic overlap) are kept for reference.
+    # The loop kernel's average launch duration: the graphed loop less the
+    # graphed anchor (CUDA events, L2 flushed before each replay), over the
+    # launches the loop makes (one for all k steps, or one per step).  Eager
+    # per-step launches with events between kernels are kept for reference.
     na = max(20, min(args.steps, 200))
     timed_loops(3, g=anchor_graph)
     eva = timed_loops(na, g=anchor_graph)
     torch.cuda.synchronize()
     anchor_us = statistics.mean([e0.elapsed_time(e1) for e0, e1 in eva]) * 1e3
+    fused = ctx.loop_kernels(a) == 2
+    launch_steps = K if fused else 1
     step_us = (mean_us - anchor_us) / K
+    kernel_us = step_us * launch_steps
     for _ in range(2):
         timed_loops(1, per_kernel=True)
     evk = timed_loops(max(10, min(args.steps, 50)), per_kernel=True)
@@ -383,7 +388,8 @@ def run_native(args, d: Dist):
     if d.rank == 0:
         peak, peak_kind = measured_peaks()
         algo = algorithmic_bytes_per_step(V, R)
-        achieved = algo / (step_us * 1e-6) / 1e9
+        algo_launch = algo * launch_steps
+        achieved = algo_launch / (kernel_us * 1e-6) / 1e9
         cpu_us, cpu_s = (None, None)
         cores = os.cpu_count() or 1
         if args.cpu_baseline and d.world == 1:
@@ -403,9 +409,11 @@ def run_native(args, d: Dist):
             "gbs_loop": algo * K / (mean_us * 1e-6) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(wl.name), "peak_kind": f"{peak_kind} hbm_gbs",
-                         "kernel": "markov_step", "kernel_us": step_us, "kernel_us_eager": eager_step_us,
-                         "kernel_us_from": "(graphed loop - graphed anchor) / k, CUDA events, L2 flushed",
-                         "algorithmic_bytes": algo},
+                         "kernel": "step_tc_kernel, all k steps in one launch" if fused else "markov step",
+                         "kernel_us": kernel_us, "step_us": step_us, "step_us_eager_per_step_launch": eager_step_us,
+                         "kernel_us_from": "graphed loop - graphed anchor (per launch), CUDA events, L2 flushed",
+                         "algorithmic_bytes": algo_launch, "algorithmic_bytes_per_step": algo,
+                         "steps_per_launch": launch_steps},
             "cpu_baseline": None if cpu_us is None else {
                 "value": cpu_us, "unit": "us", "cores": cores, "kind": "oracle",
                 "sample": f"rows 0..{args.cpu_rows - 1} of {R} x {K} steps ({cpu_s:.1f} s wall), scaled x{R / args.cpu_rows:g}"},
