@@ -23,6 +23,7 @@ FLAG_PDL = 0x1
 FLAG_FORCE_FMA = 0x2
 FLAG_FORCE_MMA = 0x4
 FLAG_PER_STEP = 0x8
+FLAG_SELECT_2LAUNCH = 0x10
 NOALLOC_MAX_VERIFY_ROWS = 8192  # DSPARK_NOALLOC_MAX_VERIFY_ROWS
 
 EXPORTED = (

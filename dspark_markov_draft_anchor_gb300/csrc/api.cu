@@ -17,6 +17,7 @@ struct dspark_markov_ctx {
   const uint16_t* w2;
   unsigned long long* slots;  // [(max_steps + 1) * max_rows] packed argmax slots
   unsigned int* counters;     // [max_steps] arrival counters, then the loop's abort word
+  unsigned long long* partials;  // [max_rows, max grid] per-CTA maxima of the two-launch select
   int* status;                // device status word
   int grid_simple;
   int grid_tc;
@@ -98,6 +99,7 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.cache_s1 = a->cache_s1;
   p.slots_s = mr;
   p.abort_word = ctx->counters + ctx->cfg.max_steps;
+  p.partials = nullptr;
   return p;
 }
 
@@ -170,6 +172,12 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   ctx->tc_ok = tc_setup && dspark::encode_w2_map(&ctx->w2_map, w2_bf16, cfg->vocab, 32) &&
               dspark::encode_w2_map(&ctx->w2_tile_map, w2_bf16, cfg->vocab, 128);
   ctx->fused_ok = ctx->tc_ok && dspark::tc_cooperative_ok(ctx->grid_tc);
+  const int max_grid = ctx->grid_simple > ctx->grid_tc ? ctx->grid_simple : ctx->grid_tc;
+  if (cudaMalloc(&ctx->partials, static_cast<size_t>(cfg->max_rows) * max_grid * sizeof(unsigned long long)) !=
+      cudaSuccess) {
+    dspark_markov_destroy(ctx);
+    return DSPARK_ERR_CUDA;
+  }
   *out = ctx;
   return DSPARK_OK;
 }
@@ -179,6 +187,7 @@ void dspark_markov_destroy(dspark_markov_ctx* ctx) {
   if (ctx->slots) cudaFree(ctx->slots);
   if (ctx->counters) cudaFree(ctx->counters);
   if (ctx->status) cudaFree(ctx->status);
+  if (ctx->partials) cudaFree(ctx->partials);
   free(ctx);
 }
 
@@ -207,28 +216,38 @@ namespace {
 
 // One step launch.  In a loop on the tensor-core path a step leaves its
 // tokens in the argmax slots and the next step's CTA 0 writes them, so that
-// no step but the last waits for a last-arriving CTA.
+// no step but the last waits for a last-arriving CTA.  With the two-launch
+// select the step writes per-CTA maxima and a select launch follows.
 int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_t step, bool in_loop,
                 cudaStream_t stream) {
   dspark::StepParams p = make_params(ctx, a, step);
   const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
+  const bool select = (ctx->cfg.flags & DSPARK_FLAG_SELECT_2LAUNCH) != 0;
+  if (select) p.partials = ctx->partials;
   cudaError_t e;
+  int grid;
   if (dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a)) {
-    if (in_loop) {
+    if (select) {
+      p.finish = 0;
+    } else if (in_loop) {
       p.finish = step == a->steps - 1;
       p.write_prev = step > 0;
     }
-    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, false, stream);
+    grid = ctx->grid_tc;
+    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, grid, pdl, false, stream);
   } else {
+    grid = ctx->grid_simple;
     e = dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream);
   }
+  if (e == cudaSuccess && select)
+    e = dspark::launch_select(ctx->partials, grid, p.slots_out, a->tokens, a->tokens_s0, step, a->rows, pdl, stream);
   return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
 // The loop runs as one multi-step launch: tensor-core path, TMA-readable base,
 // several steps, a cooperative launch possible and not switched off.
 bool loop_fused(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
-  return ctx->fused_ok && !(ctx->cfg.flags & DSPARK_FLAG_PER_STEP) && a->steps > 1 &&
+  return ctx->fused_ok && !(ctx->cfg.flags & (DSPARK_FLAG_PER_STEP | DSPARK_FLAG_SELECT_2LAUNCH)) && a->steps > 1 &&
          dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a);
 }
 
@@ -244,7 +263,8 @@ int dspark_markov_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
 
 int32_t dspark_markov_loop_kernels(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
   if (check_args(ctx, a) != DSPARK_OK) return 0;
-  return 1 + (loop_fused(ctx, a) ? 1 : a->steps);
+  if (loop_fused(ctx, a)) return 2;
+  return 1 + a->steps * ((ctx->cfg.flags & DSPARK_FLAG_SELECT_2LAUNCH) ? 2 : 1);
 }
 
 int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {

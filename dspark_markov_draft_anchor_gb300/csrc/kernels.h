@@ -15,6 +15,11 @@ cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, u
                           unsigned int* counters, unsigned int* abort_word, int rows, int steps, int max_rows,
                           cudaStream_t stream);
 
+// Two-launch select: reduce each row's per-CTA maxima (partials [rows,
+// nparts]) into slots_out and tokens[:, step] (one CTA per row).
+cudaError_t launch_select(const unsigned long long* partials, int nparts, unsigned long long* slots_out,
+                          int64_t* tokens, int64_t tokens_s0, int step, int rows, bool pdl, cudaStream_t stream);
+
 // Simple fused step: one CTA per 128-entry vocabulary tile, FP32 FMA bias.
 int simple_step_grid(int64_t vocab);
 cudaError_t setup_step_simple();

@@ -56,6 +56,10 @@ struct StepParams {
   int64_t cache_s1;
   int64_t slots_s;            // elements between consecutive steps' argmax slots
   unsigned int* abort_word;   // set by a CTA whose bounded wait gave up; cleared by the anchor
+  // Two-launch select: each CTA writes its row maxima to partials[r * grid +
+  // block] and a separate select launch reduces them (null: one atomicMax per
+  // row into slots_out).
+  unsigned long long* partials;
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this

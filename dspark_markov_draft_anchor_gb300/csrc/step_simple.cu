@@ -147,6 +147,11 @@ __global__ void __launch_bounds__(128) step_simple_kernel(const StepParams p) {
     __syncthreads();
   }
 
+  if (p.partials) {  // the select launch reduces the CTAs' maxima
+    for (int r = tid; r < p.rows; r += 128)
+      p.partials[static_cast<int64_t>(r) * gridDim.x + blockIdx.x] = best[r];
+    return;
+  }
   for (int r = tid; r < p.rows; r += 128) atomicMax(p.slots_out + r, best[r]);
   __threadfence();
   __syncthreads();
@@ -158,6 +163,37 @@ __global__ void __launch_bounds__(128) step_simple_kernel(const StepParams p) {
       const unsigned long long sv = atomicAdd(p.slots_out + r, 0ull);
       p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + p.step] = slot_token(sv);
     }
+  }
+}
+
+// Select ([P2] _markov_select_kernel): one CTA per row reduces the row's
+// per-CTA packed maxima under the total order (the u64 maximum: first NaN,
+// else the lowest id of the largest key), then writes the step's token and
+// the next step's previous token.
+__global__ void __launch_bounds__(256) select_kernel(const unsigned long long* __restrict__ partials, int nparts,
+                                                     unsigned long long* __restrict__ slots_out,
+                                                     int64_t* __restrict__ tokens, int64_t tokens_s0, int step) {
+  __shared__ unsigned long long s_warp[8];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r = blockIdx.x;
+  const unsigned long long* row = partials + static_cast<int64_t>(r) * nparts;
+  unsigned long long m = 0ull;
+  for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
+    const unsigned long long x = row[i];
+    m = x > m ? x : m;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+    m = o > m ? o : m;
+  }
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = s_warp[w] > m ? s_warp[w] : m;
+    slots_out[r] = m;
+    tokens[static_cast<int64_t>(r) * tokens_s0 + step] = slot_token(m);
   }
 }
 
@@ -177,6 +213,20 @@ cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, u
 }
 
 int simple_step_grid(int64_t vocab) { return static_cast<int>((vocab + kTile - 1) / kTile); }
+
+cudaError_t launch_select(const unsigned long long* partials, int nparts, unsigned long long* slots_out,
+                          int64_t* tokens, int64_t tokens_s0, int step, int rows, bool pdl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, select_kernel, partials, nparts, slots_out, tokens, tokens_s0, step);
+}
 
 cudaError_t setup_step_simple() {
   const int smem = static_cast<int>(simple_smem_bytes());

@@ -225,6 +225,14 @@ __device__ __forceinline__ uint32_t noise_index(uint32_t h) {
 // elements, and one copy keeps the kernel's code small.
 __device__ __noinline__ float eval_key(float l, float temp, uint32_t h) { return noised_key(l, temp, h); }
 
+// Two-launch select: this CTA's row maxima into partials[r * grid + block]
+// (out of line: it stays out of the register allocation of the hot loop).
+__device__ __noinline__ void store_partials(unsigned long long* partials, const unsigned long long* best, int rows,
+                                            int et) {
+  for (int r = et; r < rows; r += kEpiThreads)
+    partials[static_cast<int64_t>(r) * gridDim.x + blockIdx.x] = best[r];
+}
+
 // Explicit shared-space loads of per-row data, by the runtime shared address
 // (the compiler need not order them against the epilogue's global stores).
 __device__ __forceinline__ uint4 lds_u4(const void* ptr) {
@@ -803,6 +811,10 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       // until every CTA has published; a launch's last step either leaves its
       // tokens to the next launch's CTA 0 or (finish) lets the CTA that
       // arrives last write them.
+      if (p.partials) {  // the select launch reduces the CTAs' maxima (one step per launch)
+        store_partials(p.partials, sh.best, p.rows, et);
+        break;
+      }
       unsigned long long* out = p.slots_out + static_cast<int64_t>(st) * p.slots_s;
       for (int r = et; r < p.rows; r += kEpiThreads) atomicMax(out + r, sh.best[r]);
       const bool last = st == n_steps - 1;

@@ -56,6 +56,10 @@ extern "C" {
 #define DSPARK_FLAG_FORCE_FMA 0x2  /* bias on CUDA-core FMA (one launch per step) for every row count */
 #define DSPARK_FLAG_FORCE_MMA 0x4  /* bias on tcgen05 tensor cores for every row count */
 #define DSPARK_FLAG_PER_STEP 0x8   /* loop: one launch per step even where one launch could run them all */
+#define DSPARK_FLAG_SELECT_2LAUNCH 0x10 /* each step as two launches: the step kernel writes its blocks'
+                                           maxima, a select launch (one CTA per row) reduces them under the
+                                           same total order and writes the token ([P2] _markov_select_kernel);
+                                           implies one launch per step */
 
 /* Opaque context: the Markov tables, the tensor maps over them and the
  * scratch of one loop (per-step argmax slots and arrival counters), sized
@@ -143,7 +147,9 @@ DSPARK_API int dspark_markov_loop(dspark_markov_ctx *ctx, const dspark_markov_lo
 
 /* dspark_markov_anchor / dspark_markov_step -- the loop's kernels one at a
  * time ([P3] anchor_embed, markov_step): anchor first, then step 0 .. steps-1
- * in order, with the same args.  The results equal dspark_markov_loop's. */
+ * in order, with the same args (with DSPARK_FLAG_SELECT_2LAUNCH a step call
+ * enqueues the step and its select launch).  The results equal
+ * dspark_markov_loop's. */
 DSPARK_API int dspark_markov_anchor(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args,
                          cudaStream_t stream);
 DSPARK_API int dspark_markov_step(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args, int32_t step,
@@ -157,7 +163,8 @@ DSPARK_API int32_t dspark_markov_partial_count(const dspark_markov_ctx *ctx);
 DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t rows);
 
 /* The number of kernels dspark_markov_loop enqueues for `args` (2 when one
- * launch runs every step, else 1 + steps); 0 if the arguments are invalid.
+ * launch runs every step, 1 + 2 steps with DSPARK_FLAG_SELECT_2LAUNCH, else
+ * 1 + steps); 0 if the arguments are invalid.
  * No counterpart in the pages: it tells a caller what a captured loop holds. */
 DSPARK_API int32_t dspark_markov_loop_kernels(const dspark_markov_ctx *ctx, const dspark_markov_loop_args *args);
 

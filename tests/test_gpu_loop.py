@@ -24,6 +24,8 @@ FLAG_SETS = {
     "mma": binding.FLAG_PDL | binding.FLAG_FORCE_MMA,
     "nopdl": 0,
     "mma_per_step": binding.FLAG_PDL | binding.FLAG_FORCE_MMA | binding.FLAG_PER_STEP,
+    "select": binding.FLAG_PDL | binding.FLAG_SELECT_2LAUNCH,
+    "fma_select": binding.FLAG_FORCE_FMA | binding.FLAG_SELECT_2LAUNCH,
 }
 
 
@@ -175,11 +177,13 @@ def test_graph_replay_matches_eager_and_is_repeatable():
 def test_loop_launch_counts():
     """One launch runs every step on the tensor-core path (cooperative,
     several steps); the per-step flag, one step or the FMA path launch one
-    kernel per step."""
+    kernel per step, and the two-launch select two."""
     for flags, R, K, want in [(binding.FLAG_PDL, 16, 5, 2), (0, 16, 5, 2), (binding.FLAG_PDL, 16, 1, 2),
                               (binding.FLAG_PDL | binding.FLAG_PER_STEP, 16, 5, 6),
                               (binding.FLAG_PDL | binding.FLAG_FORCE_FMA, 16, 5, 6),
-                              (binding.FLAG_PDL | binding.FLAG_FORCE_MMA, 1, 3, 2)]:
+                              (binding.FLAG_PDL | binding.FLAG_FORCE_MMA, 1, 3, 2),
+                              (binding.FLAG_PDL | binding.FLAG_SELECT_2LAUNCH, 16, 5, 11),
+                              (binding.FLAG_FORCE_FMA | binding.FLAG_SELECT_2LAUNCH, 4, 3, 7)]:
         wl = _small("large16", 4096, R, K, salt=24)
         g = GpuLoop(wl, flags=flags)
         cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
@@ -209,9 +213,10 @@ def test_fused_loop_with_step_major_base_layout():
     _fed_parity(wl, gpu)
 
 
-def test_step_by_step_entry_points_equal_loop():
+@pytest.mark.parametrize("flags", ["default", "select"])
+def test_step_by_step_entry_points_equal_loop(flags):
     wl = _small("tc64", 2000, 8, 3, salt=22)
-    g = GpuLoop(wl)
+    g = GpuLoop(wl, flags=FLAG_SETS[flags])
     ref = g.run()["tokens"]
     cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
     tokens = torch.full((wl.rows, wl.steps), -9, dtype=torch.int64, device="cuda")
