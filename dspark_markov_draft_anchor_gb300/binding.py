@@ -24,6 +24,7 @@ FLAG_FORCE_FMA = 0x2
 FLAG_FORCE_MMA = 0x4
 FLAG_PER_STEP = 0x8
 FLAG_SELECT_2LAUNCH = 0x10
+FLAG_TEST_STALL = 0x100
 NOALLOC_MAX_VERIFY_ROWS = 8192  # DSPARK_NOALLOC_MAX_VERIFY_ROWS
 
 EXPORTED = (

@@ -100,6 +100,7 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.slots_s = mr;
   p.abort_word = ctx->counters + ctx->cfg.max_steps;
   p.partials = nullptr;
+  p.test_stall = (ctx->cfg.flags & DSPARK_FLAG_TEST_STALL) != 0;
   return p;
 }
 

@@ -60,6 +60,7 @@ struct StepParams {
   // block] and a separate select launch reduces them (null: one atomicMax per
   // row into slots_out).
   unsigned long long* partials;
+  int32_t test_stall;  // checking aid (host side: picks the kernel whose first grid wait cannot end)
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this

@@ -69,9 +69,11 @@ constexpr int kEpiWarps = 16;          // four quartets: tile parity x half of e
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kHalfRows = kChunkRows / 2;  // rows of a chunk one epilogue warp handles
 constexpr uint32_t kWaitLimit = 1u << 24;
-constexpr uint64_t kWaitNs = 2000000000ull;  // a role's wait gives up after 2 s
+constexpr uint64_t kWaitNs = 10000000000ull;  // a role's wait gives up after 10 s
 constexpr uint32_t kSuspendNs = 20000;        // suspend-time hint of one poll
-constexpr uint32_t kGridWaitLimit = 1u << 22;  // polls of a step's arrival counter (about a second)
+// Polls of a step's arrival counter before the grid wait gives up (each an L2
+// round trip: a few seconds at most, shorter than the roles' own waits).
+constexpr uint32_t kGridWaitLimit = 1u << 22;
 // Entries of a warp's key-evaluation queue: a push adds at most 32 to fewer
 // than 32 left after a flush, so 64 never overflows.
 constexpr int kQCap = 64;
@@ -281,7 +283,7 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
   __syncwarp();
 }
 
-template <bool kHasCap, bool kMultOne>
+template <bool kHasCap, bool kMultOne, bool kTestStall = false>
 __global__ void __launch_bounds__(kThreads, 1)
 step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_w2_tile,
                const __grid_constant__ CUtensorMap tmap_base, const TcParams tp) {
@@ -600,8 +602,10 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     // then ends it early.
     auto wait_grid = [&](int st) -> bool {
       const unsigned int* ctr = p.counter + st;
+      // (the checking aid waits for one arrival too many at the first boundary)
+      const uint32_t target = static_cast<uint32_t>(G) + (kTestStall && st == 0 ? 1u : 0u);
       for (uint32_t it = 0; it < kGridWaitLimit; ++it) {
-        if (ptx::ld_acquire_gpu(ctr) >= static_cast<uint32_t>(G)) return true;
+        if (ptx::ld_acquire_gpu(ctr) >= target) return true;
         if ((it & 15) == 15 && (*abort_flag || ptx::ld_volatile_global(p.abort_word) != 0u)) {
           *abort_flag = 1;
           return false;
@@ -881,9 +885,9 @@ int max_tc_smem() {
   return m;
 }
 
-template <bool C, bool M>
+template <bool C, bool M, bool T = false>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(step_tc_kernel<C, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_tc_smem());
+  return cudaFuncSetAttribute(step_tc_kernel<C, M, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_tc_smem());
 }
 
 // u of hash h as the kernels form it (two FP32 roundings, one of them an fma).
@@ -943,6 +947,7 @@ cudaError_t setup_step_tc() {
   if ((e = set_attrs<false, false>()) != cudaSuccess) return e;
   if ((e = set_attrs<false, true>()) != cudaSuccess) return e;
   if ((e = set_attrs<true, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<false, true, true>()) != cudaSuccess) return e;
   return set_attrs<true, true>();
 }
 
@@ -1036,6 +1041,10 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
   const bool one = p.mult == 1.0f;
   auto kernel = cap ? (one ? step_tc_kernel<true, true> : step_tc_kernel<true, false>)
                     : (one ? step_tc_kernel<false, true> : step_tc_kernel<false, false>);
+  if (p.test_stall) {  // the checking aid is built for multiplier 1 without a cap only
+    if (cap || !one) return cudaErrorNotSupported;
+    kernel = step_tc_kernel<false, true, true>;
+  }
   auto launch = [&](bool with_pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

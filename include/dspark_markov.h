@@ -56,6 +56,12 @@ extern "C" {
 #define DSPARK_FLAG_FORCE_FMA 0x2  /* bias on CUDA-core FMA (one launch per step) for every row count */
 #define DSPARK_FLAG_FORCE_MMA 0x4  /* bias on tcgen05 tensor cores for every row count */
 #define DSPARK_FLAG_PER_STEP 0x8   /* loop: one launch per step even where one launch could run them all */
+#define DSPARK_FLAG_TEST_STALL 0x100 /* checking aid, no counterpart in the pages: in the one-launch
+                                        loop the first step boundary waits for one arrival more than
+                                        the grid makes, so its bounded wait runs out (a few seconds)
+                                        and the loop ends with DSPARK_ERR_DEVICE_TIMEOUT in the status
+                                        word (site 9); tests use it to exercise the timeout path.
+                                        Multiplier 1 without a soft cap only (else DSPARK_ERR_CUDA) */
 #define DSPARK_FLAG_SELECT_2LAUNCH 0x10 /* each step as two launches: the step kernel writes its blocks'
                                            maxima, a select launch (one CTA per row) reduces them under the
                                            same total order and writes the token ([P2] _markov_select_kernel);
