@@ -18,6 +18,7 @@ struct dspark_markov_ctx {
   unsigned long long* slots;  // [(max_steps + 1) * max_rows] packed argmax slots
   unsigned int* counters;     // [max_steps] arrival counters, then the loop's abort word
   unsigned long long* partials;  // [max_rows, max grid] per-CTA maxima of the two-launch select
+  uint16_t* xform_lut;           // [65536] soft-capped transform of every BF16 sum (per call)
   int* status;                // device status word
   int grid_simple;
   int grid_tc;
@@ -101,6 +102,7 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.abort_word = ctx->counters + ctx->cfg.max_steps;
   p.partials = nullptr;
   p.test_stall = (ctx->cfg.flags & DSPARK_FLAG_TEST_STALL) != 0;
+  p.xform_lut = ctx->xform_lut;
   return p;
 }
 
@@ -175,7 +177,8 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   ctx->fused_ok = ctx->tc_ok && dspark::tc_cooperative_ok(ctx->grid_tc);
   const int max_grid = ctx->grid_simple > ctx->grid_tc ? ctx->grid_simple : ctx->grid_tc;
   if (cudaMalloc(&ctx->partials, static_cast<size_t>(cfg->max_rows) * max_grid * sizeof(unsigned long long)) !=
-      cudaSuccess) {
+          cudaSuccess ||
+      cudaMalloc(&ctx->xform_lut, 65536 * sizeof(uint16_t)) != cudaSuccess) {
     dspark_markov_destroy(ctx);
     return DSPARK_ERR_CUDA;
   }
@@ -189,6 +192,7 @@ void dspark_markov_destroy(dspark_markov_ctx* ctx) {
   if (ctx->counters) cudaFree(ctx->counters);
   if (ctx->status) cudaFree(ctx->status);
   if (ctx->partials) cudaFree(ctx->partials);
+  if (ctx->xform_lut) cudaFree(ctx->xform_lut);
   free(ctx);
 }
 
@@ -206,6 +210,8 @@ int32_t dspark_markov_partial_count(const dspark_markov_ctx* ctx) {
 int dspark_markov_anchor(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
   int rc = check_args(ctx, a);
   if (rc != DSPARK_OK) return rc;
+  if (a->cap != 0.0f && dspark::launch_xform_lut(ctx->xform_lut, a->mult, a->cap, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   if (dspark::launch_anchor(a->input_ids, a->anchor_idx, ctx->slots, ctx->counters,
                             ctx->counters + ctx->cfg.max_steps, a->rows, a->steps, ctx->cfg.max_rows,
                             stream) != cudaSuccess)

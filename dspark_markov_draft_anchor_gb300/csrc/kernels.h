@@ -15,6 +15,9 @@ cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, u
                           unsigned int* counters, unsigned int* abort_word, int rows, int steps, int max_rows,
                           cudaStream_t stream);
 
+// The soft-capped transform of all 65536 BF16 sums into lut (cap != 0).
+cudaError_t launch_xform_lut(uint16_t* lut, float mult, float cap, cudaStream_t stream);
+
 // Two-launch select: reduce each row's per-CTA maxima (partials [rows,
 // nparts]) into slots_out and tokens[:, step] (one CTA per row).
 cudaError_t launch_select(const unsigned long long* partials, int nparts, unsigned long long* slots_out,

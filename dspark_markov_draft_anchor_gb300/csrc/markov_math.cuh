@@ -103,18 +103,24 @@ __device__ __forceinline__ float own_tanhf(float z) {
 // ---------------------------------------------------------------------------
 // Output transform ([P3] _logit): BF16 add (one FP32 add rounded to BF16),
 // multiplier, optional soft cap cap * tanh(inv_cap * y), round to BF16.
-// Returns the cached BF16 bits; *l is their FP32 value.
+// Returns the cached BF16 bits; *l is their FP32 value.  transform_sum is
+// the part after the BF16 add, a function of the rounded sum x alone.
 // ---------------------------------------------------------------------------
 template <bool kHasCap>
-__device__ __forceinline__ uint16_t transform_logit(float base, float bias, float mult, float inv_cap,
-                                                    float cap, float* l) {
-  const float x = __bfloat162float(__float2bfloat16_rn(__fadd_rn(base, bias)));
+__device__ __forceinline__ uint16_t transform_sum(float x, float mult, float inv_cap, float cap, float* l) {
   const float y = __fmul_rn(mult, x);
   float w = y;
   if (kHasCap) w = __fmul_rn(cap, own_tanhf(__fmul_rn(inv_cap, y)));
   const __nv_bfloat16 c = __float2bfloat16_rn(w);
   *l = __bfloat162float(c);
   return __bfloat16_as_ushort(c);
+}
+
+template <bool kHasCap>
+__device__ __forceinline__ uint16_t transform_logit(float base, float bias, float mult, float inv_cap,
+                                                    float cap, float* l) {
+  const float x = __bfloat162float(__float2bfloat16_rn(__fadd_rn(base, bias)));
+  return transform_sum<kHasCap>(x, mult, inv_cap, cap, l);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {

@@ -61,6 +61,9 @@ struct StepParams {
   // row into slots_out).
   unsigned long long* partials;
   int32_t test_stall;  // checking aid (host side: picks the kernel whose first grid wait cannot end)
+  // With a soft cap: the cached BF16 of every BF16 sum x (x's bits index it),
+  // built by the anchor for this call's multiplier and cap.
+  const uint16_t* xform_lut;
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this

@@ -39,6 +39,16 @@ __global__ void anchor_kernel(const int32_t* __restrict__ input_ids, const int64
   }
 }
 
+// The soft-capped transform of every BF16 sum (bits i): the step kernels'
+// epilogue looks the cached value up instead of evaluating tanh per element.
+__global__ void xform_lut_kernel(uint16_t* __restrict__ lut, float mult, float inv_cap, float cap) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 65536) {
+    float l;
+    lut[i] = transform_sum<true>(bf16_bits_to_float(static_cast<uint32_t>(i)), mult, inv_cap, cap, &l);
+  }
+}
+
 __device__ __forceinline__ void unpack8(const uint4 w, float* f) {
   f[0] = __uint_as_float(w.x << 16);
   f[1] = __uint_as_float(w.x & 0xFFFF0000u);
@@ -209,6 +219,11 @@ cudaError_t launch_anchor(const int32_t* input_ids, const int64_t* anchor_idx, u
                           cudaStream_t stream) {
   anchor_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(input_ids, anchor_idx, slots, counters, abort_word, rows,
                                                          steps, max_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_xform_lut(uint16_t* lut, float mult, float cap, cudaStream_t stream) {
+  xform_lut_kernel<<<256, 256, 0, stream>>>(lut, mult, cap != 0.0f ? 1.0f / cap : 0.0f, cap);
   return cudaGetLastError();
 }
 

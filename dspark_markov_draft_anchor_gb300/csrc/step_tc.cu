@@ -663,33 +663,30 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
             if (c == chunks - 1) ptx::mbar_arrive(&sh.tmem_empty[b]);
           }
 
-          // (a) bias rounded to BF16 and the transform, for all rows; with
-          // multiplier 1 and no cap on packed BF16 pairs (x * 1 rounds to the
-          // same BF16, and the BF16 add is the FP32 add rounded once)
+          // (a) bias rounded to BF16 and the BF16 add on packed pairs (the
+          // BF16 add is the FP32 add rounded once), then the transform of the
+          // sum x: none with multiplier 1 and no cap (x * 1 rounds to x), the
+          // call's lookup table with a soft cap, else the multiplier
           uint32_t cb[R], biasb[R];
           float lv[R];
-          if (kMultOne && !kHasCap) {
 #pragma unroll
-            for (int pr = 0; pr < R / 2; ++pr) {
-              const uint32_t bias2 =
-                  ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
-              const uint32_t c2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
-              biasb[2 * pr] = bias2 & 0xFFFFu;
-              biasb[2 * pr + 1] = bias2 >> 16;
-              cb[2 * pr] = c2 & 0xFFFFu;
-              cb[2 * pr + 1] = c2 >> 16;
-              lv[2 * pr] = __uint_as_float(c2 << 16);
-              lv[2 * pr + 1] = __uint_as_float(c2 & 0xFFFF0000u);
-            }
-          } else {
-#pragma unroll
-            for (int rr = 0; rr < R; ++rr) {
-              const __nv_bfloat16 b16 = __float2bfloat16_rn(__uint_as_float(acc[rr]));
-              biasb[rr] = __bfloat16_as_ushort(b16);
-              cb[rr] = transform_logit<kHasCap>(bf16_bits_to_float(bb[rr]), __bfloat162float(b16), p.mult,
-                                                p.inv_cap, p.cap, &lv[rr]);
-            }
+          for (int pr = 0; pr < R / 2; ++pr) {
+            const uint32_t bias2 = ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
+            const uint32_t x2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
+            biasb[2 * pr] = bias2 & 0xFFFFu;
+            biasb[2 * pr + 1] = bias2 >> 16;
+            cb[2 * pr] = x2 & 0xFFFFu;
+            cb[2 * pr + 1] = x2 >> 16;
           }
+          if (kHasCap) {
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) cb[rr] = __ldg(p.xform_lut + cb[rr]);
+          } else if (!kMultOne) {
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) cb[rr] = transform_sum<false>(bf16_bits_to_float(cb[rr]), p.mult, 0.0f, 0.0f, &lv[rr]);
+          }
+#pragma unroll
+          for (int rr = 0; rr < R; ++rr) lv[rr] = bf16_bits_to_float(cb[rr]);
 
           // the rows' constants, all loaded before any global store
           uint32_t pf[R], ri[R], nsb[R];
