@@ -27,6 +27,10 @@ constexpr int kW2Pitch = 528;  // bytes per staged w2 row: 512 + 16 (no bank con
 __global__ void anchor_kernel(const int32_t* __restrict__ input_ids, const int64_t* __restrict__ anchor_idx,
                               unsigned long long* __restrict__ slots, unsigned int* __restrict__ counters,
                               unsigned int* __restrict__ abort_word, int rows, int steps, int max_rows) {
+  // The next kernel (a step launched with programmatic dependent launch) may
+  // start its prologue and its w2 prefetch now; it reads what this kernel
+  // writes only after griddepcontrol.wait, which waits for this grid.
+  pdl_launch_dependents();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < rows) {
     const int32_t token = input_ids[anchor_idx[r]];

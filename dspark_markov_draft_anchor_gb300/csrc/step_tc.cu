@@ -46,6 +46,8 @@
 // records DSPARK_ERR_DEVICE_TIMEOUT in the status word and raises the loop's
 // abort word (which ends the other CTAs' waits), and the CTA leaves its
 // loops, waits (bounded) for its copies in flight and frees its TMEM.
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -1009,7 +1011,7 @@ bool tc_cooperative_ok(int grid) {
 namespace {
 // Whether a cooperative launch may also carry programmatic stream
 // serialisation: unknown until the first such launch (1 yes, 0 no, -1 unknown).
-int g_coop_pdl = -1;
+std::atomic<int> g_coop_pdl{-1};
 }  // namespace
 
 cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
@@ -1065,14 +1067,15 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
     return cudaLaunchKernelEx(&cfg, kernel, w2_map, w2_tile_map, base_map, tp);
   };
   if (!cooperative || !pdl) return launch(pdl);
-  if (g_coop_pdl != 0) {
+  if (g_coop_pdl.load(std::memory_order_relaxed) != 0) {
     const cudaError_t e = launch(true);
-    if (e == cudaSuccess || g_coop_pdl == 1) {
-      if (e == cudaSuccess) g_coop_pdl = 1;
+    if (e == cudaSuccess) {
+      g_coop_pdl.store(1, std::memory_order_relaxed);
       return e;
     }
+    if (g_coop_pdl.load(std::memory_order_relaxed) == 1) return e;
     (void)cudaGetLastError();
-    g_coop_pdl = 0;
+    g_coop_pdl.store(0, std::memory_order_relaxed);
   }
   return launch(false);
 }
