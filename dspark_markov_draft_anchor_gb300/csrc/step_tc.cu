@@ -85,7 +85,7 @@ struct TcLayout {
   int n;         // MMA N: rows padded to 16
   int nacc;      // TMEM accumulators (tiles the MMA may run ahead)
   int stages;    // w2 ring stages
-  int nbase;     // base ring slots (two rings, one per epilogue warpgroup)
+  int nbase;     // base ring slots (two rings, one per tile parity)
   int tmem_cols;
   int smem;      // dynamic shared memory bytes
   int emb_off, w2_off, base_off, bar_off, row_off, queue_off;
@@ -116,10 +116,10 @@ constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared varia
 TcLayout tc_layout(int rows) {
   TcLayout L;
   L.n = ((rows + 15) / 16) * 16;
-  // even: each accumulator belongs to one warpgroup
+  // even: each accumulator belongs to one tile parity
   L.nacc = 8 * L.n <= 512 ? 8 : (4 * L.n <= 512 ? 4 : 2);
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
-  // 4 KB chunks, half per warpgroup ring; more slots only where a tile has
+  // 4 KB chunks, half per parity's ring; more slots only where a tile has
   // several chunks and the w2 ring can spare the room
   L.nbase = (L.n > kChunkRows && L.n < 128) ? 8 : 4;
   const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 3) + 16 +
@@ -306,9 +306,9 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   const int N = tp.n;
   const int S = tp.stages;
   const int NB = tp.nbase;
-  const int NBG = NB / 2;  // slots of each warpgroup's base ring
+  const int NBG = NB / 2;  // slots of each tile parity's base ring
   const int NACC = tp.nacc;
-  const int NA = NACC / 2;  // accumulators of each MMA warp / epilogue warpgroup
+  const int NA = NACC / 2;  // accumulators of each tile parity (MMA warp and its two quartets)
   const int n_steps = p.step_end - p.step;
 
   Shared sh;
@@ -718,7 +718,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
             bnd[rr] = __fmaf_rn(__uint_as_float(nsb[rr]), g, __fmaf_rn(fabsf(qa[rr]), 0x1p-20f, qa[rr]));
           }
 
-          // (b) the warpgroup's first tile of the step: raise each row's
+          // (b) the quartet's first tile of the step: raise each row's
           // threshold to the warp's largest exact lower bound of a key, l/t +
           // (least noise of h's bucket) with rounding margins; a threshold
           // at or below some key of this CTA's range never prunes its argmax
@@ -807,7 +807,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       }
       q.flush(1, sh);
 
-      // Both warpgroups are done with the step (a wait that gave up anywhere
+      // Every quartet is done with the step (a wait that gave up anywhere
       // in the CTA ends the loop here, the same way in every thread).
       if (ptx::named_bar_or(1, kEpiThreads, *abort_flag != 0)) break;
       // Publish this CTA's row maxima.  Within a launch the next step waits
@@ -841,7 +841,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         break;
       }
       // The next step's row constants (the rows' shared state is free: both
-      // warpgroups are past the barrier) while the other CTAs arrive.
+      // quartets are past the barrier) while the other CTAs arrive.
       row_init(st + 1);
       const bool arrived = et != 0 || wait_grid(st);
       if (ptx::named_bar_or(1, kEpiThreads, !arrived || *abort_flag != 0)) break;
