@@ -172,7 +172,8 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   }
   ctx->grid_simple = dspark::simple_step_grid(cfg->vocab);
   ctx->grid_tc = dspark::tc_step_grid(cfg->vocab, sms);
-  ctx->tc_ok = tc_setup && dspark::encode_w2_map(&ctx->w2_map, w2_bf16, cfg->vocab, 32) &&
+  // the tensor-core kernel packs vocabulary ids into 24 bits
+  ctx->tc_ok = tc_setup && cfg->vocab < (1 << 24) && dspark::encode_w2_map(&ctx->w2_map, w2_bf16, cfg->vocab, 32) &&
               dspark::encode_w2_map(&ctx->w2_tile_map, w2_bf16, cfg->vocab, 128);
   ctx->fused_ok = ctx->tc_ok && dspark::tc_cooperative_ok(ctx->grid_tc);
   const int max_grid = ctx->grid_simple > ctx->grid_tc ? ctx->grid_simple : ctx->grid_tc;

@@ -119,11 +119,11 @@ TcLayout tc_layout(int rows) {
   // even: each accumulator belongs to one tile parity
   L.nacc = 8 * L.n <= 512 ? 8 : (4 * L.n <= 512 ? 4 : 2);
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
-  // 4 KB chunks, half per parity's ring; more slots only where a tile has
-  // several chunks and the w2 ring can spare the room
-  L.nbase = (L.n > kChunkRows && L.n < 128) ? 8 : 4;
+  // 4 KB chunks, half per parity's ring; more slots where a tile has several
+  // chunks, or three per parity at 16 rows, where the w2 ring can spare them
+  L.nbase = (L.n > kChunkRows && L.n < 128) ? 8 : (L.n == kChunkRows ? 6 : 4);
   const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 3) + 16 +
-                    kRowBytes + kEpiWarps * kQCap * 16 + 1024 + 64;
+                    kRowBytes + kEpiWarps * kQCap * 8 + 1024 + 64;
   L.stages = (kSmemBudget - fixed) / kW2StageBytes;
   if (L.stages > 12) L.stages = 12;
   L.stages &= ~1;  // two w2 rings of stages / 2, one per MMA warp
@@ -141,7 +141,7 @@ TcLayout tc_layout(int rows) {
   off += kRowBytes;
   off = (off + 15) & ~15;
   L.queue_off = off;
-  off += kEpiWarps * kQCap * 16;
+  off += kEpiWarps * kQCap * 8;
   L.smem = off + 1024;  // room to align the base to 1024 bytes
   return L;
 }
@@ -161,11 +161,12 @@ struct TcParams {
 // A warp's queue of elements whose Gumbel key must be evaluated (their exact
 // bound reaches the row's current maximum).  Evaluating them 32 at a time,
 // one per lane, keeps rare survivors from costing the warp a full pass each.
+// An entry is 8 bytes (the hash is formed again at evaluation), so vocabulary
+// ids must stay below 2^24 (the host sends larger vocabularies to the other
+// step kernel).
 struct Cand {
-  uint32_t v;
   float l;
-  uint32_t h;
-  uint32_t r;
+  uint32_t vr;  // row << 24 | vocabulary id
 };
 struct Shared;
 
@@ -173,11 +174,11 @@ struct WarpQueue {
   Cand* q;
   uint32_t head = 0, count = 0;  // warp-uniform
 
-  __device__ __forceinline__ void push(bool take, int lane, uint32_t v, float l, uint32_t h, int r) {
+  __device__ __forceinline__ void push(bool take, int lane, uint32_t v, float l, int r) {
     const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
     if (take) {
       const uint32_t pos = (head + count + __popc(m & ((1u << lane) - 1u))) & (kQCap - 1);
-      q[pos] = Cand{v, l, h, static_cast<uint32_t>(r)};
+      q[pos] = Cand{l, (static_cast<uint32_t>(r) << 24) | v};
     }
     count += __popc(m);
   }
@@ -273,11 +274,12 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
     const uint32_t n = count < 32u ? count : 32u;
     if (static_cast<uint32_t>(lane) < n) {
       const Cand e = q[(head + lane) & (kQCap - 1)];
-      const float t = sh.temp[e.r];
-      const float key = t != 0.0f ? eval_key(e.l, t, e.h) : e.l;
-      const unsigned long long cand = pack_key(key, e.v);
-      const unsigned long long old = atomicMax(sh.best + e.r, cand);
-      if (cand > old) sh.thr[e.r] = key != key ? INFINITY : key;
+      const uint32_t r = e.vr >> 24, v = e.vr & 0xFFFFFFu;
+      const float t = sh.temp[r];
+      const float key = t != 0.0f ? eval_key(e.l, t, murmur_finish_mixed(sh.prefix[r], murmur_kmix(v))) : e.l;
+      const unsigned long long cand = pack_key(key, v);
+      const unsigned long long old = atomicMax(sh.best + r, cand);
+      if (cand > old) sh.thr[r] = key != key ? INFINITY : key;
     }
     head = (head + n) & (kQCap - 1);
     count -= n;
@@ -769,7 +771,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
               for (int rr = 0; rr < R; ++rr)
                 if ((take >> rr) & 1u) {
                   q.q[pos & (kQCap - 1)] =
-                      Cand{static_cast<uint32_t>(v), lv[rr], hv[rr], static_cast<uint32_t>(r0 + rr)};
+                      Cand{lv[rr], (static_cast<uint32_t>(r0 + rr) << 24) | static_cast<uint32_t>(v)};
                   ++pos;
                 }
               q.count += total;
@@ -779,7 +781,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
               for (int rr = 0; rr < R; ++rr) {
                 const bool t = (take >> rr) & 1u;
                 if (__any_sync(0xFFFFFFFFu, t)) {
-                  q.push(t, lane, static_cast<uint32_t>(v), lv[rr], hv[rr], r0 + rr);
+                  q.push(t, lane, static_cast<uint32_t>(v), lv[rr], r0 + rr);
                   q.flush(32, sh);
                 }
               }
@@ -840,7 +842,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         }
         break;
       }
-      // The next step's row constants (the rows' shared state is free: both
+      // The next step's row constants (the rows' shared state is free: all
       // quartets are past the barrier) while the other CTAs arrive.
       row_init(st + 1);
       const bool arrived = et != 0 || wait_grid(st);
