@@ -258,6 +258,17 @@ __device__ __forceinline__ uint32_t lds_u32(const void* ptr) {
   return r;
 }
 
+__device__ __forceinline__ long long lds_i64(const void* ptr) {
+  long long r;
+  asm volatile("ld.shared.s64 %0, [%1];" : "=l"(r) : "r"(ptx::smem_addr(ptr)));
+  return r;
+}
+__device__ __forceinline__ float ld_volatile_f32(const float* ptr) {
+  float r;
+  asm volatile("ld.volatile.shared.f32 %0, [%1];" : "=f"(r) : "r"(ptx::smem_addr(ptr)));
+  return r;
+}
+
 // Four floats of shared memory that other warps update (never cached).
 __device__ __forceinline__ float4 ld_volatile_f4(const float* ptr) {
   float4 r;
@@ -287,7 +298,9 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
   __syncwarp();
 }
 
-template <bool kHasCap, bool kMultOne, bool kTestStall = false>
+// kRW: rows of a chunk each epilogue warp takes -- kHalfRows, or 1 for a
+// single-row loop (the second half's warps then only keep the barriers).
+template <bool kHasCap, bool kMultOne, bool kTestStall = false, int kRW = kHalfRows>
 __global__ void __launch_bounds__(kThreads, 1)
 step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_w2_tile,
                const __grid_constant__ CUtensorMap tmap_base, const TcParams tp) {
@@ -649,16 +662,30 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           const int s = wg * NBG + k % NBG;
           ok = __all_sync(0xFFFFFFFFu, wait(&sh.full_base[s], (k / NBG) & 1, 7, (st << 24) | (i << 12) | (k & 0xFFF)));
           if (!ok) break;
-          constexpr int R = kHalfRows;
-          const int r0 = c * kChunkRows + half * R;  // this warp's first row of the chunk
-          const uint16_t* bs = reinterpret_cast<const uint16_t*>(sh.base + s * kChunkBytes) + half * R * kTileV;
+          constexpr int R = kRW;
+          const int r0 = c * kChunkRows + half * kHalfRows;  // this warp's first row of the chunk
+          if (kRW == 1 && half == 1) {
+            // single-row build: no row for this warp; the slot's data has
+            // landed, so release it (and the accumulator) in step
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(&sh.empty_base[s]);
+              if (c == chunks - 1) ptx::mbar_arrive(&sh.tmem_empty[b]);
+            }
+            continue;
+          }
+          const uint16_t* bs =
+              reinterpret_cast<const uint16_t*>(sh.base + s * kChunkBytes) + half * kHalfRows * kTileV;
           uint32_t bb[R];
 #pragma unroll
           for (int rr = 0; rr < R; ++rr) bb[rr] = bs[rr * kTileV + vr];
           uint32_t acc[R];
-          ptx::tmem_ld8_sync(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                 static_cast<uint32_t>(b * N + r0),
-                             acc);
+          const uint32_t taddr =
+              tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * N + r0);
+          if constexpr (R == 1)
+            ptx::tmem_ld1_sync(taddr, acc);
+          else
+            ptx::tmem_ld8_sync(taddr, acc);
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -673,14 +700,21 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           // call's lookup table with a soft cap, else the multiplier
           uint32_t cb[R], biasb[R];
           float lv[R];
+          if constexpr (R == 1) {
+            const uint32_t bias1 = ptx::cvt_bf16x2(__uint_as_float(acc[0]), 0.0f);
+            biasb[0] = bias1 & 0xFFFFu;
+            cb[0] = ptx::add_bf16x2(bb[0], bias1) & 0xFFFFu;
+          } else {
 #pragma unroll
-          for (int pr = 0; pr < R / 2; ++pr) {
-            const uint32_t bias2 = ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
-            const uint32_t x2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
-            biasb[2 * pr] = bias2 & 0xFFFFu;
-            biasb[2 * pr + 1] = bias2 >> 16;
-            cb[2 * pr] = x2 & 0xFFFFu;
-            cb[2 * pr + 1] = x2 >> 16;
+            for (int pr = 0; pr < R / 2; ++pr) {
+              const uint32_t bias2 =
+                  ptx::cvt_bf16x2(__uint_as_float(acc[2 * pr]), __uint_as_float(acc[2 * pr + 1]));
+              const uint32_t x2 = ptx::add_bf16x2(bb[2 * pr] | (bb[2 * pr + 1] << 16), bias2);
+              biasb[2 * pr] = bias2 & 0xFFFFu;
+              biasb[2 * pr + 1] = bias2 >> 16;
+              cb[2 * pr] = x2 & 0xFFFFu;
+              cb[2 * pr + 1] = x2 >> 16;
+            }
           }
           if (kHasCap) {
 #pragma unroll
@@ -694,6 +728,11 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
 
           // the rows' constants, all loaded before any global store
           uint32_t pf[R], ri[R], nsb[R];
+          if constexpr (R == 1) {
+            pf[0] = lds_u32(sh.prefix + r0);
+            ri[0] = lds_u32(sh.rinv + r0);
+            nsb[0] = lds_u32(sh.ns + r0);
+          }
 #pragma unroll
           for (int q4 = 0; q4 < R / 4; ++q4) {
             const uint4 a = lds_u4(sh.prefix + r0 + 4 * q4);
@@ -703,7 +742,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
             ri[4 * q4] = bq.x; ri[4 * q4 + 1] = bq.y; ri[4 * q4 + 2] = bq.z; ri[4 * q4 + 3] = bq.w;
             nsb[4 * q4] = cq.x; nsb[4 * q4 + 1] = cq.y; nsb[4 * q4 + 2] = cq.z; nsb[4 * q4 + 3] = cq.w;
           }
-          const uint32_t gm16 = lds_u32(sh.gmask + c) >> (half * R);
+          const uint32_t gm16 = lds_u32(sh.gmask + c) >> (half * kHalfRows);
           const uint32_t gm = (gm16 & 0xFFu) | (gm16 >> 16 & 0xFFu) << 16;  // store bits 0..7, live bits 16..23
           const uint32_t live = in ? gm >> 16 : 0u;  // this warp's rows that exist, this lane in range
 
@@ -746,6 +785,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           // (c) an element whose bound is below its row's threshold cannot be
           // the argmax; the rest are queued and evaluated 32 at a time
           uint32_t take = 0;
+          if constexpr (R == 1) take = bnd[0] < ld_volatile_f32(sh.thr + r0) ? 0u : 1u;
 #pragma unroll
           for (int q4 = 0; q4 < R / 4; ++q4) {
             const float4 th = ld_volatile_f4(sh.thr + r0 + 4 * q4);
@@ -790,6 +830,9 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
 
           // (d) cache and bias stores of the chunk
           if (in) {
+            if constexpr (R == 1) {
+              if (gm & 1u) __stcs(p.cache + lds_i64(sh.cache_off + r0) + v, static_cast<unsigned short>(cb[0]));
+            }
 #pragma unroll
             for (int q2 = 0; q2 < R / 2; ++q2) {
               const longlong2 co = lds_ll2(sh.cache_off + r0 + 2 * q2);
@@ -886,9 +929,10 @@ int max_tc_smem() {
   return m;
 }
 
-template <bool C, bool M, bool T = false>
+template <bool C, bool M, bool T = false, int RW = kHalfRows>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(step_tc_kernel<C, M, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_tc_smem());
+  return cudaFuncSetAttribute(step_tc_kernel<C, M, T, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              max_tc_smem());
 }
 
 // u of hash h as the kernels form it (two FP32 roundings, one of them an fma).
@@ -949,6 +993,7 @@ cudaError_t setup_step_tc() {
   if ((e = set_attrs<false, true>()) != cudaSuccess) return e;
   if ((e = set_attrs<true, false>()) != cudaSuccess) return e;
   if ((e = set_attrs<false, true, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<false, true, false, 1>()) != cudaSuccess) return e;
   return set_attrs<true, true>();
 }
 
@@ -1045,6 +1090,8 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
   if (p.test_stall) {  // the checking aid is built for multiplier 1 without a cap only
     if (cap || !one) return cudaErrorNotSupported;
     kernel = step_tc_kernel<false, true, true>;
+  } else if (p.rows == 1 && !cap && one) {  // one row: the single-row epilogue
+    kernel = step_tc_kernel<false, true, false, 1>;
   }
   auto launch = [&](bool with_pdl) {
     cudaLaunchConfig_t cfg = {};
