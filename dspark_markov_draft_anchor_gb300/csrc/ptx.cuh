@@ -200,6 +200,16 @@ __device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&v)[8]) 
       : "memory");
 }
 
+// The same for 4 consecutive columns.
+__device__ __forceinline__ void tmem_ld4_sync(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+      : "r"(taddr)
+      : "memory");
+}
+
 // The same for one column.
 __device__ __forceinline__ void tmem_ld1_sync(uint32_t taddr, uint32_t (&v)[1]) {
   asm volatile(

@@ -298,8 +298,9 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
   __syncwarp();
 }
 
-// kRW: rows of a chunk each epilogue warp takes -- kHalfRows, or 1 for a
-// single-row loop (the second half's warps then only keep the barriers).
+// kRW: rows of a chunk each epilogue warp takes -- kHalfRows, or 1 or 4 for
+// loops of at most that many rows (the second half's warps then only keep
+// the barriers).
 template <bool kHasCap, bool kMultOne, bool kTestStall = false, int kRW = kHalfRows>
 __global__ void __launch_bounds__(kThreads, 1)
 step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_w2_tile,
@@ -664,8 +665,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           if (!ok) break;
           constexpr int R = kRW;
           const int r0 = c * kChunkRows + half * kHalfRows;  // this warp's first row of the chunk
-          if (kRW == 1 && half == 1) {
-            // single-row build: no row for this warp; the slot's data has
+          if (kRW < kHalfRows && half == 1) {
+            // few-row build: no row for this warp; the slot's data has
             // landed, so release it (and the accumulator) in step
             __syncwarp();
             if (lane == 0) {
@@ -684,6 +685,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
               tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * N + r0);
           if constexpr (R == 1)
             ptx::tmem_ld1_sync(taddr, acc);
+          else if constexpr (R == 4)
+            ptx::tmem_ld4_sync(taddr, acc);
           else
             ptx::tmem_ld8_sync(taddr, acc);
           ptx::tc_fence_before();
@@ -994,6 +997,7 @@ cudaError_t setup_step_tc() {
   if ((e = set_attrs<true, false>()) != cudaSuccess) return e;
   if ((e = set_attrs<false, true, true>()) != cudaSuccess) return e;
   if ((e = set_attrs<false, true, false, 1>()) != cudaSuccess) return e;
+  if ((e = set_attrs<false, true, false, 4>()) != cudaSuccess) return e;
   return set_attrs<true, true>();
 }
 
@@ -1090,8 +1094,8 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
   if (p.test_stall) {  // the checking aid is built for multiplier 1 without a cap only
     if (cap || !one) return cudaErrorNotSupported;
     kernel = step_tc_kernel<false, true, true>;
-  } else if (p.rows == 1 && !cap && one) {  // one row: the single-row epilogue
-    kernel = step_tc_kernel<false, true, false, 1>;
+  } else if (p.rows <= 4 && !cap && one) {  // few rows: the few-row epilogue
+    kernel = p.rows == 1 ? step_tc_kernel<false, true, false, 1> : step_tc_kernel<false, true, false, 4>;
   }
   auto launch = [&](bool with_pdl) {
     cudaLaunchConfig_t cfg = {};
