@@ -100,7 +100,7 @@ __host__ __device__ inline int pow2_at_least(int x) {
 // Per-row arrays in shared memory (structure of arrays, kMaxRows entries
 // each) and their byte offsets inside the row region.
 constexpr int kRowBest = 0;                            // u64 packed maxima
-constexpr int kRowCoff = kRowBest + 8 * kMaxRows;      // i64 cache offsets
+constexpr int kRowCoff = kRowBest + 8 * kMaxRows;      // i64 cache row addresses
 constexpr int kRowPrefix = kRowCoff + 8 * kMaxRows;    // u32 Murmur3 prefixes
 constexpr int kRowRinv = kRowPrefix + 4 * kMaxRows;    // f32 RN(1/t) (1 for greedy rows)
 constexpr int kRowNs = kRowRinv + 4 * kMaxRows;        // f32 noise scale (0 greedy, 1 else)
@@ -198,7 +198,7 @@ struct Shared {
   uint64_t* emb_ready;
   uint64_t* spare;       // [2], one per MMA warp
   unsigned long long* best;
-  int64_t* cache_off;
+  int64_t* cache_off;  // per row: the address of its cache row (an int64)
   uint32_t* prefix;
   float* rinv;
   float* ns;
@@ -578,7 +578,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         thr = -INFINITY;
       }
       sh.best[r] = 0ull;
-      sh.cache_off[r] = coff;
+      // the row's cache row as an address (read only where the row stores)
+      sh.cache_off[r] = store ? reinterpret_cast<int64_t>(p.cache + coff) : 0;
       sh.prefix[r] = prefix;
       sh.rinv[r] = rinv;
       sh.ns[r] = ns;
@@ -834,14 +835,18 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           // (d) cache and bias stores of the chunk
           if (in) {
             if constexpr (R == 1) {
-              if (gm & 1u) __stcs(p.cache + lds_i64(sh.cache_off + r0) + v, static_cast<unsigned short>(cb[0]));
+              if (gm & 1u)
+                __stcs(reinterpret_cast<unsigned short*>(lds_i64(sh.cache_off + r0)) + v,
+                       static_cast<unsigned short>(cb[0]));
             }
 #pragma unroll
             for (int q2 = 0; q2 < R / 2; ++q2) {
               const longlong2 co = lds_ll2(sh.cache_off + r0 + 2 * q2);
               // streaming stores: the cache is not read back by the loop
-              if (gm & (1u << (2 * q2))) __stcs(p.cache + co.x + v, static_cast<unsigned short>(cb[2 * q2]));
-              if (gm & (2u << (2 * q2))) __stcs(p.cache + co.y + v, static_cast<unsigned short>(cb[2 * q2 + 1]));
+              if (gm & (1u << (2 * q2)))
+                __stcs(reinterpret_cast<unsigned short*>(co.x) + v, static_cast<unsigned short>(cb[2 * q2]));
+              if (gm & (2u << (2 * q2)))
+                __stcs(reinterpret_cast<unsigned short*>(co.y) + v, static_cast<unsigned short>(cb[2 * q2 + 1]));
             }
             if (p.bias_out) {
 #pragma unroll
