@@ -247,7 +247,7 @@ def dspark_check_tanhf(x, y, n, stream=None):
     _check(load().dspark_check_tanhf(_ptr(x), _ptr(y), n, _stream(stream)), "dspark_check_tanhf")
 
 
-def dspark_noise_bound_tables(n: int = 528):
+def dspark_noise_bound_tables(n: int = 512):
     """The step kernel's noise bounds (host code): (ub, lb) float32 arrays."""
     ub = (ctypes.c_float * n)()
     lb = (ctypes.c_float * n)()

@@ -45,9 +45,10 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
 bool tc_cooperative_ok(int grid);
 
 // Bounds of the Gumbel noise -L(h) used to skip elements that cannot win:
-// bucket (clz(h) << 4) | (the 4 bits after h's leading one), h = 0 in bucket
-// 512; ub[b] >= -L(h) >= lb[b] for every h of bucket b (host code, no GPU).
-constexpr int kNoiseBuckets = 33 * 16;
+// bucket 16 k + m of g = h | 1 (k: the position of g's leading one, m: the
+// 4 bits after it); ub[b] >= -L(h) >= lb[b] for every h of bucket b (host
+// code, no GPU).
+constexpr int kNoiseBuckets = 32 * 16;
 void noise_bound_tables(float* ub, float* lb);
 
 }  // namespace dspark

@@ -210,20 +210,20 @@ struct Shared {
   Cand* queues;
 };
 
-// Bounds of the noise -L(h) by bucket of the hash h: h's leading-zero count
-// c and the 4 bits m after its leading one (h = 0 is bucket 512).  -L falls as
-// u = RN((h + 0.5) 2^-32) grows, so a bucket's bounds are the noise at the
-// float u of its smallest and of its largest h, computed on the host in
-// double with a margin (1e-3) far above the FP32 evaluation's error.  Where u
-// < 1/16 (the large noise values that can win) a bucket spans a factor of at
-// most 17/16 in u, so its noise range is about ln(17/16) = 0.06 wide.
+// Bounds of the noise -L(h) by bucket of the hash h: with g = h | 1, the
+// position k of g's leading one and the 4 bits m after it, bucket 16 k + m
+// (the exponent and top mantissa bits of g converted to float rounding toward
+// zero).  -L falls as u = RN((h + 0.5) 2^-32) grows, so a bucket's bounds are
+// the noise at the float u of its smallest and of its largest h, computed on
+// the host in double with a margin (1e-3) far above the FP32 evaluation's
+// error.  Where u < 1/16 (the large noise values that can win) a bucket spans
+// a factor of at most 17/16 in u, so its noise range is about ln(17/16) = 0.06
+// wide.
 __constant__ float c_noise_ub[kNoiseT];
 __constant__ float c_noise_lb[kNoiseT];
 
 __device__ __forceinline__ uint32_t noise_index(uint32_t h) {
-  const uint32_t c = __clz(h);
-  const uint32_t n = h << (c & 31u);  // leading one at bit 31 (0 for h = 0)
-  return (c << 4) | ((n >> 27) & 15u);
+  return (__float_as_uint(__uint2float_rz(h | 1u)) >> 19) - (127u << 4);
 }
 
 // The Gumbel key of one element, out of line: it is evaluated for few
@@ -960,23 +960,32 @@ double neg_noise_L(float u) {
 
 void noise_bound_tables(float* ub, float* lb) {
   const double margin = 1e-3;
-  for (int idx = 0; idx < kNoiseT; ++idx) {
-    const int c = idx >> 4, m = idx & 15;
-    int64_t lo = -1, hi = -1;  // the bucket's hashes [lo, hi]; none if lo < 0
-    if (c == 32) {
-      if (m == 0) lo = hi = 0;
-    } else if (c <= 27) {
-      lo = (int64_t{1} << (31 - c)) + (static_cast<int64_t>(m) << (27 - c));
-      hi = lo + (int64_t{1} << (27 - c)) - 1;
-    } else if (m % (1 << (c - 27)) == 0) {
-      lo = hi = (int64_t{1} << (31 - c)) + (m >> (c - 27));
+  // The bucket's smallest and largest hash: enumerated below 2^16, a range
+  // above (there h | 1 leaves the 4 bits after the leading one alone).
+  int64_t lo[kNoiseT], hi[kNoiseT];
+  for (int b = 0; b < kNoiseT; ++b) lo[b] = hi[b] = -1;
+  for (int64_t h = 0; h < (int64_t{1} << 16); ++h) {
+    const int64_t g = h | 1;
+    int k = 0;
+    while ((g >> (k + 1)) != 0) ++k;
+    const int m = static_cast<int>(k >= 4 ? (g >> (k - 4)) & 15 : (g << (4 - k)) & 15);
+    const int b = 16 * k + m;
+    if (lo[b] < 0) lo[b] = h;
+    hi[b] = h;
+  }
+  for (int k = 16; k < 32; ++k)
+    for (int m = 0; m < 16; ++m) {
+      const int b = 16 * k + m;
+      lo[b] = (int64_t{1} << k) + (static_cast<int64_t>(m) << (k - 4));
+      hi[b] = lo[b] + (int64_t{1} << (k - 4)) - 1;
     }
-    if (lo < 0) {
-      ub[idx] = lb[idx] = 0.0f;  // never looked up
+  for (int b = 0; b < kNoiseT; ++b) {
+    if (lo[b] < 0) {
+      ub[b] = lb[b] = 0.0f;  // never looked up
       continue;
     }
-    ub[idx] = static_cast<float>(neg_noise_L(noise_u(static_cast<uint32_t>(lo))) + margin);
-    lb[idx] = static_cast<float>(neg_noise_L(noise_u(static_cast<uint32_t>(hi))) - margin);
+    ub[b] = static_cast<float>(neg_noise_L(noise_u(static_cast<uint32_t>(lo[b]))) + margin);
+    lb[b] = static_cast<float>(neg_noise_L(noise_u(static_cast<uint32_t>(hi[b]))) - margin);
   }
 }
 

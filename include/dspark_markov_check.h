@@ -44,10 +44,10 @@ DSPARK_API int dspark_check_tanhf(const float *x, float *y, int64_t n, cudaStrea
 /* The step kernel's bounds of the Gumbel noise -L(h), which let it skip
  * elements that cannot be the argmax (no counterpart in the pages: the pages
  * evaluate every key).  Host code only, no GPU and no stream: fills HOST
- * arrays ub[n], lb[n] with n >= 528; bucket b = (clz(h) << 4) | (the 4 bits
- * after h's leading one), h = 0 in bucket 512; for every h of bucket b,
- * lb[b] <= -L(h) <= ub[b]; empty buckets hold 0.  Returns the number of
- * buckets (528) or DSPARK_ERR_INVALID_ARG. */
+ * arrays ub[n], lb[n] with n >= 512; bucket b = 16 k + m of g = h | 1, k the
+ * position of g's leading one and m the 4 bits after it; for every h of
+ * bucket b, lb[b] <= -L(h) <= ub[b]; empty buckets hold 0.  Returns the
+ * number of buckets (512) or DSPARK_ERR_INVALID_ARG. */
 DSPARK_API int dspark_noise_bound_tables(float *ub, float *lb, int32_t n);
 
 #ifdef __cplusplus

@@ -13,13 +13,14 @@ from dspark_markov_draft_anchor_gb300 import binding
 
 
 def _bucket(h):
-    """Bucket of each hash: clz(h) * 16 + the 4 bits after h's leading one
-    (h = 0: 512)."""
-    h64 = h.astype(np.uint64)
-    _, e = np.frexp(h64.astype(np.float64))  # bit length (exact: h < 2^53)
-    c = (32 - e).astype(np.uint64)
-    n = (h64 << c) & np.uint64(0xFFFFFFFF)
-    return (c * np.uint64(16) + ((n >> np.uint64(27)) & np.uint64(15))).astype(np.int64)
+    """Bucket of each hash: with g = h | 1, 16 k + m for k the position of g's
+    leading one and m the 4 bits after it (zeros below bit 0)."""
+    g = h.astype(np.uint64) | np.uint64(1)
+    _, e = np.frexp(g.astype(np.float64))  # bit length (exact: g < 2^53)
+    k = (e - 1).astype(np.int64)
+    m = np.where(k >= 4, (g >> np.maximum(k - 4, 0).astype(np.uint64)) & np.uint64(15),
+                 (g << np.maximum(4 - k, 0).astype(np.uint64)) & np.uint64(15)).astype(np.int64)
+    return 16 * k + m
 
 
 def _samples():
@@ -38,7 +39,7 @@ def _samples():
 
 def test_noise_bound_tables_bracket_the_oracle_noise_tightly():
     ub, lb = binding.dspark_noise_bound_tables()
-    assert len(ub) == len(lb) == 528
+    assert len(ub) == len(lb) == 512
     ub, lb = np.asarray(ub, np.float64), np.asarray(lb, np.float64)
     h = _samples()
     b = _bucket(h)
@@ -49,21 +50,24 @@ def test_noise_bound_tables_bracket_the_oracle_noise_tightly():
     assert not bad.any(), (h[bad][:5], noise[bad][:5], ub[b][bad][:5], lb[b][bad][:5])
     # tight: each bound is within the 1e-3 margin (plus rounding) of the
     # bucket's extreme noise; every sampled bucket holds its end points
-    hi_n = np.full(528, -np.inf)
-    lo_n = np.full(528, np.inf)
+    hi_n = np.full(512, -np.inf)
+    lo_n = np.full(512, np.inf)
     np.maximum.at(hi_n, b, noise)
     np.minimum.at(lo_n, b, noise)
     used = np.isfinite(hi_n)
-    # nonempty buckets: clz 0..27 x 16, clz 28..31 with 8, 4, 2, 1, and h = 0
-    assert used.sum() == 28 * 16 + 8 + 4 + 2 + 1 + 1
+    # nonempty buckets: every one from the hashes below 2^16, 16 per leading-one
+    # position above
+    assert used.sum() == np.unique(_bucket(np.arange(1 << 16, dtype=np.uint32))).size + 16 * 16
     assert np.all(ub[used] - hi_n[used] <= 1.2e-3) and np.all(ub[used] - hi_n[used] >= 0.9e-3)
     assert np.all(lo_n[used] - lb[used] <= 1.2e-3) and np.all(lo_n[used] - lb[used] >= 0.9e-3)
     # narrow where the noise is large (the elements that can win): for
-    # u < 1/16 (clz >= 4) the noise is -log u to within 2^-5, and a bucket
-    # spans at most a factor 17/16 of u
-    small_u = used & (np.arange(528) >= 4 * 16)
+    # u < 1/16 (leading one below bit 28) the noise is -log u to within 2^-5,
+    # and a bucket spans at most a factor 17/16 of u -- except the buckets of
+    # the 16 smallest hashes (leading one below bit 4: u < 2^-28), which the
+    # low bit folded into h | 1 widens up to a factor 3
+    small_u = used & (np.arange(512) < 28 * 16) & (np.arange(512) >= 4 * 16)
     assert np.all(ub[small_u] - lb[small_u] <= math.log(17 / 16) + 4e-3)
-    pos = used & (lb > 0)
+    pos = used & (lb > 0) & (np.arange(512) >= 4 * 16)
     assert np.all(ub[pos] - lb[pos] <= 0.1)
 
 
