@@ -116,6 +116,11 @@ def lib():
             "oracle_dot_bf16_rows": (None, [P, P, P, i64, ctypes.c_int]),
             "oracle_f32_to_bf16_array": (None, [P, P, i64]),
             "oracle_key_array": (None, [P, f32, P, P, i64]),
+            "oracle_philox4x32_10": (None, [P, P, P]),
+            "oracle_fill_uniforms": (None, [P, i64, ctypes.c_uint64, ctypes.c_uint64]),
+            "oracle_weight": (ctypes.c_uint64, [f32]),
+            "oracle_sample_weights": (i64, [P, i64, f32]),
+            "oracle_probabilistic_accept": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i64]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -322,4 +327,51 @@ def greedy_accept(logits, draft, proposal_len, P):
                                     _ptr(accepted), _ptr(accept_len), B, draft.strides[0] // 8, P, V)
     if rc != 0:
         raise RuntimeError(f"oracle_greedy_accept failed: {rc}")
+    return accepted, accept_len
+
+
+def philox4x32_10(ctr, key):
+    """One Philox4x32-10 block: ``ctr`` 4 words, ``key`` 2 words -> 4 words."""
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.empty(4, np.uint32)
+    lib().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def fill_uniforms(n, seed, offset):
+    """[P1] dsparkFillUniforms: ``n`` uniforms in [0, 1) (float32)."""
+    u = np.empty(n, np.float32)
+    lib().oracle_fill_uniforms(_ptr(u), n, seed & (2**64 - 1), offset & (2**64 - 1))
+    return u
+
+
+def sample_weights(w, u):
+    """Inverse-CDF index of fixed-point weights ``w`` (uint64) at uniform ``u``."""
+    w = _c(w, np.uint64)
+    return int(lib().oracle_sample_weights(_ptr(w), w.size, float(u)))
+
+
+def weight(p):
+    return int(lib().oracle_weight(float(p)))
+
+
+def probabilistic_accept(target, draft_probs, draft, proposal_len, uniforms, P):
+    """[P1] dsparkProbabilisticAccept.  ``target`` [B, P+1, V], ``draft_probs``
+    [B, P, V] float32, ``uniforms`` [B, 2P+1]; returns (accepted, accept_len)."""
+    target = _c(target, np.float32)
+    draft_probs = _c(draft_probs, np.float32)
+    draft = np.asarray(draft, dtype=np.int64)
+    assert draft.strides[1] == 8
+    proposal_len = _c(proposal_len, np.int32)
+    uniforms = _c(uniforms, np.float32)
+    B, P1, V = target.shape
+    assert P1 == P + 1 and draft_probs.shape == (B, P, V) and uniforms.shape == (B, 2 * P + 1)
+    accepted = np.empty((B, P + 1), np.int64)
+    accept_len = np.empty(B, np.int32)
+    rc = lib().oracle_probabilistic_accept(_ptr(target), _ptr(draft_probs), draft.ctypes.data,
+                                           _ptr(proposal_len), _ptr(uniforms), _ptr(accepted),
+                                           _ptr(accept_len), B, draft.strides[0] // 8, P, V)
+    if rc != 0:
+        raise RuntimeError(f"oracle_probabilistic_accept failed: {rc}")
     return accepted, accept_len

@@ -607,6 +607,139 @@ int oracle_greedy_accept(const uint16_t *logits, const int64_t *draft, const int
 }
 
 /* ------------------------------------------------------------------------ */
+/* Probabilistic verify side ([P1] dsparkFillUniforms,                       */
+/* dsparkProbabilisticAccept).                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011): ten rounds of
+ *   (c0, c1, c2, c3) -> (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+ * with M0 = 0xD2511F53, M1 = 0xCD9E8D57, the key bumped by the Weyl
+ * constants (0x9E3779B9, 0xBB67AE85) between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; round++) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+    const uint32_t n1 = (uint32_t)p1;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+    const uint32_t n3 = (uint32_t)p0;
+    c[0] = n0;
+    c[1] = n1;
+    c[2] = n2;
+    c[3] = n3;
+  }
+  for (int i = 0; i < 4; i++) out[i] = c[i];
+}
+
+/* [P1] dsparkFillUniforms: deterministic uniforms in [0, 1).  Reading:
+ * element i takes word i % 4 of Philox4x32-10 at counter (offset + i / 4) as
+ * a 64-bit number in the low two words (the high two zero) and key (lo, hi)
+ * of the seed; the word's top 24 bits scaled by 2^-24 are the uniform. */
+void oracle_fill_uniforms(float *u, int64_t n, uint64_t seed, uint64_t offset) {
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  for (int64_t i = 0; i < n; i++) {
+    const uint64_t block = offset + (uint64_t)i / 4u;
+    const uint32_t ctr[4] = {(uint32_t)block, (uint32_t)(block >> 32), 0u, 0u};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    u[i] = (float)(out[i % 4] >> 8) * (1.0f / 16777216.0f);
+  }
+}
+
+/* A probability as a fixed-point weight in units of 2^-40: clamp to [0, 1]
+ * (NaN and negatives weigh 0) and truncate.  Sums of weights are exact, so
+ * the sampled index does not depend on the order of the additions. */
+uint64_t oracle_weight(float p) {
+  if (!(p > 0.0f)) return 0u;
+  if (p >= 1.0f) return (uint64_t)1 << 40;
+  return (uint64_t)ldexp((double)p, 40);
+}
+
+/* Inverse-CDF sample of n weights with uniform u: U = floor(u 2^24),
+ * T = floor(U S / 2^24) for the total S, the smallest index whose inclusive
+ * prefix sum exceeds T; -1 when S = 0. */
+int64_t oracle_sample_weights(const uint64_t *w, int64_t n, float u) {
+  uint64_t total = 0;
+  for (int64_t v = 0; v < n; v++) total += w[v];
+  if (total == 0) return -1;
+  float uu = u;
+  if (!(uu > 0.0f)) uu = 0.0f;
+  uint64_t U = (uint64_t)ldexp((double)uu, 24);
+  if (U > 0xFFFFFFu) U = 0xFFFFFFu;
+  const uint64_t T = (uint64_t)(((unsigned __int128)U * total) >> 24);
+  uint64_t prefix = 0;
+  for (int64_t v = 0; v < n; v++) {
+    prefix += w[v];
+    if (prefix > T) return v;
+  }
+  return n - 1; /* unreachable: T < S */
+}
+
+/* [P1] dsparkProbabilisticAccept, speculative sampling with residual
+ * sampling.  target [B, P+1, V], draft [B, P, V] (FP32 probabilities),
+ * uniforms [B, 2P+1]: u[j] decides draft position j, u[P + j] drives the
+ * residual sample after a rejection at j, u[2P] the bonus sample after a full
+ * accept.  Readings: position j accepts its draft token d when
+ * RN(u[j] * q) < t, t = target[b, j, d], q = draft[b, j, d] (the multiplied
+ * form of u < t / q; an id outside [0, V) is rejected); the residual is
+ * max(0, RN(target - draft)) per id, sampled by oracle_sample_weights; a
+ * residual of weight 0 samples the target row instead, and a target row of
+ * weight 0 gives id 0; accepted[b] holds the accepted drafts then the sample,
+ * then -1; accept_len = accepted drafts + 1 (as for greedy accept). */
+int oracle_probabilistic_accept(const float *target, const float *draft_probs, const int64_t *draft,
+                                const int32_t *proposal_len, const float *uniforms, int64_t *accepted,
+                                int32_t *accept_len, int32_t batch, int32_t draft_stride, int32_t P,
+                                int64_t vocab) {
+  uint64_t *w = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(vocab > 0 ? vocab : 1));
+  if (!w) return -2;
+  for (int32_t b = 0; b < batch; b++) {
+    int32_t pl = proposal_len[b];
+    if (pl < 0) pl = 0;
+    if (pl > P) pl = P;
+    const float *tb = target + (int64_t)b * (P + 1) * vocab;
+    const float *qb = draft_probs + (int64_t)b * P * vocab;
+    const float *ub = uniforms + (int64_t)b * (2 * P + 1);
+    int64_t *acc = accepted + (int64_t)b * (P + 1);
+    int32_t j = 0;
+    while (j < pl) {
+      const int64_t d = draft[(int64_t)b * draft_stride + j];
+      if (d < 0 || d >= vocab) break;
+      const float t = tb[(int64_t)j * vocab + d];
+      const float q = qb[(int64_t)j * vocab + d];
+      if (!(ub[j] * q < t)) break;
+      acc[j] = d;
+      j++;
+    }
+    int64_t pick = -1;
+    if (j < pl) {
+      for (int64_t v = 0; v < vocab; v++) {
+        float r = tb[(int64_t)j * vocab + v] - qb[(int64_t)j * vocab + v];
+        w[v] = oracle_weight(r);
+      }
+      pick = oracle_sample_weights(w, vocab, ub[P + j]);
+    }
+    if (pick < 0) {
+      const float ut = j < pl ? ub[P + j] : ub[2 * P];
+      for (int64_t v = 0; v < vocab; v++) w[v] = oracle_weight(tb[(int64_t)j * vocab + v]);
+      pick = oracle_sample_weights(w, vocab, ut);
+      if (pick < 0) pick = 0;
+    }
+    acc[j] = pick;
+    for (int32_t i = j + 1; i <= P; i++) acc[i] = -1;
+    accept_len[b] = j + 1;
+  }
+  free(w);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Array helpers for the tests (plain loops over the scalar functions).    */
 /* ------------------------------------------------------------------------ */
 

@@ -70,6 +70,15 @@ int oracle_greedy_accept(const uint16_t *logits, const int64_t *draft, const int
                          int64_t *accepted, int32_t *accept_len, int32_t batch,
                          int32_t draft_stride, int32_t P, int64_t vocab);
 
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+void oracle_fill_uniforms(float *u, int64_t n, uint64_t seed, uint64_t offset);
+uint64_t oracle_weight(float p);
+int64_t oracle_sample_weights(const uint64_t *w, int64_t n, float u);
+int oracle_probabilistic_accept(const float *target, const float *draft_probs, const int64_t *draft,
+                                const int32_t *proposal_len, const float *uniforms, int64_t *accepted,
+                                int32_t *accept_len, int32_t batch, int32_t draft_stride, int32_t P,
+                                int64_t vocab);
+
 #ifdef __cplusplus
 }
 #endif
