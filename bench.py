@@ -93,10 +93,15 @@ def algorithmic_bytes_per_step(vocab: int, rows: int, rank: int = 256) -> int:
     return vocab * rank * 2 + 2 * rows * vocab * 2
 
 
+LOOP_SOURCES = ("api.cu", "step_tc.cu", "step_simple.cu", "step_common.cuh", "markov_math.cuh", "ptx.cuh",
+                "kernels.h")
+
+
 def source_digest() -> str:
+    """Digest of the sources the loop's kernels and their launches are built from."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "dspark_markov_draft_anchor_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
+    for name in LOOP_SOURCES:
+        with open(os.path.join(ROOT, "dspark_markov_draft_anchor_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 

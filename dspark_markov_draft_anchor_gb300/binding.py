@@ -32,7 +32,8 @@ EXPORTED = (
     "dspark_markov_partial_count", "dspark_markov_bias_path", "dspark_markov_loop_kernels", "dspark_markov_get_status",
     "dspark_markov_get_status_detail",
     "dspark_markov_destroy", "dspark_build_verify_tokens", "dspark_greedy_accept_scratch_bytes",
-    "dspark_greedy_accept", "dspark_greedy_accept_noalloc", "dspark_strerror",
+    "dspark_greedy_accept", "dspark_greedy_accept_noalloc", "dspark_fill_uniforms",
+    "dspark_probabilistic_accept", "dspark_strerror",
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
     "dspark_check_logf", "dspark_check_tanhf", "dspark_noise_bound_tables",
 )
@@ -98,6 +99,8 @@ def load(build_if_missing: bool = False):
         "dspark_greedy_accept_scratch_bytes": (sz, [i32, i32, i32]),
         "dspark_greedy_accept": (ctypes.c_int, [P, P, P, P, P, P, sz, i32, i32, i32, i32, P]),
         "dspark_greedy_accept_noalloc": (ctypes.c_int, [P, P, P, P, P, i32, i32, i32, i32, P]),
+        "dspark_fill_uniforms": (ctypes.c_int, [P, i64, ctypes.c_uint64, ctypes.c_uint64, P]),
+        "dspark_probabilistic_accept": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i32, P]),
         "dspark_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "dspark_check_noise_range": (ctypes.c_int, [ctypes.c_uint32, P, i64, P]),
         "dspark_check_hash": (ctypes.c_int, [i64, i32, i64, ctypes.c_uint32, P, P, i64, P]),
@@ -245,6 +248,19 @@ def dspark_check_logf(x, y, n, stream=None):
 
 def dspark_check_tanhf(x, y, n, stream=None):
     _check(load().dspark_check_tanhf(_ptr(x), _ptr(y), n, _stream(stream)), "dspark_check_tanhf")
+
+
+def dspark_fill_uniforms(uniforms, n, seed, offset, stream=None):
+    _check(load().dspark_fill_uniforms(_ptr(uniforms), n, seed & (2**64 - 1), offset & (2**64 - 1),
+                                       _stream(stream)), "dspark_fill_uniforms")
+
+
+def dspark_probabilistic_accept(target_probs, draft_probs, draft, proposal_len, uniforms, accepted, accept_len,
+                                batch, draft_stride, P, vocab, stream=None):
+    _check(load().dspark_probabilistic_accept(_ptr(target_probs), _ptr(draft_probs), _ptr(draft),
+                                              _ptr(proposal_len), _ptr(uniforms), _ptr(accepted),
+                                              _ptr(accept_len), batch, draft_stride, P, vocab, _stream(stream)),
+           "dspark_probabilistic_accept")
 
 
 def dspark_noise_bound_tables(n: int = 512):

@@ -254,6 +254,45 @@ DSPARK_API int dspark_greedy_accept_noalloc(const void *logits, const int64_t *d
                                  int64_t *accepted, int32_t *accept_len, int32_t batch,
                                  int32_t draft_stride, int32_t P, int32_t vocab, cudaStream_t stream);
 
+/*
+ * dspark_fill_uniforms -- [P1] dsparkFillUniforms: n deterministic uniforms
+ * in [0, 1) into `uniforms` (device, float32).  Element i is word i % 4 of
+ * Philox4x32-10 (Salmon et al., SC 2011) at counter offset + i / 4 (a 64-bit
+ * number in the low two words, the high two zero) with key (lo32(seed),
+ * hi32(seed)), its top 24 bits times 2^-24 (a reading: the pages name the
+ * generator's seed and offset only).  n >= 0.  One kernel on `stream`.
+ */
+DSPARK_API int dspark_fill_uniforms(float *uniforms, int64_t n, uint64_t seed, uint64_t offset,
+                                    cudaStream_t stream);
+
+/*
+ * dspark_probabilistic_accept -- [P1] dsparkProbabilisticAccept, speculative
+ * sampling with residual sampling.  Device pointers:
+ *   target_probs [batch, P+1, vocab] float32, draft_probs [batch, P, vocab]
+ *   float32 (contiguous), draft [batch, draft_stride] int64, proposal_len
+ *   [batch] int32 (clamped to [0, P]), uniforms [batch, 2P+1] float32:
+ *   u[j] decides draft position j, u[P+j] the residual sample after a
+ *   rejection at j, u[2P] the bonus sample after a full accept.
+ * Position j accepts its draft token d when RN(u[j] * q) < t (t and q the
+ * target and draft probabilities of d; an id outside [0, vocab) is rejected).
+ * After a rejection at j the token is sampled from max(0, RN(t - q)) over the
+ * vocabulary (from the target row if that weighs nothing); after a full
+ * accept from target row P_b.  Sampling is an inverse CDF over fixed-point
+ * weights (probabilities clamped to [0, 1], truncated to units of 2^-40):
+ * U = floor(u 2^24), T = floor(U S / 2^24) for the total S, the smallest id
+ * whose inclusive prefix exceeds T (id 0 if the row weighs nothing) -- exact
+ * sums, so the id does not depend on any summation order (readings; the pages
+ * give the uniforms' layout and the method).  Writes accepted [batch, P+1]
+ * int64 (accepted drafts, the sample, then -1) and accept_len [batch] int32
+ * (accepted drafts + 1).  batch, P >= 0, vocab >= 1, draft_stride >= P.
+ * Allocates nothing; one kernel on `stream`.
+ */
+DSPARK_API int dspark_probabilistic_accept(const float *target_probs, const float *draft_probs,
+                                           const int64_t *draft, const int32_t *proposal_len,
+                                           const float *uniforms, int64_t *accepted, int32_t *accept_len,
+                                           int32_t batch, int32_t draft_stride, int32_t P, int32_t vocab,
+                                           cudaStream_t stream);
+
 /* A short English description of a DSPARK_* code (static storage). */
 DSPARK_API const char *dspark_strerror(int code);
 

@@ -361,17 +361,18 @@ def probabilistic_accept(target, draft_probs, draft, proposal_len, uniforms, P):
     [B, P, V] float32, ``uniforms`` [B, 2P+1]; returns (accepted, accept_len)."""
     target = _c(target, np.float32)
     draft_probs = _c(draft_probs, np.float32)
-    draft = np.asarray(draft, dtype=np.int64)
-    assert draft.strides[1] == 8
+    B, P1, V = target.shape
+    draft = np.asarray(draft, dtype=np.int64).reshape(B, -1)
+    assert draft.shape[1] < 2 or draft.strides[1] == 8
+    stride = draft.strides[0] // 8 if draft.size else max(P, 0)
     proposal_len = _c(proposal_len, np.int32)
     uniforms = _c(uniforms, np.float32)
-    B, P1, V = target.shape
     assert P1 == P + 1 and draft_probs.shape == (B, P, V) and uniforms.shape == (B, 2 * P + 1)
     accepted = np.empty((B, P + 1), np.int64)
     accept_len = np.empty(B, np.int32)
     rc = lib().oracle_probabilistic_accept(_ptr(target), _ptr(draft_probs), draft.ctypes.data,
                                            _ptr(proposal_len), _ptr(uniforms), _ptr(accepted),
-                                           _ptr(accept_len), B, draft.strides[0] // 8, P, V)
+                                           _ptr(accept_len), B, stride, P, V)
     if rc != 0:
         raise RuntimeError(f"oracle_probabilistic_accept failed: {rc}")
     return accepted, accept_len
