@@ -97,10 +97,11 @@ LOOP_SOURCES = ("api.cu", "step_tc.cu", "step_simple.cu", "step_common.cuh", "ma
                 "kernels.h")
 
 
-def source_digest() -> str:
-    """Digest of the sources the loop's kernels and their launches are built from."""
+def source_digest(sources=None) -> str:
+    """Digest of the sources a kernel and its launch are built from (the
+    loop's by default)."""
     h = hashlib.sha256()
-    for name in LOOP_SOURCES:
+    for name in sources or LOOP_SOURCES:
         with open(os.path.join(ROOT, "dspark_markov_draft_anchor_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -115,17 +116,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the loop kernel from the committed ncu
-    summary, if it was taken on the current kernel sources and this workload
-    (else None)."""
+def recorded_traffic(workload: str, sources=None):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, if
+    it was taken on the current sources of that kernel (the loop's by
+    default) and this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     entry = d.get(workload)
-    if not entry or entry.get("source_digest") != source_digest():
+    if not entry or entry.get("source_digest") != source_digest(sources):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -434,6 +435,153 @@ def run_native(args, d: Dist):
     return 0
 
 
+PV_B, PV_P, PV_V = 256, 5, 129280  # probabilistic verify: rows, drafts per row, vocabulary
+PV_SOURCES = ("prob_verify.cu", "ptx.cuh")
+PV_WORKLOAD = f"prob_verify_{PV_B}x{PV_P}x{PV_V}"
+
+
+def prob_verify_inputs(dev, seed: int):
+    """Seeded synthetic verify batch: target rows softmax(2.5 z), draft rows
+    softmax of the same logits plus 0.7 z' (so that drafts are accepted and
+    rejected), draft tokens drawn from the draft rows, full proposals."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(seed)
+    logits = torch.randn(PV_B, PV_P + 1, PV_V, device=dev, generator=g) * 2.5
+    target = torch.softmax(logits, -1)
+    draftp = torch.softmax(logits[:, :PV_P] + 0.7 * torch.randn(PV_B, PV_P, PV_V, device=dev, generator=g), -1)
+    draft = torch.multinomial(draftp.reshape(-1, PV_V), 1, generator=g).reshape(PV_B, PV_P).contiguous()
+    plen = torch.full((PV_B,), PV_P, dtype=torch.int32, device=dev)
+    return target.contiguous(), draftp.contiguous(), draft, plen
+
+
+def run_prob_verify(args, d: Dist):
+    """One step = uniforms for the batch (dspark_fill_uniforms) + the accept
+    with residual / bonus sampling (dspark_probabilistic_accept) over 256 rows
+    x 5 drafts, V = 129280, inputs resident in HBM, L2 flushed before each."""
+    import torch
+    from dspark_markov_draft_anchor_gb300 import binding
+
+    torch.cuda.set_device(d.local_rank)
+    dev = torch.device("cuda", d.local_rank)
+    d.init("nccl")
+    B, P, V = PV_B, PV_P, PV_V
+    target, draftp, draft, plen = prob_verify_inputs(dev, 1234 + d.rank)
+    nu = B * (2 * P + 1)
+    u = torch.empty(nu, dtype=torch.float32, device=dev)
+    acc = torch.empty(B, P + 1, dtype=torch.int64, device=dev)
+    alen = torch.empty(B, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def verify():
+        binding.dspark_fill_uniforms(u, nu, 99, 0, stream)
+        binding.dspark_probabilistic_accept(target, draftp, draft, plen, u, acc, alen, B, P, P, V, stream)
+
+    def timed(n, fn):
+        ev = []
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                flush.fill_(1)  # enqueued first: the launches below queue behind it
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                ev.append((e0, e1))
+        return ev
+
+    def mean_us(ev):
+        torch.cuda.synchronize()
+        return statistics.mean([e0.elapsed_time(e1) for e0, e1 in ev]) * 1e3
+
+    timed(max(args.warmup, 3), verify)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(d.local_rank)
+    if d.rank == 0:
+        clocks.start()
+    d.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    ev = timed(args.steps, verify)
+    torch.cuda.synchronize()
+    d.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clock_info = clocks.stop() if d.rank == 0 else None
+    step_us = d.max(mean_us(ev), dev)
+
+    def accept_only():
+        binding.dspark_probabilistic_accept(target, draftp, draft, plen, u, acc, alen, B, P, P, V, stream)
+
+    timed(3, accept_only)
+    kernel_us = mean_us(timed(max(10, min(args.steps, 200)), accept_only))
+    torch.cuda.synchronize()
+    lens = alen.cpu().numpy()
+    rejected = int((lens <= plen.cpu().numpy()).sum())
+    algo = rejected * 8 * V + (B - rejected) * 4 * V  # residual: t and q rows; full accept: the bonus row
+
+    # end to end through the C ABI from pinned host buffers
+    hb = {"target": target.cpu().pin_memory(), "draftp": draftp.cpu().pin_memory(),
+          "draft": draft.cpu().pin_memory(), "plen": plen.cpu().pin_memory()}
+    h_acc = torch.empty_like(acc, device="cpu").pin_memory()
+    h_len = torch.empty_like(alen, device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hb.values())
+    d2h = h_acc.numel() * 8 + h_len.numel() * 4
+
+    def e2e():
+        target.copy_(hb["target"], non_blocking=True)
+        draftp.copy_(hb["draftp"], non_blocking=True)
+        draft.copy_(hb["draft"], non_blocking=True)
+        plen.copy_(hb["plen"], non_blocking=True)
+        verify()
+        h_acc.copy_(acc, non_blocking=True)
+        h_len.copy_(alen, non_blocking=True)
+
+    timed(2, e2e)
+    e2e_us = d.max(mean_us(timed(max(5, min(args.steps, 20)), e2e)), dev)
+    torch.cuda.synchronize()
+
+    result = None
+    if d.rank == 0:
+        peak, peak_kind = measured_peaks()
+        achieved = algo / (kernel_us * 1e-6) / 1e9
+        cpu = None
+        if args.cpu_baseline and d.world == 1:
+            import oracle
+            rs = B  # the whole batch: well under a second of oracle time
+            tt, qq = target[:rs].cpu().numpy(), draftp[:rs].cpu().numpy()
+            dd, pp = draft[:rs].cpu().numpy(), plen[:rs].cpu().numpy()
+            uu = u.view(B, 2 * P + 1)[:rs].cpu().numpy()
+            t0 = time.perf_counter()
+            oracle.fill_uniforms(nu, 99, 0)
+            oracle.probabilistic_accept(tt, qq, dd, pp, uu, P)
+            dt = time.perf_counter() - t0
+            cpu = {"value": dt * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+                   "sample": f"the whole batch of {B} rows, one step ({dt:.2f} s wall)"}
+        result = {
+            "metric": "µs per probabilistic verify (uniforms + speculative accept with residual sampling)",
+            "value": step_us, "unit": "us", "n_gpus": d.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_us / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 probabilities, u64 fixed-point sums", "data": "synthetic (seeded)",
+            "config": {"workload": f"probabilistic verify: {B} rows x {P} drafts, vocab {V}, full proposals",
+                       "parallelism": f"replicas x{d.world} (rows sharded, no collective)",
+                       "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed step"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": recorded_traffic(PV_WORKLOAD, PV_SOURCES), "peak_kind": f"{peak_kind} hbm_gbs",
+                         "kernel": "prob_accept_kernel", "kernel_us": kernel_us,
+                         "algorithmic_bytes": algo, "rows_rejected": rejected,
+                         "kernel_us_from": "CUDA events around the accept launch alone, L2 flushed"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * 2,
+            "clocks": clock_info,
+            "wall_timed_s": t_wall,
+        }
+    d.close()
+    if result is not None:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -446,8 +594,15 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     p.add_argument("--bias-path", choices=["auto", "fma", "mma"], default="auto",
                    help="bias contraction: the library's choice by row count, or forced")
+    p.add_argument("--path", choices=["draft_loop", "prob_verify"], default="draft_loop",
+                   help="the draft loop (headline) or the probabilistic verify of a 256 x 5 x 129280 batch")
     args = p.parse_args(argv)
     d = Dist()
+    if args.path == "prob_verify":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the draft loop only"}))
+            return 0
+        return run_prob_verify(args, d)
     if args.impl == "reference":
         return run_reference(args, d)
     return run_native(args, d)

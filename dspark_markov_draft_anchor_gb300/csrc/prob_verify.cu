@@ -12,6 +12,7 @@
 #include <stdint.h>
 
 #include "dspark_markov.h"
+#include "ptx.cuh"
 
 namespace dspark {
 namespace {
@@ -52,11 +53,19 @@ __global__ void fill_uniforms_kernel(float* __restrict__ u, int64_t n, uint64_t 
 }
 
 // A probability as a weight in units of 2^-40: [0, 1] clamped (NaN and
-// negatives weigh 0), truncated.  p * 2^40 is exact in FP32.
+// negatives weigh 0), truncated.  For 0 < p < 1 the value is the 24-bit
+// significand m (implicit bit included; subnormals use exponent field 1)
+// shifted by e - 110 (e the biased exponent field), i.e. floor(p 2^40), in
+// integer instructions only: a float-to-64-bit conversion would run on the
+// FP64 pipe, which this part has little of.
 __device__ __forceinline__ uint64_t weight(float p) {
   if (!(p > 0.0f)) return 0ull;
   if (p >= 1.0f) return 1ull << 40;
-  return __float2ull_rz(p * 0x1p40f);
+  const uint32_t b = __float_as_uint(p);
+  const uint32_t e = b >> 23;
+  const uint32_t m = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+  const int sh = static_cast<int>(e ? e : 1u) - 110;  // <= 16
+  return sh >= 0 ? static_cast<uint64_t>(m) << sh : static_cast<uint64_t>(m >> (-sh < 31 ? -sh : 31));
 }
 
 // T = floor(U S / 2^24), U = floor(u 2^24) clamped to [0, 2^24 - 1].
@@ -74,111 +83,409 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t x) {
   return x;
 }
 
-constexpr int kAcceptThreads = 256;
-constexpr int kAcceptWarps = kAcceptThreads / 32;
-
-// The weight of id v of the row being sampled: the residual max(0, RN(t - q))
-// when q is given, else the target probability.
-__device__ __forceinline__ uint64_t row_weight(const float* t, const float* q, int64_t v) {
-  return q ? weight(__fsub_rn(t[v], q[v])) : weight(t[v]);
+__device__ __forceinline__ uint64_t warp_incl_scan_u64(uint64_t x, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  return x;
 }
 
-// Inverse-CDF sample of one row by the whole CTA: warp w sums the weights of
-// its contiguous segment (lanes strided, loads coalesced), thread 0 finds the
-// segment holding the threshold, and that warp rescans it 32 ids at a time
-// with a warp prefix sum.  Returns -1 (in every thread) when the row weighs 0.
-__device__ int64_t sample_row(const float* t, const float* q, int64_t vocab, float u, uint64_t* s_seg,
-                              int64_t* s_pick) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t seg = (vocab + kAcceptWarps - 1) / kAcceptWarps;
-  const int64_t b0 = warp * seg, b1 = b0 + seg < vocab ? b0 + seg : vocab;
-  uint64_t part = 0;
-  for (int64_t v = b0 + lane; v < b1; v += 32) part += row_weight(t, q, v);
-  part = warp_sum_u64(part);
-  if (lane == 0) s_seg[warp] = part;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint64_t total = 0;
-    for (int w = 0; w < kAcceptWarps; ++w) total += s_seg[w];
-    int64_t pick = -1;
-    if (total > 0) {
-      const uint64_t T = threshold(u, total);
-      uint64_t before = 0;
-      int w = 0;
-      while (before + s_seg[w] <= T) before += s_seg[w++];  // T < total: stops at a segment
-      s_seg[kAcceptWarps] = T - before;                   // threshold within segment w
-      pick = -2 - w;                                      // segment to rescan
+constexpr int kAcceptThreads = 512;
+constexpr int kAcceptWarps = kAcceptThreads / 32;
+constexpr int kScanSpan = 4 * kAcceptThreads;  // ids one block-wide scan covers
+constexpr int kMaxChunks = 1024;               // chunk totals kept in shared memory
+constexpr int kPiece = 512;                    // ids one warp streams per bulk copy
+static_assert(kPiece / 32 <= 16, "wacc adds at most 16 halves exactly");
+constexpr uint32_t kCopyWaitLimit = 1u << 24;  // polls of a copy's mbarrier
+constexpr size_t kStageBytes = size_t{kAcceptWarps} * 2 * kPiece * sizeof(float);
+
+// One row being sampled: the target row t and, for a residual, the draft
+// row q (null for the target row itself).  vec: both rows start on a
+// 16-byte boundary, so groups of four ids load as float4; bulk: also a
+// vocabulary of a multiple of four ids, so that every piece of the row is a
+// whole number of 16-byte units and streams by bulk copies.
+struct Row {
+  const float* t;
+  const float* q;
+  int64_t vocab;
+  bool vec;
+  bool bulk;
+};
+
+// Warp w's staging area: one piece of t and one of q, refilled by the warp
+// itself once it has read them, completing on mbarrier full[w].  `used`
+// counts the pieces the warp has taken from it (the next one's phase parity
+// is used & 1); `failed` is set when a wait gave up.
+struct Stage {
+  float* buf;
+  uint64_t* full;
+  uint32_t used;
+  bool failed;
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   ptx::smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(ptx::smem_addr(bar))
+               : "memory");
+}
+
+// The weights of ids v .. v+3 (ids past the end weigh 0): max(0, RN(t - q))
+// for a residual, else t, each through weight().
+__device__ __forceinline__ void weights4(const Row& r, int64_t v, uint64_t w[4]) {
+  if (r.vec && v + 4 <= r.vocab) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(r.t + v));
+    if (r.q) {
+      const float4 b = __ldg(reinterpret_cast<const float4*>(r.q + v));
+      w[0] = weight(__fsub_rn(a.x, b.x));
+      w[1] = weight(__fsub_rn(a.y, b.y));
+      w[2] = weight(__fsub_rn(a.z, b.z));
+      w[3] = weight(__fsub_rn(a.w, b.w));
+    } else {
+      w[0] = weight(a.x);
+      w[1] = weight(a.y);
+      w[2] = weight(a.z);
+      w[3] = weight(a.w);
     }
-    *s_pick = pick;
+    return;
   }
-  __syncthreads();
-  const int64_t code = *s_pick;
-  if (code == -1) return -1;
-  const int target_warp = static_cast<int>(-2 - code);
-  if (warp == target_warp) {
-    const uint64_t Tw = s_seg[kAcceptWarps];
-    uint64_t run = 0;
-    for (int64_t base = b0; base < b1; base += 32) {
-      const int64_t v = base + lane;
-      const uint64_t x = v < b1 ? row_weight(t, q, v) : 0ull;
-      uint64_t incl = x;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
+  for (int k = 0; k < 4; ++k) {
+    const int64_t x = v + k;
+    w[k] = x < r.vocab ? (r.q ? weight(__fsub_rn(r.t[x], r.q[x])) : weight(r.t[x])) : 0ull;
+  }
+}
+
+template <bool kRes>
+__device__ __forceinline__ uint64_t weight_at(const Row& r, int64_t x) {
+  return kRes ? weight(__fsub_rn(r.t[x], r.q[x])) : weight(r.t[x]);
+}
+
+// The same weight on the FP32 pipe, split in two exact halves and added to
+// two float accumulators: with y = c 2^20 (c the probability clamped to
+// [0, 1], NaN to 0 by fmaxf), floor(c 2^40) = floor(y) 2^20 +
+// floor(frac(y) 2^20); each floor is a round-toward-zero add of 2^23 (exact
+// for values below 2^23), frac(y) = y - floor(y) is exact, and each half is an
+// integer of at most 2^20, so up to 16 of them add exactly in FP32.  Sixteen
+// ids cost ten FP32 operations each and one conversion pair (wflush) instead
+// of about twenty integer ones each.
+__device__ __forceinline__ void wacc(float p, float& hi, float& lo) {
+  const float c = fminf(fmaxf(p, 0.0f), 1.0f);
+  const float y = c * 0x1p20f;
+  const float fl = __fsub_rn(__fadd_rz(y, 0x1p23f), 0x1p23f);
+  hi += fl;
+  lo += __fsub_rn(__fmaf_rz(__fsub_rn(y, fl), 0x1p20f, 0x1p23f), 0x1p23f);
+}
+
+__device__ __forceinline__ uint64_t wflush(float hi, float lo) {
+  return (static_cast<uint64_t>(__float2uint_rz(hi)) << 20) + __float2uint_rz(lo);
+}
+
+template <bool kRes>
+__device__ __forceinline__ void wacc4(float4 a, float4 b, float& hi, float& lo) {
+  wacc(kRes ? __fsub_rn(a.x, b.x) : a.x, hi, lo);
+  wacc(kRes ? __fsub_rn(a.y, b.y) : a.y, hi, lo);
+  wacc(kRes ? __fsub_rn(a.z, b.z) : a.z, hi, lo);
+  wacc(kRes ? __fsub_rn(a.w, b.w) : a.w, hi, lo);
+}
+
+template <bool kRes>
+__device__ __forceinline__ uint64_t weight_sum4(float4 a, float4 b) {
+  float hi = 0.0f, lo = 0.0f;
+  wacc4<kRes>(a, b, hi, lo);
+  return wflush(hi, lo);
+}
+
+// The weight of ids [c0, c1) summed by one warp (all lanes get the total).
+// The main loops issue four loads per row before using any, with no branch
+// between them, so that each lane keeps several requests in flight.
+template <bool kRes>
+__device__ __forceinline__ uint64_t chunk_sum(const Row& r, int64_t c0, int64_t c1, int lane) {
+  uint64_t part = 0;
+  if (r.vec) {
+    const int64_t groups = (c1 - c0) >> 2;  // whole float4 groups
+    const float4* t4 = reinterpret_cast<const float4*>(r.t + c0);
+    const float4* q4 = reinterpret_cast<const float4*>(kRes ? r.q + c0 : r.t + c0);
+    int64_t g = lane;
+    for (; g + 96 < groups; g += 128) {
+      const float4 a0 = __ldg(t4 + g), a1 = __ldg(t4 + g + 32), a2 = __ldg(t4 + g + 64), a3 = __ldg(t4 + g + 96);
+      float4 b0 = a0, b1 = a1, b2 = a2, b3 = a3;
+      if (kRes) {
+        b0 = __ldg(q4 + g);
+        b1 = __ldg(q4 + g + 32);
+        b2 = __ldg(q4 + g + 64);
+        b3 = __ldg(q4 + g + 96);
       }
-      const unsigned hit = __ballot_sync(0xFFFFFFFFu, run + incl > Tw);
-      if (hit) {
-        if (lane == 0) *s_pick = base + __ffs(hit) - 1;
-        break;
+      float hi = 0.0f, lo = 0.0f;  // 16 ids: exact (see wacc)
+      wacc4<kRes>(a0, b0, hi, lo);
+      wacc4<kRes>(a1, b1, hi, lo);
+      wacc4<kRes>(a2, b2, hi, lo);
+      wacc4<kRes>(a3, b3, hi, lo);
+      part += wflush(hi, lo);
+    }
+    for (; g < groups; g += 32) part += weight_sum4<kRes>(__ldg(t4 + g), kRes ? __ldg(q4 + g) : float4{});
+    const int64_t x = c0 + 4 * groups + lane;  // at most three ids left
+    if (x < c1) part += weight_at<kRes>(r, x);
+  } else {
+    int64_t x = c0 + lane;
+    for (; x + 96 < c1; x += 128) {
+      const float a0 = r.t[x], a1 = r.t[x + 32], a2 = r.t[x + 64], a3 = r.t[x + 96];
+      if (kRes) {
+        const float b0 = r.q[x], b1 = r.q[x + 32], b2 = r.q[x + 64], b3 = r.q[x + 96];
+        part += (weight(__fsub_rn(a0, b0)) + weight(__fsub_rn(a1, b1))) +
+                (weight(__fsub_rn(a2, b2)) + weight(__fsub_rn(a3, b3)));
+      } else {
+        part += (weight(a0) + weight(a1)) + (weight(a2) + weight(a3));
       }
-      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    for (; x < c1; x += 32) part += weight_at<kRes>(r, x);
+  }
+  return warp_sum_u64(part);
+}
+
+// Stage 1 over bulk copies: warp w streams pieces w, w + kAcceptWarps, ...
+// of the row (kPiece ids of t, and of q for a residual) into its own stage,
+// sums each piece's weights (16 ids a lane, float4 reads of shared memory),
+// hands the stage back to the copy engine for its next piece as soon as the
+// values are in registers, and adds the piece's total to its chunk's.
+template <bool kRes>
+__device__ __forceinline__ void stream_sums(const Row& r, int64_t chunk_len, uint64_t* chunk, Stage& st, int warp,
+                                            int lane) {
+  const int64_t n_pieces = (r.vocab + kPiece - 1) / kPiece;
+  float* st_t = st.buf;
+  float* st_q = st.buf + kPiece;
+  auto issue = [&](int64_t piece) {
+    const int64_t v0 = piece * kPiece;
+    const uint32_t bytes = static_cast<uint32_t>((r.vocab - v0 < kPiece ? r.vocab - v0 : kPiece) * sizeof(float));
+    ptx::mbar_arrive_expect_tx(st.full, kRes ? 2 * bytes : bytes);
+    bulk_load(st_t, r.t + v0, bytes, st.full);
+    if (kRes) bulk_load(st_q, r.q + v0, bytes, st.full);
+  };
+  int64_t piece = warp;
+  if (lane == 0 && piece < n_pieces) issue(piece);
+  for (; piece < n_pieces; piece += kAcceptWarps) {
+    if (!ptx::mbar_wait(st.full, st.used & 1, kCopyWaitLimit)) {
+      st.failed = true;  // leave the copy to land (bounded) before the kernel exits
+      ptx::mbar_wait(st.full, st.used & 1, kCopyWaitLimit);
+      return;
+    }
+    ++st.used;
+    const int64_t v0 = piece * kPiece;
+    const int64_t cnt = r.vocab - v0 < kPiece ? r.vocab - v0 : kPiece;  // a multiple of 4
+    float hi = 0.0f, lo = 0.0f;  // kPiece / 32 = 16 ids a lane: exact (see wacc)
+#pragma unroll
+    for (int k = 0; k < kPiece / 128; ++k) {
+      const int e = 4 * (lane + 32 * k);
+      if (e < cnt) {
+        const float4 a = *reinterpret_cast<const float4*>(st_t + e);
+        const float4 b = kRes ? *reinterpret_cast<const float4*>(st_q + e) : a;
+        wacc4<kRes>(a, b, hi, lo);
+      }
+    }
+    uint64_t part = wflush(hi, lo);
+    __syncwarp();
+    if (lane == 0 && piece + kAcceptWarps < n_pieces) issue(piece + kAcceptWarps);
+    part = warp_sum_u64(part);
+    if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&chunk[v0 / chunk_len]), part);
+  }
+}
+
+struct SampleSmem {
+  uint64_t chunk[kMaxChunks];  // weight of each chunk of the row
+  uint64_t wsum[kAcceptWarps];  // block scan: each warp's total
+  uint64_t rest;                // threshold left inside the chosen chunk
+  int64_t chunk_id;             // chosen chunk, -1 when the row weighs 0
+  int64_t pick;
+};
+
+// Inverse-CDF sample of one row by the whole CTA, in three steps:
+//  1. the row is cut into chunks of chunk_len ids (kScanSpan, or a multiple
+//     of it for rows of more than kMaxChunks spans) and each chunk's total
+//     weight is kept: streamed through shared memory by bulk copies where
+//     the row allows (stream_sums), else warp w sums chunks w,
+//     w + kAcceptWarps, ... with float4 or scalar loads;
+//  2. warp 0 adds the totals, takes T from u, and finds the chunk whose
+//     running total first exceeds T (a warp scan over 32 chunks at a time);
+//  3. the CTA scans that chunk kScanSpan ids at a time (four ids a thread,
+//     a block-wide exclusive scan of the thread sums) and the one thread
+//     whose range holds the threshold picks the id.
+// Returns -1 (in every thread) when the row weighs 0.
+__device__ int64_t sample_row(const Row& r, float u, SampleSmem& sm, Stage& st) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t spans = (r.vocab + kScanSpan - 1) / kScanSpan;
+  const int64_t chunk_len = kScanSpan * ((spans + kMaxChunks - 1) / kMaxChunks);
+  const int64_t n_chunks = (r.vocab + chunk_len - 1) / chunk_len;
+
+  if (r.bulk) {
+    for (int64_t c = threadIdx.x; c < n_chunks; c += kAcceptThreads) sm.chunk[c] = 0;
+    __syncthreads();
+    if (r.q)
+      stream_sums<true>(r, chunk_len, sm.chunk, st, warp, lane);
+    else
+      stream_sums<false>(r, chunk_len, sm.chunk, st, warp, lane);
+  } else {
+    for (int64_t c = warp; c < n_chunks; c += kAcceptWarps) {
+      const int64_t c0 = c * chunk_len;
+      const int64_t c1 = c0 + chunk_len < r.vocab ? c0 + chunk_len : r.vocab;
+      const uint64_t part = r.q ? chunk_sum<true>(r, c0, c1, lane) : chunk_sum<false>(r, c0, c1, lane);
+      if (lane == 0) sm.chunk[c] = part;
     }
   }
   __syncthreads();
-  const int64_t pick = *s_pick;
-  __syncthreads();  // s_pick and s_seg are reused by the next call
+
+  if (warp == 0) {
+    uint64_t total = 0;
+    for (int64_t c = lane; c < n_chunks; c += 32) total += sm.chunk[c];
+    total = warp_sum_u64(total);
+    int64_t chosen = -1;
+    uint64_t rest = 0;
+    if (total > 0) {
+      const uint64_t T = threshold(u, total);  // T < total: some chunk holds it
+      uint64_t run = 0;
+      for (int64_t base = 0; base < n_chunks; base += 32) {
+        const int64_t c = base + lane;
+        const uint64_t x = c < n_chunks ? sm.chunk[c] : 0ull;
+        const uint64_t incl = warp_incl_scan_u64(x, lane);
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, run + incl > T);
+        if (hit) {
+          const int src = __ffs(hit) - 1;
+          const uint64_t before = run + __shfl_sync(0xFFFFFFFFu, incl - x, src);
+          chosen = base + src;
+          rest = T - before;
+          break;
+        }
+        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+    }
+    if (lane == 0) {
+      sm.chunk_id = chosen;
+      sm.rest = rest;
+      sm.pick = -1;
+    }
+  }
+  __syncthreads();
+  const int64_t chosen = sm.chunk_id;
+  if (chosen < 0) {
+    __syncthreads();  // sm is reused by the next call
+    return -1;
+  }
+
+  uint64_t rest = sm.rest;
+  const int64_t c_end = (chosen + 1) * chunk_len < r.vocab ? (chosen + 1) * chunk_len : r.vocab;
+  for (int64_t s0 = chosen * chunk_len; s0 < c_end; s0 += kScanSpan) {
+    const int64_t v = s0 + 4 * threadIdx.x;
+    uint64_t w[4];
+    weights4(r, v, w);
+    const uint64_t mine = (w[0] + w[1]) + (w[2] + w[3]);
+    const uint64_t incl = warp_incl_scan_u64(mine, lane);
+    if (lane == 31) sm.wsum[warp] = incl;
+    __syncthreads();
+    uint64_t offset = 0, span_total = 0;
+#pragma unroll
+    for (int k = 0; k < kAcceptWarps; ++k) {
+      const uint64_t x = sm.wsum[k];
+      if (k < warp) offset += x;
+      span_total += x;
+    }
+    const uint64_t excl = offset + incl - mine;
+    if (rest >= excl && rest - excl < mine) {  // exactly one thread, when rest < span_total
+      uint64_t left = rest - excl;  // < mine, so one of the four ids holds it
+      int k = 3;
+      if (left < w[0]) {
+        k = 0;
+      } else if ((left -= w[0]) < w[1]) {
+        k = 1;
+      } else if (left - w[1] < w[2]) {
+        k = 2;
+      }
+      sm.pick = v + k;
+    }
+    __syncthreads();
+    if (sm.pick >= 0) break;
+    rest -= span_total;
+  }
+  const int64_t pick = sm.pick;
+  __syncthreads();  // sm is reused by the next call
   return pick;
 }
 
-// One CTA per batch row: the accept chain on thread 0, then one inverse-CDF
-// sample (the residual after a rejection, else the bonus) by the whole CTA.
-__global__ void __launch_bounds__(kAcceptThreads)
+// One CTA per batch row.  Warp 0 evaluates up to 32 positions of the accept
+// chain at once (draft id, then the two probabilities at it) and the first
+// rejection ends it; then the CTA draws one inverse-CDF sample: the residual
+// after a rejection (the target row when that weighs 0), else the bonus.
+__global__ void __launch_bounds__(kAcceptThreads, 2)
     prob_accept_kernel(const float* __restrict__ target, const float* __restrict__ draft_probs,
                        const int64_t* __restrict__ draft, const int32_t* __restrict__ proposal_len,
                        const float* __restrict__ uniforms, int64_t* __restrict__ accepted,
                        int32_t* __restrict__ accept_len, int32_t draft_stride, int32_t P, int64_t vocab) {
-  __shared__ uint64_t s_seg[kAcceptWarps + 1];
-  __shared__ int64_t s_pick;
-  __shared__ int s_j, s_pl;
+  extern __shared__ __align__(128) float s_stage[];  // kStageBytes: one stage per warp
+  __shared__ SampleSmem sm;
+  __shared__ __align__(8) uint64_t s_full[kAcceptWarps];
+  __shared__ int s_j, s_pl, s_failed;
+  if (threadIdx.x < kAcceptWarps) ptx::mbar_init(&s_full[threadIdx.x], 1);
+  if (threadIdx.x == 0) s_failed = 0;
+  ptx::fence_mbar_init();
   const int b = blockIdx.x;
   const float* tb = target + static_cast<int64_t>(b) * (P + 1) * vocab;
   const float* qb = draft_probs + static_cast<int64_t>(b) * P * vocab;
   const float* ub = uniforms + static_cast<int64_t>(b) * (2 * P + 1);
   int64_t* acc = accepted + static_cast<int64_t>(b) * (P + 1);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
     int pl = proposal_len[b];
     pl = pl < 0 ? 0 : (pl > P ? P : pl);
-    int j = 0;
-    while (j < pl) {
-      const int64_t d = draft[static_cast<int64_t>(b) * draft_stride + j];
-      if (d < 0 || d >= vocab) break;
-      const float t = tb[static_cast<int64_t>(j) * vocab + d];
-      const float q = qb[static_cast<int64_t>(j) * vocab + d];
-      if (!(__fmul_rn(ub[j], q) < t)) break;
-      acc[j] = d;
-      ++j;
+    int j = pl;
+    for (int base = 0; base < pl; base += 32) {
+      const int i = base + lane;
+      bool ok = false;
+      int64_t d = 0;
+      if (i < pl) {
+        d = draft[static_cast<int64_t>(b) * draft_stride + i];
+        if (d >= 0 && d < vocab) {
+          const float t = tb[static_cast<int64_t>(i) * vocab + d];
+          const float q = qb[static_cast<int64_t>(i) * vocab + d];
+          ok = __fmul_rn(ub[i], q) < t;
+        }
+      }
+      const unsigned fail = __ballot_sync(0xFFFFFFFFu, i < pl && !ok);
+      const int first = fail ? base + __ffs(fail) - 1 : pl;
+      if (i < first) acc[i] = d;
+      if (fail) {
+        j = first;
+        break;
+      }
     }
-    s_j = j;
-    s_pl = pl;
+    if (lane == 0) {
+      s_j = j;
+      s_pl = pl;
+    }
   }
   __syncthreads();
   const int j = s_j, pl = s_pl;
+  const int warp = threadIdx.x >> 5;
+  Stage st{s_stage + warp * 2 * kPiece, &s_full[warp], 0u, false};
   const float* trow = tb + static_cast<int64_t>(j) * vocab;
+  const bool t_vec = (reinterpret_cast<uintptr_t>(trow) & 15u) == 0;
+  const bool four = (vocab & 3) == 0;
   int64_t pick = -1;
-  if (j < pl) pick = sample_row(trow, qb + static_cast<int64_t>(j) * vocab, vocab, ub[P + j], s_seg, &s_pick);
-  if (pick < 0) pick = sample_row(trow, nullptr, vocab, j < pl ? ub[P + j] : ub[2 * P], s_seg, &s_pick);
+  if (j < pl) {
+    const float* qrow = qb + static_cast<int64_t>(j) * vocab;
+    const bool vec = t_vec && (reinterpret_cast<uintptr_t>(qrow) & 15u) == 0;
+    pick = sample_row(Row{trow, qrow, vocab, vec, vec && four}, ub[P + j], sm, st);
+  }
+  if (st.failed) s_failed = 1;
+  __syncthreads();
+  if (pick < 0 && !s_failed)
+    pick = sample_row(Row{trow, nullptr, vocab, t_vec, t_vec && four}, j < pl ? ub[P + j] : ub[2 * P], sm, st);
+  if (st.failed) s_failed = 1;
+  __syncthreads();
   if (threadIdx.x == 0) {
+    if (s_failed) {  // a copy wait gave up: the row is marked, not sampled
+      accept_len[b] = 0;
+      return;
+    }
     acc[j] = pick < 0 ? 0 : pick;
     for (int i = j + 1; i <= P; ++i) acc[i] = -1;
     accept_len[b] = j + 1;
@@ -211,7 +518,14 @@ int dspark_probabilistic_accept(const float* target_probs, const float* draft_pr
   if (!target_probs || !uniforms || !accepted || !accept_len || !proposal_len ||
       (P > 0 && (!draft_probs || !draft)))
     return DSPARK_ERR_INVALID_ARG;
-  dspark::prob_accept_kernel<<<batch, dspark::kAcceptThreads, 0, stream>>>(
+  static bool attr_set = false;  // the attribute is idempotent; a race only repeats it
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(dspark::prob_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dspark::kStageBytes)) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    attr_set = true;
+  }
+  dspark::prob_accept_kernel<<<batch, dspark::kAcceptThreads, dspark::kStageBytes, stream>>>(
       target_probs, draft_probs, draft, proposal_len, uniforms, accepted, accept_len, draft_stride, P, vocab);
   return dspark::done();
 }

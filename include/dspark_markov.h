@@ -285,7 +285,9 @@ DSPARK_API int dspark_fill_uniforms(float *uniforms, int64_t n, uint64_t seed, u
  * give the uniforms' layout and the method).  Writes accepted [batch, P+1]
  * int64 (accepted drafts, the sample, then -1) and accept_len [batch] int32
  * (accepted drafts + 1).  batch, P >= 0, vocab >= 1, draft_stride >= P.
- * Allocates nothing; one kernel on `stream`.
+ * Allocates nothing; one kernel on `stream`.  A row whose bounded wait for a
+ * shared-memory copy gave up (never in correct operation) gets accept_len 0
+ * and its accepted entries are left unwritten.
  */
 DSPARK_API int dspark_probabilistic_accept(const float *target_probs, const float *draft_probs,
                                            const int64_t *draft, const int32_t *proposal_len,

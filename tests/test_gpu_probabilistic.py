@@ -54,7 +54,8 @@ def _gpu_accept(target, draftp, draft, plen, u, P, draft_stride=None):
     return acc.cpu().numpy(), alen.cpu().numpy()
 
 
-@pytest.mark.parametrize("B,P,V", [(64, 5, 4099), (33, 1, 1), (17, 3, 300), (8, 0, 1000), (40, 6, 32768 + 5)])
+@pytest.mark.parametrize("B,P,V", [(64, 5, 4099), (33, 1, 1), (17, 3, 300), (8, 0, 1000), (40, 6, 32768 + 5),
+                                   (24, 4, 4096), (20, 3, 12000), (3, 2, 2 * 1024 * 2048 + 4100)])
 def test_probabilistic_accept_matches_oracle(B, P, V):
     rng = np.random.default_rng(B * 1000 + P * 10 + V % 97)
     target, draftp, draft, plen, u = _case(rng, B, P, V)
@@ -95,7 +96,8 @@ def test_probabilistic_accept_strided_draft_and_errors():
 
 
 def test_probabilistic_accept_full_size():
-    """The stress256 verify shape: 256 rows, P = 5, V = 129280."""
+    """256 rows, P = 5, V = 129280 (the vocabulary of the step kernel's
+    largest workloads)."""
     rng = np.random.default_rng(17)
     B, P, V = 256, 5, 129280
     target, draftp, draft, plen, u = _case(rng, B, P, V, scale=2.5)
