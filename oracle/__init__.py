@@ -121,6 +121,9 @@ def lib():
             "oracle_weight": (ctypes.c_uint64, [f32]),
             "oracle_sample_weights": (i64, [P, i64, f32]),
             "oracle_probabilistic_accept": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i64]),
+            "oracle_expf_nonpos": (f32, [f32]),
+            "oracle_expf_nonpos_array": (None, [P, P, i64]),
+            "oracle_logits_to_probs": (ctypes.c_int, [P, P, i32, i64, f32, i32, f32]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -376,3 +379,25 @@ def probabilistic_accept(target, draft_probs, draft, proposal_len, uniforms, P):
     if rc != 0:
         raise RuntimeError(f"oracle_probabilistic_accept failed: {rc}")
     return accepted, accept_len
+
+
+def expf_nonpos(x):
+    """The oracle's own exp for x <= 0 (float32 in, float32 out)."""
+    x = _c(x, np.float32)
+    out = np.empty_like(x)
+    lib().oracle_expf_nonpos_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def logits_to_probs(logits, temperature, top_k, top_p):
+    """[P1] dsparkLogitsToProbabilities: ``logits`` [rows, V] float32 to a
+    dense probability row after temperature, top-k and top-p (readings in
+    the C source)."""
+    logits = _c(logits, np.float32)
+    rows, V = logits.shape
+    probs = np.empty_like(logits)
+    rc = lib().oracle_logits_to_probs(_ptr(logits), _ptr(probs), rows, V, float(temperature), int(top_k),
+                                      float(top_p))
+    if rc != 0:
+        raise RuntimeError(f"oracle_logits_to_probs failed: {rc}")
+    return probs

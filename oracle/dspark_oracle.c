@@ -740,6 +740,142 @@ int oracle_probabilistic_accept(const float *target, const float *draft_probs, c
 }
 
 /* ------------------------------------------------------------------------ */
+/* [P1] dsparkLogitsToProbabilities: a dense probability row after         */
+/* temperature, top-k and top-p.  The pages name the three filters only;   */
+/* the arithmetic below is this build's reading, chosen so that every      */
+/* decision is an exact comparison:                                        */
+/*   - NaN logits are dropped (probability 0).  temperature <= 0 or NaN    */
+/*     is greedy: probability 1 at the lowest id of the largest logit.     */
+/*   - z = RN(l / T); -0 counts as +0.                                      */
+/*   - top-k (0 < K < number of non-NaN logits): the K first ids in the    */
+/*     order (z descending, id ascending).                                  */
+/*   - e = own exp(x), x = z - m for the kept maximum m (x = 0 where        */
+/*     z == m, so infinite logits share their mass); w = floor(e 2^40).    */
+/*   - top-p (p < 1): the shortest prefix of the kept ids in the order     */
+/*     (w descending, id ascending) whose weight sum reaches               */
+/*     max(1, ceil(p W)), W the kept total (p <= 0: one id).               */
+/*   - probability = RN(e / S) over the final set, S = RN(sum of its w)    */
+/*     2^-40; 0 elsewhere.                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Own exp for x <= 0 (Cody-Waite with the ln 2 split above, Taylor degree
+ * 7 on |r| <= ln2/2, scaling by 2^k in one rounding): NaN propagates, below
+ * -104 (exp rounds to 0 in binary32) gives 0. */
+float oracle_expf_nonpos(float x) {
+  if (isnan(x)) return x;
+  if (x < -104.0f) return 0.0f;
+  float kf = rintf(x * INV_LN2);
+  float r = fmaf(-kf, LN2_HI, x);
+  r = fmaf(-kf, LN2_LO, r);
+  float p = fmaf(r, EXP_C7, EXP_C6);
+  p = fmaf(r, p, EXP_C5);
+  p = fmaf(r, p, EXP_C4);
+  p = fmaf(r, p, EXP_C3);
+  p = fmaf(r, p, EXP_C2);
+  p = fmaf(r, p, 1.0f);
+  p = fmaf(r, p, 1.0f);
+  int k = (int)kf;
+  if (k >= -125) return p * ldexpf(1.0f, k);          /* exact */
+  return (p * ldexpf(1.0f, k + 64)) * ldexpf(1.0f, -64); /* one rounding */
+}
+
+typedef struct {
+  float key;
+  uint64_t w;
+  int64_t id;
+} l2p_item;
+
+static int cmp_key_desc(const void *a, const void *b) {
+  const l2p_item *x = (const l2p_item *)a, *y = (const l2p_item *)b;
+  if (x->key > y->key) return -1;
+  if (x->key < y->key) return 1;
+  return x->id < y->id ? -1 : (x->id > y->id);
+}
+
+static int cmp_w_desc(const void *a, const void *b) {
+  const l2p_item *x = (const l2p_item *)a, *y = (const l2p_item *)b;
+  if (x->w > y->w) return -1;
+  if (x->w < y->w) return 1;
+  return x->id < y->id ? -1 : (x->id > y->id);
+}
+
+/* max(1, ceil(p W)) for 0 < p < 1, exactly: p = M 2^E with M a 24-bit
+ * integer. */
+static uint64_t top_p_threshold(float p, uint64_t W) {
+  if (!(p > 0.0f)) return 1;
+  int e;
+  float f = frexpf(p, &e); /* p = f 2^e, f in [0.5, 1) */
+  uint64_t M = (uint64_t)ldexpf(f, 24);
+  int shift = 24 - e;      /* p W = M W / 2^shift */
+  if (shift >= 100) return 1;
+  unsigned __int128 prod = (unsigned __int128)M * W;
+  unsigned __int128 c = (prod + (((unsigned __int128)1 << shift) - 1)) >> shift;
+  return c < 1 ? 1 : (uint64_t)c;
+}
+
+int oracle_logits_to_probs(const float *logits, float *probs, int32_t rows, int64_t vocab, float temperature,
+                           int32_t top_k, float top_p) {
+  l2p_item *it = (l2p_item *)malloc(sizeof(l2p_item) * (size_t)(vocab > 0 ? vocab : 1));
+  float *e = (float *)malloc(sizeof(float) * (size_t)(vocab > 0 ? vocab : 1));
+  if (!it || !e) {
+    free(it);
+    free(e);
+    return -2;
+  }
+  for (int32_t r = 0; r < rows; r++) {
+    const float *l = logits + (int64_t)r * vocab;
+    float *out = probs + (int64_t)r * vocab;
+    for (int64_t v = 0; v < vocab; v++) out[v] = 0.0f;
+    if (!(temperature > 0.0f)) { /* greedy */
+      int64_t best = -1;
+      for (int64_t v = 0; v < vocab; v++)
+        if (!isnan(l[v]) && (best < 0 || l[v] > l[best])) best = v;
+      if (best >= 0) out[best] = 1.0f;
+      continue;
+    }
+    int64_t n = 0;
+    for (int64_t v = 0; v < vocab; v++) {
+      if (isnan(l[v])) continue;
+      float z = l[v] / temperature;
+      if (z == 0.0f) z = 0.0f;
+      it[n].key = z;
+      it[n].id = v;
+      n++;
+    }
+    if (n == 0) continue;
+    qsort(it, (size_t)n, sizeof(l2p_item), cmp_key_desc);
+    int64_t kept = (top_k > 0 && top_k < n) ? top_k : n;
+    const float m = it[0].key;
+    uint64_t W = 0;
+    for (int64_t i = 0; i < kept; i++) {
+      float x = it[i].key == m ? 0.0f : it[i].key - m;
+      e[it[i].id] = oracle_expf_nonpos(x);
+      it[i].w = oracle_weight(e[it[i].id]);
+      W += it[i].w;
+    }
+    int64_t fin = kept;
+    uint64_t S = W;
+    if (top_p < 1.0f) {
+      qsort(it, (size_t)kept, sizeof(l2p_item), cmp_w_desc);
+      const uint64_t thr = top_p_threshold(top_p, W);
+      uint64_t cum = 0;
+      fin = 0;
+      while (fin < kept && cum < thr) cum += it[fin++].w;
+      S = cum;
+    }
+    const float Sf = ldexpf((float)S, -40);
+    for (int64_t i = 0; i < fin; i++) out[it[i].id] = e[it[i].id] / Sf;
+  }
+  free(it);
+  free(e);
+  return 0;
+}
+
+void oracle_expf_nonpos_array(const float *x, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_expf_nonpos(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Array helpers for the tests (plain loops over the scalar functions).    */
 /* ------------------------------------------------------------------------ */
 

@@ -79,6 +79,11 @@ int oracle_probabilistic_accept(const float *target, const float *draft_probs, c
                                 int32_t *accept_len, int32_t batch, int32_t draft_stride, int32_t P,
                                 int64_t vocab);
 
+float oracle_expf_nonpos(float x);
+void oracle_expf_nonpos_array(const float *x, float *out, int64_t n);
+int oracle_logits_to_probs(const float *logits, float *probs, int32_t rows, int64_t vocab, float temperature,
+                           int32_t top_k, float top_p);
+
 #ifdef __cplusplus
 }
 #endif
