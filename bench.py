@@ -519,6 +519,21 @@ def run_prob_verify(args, d: Dist):
     rejected = int((lens <= plen.cpu().numpy()).sum())
     algo = rejected * 8 * V + (B - rejected) * 4 * V  # residual: t and q rows; full accept: the bonus row
 
+    # logits to probabilities over rows of the verify's target shape
+    # ([B, P+1, V] logits), unfiltered and with temperature, top-k and top-p
+    rows_l = B * (P + 1)
+    lg = torch.randn(rows_l, V, device=dev, generator=torch.Generator(device=dev).manual_seed(77)) * 2.5
+    pr = torch.empty_like(lg)
+    l2p = {}
+    for name, (T, K, Pp) in {"plain": (1.0, 0, 1.0), "filtered": (0.8, 50, 0.95)}.items():
+        def run_l2p(T=T, K=K, Pp=Pp):
+            binding.dspark_logits_to_probs(lg, pr, rows_l, V, T, K, Pp, stream)
+        timed(2, run_l2p)
+        us = mean_us(timed(max(5, min(args.steps, 20)), run_l2p))
+        l2p[name] = {"temperature": T, "top_k": K, "top_p": Pp, "kernel_us": us,
+                     "algorithmic_bytes": 8 * V * rows_l, "achieved_gbs": 8 * V * rows_l / us / 1e3}
+    del lg, pr
+
     # end to end through the C ABI from pinned host buffers
     hb = {"target": target.cpu().pin_memory(), "draftp": draftp.cpu().pin_memory(),
           "draft": draft.cpu().pin_memory(), "plen": plen.cpu().pin_memory()}
@@ -571,6 +586,9 @@ def run_prob_verify(args, d: Dist):
                          "algorithmic_bytes": algo, "rows_rejected": rejected,
                          "kernel_us_from": "CUDA events around the accept launch alone, L2 flushed"},
             "cpu_baseline": cpu,
+            "logits_to_probs": {"rows": rows_l, "vocab": V, "kernel": "logits_probs_kernel",
+                                "bytes_note": "algorithmic: one read and one write of every row",
+                                "peak_gbs": peak, **l2p},
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * 2,
             "clocks": clock_info,

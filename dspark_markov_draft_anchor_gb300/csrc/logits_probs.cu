@@ -1,0 +1,397 @@
+// logits_probs.cu -- [P1] dsparkLogitsToProbabilities: a dense probability
+// row after temperature, top-k and top-p, behind the C ABI of
+// include/dspark_markov.h.
+//
+// Every decision is an exact comparison, so the result does not depend on
+// how threads split a row:
+//   - temperature <= 0 (or NaN) is greedy: 1 at the lowest id of the
+//     largest non-NaN logit;
+//   - z = RN(l / T), -0 as +0; an id whose z is NaN (a NaN logit, or an
+//     infinite one over an infinite temperature) weighs nothing; top-k
+//     (0 < K < count of the others) keeps the first K ids in the order
+//     (z descending, id ascending);
+//   - e = exp(x) by this file's own exp, x = z - m (m the largest z; x = 0
+//     where z == m), w = floor(e 2^40);
+//   - top-p (p < 1) keeps the shortest prefix in the order (w descending, id
+//     ascending) whose weight reaches max(1, ceil(p W)), W the kept total;
+//   - probability = RN(e / S), S = RN(sum of the final w) 2^-40; 0 elsewhere.
+//
+// One CTA of 512 threads per row.  The k-th largest key and the top-p cut
+// are radix selects over the row (8 bits a pass: four passes of counts over
+// the 32-bit logit keys, six passes of weight sums over the 48-bit weights),
+// ties at a cut are resolved by one ordered scan, and a last pass writes the
+// row.  Passes re-read the row (L2-resident for the row's lifetime at these
+// sizes) and recompute z, e and w rather than keep them.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "dspark_markov.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+
+// Cody-Waite reduction by ln 2 (its high part with the last 8 significand
+// bits cleared, so k * hi is exact for |k| < 2^8) and the Taylor series of
+// exp to degree 7 on |r| <= ln2/2.
+constexpr double kLn2 = 0.69314718055994530941723212145818;
+constexpr float kInvLn2 = static_cast<float>(1.0 / kLn2);
+constexpr float kLn2Hi = 0.693145751953125f;
+constexpr float kLn2Lo = static_cast<float>(kLn2 - 0.693145751953125);
+constexpr float kC2 = static_cast<float>(1.0 / 2.0);
+constexpr float kC3 = static_cast<float>(1.0 / 6.0);
+constexpr float kC4 = static_cast<float>(1.0 / 24.0);
+constexpr float kC5 = static_cast<float>(1.0 / 120.0);
+constexpr float kC6 = static_cast<float>(1.0 / 720.0);
+constexpr float kC7 = static_cast<float>(1.0 / 5040.0);
+
+// exp(x) for x <= 0: NaN propagates, below -104 gives 0, and 2^k scales the
+// polynomial exactly (k >= -125) or with one rounding into the subnormals.
+__device__ __forceinline__ float exp_nonpos(float x) {
+  if (isnan(x)) return x;
+  if (x < -104.0f) return 0.0f;
+  const float kf = rintf(__fmul_rn(x, kInvLn2));
+  float r = __fmaf_rn(-kf, kLn2Hi, x);
+  r = __fmaf_rn(-kf, kLn2Lo, r);
+  float p = __fmaf_rn(r, kC7, kC6);
+  p = __fmaf_rn(r, p, kC5);
+  p = __fmaf_rn(r, p, kC4);
+  p = __fmaf_rn(r, p, kC3);
+  p = __fmaf_rn(r, p, kC2);
+  p = __fmaf_rn(r, p, 1.0f);
+  p = __fmaf_rn(r, p, 1.0f);
+  const int k = static_cast<int>(kf);  // in [-150, 0]
+  if (k >= -125) return __fmul_rn(p, __int_as_float((k + 127) << 23));
+  return __fmul_rn(__fmul_rn(p, __int_as_float((k + 64 + 127) << 23)), 0x1p-64f);
+}
+
+// floor(e 2^40) for e in [0, 1], in integer instructions (significand
+// shifted by the exponent).
+__device__ __forceinline__ uint64_t weight(float e) {
+  if (!(e > 0.0f)) return 0ull;
+  if (e >= 1.0f) return 1ull << 40;
+  const uint32_t b = __float_as_uint(e);
+  const uint32_t ex = b >> 23;
+  const uint32_t m = (b & 0x7FFFFFu) | (ex ? 0x800000u : 0u);
+  const int sh = static_cast<int>(ex ? ex : 1u) - 110;
+  return sh >= 0 ? static_cast<uint64_t>(m) << sh : static_cast<uint64_t>(m >> (-sh < 31 ? -sh : 31));
+}
+
+// An order-preserving 32-bit key of a non-NaN float (+0 and -0 equal).
+__device__ __forceinline__ uint32_t order_key(float z) {
+  const uint32_t b = __float_as_uint(z == 0.0f ? 0.0f : z);
+  return b ^ ((b >> 31) ? 0xFFFFFFFFu : 0x80000000u);
+}
+
+// max(1, ceil(p W)) for p < 1, exactly: p = M 2^(E - 150) with M the 24-bit
+// significand and E the biased exponent field, so p W = M W / 2^(150 - E).
+__device__ uint64_t top_p_threshold(float p, uint64_t W) {
+  if (!(p > 0.0f)) return 1ull;
+  const uint32_t b = __float_as_uint(p);
+  const int E = static_cast<int>(b >> 23);
+  const int shift = 150 - E;  // >= 24 since p < 1; subnormals give 150
+  if (shift >= 100) return 1ull;
+  const uint64_t M = (b & 0x7FFFFFu) | 0x800000u;
+  uint64_t lo = M * W, hi = __umul64hi(M, W);
+  // + 2^shift - 1, then >> shift
+  const uint64_t add_lo = shift >= 64 ? ~0ull : (1ull << shift) - 1;
+  const uint64_t add_hi = shift >= 64 ? (1ull << (shift - 64)) - 1 : 0ull;
+  const uint64_t lo2 = lo + add_lo;
+  hi += add_hi + (lo2 < lo ? 1ull : 0ull);
+  lo = lo2;
+  const uint64_t c = shift >= 64 ? hi >> (shift - 64) : (lo >> shift) | (hi << (64 - shift));
+  return c < 1 ? 1ull : c;
+}
+
+struct RowSmem {
+  unsigned int hist[256];
+  unsigned long long whist[256];
+  unsigned long long red_u64[kWarps];
+  float red_f[kWarps];
+  int red_i[kWarps];
+  int64_t red_id[kWarps];
+  int64_t found;
+  // decisions, written by thread 0
+  uint32_t k_prefix, k_mask;
+  int64_t k_rem;
+  uint64_t p_prefix, p_mask, p_above, p_thr;
+};
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  return x;
+}
+
+__device__ uint64_t block_sum_u64(uint64_t x, RowSmem& sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  x = warp_sum_u64(x);
+  if (lane == 0) sm.red_u64[warp] = x;
+  __syncthreads();
+  uint64_t t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += sm.red_u64[w];
+  __syncthreads();
+  return t;
+}
+
+// The id of the r-th id (1-based, id order) that satisfies pred, by one
+// ordered scan of the row 512 ids at a time; vocab if there are fewer.
+template <class Pred>
+__device__ int64_t nth_in_order(int64_t vocab, int64_t r, Pred pred, RowSmem& sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int64_t seen = 0;
+  for (int64_t c0 = 0; c0 < vocab; c0 += kThreads) {
+    const int64_t v = c0 + threadIdx.x;
+    const bool f = v < vocab && pred(v);
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
+    if (lane == 0) sm.red_i[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = sm.red_i[w];
+      if (w < warp) before += c;
+      total += c;
+    }
+    if (seen + total >= r) {  // the same in every thread
+      const int64_t rank = seen + before + __popc(bal & ((1u << lane) - 1u)) + 1;
+      if (f && rank == r) sm.found = v;
+      __syncthreads();
+      const int64_t id = sm.found;
+      __syncthreads();
+      return id;
+    }
+    seen += total;
+    __syncthreads();
+  }
+  return vocab;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    logits_probs_kernel(const float* logits, float* probs, int64_t vocab, float temperature, int32_t top_k,
+                        float top_p) {
+  __shared__ RowSmem sm;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* l = logits + static_cast<int64_t>(blockIdx.x) * vocab;
+  float* out = probs + static_cast<int64_t>(blockIdx.x) * vocab;
+
+  if (!(temperature > 0.0f)) {  // greedy: lowest id of the largest non-NaN logit
+    float best = 0.0f;
+    int64_t best_id = -1;
+    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
+      const float x = l[v];
+      if (!isnan(x) && (best_id < 0 || x > best)) {
+        best = x;
+        best_id = v;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+      const int64_t oi = __shfl_xor_sync(0xFFFFFFFFu, best_id, off);
+      if (oi >= 0 && (best_id < 0 || ob > best || (ob == best && oi < best_id))) {
+        best = ob;
+        best_id = oi;
+      }
+    }
+    if (lane == 0) {
+      sm.red_f[warp] = best;
+      sm.red_id[warp] = best_id;
+    }
+    __syncthreads();
+    best = 0.0f;
+    best_id = -1;
+    for (int w = 0; w < kWarps; ++w) {
+      const float ob = sm.red_f[w];
+      const int64_t oi = sm.red_id[w];
+      if (oi >= 0 && (best_id < 0 || ob > best || (ob == best && oi < best_id))) {
+        best = ob;
+        best_id = oi;
+      }
+    }
+    __syncthreads();
+    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) out[v] = v == best_id ? 1.0f : 0.0f;
+    return;
+  }
+
+  // pass 1: non-NaN count and the largest z
+  int n_local = 0;
+  float m = -INFINITY;
+  for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
+    const float z = __fdiv_rn(l[v], temperature);
+    if (isnan(z)) continue;
+    ++n_local;
+    m = fmaxf(m, z);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    n_local += __shfl_xor_sync(0xFFFFFFFFu, n_local, off);
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  }
+  if (lane == 0) {
+    sm.red_i[warp] = n_local;
+    sm.red_f[warp] = m;
+  }
+  __syncthreads();
+  int64_t n_valid = 0;
+  m = -INFINITY;
+  for (int w = 0; w < kWarps; ++w) {
+    n_valid += sm.red_i[w];
+    m = fmaxf(m, sm.red_f[w]);
+  }
+  __syncthreads();
+  if (n_valid == 0) {
+    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) out[v] = 0.0f;
+    return;
+  }
+
+  // top-k: the k-th largest key by four 8-bit passes, then the tie cut
+  const bool topk = top_k > 0 && top_k < n_valid;
+  uint32_t k_key = 0;
+  int64_t k_id = vocab;
+  if (topk) {
+    if (threadIdx.x == 0) {
+      sm.k_prefix = 0;
+      sm.k_mask = 0;
+      sm.k_rem = top_k;
+    }
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += kThreads) sm.hist[i] = 0;
+      __syncthreads();
+      const uint32_t prefix = sm.k_prefix, mask = sm.k_mask;
+      for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
+        const float z = __fdiv_rn(l[v], temperature);
+        if (isnan(z)) continue;
+        const uint32_t key = order_key(z);
+        if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int64_t rem = sm.k_rem;
+        int b = 255;
+        for (; b > 0; --b) {
+          const int64_t c = sm.hist[b];
+          if (c >= rem) break;
+          rem -= c;
+        }
+        sm.k_prefix = prefix | (static_cast<uint32_t>(b) << shift);
+        sm.k_mask = mask | (255u << shift);
+        sm.k_rem = rem;
+        if (shift == 0) sm.found = sm.hist[b];  // ids with exactly this key
+      }
+      __syncthreads();
+    }
+    k_key = sm.k_prefix;
+    const int64_t rem = sm.k_rem, ties = sm.found;
+    __syncthreads();
+    if (rem < ties)
+      k_id = nth_in_order(
+          vocab, rem,
+          [&](int64_t v) {
+            const float z = __fdiv_rn(l[v], temperature);
+            return !isnan(z) && order_key(z) == k_key;
+          },
+          sm);
+  }
+  auto kept_k = [&](int64_t v, float x, float& z) {
+    z = __fdiv_rn(x, temperature);
+    if (isnan(z)) return false;
+    if (!topk) return true;
+    const uint32_t key = order_key(z);
+    return key > k_key || (key == k_key && v <= k_id);
+  };
+  auto weight_of = [&](float z, float& e) {
+    e = exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
+    return weight(e);
+  };
+
+  // the kept total
+  uint64_t part = 0;
+  for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
+    float z, e;
+    if (kept_k(v, l[v], z)) part += weight_of(z, e);
+  }
+  const uint64_t W = block_sum_u64(part, sm);
+
+  // top-p: the cut weight by six 8-bit passes of weight sums, then the tie cut
+  const bool topp = top_p < 1.0f;
+  uint64_t S = W, p_w = 0;
+  int64_t p_id = vocab;
+  if (topp) {
+    if (threadIdx.x == 0) {
+      sm.p_thr = top_p_threshold(top_p, W);
+      sm.p_prefix = 0;
+      sm.p_mask = 0;
+      sm.p_above = 0;
+    }
+    for (int shift = 40; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += kThreads) sm.whist[i] = 0;
+      __syncthreads();
+      const uint64_t prefix = sm.p_prefix, mask = sm.p_mask;
+      for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
+        float z, e;
+        if (!kept_k(v, l[v], z)) continue;
+        const uint64_t w = weight_of(z, e);
+        if ((w & mask) == prefix) atomicAdd(&sm.whist[(w >> shift) & 255u], static_cast<unsigned long long>(w));
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        uint64_t above = sm.p_above;
+        const uint64_t thr = sm.p_thr;
+        int b = 255;
+        for (; b > 0; --b) {
+          if (above + sm.whist[b] >= thr) break;
+          above += sm.whist[b];
+        }
+        sm.p_prefix = prefix | (static_cast<uint64_t>(b) << shift);
+        sm.p_mask = mask | (255ull << shift);
+        sm.p_above = above;
+        if (shift == 0) sm.found = static_cast<int64_t>(sm.whist[b]);  // mass at exactly this weight
+      }
+      __syncthreads();
+    }
+    p_w = sm.p_prefix;
+    const uint64_t above = sm.p_above, thr = sm.p_thr, at_cut = static_cast<uint64_t>(sm.found);
+    __syncthreads();
+    const uint64_t tau = p_w > 0 ? p_w : 1ull;
+    const uint64_t need = (thr - above + tau - 1) / tau;  // ids of weight p_w to take
+    const uint64_t ties = at_cut / tau;
+    S = above + need * p_w;
+    if (need < ties)
+      p_id = nth_in_order(
+          vocab, static_cast<int64_t>(need),
+          [&](int64_t v) {
+            float z, e;
+            return kept_k(v, l[v], z) && weight_of(z, e) == p_w;
+          },
+          sm);
+  }
+
+  const float Sf = __fmul_rn(__ull2float_rn(S), 0x1p-40f);
+  for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
+    float z, e = 0.0f;
+    bool keep = kept_k(v, l[v], z);
+    if (keep) {
+      const uint64_t w = weight_of(z, e);
+      if (topp) keep = w > p_w || (w == p_w && v <= p_id);
+    }
+    out[v] = keep ? __fdiv_rn(e, Sf) : 0.0f;
+  }
+}
+
+}  // namespace
+}  // namespace dspark
+
+extern "C" int dspark_logits_to_probs(const float* logits, float* probs, int32_t rows, int32_t vocab,
+                                      float temperature, int32_t top_k, float top_p, cudaStream_t stream) {
+  if (rows < 0 || vocab < 1) return DSPARK_ERR_INVALID_ARG;
+  if (rows == 0) return DSPARK_OK;
+  if (!logits || !probs) return DSPARK_ERR_INVALID_ARG;
+  dspark::logits_probs_kernel<<<rows, dspark::kThreads, 0, stream>>>(logits, probs, vocab, temperature, top_k,
+                                                                      top_p);
+  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}

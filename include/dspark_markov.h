@@ -295,6 +295,31 @@ DSPARK_API int dspark_probabilistic_accept(const float *target_probs, const floa
                                            int32_t batch, int32_t draft_stride, int32_t P, int32_t vocab,
                                            cudaStream_t stream);
 
+/*
+ * dspark_logits_to_probs -- [P1] dsparkLogitsToProbabilities: dense
+ * probability rows after temperature, top-k and top-p.  Device pointers:
+ * logits [rows, vocab] float32 (contiguous), probs [rows, vocab] float32
+ * (contiguous; may be the same buffer as logits).
+ *   temperature <= 0 (or NaN): greedy, 1 at the lowest id of the largest
+ *     non-NaN logit (all zeros if every logit is NaN).
+ *   Otherwise z = RN(l / temperature) (-0 as +0); ids whose z is NaN get 0.
+ *   top_k: 0 < top_k < (ids with a non-NaN z) keeps the top_k first ids in
+ *     the order (z descending, id ascending); other values keep all.
+ *   e = exp(z - m), m the largest z (exactly 1 where z == m, so infinite
+ *     logits share their mass), by the library's own exp (within 2 ulp);
+ *     fixed-point weights w = floor(e 2^40).
+ *   top_p < 1 keeps the shortest prefix of the kept ids in the order
+ *     (w descending, id ascending) whose weights reach max(1, ceil(top_p W)),
+ *     W their total (top_p <= 0 keeps one id); top_p >= 1 or NaN keeps all.
+ *   probs = RN(e / S) on the final ids, S = RN(sum of their w) 2^-40;
+ *     0 elsewhere.
+ * Every decision is an exact comparison (readings: the pages name the three
+ * filters only).  rows >= 0, vocab >= 1.  Allocates nothing; one kernel on
+ * `stream` (one CTA per row).
+ */
+DSPARK_API int dspark_logits_to_probs(const float *logits, float *probs, int32_t rows, int32_t vocab,
+                                      float temperature, int32_t top_k, float top_p, cudaStream_t stream);
+
 /* A short English description of a DSPARK_* code (static storage). */
 DSPARK_API const char *dspark_strerror(int code);
 

@@ -744,9 +744,10 @@ int oracle_probabilistic_accept(const float *target, const float *draft_probs, c
 /* temperature, top-k and top-p.  The pages name the three filters only;   */
 /* the arithmetic below is this build's reading, chosen so that every      */
 /* decision is an exact comparison:                                        */
-/*   - NaN logits are dropped (probability 0).  temperature <= 0 or NaN    */
-/*     is greedy: probability 1 at the lowest id of the largest logit.     */
-/*   - z = RN(l / T); -0 counts as +0.                                      */
+/*   - temperature <= 0 or NaN is greedy: probability 1 at the lowest id   */
+/*     of the largest non-NaN logit.                                        */
+/*   - z = RN(l / T); -0 counts as +0; an id whose z is NaN (a NaN logit,  */
+/*     or an infinite one over an infinite T) is dropped (probability 0).  */
 /*   - top-k (0 < K < number of non-NaN logits): the K first ids in the    */
 /*     order (z descending, id ascending).                                  */
 /*   - e = own exp(x), x = z - m for the kept maximum m (x = 0 where        */
@@ -835,8 +836,8 @@ int oracle_logits_to_probs(const float *logits, float *probs, int32_t rows, int6
     }
     int64_t n = 0;
     for (int64_t v = 0; v < vocab; v++) {
-      if (isnan(l[v])) continue;
       float z = l[v] / temperature;
+      if (isnan(z)) continue;
       if (z == 0.0f) z = 0.0f;
       it[n].key = z;
       it[n].id = v;

@@ -1,0 +1,93 @@
+"""Parity of dspark_logits_to_probs ([P1] dsparkLogitsToProbabilities) with
+the oracle, bit for bit (GPU, through the C ABI): every decision is an exact
+comparison and every value one IEEE operation chain on both sides."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dspark_markov_draft_anchor_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(l, T, K, P, in_place=False):
+    rows, V = l.shape
+    x = torch.from_numpy(np.ascontiguousarray(l)).cuda()
+    out = x if in_place else torch.full_like(x, -7.0)
+    binding.dspark_logits_to_probs(x, out, rows, V, T, K, P)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _check(l, T, K, P, in_place=False):
+    want = oracle.logits_to_probs(l, T, K, P)
+    got = _gpu(l, T, K, P, in_place)
+    bad = np.argwhere(got.view(np.uint32) != want.view(np.uint32))
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])], want[tuple(bad[0])])
+
+
+def _logits(rng, rows, V, scale=3.0):
+    return (rng.standard_normal((rows, V)) * scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("rows,V,T,K,P", [
+    (7, 1000, 1.0, 0, 1.0), (5, 4099, 0.7, 50, 0.9), (4, 32773, 1.3, 1000, 0.95), (6, 777, 2.0, 3, 0.5),
+    (3, 129280, 1.0, 50, 0.9), (3, 129280, 0.8, 0, 0.95), (9, 2048, 1.0, 0, 1.0), (2, 513, 0.5, 512, 0.3),
+    (1, 1, 1.0, 0, 0.9), (3, 5, 1.0, 2, 0.99)])
+def test_random_rows(rows, V, T, K, P):
+    rng = np.random.default_rng(rows * 7919 + V)
+    _check(_logits(rng, rows, V), T, K, P)
+
+
+@pytest.mark.parametrize("K,P", [(0, 0.3), (100, 1.0), (100, 0.5), (1500, 0.7), (0, 0.999)])
+def test_ties_at_both_cuts(K, P):
+    """Logits on a coarse grid: long runs of equal z and equal weights, so
+    both cuts fall inside a tie and the ordered scans decide them."""
+    rng = np.random.default_rng(K + int(P * 100))
+    l = rng.integers(0, 4, (4, 5000)).astype(np.float32)
+    _check(l, 1.0, K, P)
+    l2 = np.round(_logits(rng, 3, 20000, 2.0) * 2) / 2
+    _check(l2.astype(np.float32), 0.9, K, P)
+
+
+def test_degenerate_rows_and_settings():
+    rng = np.random.default_rng(3)
+    V = 3000
+    l = _logits(rng, 8, V)
+    l[0, ::5] = np.nan                      # scattered NaN
+    l[1, [7, 900]] = np.inf                 # infinite logits share the mass
+    l[2, :] = -np.inf                       # all -inf: uniform
+    l[3, :] = np.nan                        # all NaN: zeros
+    l[4, 1:] = np.nan                       # one valid id
+    l[5, :] = 2.5                           # all equal
+    l[6, ::3] = -0.0
+    l[6, 1::3] = 0.0                        # signed zeros
+    l[7, 100] = 1e30                        # one huge logit
+    for T in (1.0, 0.0, -1.0, float("nan"), float("inf"), 1e-30, 3e38):
+        _check(l, T, 0, 1.0)
+    for K in (-3, 1, V, V + 5):
+        _check(l, 1.0, K, 1.0)
+    for P in (0.0, -1.0, 1e-30, 1.5, float("nan"), 0.5):
+        _check(l, 1.0, 0, P)
+    _check(l, 1.0, 10, 0.2)
+
+
+def test_in_place_and_errors():
+    rng = np.random.default_rng(4)
+    l = _logits(rng, 5, 4096)
+    _check(l, 0.9, 64, 0.9, in_place=True)
+    _check(l, 0.0, 0, 1.0, in_place=True)
+    t = torch.zeros(4, device="cuda")
+    with pytest.raises(binding.DsparkError) as e:
+        binding.dspark_logits_to_probs(t, t, 1, 0, 1.0, 0, 1.0)
+    assert e.value.code == -1
+    binding.dspark_logits_to_probs(None, None, 0, 5, 1.0, 0, 1.0)  # no rows: nothing to do
+
+
+def test_full_vocabulary_rows():
+    """64 rows of V = 129280 (the verify shape's vocabulary)."""
+    rng = np.random.default_rng(17)
+    l = _logits(rng, 64, 129280, 2.5)
+    _check(l, 1.0, 0, 1.0)
+    _check(l, 0.8, 50, 0.95)

@@ -124,6 +124,10 @@ def test_greedy_nan_and_infinities():
     assert p.tolist() == [0.5, 0.0, 0.5, 0.0]
     p = oracle.logits_to_probs(np.full((1, 4), -np.inf, np.float32), 1.0, 0, 1.0)[0]
     assert p.tolist() == [0.25] * 4
+    # an infinite temperature: finite logits all scale to 0 (uniform), and an
+    # infinite logit's z = inf / inf is NaN, so it weighs nothing
+    p = oracle.logits_to_probs(np.float32([[1.0, np.inf, -2.0, 7.0]]), np.inf, 0, 1.0)[0]
+    assert p.tolist() == [np.float32(1 / 3), 0.0, np.float32(1 / 3), np.float32(1 / 3)]
 
 
 def test_monotone_and_normalised_under_both_filters():
