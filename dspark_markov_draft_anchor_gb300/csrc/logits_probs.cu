@@ -16,12 +16,12 @@
 //     ascending) whose weight reaches max(1, ceil(p W)), W the kept total;
 //   - probability = RN(e / S), S = RN(sum of the final w) 2^-40; 0 elsewhere.
 //
-// One CTA of 512 threads per row.  The k-th largest key and the top-p cut
+// One CTA of 1024 threads per row.  The k-th largest key and the top-p cut
 // are radix selects over the row (8 bits a pass: four passes of counts over
 // the 32-bit logit keys, six passes of weight sums over the 48-bit weights),
 // ties at a cut are resolved by one ordered scan, and a last pass writes the
-// row.  Passes re-read the row (L2-resident for the row's lifetime at these
-// sizes) and recompute z, e and w rather than keep them.
+// row.  The output row holds z, then e, between passes (see
+// logits_probs_row).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -31,7 +31,7 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
 // Cody-Waite reduction by ln 2 (its high part with the last 8 significand
@@ -139,7 +139,7 @@ __device__ uint64_t block_sum_u64(uint64_t x, RowSmem& sm) {
 }
 
 // The id of the r-th id (1-based, id order) that satisfies pred, by one
-// ordered scan of the row 512 ids at a time; vocab if there are fewer.
+// ordered scan of the row kThreads ids at a time; vocab if there are fewer.
 template <class Pred>
 __device__ int64_t nth_in_order(int64_t vocab, int64_t r, Pred pred, RowSmem& sm) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -171,24 +171,69 @@ __device__ int64_t nth_in_order(int64_t vocab, int64_t r, Pred pred, RowSmem& sm
   return vocab;
 }
 
-__global__ void __launch_bounds__(kThreads)
-    logits_probs_kernel(const float* logits, float* probs, int64_t vocab, float temperature, int32_t top_k,
-                        float top_p) {
-  __shared__ RowSmem sm;
+// Row iteration: every id of a row, four at a time (float4) where the row
+// allows it.  row_map writes f's value back in place of what it read (the
+// same thread reads and then writes each id, so src may equal dst).
+template <class F>
+__device__ __forceinline__ void row_each(const float* src, int64_t vocab, bool vec, F&& f) {
+  if (vec) {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) {
+      const float4 x = s4[g];
+      f(4 * g, x.x);
+      f(4 * g + 1, x.y);
+      f(4 * g + 2, x.z);
+      f(4 * g + 3, x.w);
+    }
+  } else {
+    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) f(v, src[v]);
+  }
+}
+
+template <bool kStreamIn, bool kStreamOut, class F>
+__device__ __forceinline__ void row_map(const float* src, float* dst, int64_t vocab, bool vec, F&& f) {
+  if (vec) {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    float4* d4 = reinterpret_cast<float4*>(dst);
+    for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) {
+      const float4 x = kStreamIn ? __ldcs(s4 + g) : s4[g];
+      const float4 y = make_float4(f(4 * g, x.x), f(4 * g + 1, x.y), f(4 * g + 2, x.z), f(4 * g + 3, x.w));
+      if (kStreamOut)
+        __stcs(d4 + g, y);
+      else
+        d4[g] = y;
+    }
+  } else {
+    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
+      const float y = f(v, kStreamIn ? __ldcs(src + v) : src[v]);
+      if (kStreamOut)
+        __stcs(dst + v, y);
+      else
+        dst[v] = y;
+    }
+  }
+}
+
+// One row.  The output row doubles as scratch: pass 1 stores z there, the
+// weight pass replaces it by e (or -1 for an id that top-k or a NaN z
+// dropped), and the last pass by the probability, so later passes read a
+// value instead of recomputing a division and an exp, from L2 (one row per
+// SM is in flight).
+__device__ void logits_probs_row(const float* l, float* out, int64_t vocab, float temperature, int32_t top_k,
+                                 float top_p, RowSmem& sm) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float* l = logits + static_cast<int64_t>(blockIdx.x) * vocab;
-  float* out = probs + static_cast<int64_t>(blockIdx.x) * vocab;
+  const bool vec = (((reinterpret_cast<uintptr_t>(l) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0) &&
+                   (vocab & 3) == 0;
 
   if (!(temperature > 0.0f)) {  // greedy: lowest id of the largest non-NaN logit
     float best = 0.0f;
     int64_t best_id = -1;
-    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
-      const float x = l[v];
-      if (!isnan(x) && (best_id < 0 || x > best)) {
+    row_each(l, vocab, vec, [&](int64_t v, float x) {
+      if (!isnan(x) && (best_id < 0 || x > best || (x == best && v < best_id))) {
         best = x;
         best_id = v;
       }
-    }
+    });
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
@@ -214,19 +259,22 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     __syncthreads();
-    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) out[v] = v == best_id ? 1.0f : 0.0f;
+    row_map<false, true>(out, out, vocab, vec, [&](int64_t v, float) { return v == best_id ? 1.0f : 0.0f; });
     return;
   }
 
-  // pass 1: non-NaN count and the largest z
+  // pass 1: z into the output row; non-NaN count and the largest z
   int n_local = 0;
   float m = -INFINITY;
-  for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
-    const float z = __fdiv_rn(l[v], temperature);
-    if (isnan(z)) continue;
-    ++n_local;
-    m = fmaxf(m, z);
-  }
+  row_map<true, false>(l, out, vocab, vec, [&](int64_t, float x) {
+    float z = __fdiv_rn(x, temperature);
+    if (!isnan(z)) {
+      ++n_local;
+      if (z == 0.0f) z = 0.0f;
+      m = fmaxf(m, z);
+    }
+    return z;
+  });
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     n_local += __shfl_xor_sync(0xFFFFFFFFu, n_local, off);
@@ -245,11 +293,11 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
   if (n_valid == 0) {
-    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) out[v] = 0.0f;
+    row_map<false, true>(out, out, vocab, vec, [](int64_t, float) { return 0.0f; });
     return;
   }
 
-  // top-k: the k-th largest key by four 8-bit passes, then the tie cut
+  // top-k: the k-th largest key by four 8-bit passes over z, then the tie cut
   const bool topk = top_k > 0 && top_k < n_valid;
   uint32_t k_key = 0;
   int64_t k_id = vocab;
@@ -263,12 +311,11 @@ __global__ void __launch_bounds__(kThreads)
       for (int i = threadIdx.x; i < 256; i += kThreads) sm.hist[i] = 0;
       __syncthreads();
       const uint32_t prefix = sm.k_prefix, mask = sm.k_mask;
-      for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
-        const float z = __fdiv_rn(l[v], temperature);
-        if (isnan(z)) continue;
+      row_each(out, vocab, vec, [&](int64_t, float z) {
+        if (isnan(z)) return;
         const uint32_t key = order_key(z);
         if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
-      }
+      });
       __syncthreads();
       if (threadIdx.x == 0) {
         int64_t rem = sm.k_rem;
@@ -292,29 +339,24 @@ __global__ void __launch_bounds__(kThreads)
       k_id = nth_in_order(
           vocab, rem,
           [&](int64_t v) {
-            const float z = __fdiv_rn(l[v], temperature);
+            const float z = out[v];
             return !isnan(z) && order_key(z) == k_key;
           },
           sm);
   }
-  auto kept_k = [&](int64_t v, float x, float& z) {
-    z = __fdiv_rn(x, temperature);
-    if (isnan(z)) return false;
-    if (!topk) return true;
-    const uint32_t key = order_key(z);
-    return key > k_key || (key == k_key && v <= k_id);
-  };
-  auto weight_of = [&](float z, float& e) {
-    e = exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
-    return weight(e);
-  };
 
-  // the kept total
+  // weight pass: e (or -1 for a dropped id) into the output row; the kept total
   uint64_t part = 0;
-  for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
-    float z, e;
-    if (kept_k(v, l[v], z)) part += weight_of(z, e);
-  }
+  row_map<false, false>(out, out, vocab, vec, [&](int64_t v, float z) {
+    if (isnan(z)) return -1.0f;
+    if (topk) {
+      const uint32_t key = order_key(z);
+      if (!(key > k_key || (key == k_key && v <= k_id))) return -1.0f;
+    }
+    const float e = exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
+    part += weight(e);
+    return e;
+  });
   const uint64_t W = block_sum_u64(part, sm);
 
   // top-p: the cut weight by six 8-bit passes of weight sums, then the tie cut
@@ -332,12 +374,11 @@ __global__ void __launch_bounds__(kThreads)
       for (int i = threadIdx.x; i < 256; i += kThreads) sm.whist[i] = 0;
       __syncthreads();
       const uint64_t prefix = sm.p_prefix, mask = sm.p_mask;
-      for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
-        float z, e;
-        if (!kept_k(v, l[v], z)) continue;
-        const uint64_t w = weight_of(z, e);
+      row_each(out, vocab, vec, [&](int64_t, float e) {
+        if (e < 0.0f) return;
+        const uint64_t w = weight(e);
         if ((w & mask) == prefix) atomicAdd(&sm.whist[(w >> shift) & 255u], static_cast<unsigned long long>(w));
-      }
+      });
       __syncthreads();
       if (threadIdx.x == 0) {
         uint64_t above = sm.p_above;
@@ -365,21 +406,32 @@ __global__ void __launch_bounds__(kThreads)
       p_id = nth_in_order(
           vocab, static_cast<int64_t>(need),
           [&](int64_t v) {
-            float z, e;
-            return kept_k(v, l[v], z) && weight_of(z, e) == p_w;
+            const float e = out[v];
+            return e >= 0.0f && weight(e) == p_w;
           },
           sm);
   }
 
   const float Sf = __fmul_rn(__ull2float_rn(S), 0x1p-40f);
-  for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
-    float z, e = 0.0f;
-    bool keep = kept_k(v, l[v], z);
-    if (keep) {
-      const uint64_t w = weight_of(z, e);
-      if (topp) keep = w > p_w || (w == p_w && v <= p_id);
+  row_map<false, true>(out, out, vocab, vec, [&](int64_t v, float e) {
+    bool keep = e >= 0.0f;
+    if (keep && topp) {
+      const uint64_t w = weight(e);
+      keep = w > p_w || (w == p_w && v <= p_id);
     }
-    out[v] = keep ? __fdiv_rn(e, Sf) : 0.0f;
+    return keep ? __fdiv_rn(e, Sf) : 0.0f;
+  });
+}
+
+// A persistent grid of one CTA per SM takes rows in turn, so that the rows in
+// flight (one output row each) stay in L2 across their passes.
+__global__ void __launch_bounds__(kThreads)
+    logits_probs_kernel(const float* logits, float* probs, int32_t rows, int64_t vocab, float temperature,
+                        int32_t top_k, float top_p) {
+  __shared__ RowSmem sm;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    logits_probs_row(logits + r * vocab, probs + r * vocab, vocab, temperature, top_k, top_p, sm);
+    __syncthreads();  // shared state is reused by the next row
   }
 }
 
@@ -391,7 +443,11 @@ extern "C" int dspark_logits_to_probs(const float* logits, float* probs, int32_t
   if (rows < 0 || vocab < 1) return DSPARK_ERR_INVALID_ARG;
   if (rows == 0) return DSPARK_OK;
   if (!logits || !probs) return DSPARK_ERR_INVALID_ARG;
-  dspark::logits_probs_kernel<<<rows, dspark::kThreads, 0, stream>>>(logits, probs, vocab, temperature, top_k,
-                                                                      top_p);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  const int grid = rows < sms ? rows : sms;
+  dspark::logits_probs_kernel<<<grid, dspark::kThreads, 0, stream>>>(logits, probs, rows, vocab, temperature, top_k,
+                                                                     top_p);
   return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
