@@ -172,44 +172,91 @@ __device__ int64_t nth_in_order(int64_t vocab, int64_t r, Pred pred, RowSmem& sm
 }
 
 // Row iteration: every id of a row, four at a time (float4) where the row
-// allows it.  row_map writes f's value back in place of what it read (the
-// same thread reads and then writes each id, so src may equal dst).
-template <class F>
+// allows it.  Each thread issues the loads of kBatch groups (or ids) before
+// it uses any: the passes that stream from or to HBM batch 4 so that one CTA
+// per SM keeps enough requests in flight; the passes over L2 take 1 (more
+// would spill the inlined per-id work).
+// row_map writes f's value back in place of what it read (the same thread
+// reads and then writes each id, so src may equal dst).
+template <int kBatch = 1, class F>
 __device__ __forceinline__ void row_each(const float* src, int64_t vocab, bool vec, F&& f) {
   if (vec) {
     const float4* s4 = reinterpret_cast<const float4*>(src);
-    for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) {
-      const float4 x = s4[g];
-      f(4 * g, x.x);
-      f(4 * g + 1, x.y);
-      f(4 * g + 2, x.z);
-      f(4 * g + 3, x.w);
+    const int64_t n4 = vocab >> 2;
+    for (int64_t g0 = threadIdx.x; g0 < n4; g0 += kBatch * kThreads) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (g0 + k * kThreads < n4) x[k] = s4[g0 + k * kThreads];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t g = g0 + k * kThreads;
+        if (g < n4) {
+          f(4 * g, x[k].x);
+          f(4 * g + 1, x[k].y);
+          f(4 * g + 2, x[k].z);
+          f(4 * g + 3, x[k].w);
+        }
+      }
     }
   } else {
-    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) f(v, src[v]);
+    for (int64_t v0 = threadIdx.x; v0 < vocab; v0 += kBatch * kThreads) {
+      float x[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (v0 + k * kThreads < vocab) x[k] = src[v0 + k * kThreads];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (v0 + k * kThreads < vocab) f(v0 + k * kThreads, x[k]);
+    }
   }
 }
 
-template <bool kStreamIn, bool kStreamOut, class F>
+template <bool kStreamIn, bool kStreamOut, int kBatch = 1, class F>
 __device__ __forceinline__ void row_map(const float* src, float* dst, int64_t vocab, bool vec, F&& f) {
   if (vec) {
     const float4* s4 = reinterpret_cast<const float4*>(src);
     float4* d4 = reinterpret_cast<float4*>(dst);
-    for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) {
-      const float4 x = kStreamIn ? __ldcs(s4 + g) : s4[g];
-      const float4 y = make_float4(f(4 * g, x.x), f(4 * g + 1, x.y), f(4 * g + 2, x.z), f(4 * g + 3, x.w));
-      if (kStreamOut)
-        __stcs(d4 + g, y);
-      else
-        d4[g] = y;
+    const int64_t n4 = vocab >> 2;
+    for (int64_t g0 = threadIdx.x; g0 < n4; g0 += kBatch * kThreads) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t g = g0 + k * kThreads;
+        if (g < n4) x[k] = kStreamIn ? __ldcs(s4 + g) : s4[g];
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t g = g0 + k * kThreads;
+        if (g < n4) {
+          const float4 y =
+              make_float4(f(4 * g, x[k].x), f(4 * g + 1, x[k].y), f(4 * g + 2, x[k].z), f(4 * g + 3, x[k].w));
+          if (kStreamOut)
+            __stcs(d4 + g, y);
+          else
+            d4[g] = y;
+        }
+      }
     }
   } else {
-    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) {
-      const float y = f(v, kStreamIn ? __ldcs(src + v) : src[v]);
-      if (kStreamOut)
-        __stcs(dst + v, y);
-      else
-        dst[v] = y;
+    for (int64_t v0 = threadIdx.x; v0 < vocab; v0 += kBatch * kThreads) {
+      float x[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t v = v0 + k * kThreads;
+        if (v < vocab) x[k] = kStreamIn ? __ldcs(src + v) : src[v];
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t v = v0 + k * kThreads;
+        if (v < vocab) {
+          const float y = f(v, x[k]);
+          if (kStreamOut)
+            __stcs(dst + v, y);
+          else
+            dst[v] = y;
+        }
+      }
     }
   }
 }
@@ -266,7 +313,7 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
   // pass 1: z into the output row; non-NaN count and the largest z
   int n_local = 0;
   float m = -INFINITY;
-  row_map<true, false>(l, out, vocab, vec, [&](int64_t, float x) {
+  row_map<true, false, 4>(l, out, vocab, vec, [&](int64_t, float x) {
     float z = __fdiv_rn(x, temperature);
     if (!isnan(z)) {
       ++n_local;
