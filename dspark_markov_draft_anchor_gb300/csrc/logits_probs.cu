@@ -261,13 +261,133 @@ __device__ __forceinline__ void row_map(const float* src, float* dst, int64_t vo
   }
 }
 
+// Small top-k: the kept ids in shared memory (at most kCompactMax).
+constexpr int kCompactMax = 2048;
+
+struct CompactSmem {
+  int32_t id[kCompactMax];
+  float e[kCompactMax];  // z, then e
+  unsigned long long w[kCompactMax];
+  int n;
+};
+
+// After a top-k cut of K <= kCompactMax ids: gather them (and their z) into
+// shared memory, take e and w there, cut top-p on the K entries sorted by
+// (w descending, id ascending) (a bitonic sort, then a block scan for the
+// shortest prefix reaching the threshold), then zero the row and scatter
+// the probabilities.  Equal to the full-row passes: the same sets, sums and
+// roundings.
+__device__ __noinline__ void compact_finish(float* out, int64_t vocab, bool vec, int K, uint32_t k_key, int64_t k_id,
+                                            float m, float top_p, RowSmem& sm, CompactSmem& cs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) cs.n = 0;
+  __syncthreads();
+  row_each(out, vocab, vec, [&](int64_t v, float z) {
+    if (isnan(z)) return;
+    const uint32_t key = order_key(z);
+    if (key > k_key || (key == k_key && v <= k_id)) {
+      const int slot = atomicAdd(&cs.n, 1);
+      if (slot < kCompactMax) {  // exactly K ids pass the cut
+        cs.id[slot] = static_cast<int32_t>(v);
+        cs.e[slot] = z;
+      }
+    }
+  });
+  __syncthreads();
+  K = cs.n < K ? cs.n : K;  // equal in correct operation; never past what was gathered
+  const bool topp = top_p < 1.0f;
+  int P2 = 1;
+  while (P2 < K) P2 <<= 1;
+  uint64_t part = 0;
+  for (int i = threadIdx.x; i < (topp ? P2 : K); i += kThreads) {
+    if (i < K) {
+      const float z = cs.e[i];
+      const float e = exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
+      const uint64_t w = weight(e);
+      cs.e[i] = e;
+      cs.w[i] = w;
+      part += w;
+    } else {  // padding that sorts after every real entry
+      cs.e[i] = 0.0f;
+      cs.w[i] = 0ull;
+      cs.id[i] = 0x7FFFFFFF;
+    }
+  }
+  const uint64_t W = block_sum_u64(part, sm);
+  int n_final = K;
+  uint64_t S = W;
+  if (topp) {
+    for (int k = 2; k <= P2; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = threadIdx.x; i < P2; i += kThreads) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const uint64_t wa = cs.w[i], wb = cs.w[ixj];
+            const int32_t ia = cs.id[i], ib = cs.id[ixj];
+            const bool a_first = wa > wb || (wa == wb && ia < ib);
+            if (((i & k) == 0) != a_first) {
+              cs.w[i] = wb;
+              cs.w[ixj] = wa;
+              cs.id[i] = ib;
+              cs.id[ixj] = ia;
+              const float ea = cs.e[i];
+              cs.e[i] = cs.e[ixj];
+              cs.e[ixj] = ea;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // shortest prefix whose weight reaches the threshold: two entries a thread
+    if (threadIdx.x == 0) {
+      sm.p_thr = top_p_threshold(top_p, W);
+      sm.found = K;  // replaced by the crossing thread
+      sm.p_above = W;
+    }
+    const int i0 = 2 * threadIdx.x;
+    const uint64_t w0 = i0 < P2 ? cs.w[i0] : 0ull, w1 = i0 + 1 < P2 ? cs.w[i0 + 1] : 0ull;
+    const uint64_t mine = w0 + w1;
+    uint64_t incl = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) sm.red_u64[warp] = incl;
+    __syncthreads();
+    uint64_t before = 0;
+    for (int w = 0; w < warp; ++w) before += sm.red_u64[w];
+    const uint64_t thr = sm.p_thr;
+    const uint64_t excl = before + incl - mine;
+    if (excl < thr && thr <= excl + mine) {  // one thread: the prefix crosses here
+      const bool first = excl + w0 >= thr;
+      sm.found = first ? i0 + 1 : i0 + 2;
+      sm.p_above = first ? excl + w0 : excl + mine;
+    }
+    __syncthreads();
+    n_final = static_cast<int>(sm.found);
+    S = sm.p_above;
+    __syncthreads();
+  }
+  const float Sf = __fmul_rn(__ull2float_rn(S), 0x1p-40f);
+  if (vec) {
+    float4* d4 = reinterpret_cast<float4*>(out);
+    for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) __stcs(d4 + g, make_float4(0.f, 0.f, 0.f, 0.f));
+  } else {
+    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) __stcs(out + v, 0.0f);
+  }
+  __syncthreads();  // the zeros are ordered before the scattered values
+  for (int i = threadIdx.x; i < n_final; i += kThreads) out[cs.id[i]] = __fdiv_rn(cs.e[i], Sf);
+}
+
 // One row.  The output row doubles as scratch: pass 1 stores z there, the
 // weight pass replaces it by e (or -1 for an id that top-k or a NaN z
 // dropped), and the last pass by the probability, so later passes read a
 // value instead of recomputing a division and an exp, from L2 (one row per
 // SM is in flight).
 __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, float temperature, int32_t top_k,
-                                 float top_p, RowSmem& sm) {
+                                 float top_p, RowSmem& sm, CompactSmem& cs) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool vec = (((reinterpret_cast<uintptr_t>(l) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0) &&
                    (vocab & 3) == 0;
@@ -390,6 +510,10 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
             return !isnan(z) && order_key(z) == k_key;
           },
           sm);
+    if (top_k <= kCompactMax) {
+      compact_finish(out, vocab, vec, top_k, k_key, k_id, m, top_p, sm, cs);
+      return;
+    }
   }
 
   // weight pass: e (or -1 for a dropped id) into the output row; the kept total
@@ -476,8 +600,9 @@ __global__ void __launch_bounds__(kThreads)
     logits_probs_kernel(const float* logits, float* probs, int32_t rows, int64_t vocab, float temperature,
                         int32_t top_k, float top_p) {
   __shared__ RowSmem sm;
+  __shared__ CompactSmem cs;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    logits_probs_row(logits + r * vocab, probs + r * vocab, vocab, temperature, top_k, top_p, sm);
+    logits_probs_row(logits + r * vocab, probs + r * vocab, vocab, temperature, top_k, top_p, sm, cs);
     __syncthreads();  // shared state is reused by the next row
   }
 }

@@ -34,13 +34,14 @@ def _logits(rng, rows, V, scale=3.0):
 @pytest.mark.parametrize("rows,V,T,K,P", [
     (7, 1000, 1.0, 0, 1.0), (5, 4099, 0.7, 50, 0.9), (4, 32773, 1.3, 1000, 0.95), (6, 777, 2.0, 3, 0.5),
     (3, 129280, 1.0, 50, 0.9), (3, 129280, 0.8, 0, 0.95), (9, 2048, 1.0, 0, 1.0), (2, 513, 0.5, 512, 0.3),
-    (1, 1, 1.0, 0, 0.9), (3, 5, 1.0, 2, 0.99)])
+    (1, 1, 1.0, 0, 0.9), (3, 5, 1.0, 2, 0.99), (2, 40000, 1.1, 4096, 0.8), (2, 20000, 1.0, 2049, 1.0),
+    (2, 20000, 1.0, 2048, 0.7)])
 def test_random_rows(rows, V, T, K, P):
     rng = np.random.default_rng(rows * 7919 + V)
     _check(_logits(rng, rows, V), T, K, P)
 
 
-@pytest.mark.parametrize("K,P", [(0, 0.3), (100, 1.0), (100, 0.5), (1500, 0.7), (0, 0.999)])
+@pytest.mark.parametrize("K,P", [(0, 0.3), (100, 1.0), (100, 0.5), (1500, 0.7), (0, 0.999), (3000, 0.6)])
 def test_ties_at_both_cuts(K, P):
     """Logits on a coarse grid: long runs of equal z and equal weights, so
     both cuts fall inside a tie and the ordered scans decide them."""
