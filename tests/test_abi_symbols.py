@@ -60,3 +60,29 @@ def test_init_rejects_bad_config_before_touching_the_device(lib):
     cfg = binding.MarkovConfig(1000, 256, 1000, 4, 5, 0)
     assert lib.dspark_markov_init(ctypes.byref(ctx), ctypes.byref(cfg), 8, 16, None) == -3
     assert lib.dspark_markov_init(ctypes.byref(ctx), ctypes.byref(cfg), None, 16, None) == -1
+
+
+def test_verify_side_rejects_bad_arguments_before_touching_the_device(lib):
+    """Argument checks of the probabilistic-verify entry points come before
+    any CUDA call, and empty work returns at once (no device needed)."""
+    P = ctypes.c_void_p
+    i32, i64, u64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
+    lib.dspark_fill_uniforms.argtypes = [P, i64, u64, u64, P]
+    lib.dspark_probabilistic_accept.argtypes = [P] * 7 + [i32] * 4 + [P]
+    lib.dspark_logits_to_probs.argtypes = [P, P, i32, i32, f32, i32, f32, P]
+    fake = ctypes.c_void_p(16)  # never dereferenced: every call below returns before a launch
+    assert lib.dspark_fill_uniforms(None, -1, 0, 0, None) == -1
+    assert lib.dspark_fill_uniforms(None, 5, 0, 0, None) == -1
+    assert lib.dspark_fill_uniforms(None, 0, 0, 0, None) == 0
+    acc = lib.dspark_probabilistic_accept
+    assert acc(*([fake] * 7), -1, 5, 5, 100, None) == -1   # batch < 0
+    assert acc(*([fake] * 7), 4, 5, -1, 100, None) == -1   # P < 0
+    assert acc(*([fake] * 7), 4, 5, 5, 0, None) == -1      # vocab < 1
+    assert acc(*([fake] * 7), 4, 4, 5, 100, None) == -1    # draft_stride < P
+    assert acc(*([None] * 7), 0, 5, 5, 100, None) == 0     # empty batch
+    assert acc(None, *([fake] * 6), 4, 5, 5, 100, None) == -1  # a null pointer
+    l2p = lib.dspark_logits_to_probs
+    assert l2p(fake, fake, -1, 10, 1.0, 0, 1.0, None) == -1
+    assert l2p(fake, fake, 3, 0, 1.0, 0, 1.0, None) == -1
+    assert l2p(None, fake, 3, 10, 1.0, 0, 1.0, None) == -1
+    assert l2p(None, None, 0, 10, 1.0, 0, 1.0, None) == 0
