@@ -6,6 +6,7 @@ contract's barrier and the max (and sum) over ranks.  These tests run those
 steps as two spawned processes on 127.0.0.1.
 """
 import argparse
+import json
 import os
 import socket
 
@@ -87,3 +88,14 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 def test_algorithmic_bytes_per_step():
     # w2 read + base read + cache write, BF16
     assert bench.algorithmic_bytes_per_step(163840, 16) == 163840 * 256 * 2 + 2 * 16 * 163840 * 2
+
+
+def test_prob_verify_path_reference_arm_is_declared_unavailable(capsys):
+    assert bench.main(["--path", "prob_verify", "--impl", "reference"]) == 0
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "reference" and "unavailable" in line
+
+
+def test_prob_verify_traffic_lookup_is_keyed_by_its_own_sources():
+    assert bench.PV_WORKLOAD == "prob_verify_256x5x129280"
+    assert bench.source_digest(bench.PV_SOURCES) != bench.source_digest()
