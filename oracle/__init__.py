@@ -78,6 +78,8 @@ class LoopArgs(ctypes.Structure):
         ("bias_out", ctypes.c_void_p),
         ("keys_out", ctypes.c_void_p),
         ("nthreads", ctypes.c_int),
+        ("w2_fp8", ctypes.c_void_p),
+        ("w2_scale", ctypes.c_void_p),
     ]
 
 
@@ -121,6 +123,12 @@ def lib():
             "oracle_weight": (ctypes.c_uint64, [f32]),
             "oracle_sample_weights": (i64, [P, i64, f32]),
             "oracle_probabilistic_accept": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i64]),
+            "oracle_quantize_w2_fp8": (None, [P, P, P, i64, ctypes.c_int]),
+            "oracle_dot_fp8_rows": (None, [P, P, P, P, i64, ctypes.c_int]),
+            "oracle_e4m3_value_array": (None, [P, P, i64]),
+            "oracle_e4m3_from_f32_array": (None, [P, P, i64]),
+            "oracle_f16_value_array": (None, [P, P, i64]),
+            "oracle_f16_from_f32_array": (None, [P, P, i64]),
             "oracle_expf_nonpos": (f32, [f32]),
             "oracle_expf_nonpos_array": (None, [P, P, i64]),
             "oracle_logits_to_probs": (ctypes.c_int, [P, P, i32, i64, f32, i32, f32]),
@@ -247,15 +255,24 @@ def murmur_fmix(h):
 
 def markov_loop(*, w1, w2, base, input_ids, anchor_idx, sample_pos, seeds, temperature,
                 req_idx=None, num_req=None, mult=1.0, cap=0.0, salt=1 << 30, fed_bias=None,
-                cache=None, want_bias=False, want_keys=False, rows=None, nthreads=None):
+                cache=None, want_bias=False, want_keys=False, rows=None, nthreads=None,
+                w2_fp8=None, w2_scale=None):
     """Run the oracle loop.
 
     ``base`` is a BF16 bit array ``[rows, steps, V]`` (any strides with last
     stride 1); ``cache`` (optional) is updated in place, ``[num_req, steps, V]``.
     Returns ``dict(tokens=[rows, steps] int64, bias=..., keys=...)``.
-    ``rows`` restricts the call to the first ``rows`` rows.
+    ``rows`` restricts the call to the first ``rows`` rows.  With ``w2_fp8``
+    (E4M3 bytes ``[V, rank]``) and ``w2_scale`` (FP16 bits ``[V]``) the bias
+    comes from them instead of ``w2`` (which may then be None).
     """
     w1 = _c(w1, np.uint16)
+    if w2_fp8 is not None:
+        w2_fp8 = _c(w2_fp8, np.uint8)
+        w2_scale = _c(w2_scale, np.uint16)
+        assert w2_scale.shape == (w2_fp8.shape[0],)
+        if w2 is None:
+            w2 = np.zeros((w2_fp8.shape[0], w2_fp8.shape[1]), np.uint16)  # unread
     w2 = _c(w2, np.uint16)
     assert base.dtype == np.uint16 and base.strides[-1] == 2
     R = base.shape[0] if rows is None else rows
@@ -299,6 +316,7 @@ def markov_loop(*, w1, w2, base, input_ids, anchor_idx, sample_pos, seeds, tempe
     a.tokens, a.tokens_s0 = _ptr(tokens), K
     a.bias_out, a.keys_out = _ptr(bias_out), _ptr(keys_out)
     a.nthreads = int(nthreads or os.cpu_count() or 1)
+    a.w2_fp8, a.w2_scale = _ptr(w2_fp8), _ptr(w2_scale)
     rc = lib().oracle_markov_loop(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_markov_loop failed: {rc}")
@@ -401,3 +419,57 @@ def logits_to_probs(logits, temperature, top_k, top_p):
     if rc != 0:
         raise RuntimeError(f"oracle_logits_to_probs failed: {rc}")
     return probs
+
+
+def e4m3_value(q):
+    """E4M3 bytes to float32 (exact)."""
+    q = _c(q, np.uint8)
+    out = np.empty(q.shape, np.float32)
+    lib().oracle_e4m3_value_array(_ptr(q), _ptr(out), q.size)
+    return out
+
+
+def e4m3_from_f32(x):
+    """float32 to E4M3 bytes: nearest even, saturating to +-448, NaN to 0x7F."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    lib().oracle_e4m3_from_f32_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def f16_value(h):
+    h = _c(h, np.uint16)
+    out = np.empty(h.shape, np.float32)
+    lib().oracle_f16_value_array(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def f16_from_f32(x):
+    """float32 to FP16 bits: nearest even, saturating to +-65504, NaN to 0x7E00."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().oracle_f16_from_f32_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def quantize_w2_fp8(w2):
+    """[P1] dsparkQuantizeMarkovW2Fp8: BF16 bits [V, R] -> (E4M3 bytes [V, R],
+    FP16 scale bits [V])."""
+    w2 = _c(w2, np.uint16)
+    V, R = w2.shape
+    q = np.empty((V, R), np.uint8)
+    scale = np.empty(V, np.uint16)
+    lib().oracle_quantize_w2_fp8(_ptr(w2), _ptr(q), _ptr(scale), V, R)
+    return q, scale
+
+
+def dot_fp8(e, q, scale):
+    """Row-wise exactly rounded BF16 of scale * sum(e * decode(q)): ``e`` BF16
+    bits [n, R], ``q`` E4M3 bytes [n, R], ``scale`` FP16 bits [n]."""
+    e = _c(np.atleast_2d(e), np.uint16)
+    q = _c(np.atleast_2d(q), np.uint8)
+    scale = _c(np.atleast_1d(scale), np.uint16)
+    n, R = e.shape
+    out = np.empty(n, np.uint16)
+    lib().oracle_dot_fp8_rows(_ptr(e), _ptr(q), _ptr(scale), _ptr(out), n, R)
+    return out

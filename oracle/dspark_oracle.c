@@ -460,6 +460,199 @@ uint16_t oracle_dot_bf16(const uint16_t *a, const uint16_t *b, int n) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* [P1] dsparkQuantizeMarkovW2Fp8 / dsparkMarkovGreedyFusedStepFp8: w2 as   */
+/* E4M3 bytes (bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN,   */
+/* largest 448) with one FP16 scale per row, rowScale = rowAbsMax / 448.   */
+/* Readings (the pages give the format and the scale rule only):           */
+/*   - rowAbsMax = max |w| over the row's non-NaN BF16 values; the scale is */
+/*     RN(rowAbsMax / 448) in FP32, then to FP16 (nearest even; beyond      */
+/*     65504 it saturates to 65504);                                        */
+/*   - q = E4M3(RN(w / s)) in FP32, nearest even, saturating to +-448 (the  */
+/*     hardware conversion's satfinite mode); NaN gives 0x7F; a row whose  */
+/*     scale is 0 stores zeros;                                             */
+/*   - the step's bias is s * (sum_j e_j * decode(q_j)), the scale applied  */
+/*     to the exact sum, rounded once to BF16, as the BF16 path's dot       */
+/*     ([P2] module docstring).                                             */
+/* ------------------------------------------------------------------------ */
+
+float oracle_e4m3_value(uint8_t q) {
+  const int E = (q >> 3) & 15, M = q & 7;
+  const double sg = (q & 0x80) ? -1.0 : 1.0;
+  if (E == 15 && M == 7) return NAN;
+  if (E == 0) return (float)(sg * ldexp((double)M, -9));
+  return (float)(sg * ldexp((double)(8 + M), E - 10));
+}
+
+uint8_t oracle_e4m3_from_f32(float x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  if (a < ldexp(1.0, -6)) { /* subnormals: multiples of 2^-9; 8 is the smallest normal */
+    const double m = nearbyint(ldexp(a, 9));
+    return (uint8_t)(sign | (uint8_t)m);
+  }
+  int e;
+  frexp(a, &e); /* a in [2^(e-1), 2^e) */
+  int E = e - 1 + 7;
+  double m = nearbyint(ldexp(a, 3 - (e - 1))); /* [8, 16] */
+  if (m == 16.0) {
+    m = 8.0;
+    E += 1;
+  }
+  return (uint8_t)(sign | (uint8_t)((E << 3) | ((int)m - 8)));
+}
+
+float oracle_f16_value(uint16_t h) {
+  const int E = (h >> 10) & 31, M = h & 1023;
+  const double sg = (h & 0x8000) ? -1.0 : 1.0;
+  if (E == 31) return M ? NAN : (float)(sg * INFINITY);
+  if (E == 0) return (float)(sg * ldexp((double)M, -24));
+  return (float)(sg * ldexp((double)(1024 + M), E - 25));
+}
+
+uint16_t oracle_f16_from_f32(float x) {
+  if (isnan(x)) return 0x7E00;
+  const uint16_t sign = signbit(x) ? 0x8000 : 0x0000;
+  const double a = fabs((double)x);
+  if (a >= 65504.0) return (uint16_t)(sign | 0x7BFF);
+  if (a < ldexp(1.0, -14)) { /* subnormals: multiples of 2^-24; 1024 is the smallest normal */
+    const double m = nearbyint(ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)m);
+  }
+  int e;
+  frexp(a, &e);
+  int E = e - 1 + 15;
+  double m = nearbyint(ldexp(a, 10 - (e - 1))); /* [1024, 2048] */
+  if (m == 2048.0) {
+    m = 1024.0;
+    E += 1;
+  }
+  return (uint16_t)(sign | (uint16_t)((E << 10) | ((int)m - 1024)));
+}
+
+void oracle_quantize_w2_fp8(const uint16_t *w2, uint8_t *q, uint16_t *scale, int64_t vocab, int rank) {
+  for (int64_t v = 0; v < vocab; v++) {
+    const uint16_t *row = w2 + v * rank;
+    float amax = 0.0f;
+    for (int j = 0; j < rank; j++) {
+      const float w = oracle_bf16_to_f32(row[j]);
+      if (!isnan(w) && fabsf(w) > amax) amax = fabsf(w);
+    }
+    const uint16_t s16 = oracle_f16_from_f32(amax / 448.0f);
+    const float s = oracle_f16_value(s16);
+    scale[v] = s16;
+    for (int j = 0; j < rank; j++)
+      q[v * rank + j] = s == 0.0f ? 0x00 : oracle_e4m3_from_f32(oracle_bf16_to_f32(row[j]) / s);
+  }
+}
+
+static void f16_parts(uint16_t h, uint32_t *sig, int *exp) {
+  const int E = (h >> 10) & 31;
+  const uint32_t M = h & 1023u;
+  if (E == 0) {
+    *sig = M;
+    *exp = -24;
+  } else {
+    *sig = 1024u + M;
+    *exp = E - 25;
+  }
+}
+
+static void e4m3_parts(uint8_t q, uint32_t *sig, int *exp) {
+  const int E = (q >> 3) & 15;
+  const uint32_t M = q & 7u;
+  if (E == 0) {
+    *sig = M;
+    *exp = -9;
+  } else {
+    *sig = 8u + M;
+    *exp = E - 10;
+  }
+}
+
+/* RN_bf16(s * sum_j e_j * decode(q_j)) exactly, the scale applied to the
+ * exact sum.  For a finite nonzero scale each product of the three factors
+ * is an integer below 2^23 times 2^(sum of exponents) >= 2^-166, kept in the
+ * same 640-bit accumulators as the BF16 dot; a zero, infinite or NaN scale
+ * meets the exact sum's class (zero with its sign, infinite, NaN) by the
+ * IEEE rules of one multiplication. */
+uint16_t oracle_dot_fp8(const uint16_t *e, const uint8_t *q, uint16_t scale, int n) {
+  const int s_nan = ((scale & 0x7C00) == 0x7C00) && (scale & 0x3FF);
+  const int s_inf = (scale & 0x7FFF) == 0x7C00;
+  const int s_zero = (scale & 0x7FFF) == 0;
+  const int s_neg = (scale & 0x8000) != 0;
+  const int s_finite = !s_nan && !s_inf && !s_zero;
+  int has_nan = 0, has_pinf = 0, has_ninf = 0, all_negzero = 1;
+  wide_t pos, neg;
+  memset(&pos, 0, sizeof(pos));
+  memset(&neg, 0, sizeof(neg));
+  uint32_t ss = 1;
+  int es = 0;
+  if (s_finite) f16_parts(scale, &ss, &es);
+  for (int j = 0; j < n; j++) {
+    const uint16_t x = e[j];
+    const uint8_t y = q[j];
+    const int x_nan = ((x & 0x7F80) == 0x7F80) && (x & 0x7F);
+    const int y_nan = (y & 0x7F) == 0x7F;
+    const int x_inf = (x & 0x7FFF) == 0x7F80;
+    const int x_zero = (x & 0x7FFF) == 0, y_zero = (y & 0x7F) == 0;
+    const int negative = (((x & 0x8000) != 0) ^ ((y & 0x80) != 0)) != 0; /* sign of e_j * d_j */
+    if (x_nan || y_nan) {
+      has_nan = 1;
+      continue;
+    }
+    if (x_inf) {
+      if (y_zero) has_nan = 1; /* inf * 0 */
+      else if (negative) has_ninf = 1;
+      else has_pinf = 1;
+      continue;
+    }
+    if (x_zero || y_zero) {
+      if (!negative) all_negzero = 0;
+      continue;
+    }
+    all_negzero = 0;
+    uint32_t sx, sy;
+    int ex, ey;
+    bf16_parts(x, &sx, &ex);
+    e4m3_parts(y, &sy, &ey);
+    wide_add_shifted(negative ? &neg : &pos, (uint64_t)sx * sy * ss, ex + ey + es + ACC_OFFSET);
+  }
+  const int sum_nan = has_nan || (has_pinf && has_ninf);
+  const int sum_inf = has_pinf || has_ninf;
+  const int c = wide_cmp(&pos, &neg);
+  /* sign of the exact sum: an infinity's, else the accumulators', else -0 when every product was -0 */
+  const int sum_neg = sum_inf ? has_ninf : (c != 0 ? c < 0 : (n > 0 && all_negzero));
+  const uint16_t sign = (uint16_t)((sum_neg ^ s_neg) ? 0x8000 : 0x0000);
+  if (s_nan || sum_nan) return 0x7FFF;
+  if (sum_inf) return s_zero ? 0x7FFF : (uint16_t)(sign | 0x7F80);
+  if (s_inf) return c == 0 ? 0x7FFF : (uint16_t)(sign | 0x7F80); /* inf * 0 */
+  if (s_zero || c == 0) return sign;
+  wide_t mag;
+  if (c > 0) wide_sub(&mag, &pos, &neg);
+  else wide_sub(&mag, &neg, &pos);
+  return (uint16_t)(wide_to_bf16(&mag, 0) | sign);
+}
+
+void oracle_dot_fp8_rows(const uint16_t *e, const uint8_t *q, const uint16_t *scale, uint16_t *out, int64_t rows,
+                         int n) {
+  for (int64_t r = 0; r < rows; r++) out[r] = oracle_dot_fp8(e + r * n, q + r * n, scale[r], n);
+}
+void oracle_e4m3_value_array(const uint8_t *q, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_value(q[i]);
+}
+void oracle_e4m3_from_f32_array(const float *x, uint8_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_from_f32(x[i]);
+}
+void oracle_f16_value_array(const uint16_t *h, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_f16_value(h[i]);
+}
+void oracle_f16_from_f32_array(const float *x, uint16_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; i++) out[i] = oracle_f16_from_f32(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
 /* The loop ([P2] _loop_rest; [P3] module docstring, _StepKernel.kernel,   */
 /* anchor_embed, _w1_row).  For each step s and row r:                     */
 /*   prev(0)   = sext32(input_ids[anchor_idx[r]])                           */
@@ -495,6 +688,8 @@ static void *row_step_range(void *arg) {
     uint16_t b;
     if (a->fed_bias)
       b = a->fed_bias[((int64_t)j->r * a->steps + j->s) * V + v];
+    else if (a->w2_fp8)
+      b = oracle_dot_fp8(j->e, a->w2_fp8 + v * a->rank, a->w2_scale[v], a->rank);
     else
       b = oracle_dot_bf16(j->e, a->w2 + v * a->rank, a->rank);
     if (a->bias_out) a->bias_out[((int64_t)j->r * a->steps + j->s) * V + v] = b;

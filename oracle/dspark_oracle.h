@@ -61,6 +61,8 @@ typedef struct {
   uint16_t *bias_out; /* optional [rows, steps, vocab] */
   float *keys_out;    /* optional [rows, steps, vocab] */
   int nthreads;
+  const uint8_t *w2_fp8;   /* optional [vocab, rank] E4M3: the bias from it (and w2_scale) instead of w2 */
+  const uint16_t *w2_scale; /* [vocab] FP16 row scales, with w2_fp8 */
 } oracle_loop_args;
 
 int oracle_markov_loop(const oracle_loop_args *a);
@@ -79,6 +81,18 @@ int oracle_probabilistic_accept(const float *target, const float *draft_probs, c
                                 int32_t *accept_len, int32_t batch, int32_t draft_stride, int32_t P,
                                 int64_t vocab);
 
+float oracle_e4m3_value(uint8_t q);
+uint8_t oracle_e4m3_from_f32(float x);
+float oracle_f16_value(uint16_t h);
+uint16_t oracle_f16_from_f32(float x);
+void oracle_quantize_w2_fp8(const uint16_t *w2, uint8_t *q, uint16_t *scale, int64_t vocab, int rank);
+uint16_t oracle_dot_fp8(const uint16_t *e, const uint8_t *q, uint16_t scale, int n);
+void oracle_dot_fp8_rows(const uint16_t *e, const uint8_t *q, const uint16_t *scale, uint16_t *out, int64_t rows,
+                         int n);
+void oracle_e4m3_value_array(const uint8_t *q, float *out, int64_t n);
+void oracle_e4m3_from_f32_array(const float *x, uint8_t *out, int64_t n);
+void oracle_f16_value_array(const uint16_t *h, float *out, int64_t n);
+void oracle_f16_from_f32_array(const float *x, uint16_t *out, int64_t n);
 float oracle_expf_nonpos(float x);
 void oracle_expf_nonpos_array(const float *x, float *out, int64_t n);
 int oracle_logits_to_probs(const float *logits, float *probs, int32_t rows, int64_t vocab, float temperature,
