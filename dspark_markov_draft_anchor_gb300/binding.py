@@ -33,7 +33,7 @@ EXPORTED = (
     "dspark_markov_get_status_detail",
     "dspark_markov_destroy", "dspark_build_verify_tokens", "dspark_greedy_accept_scratch_bytes",
     "dspark_greedy_accept", "dspark_greedy_accept_noalloc", "dspark_fill_uniforms",
-    "dspark_probabilistic_accept", "dspark_logits_to_probs", "dspark_strerror",
+    "dspark_probabilistic_accept", "dspark_logits_to_probs", "dspark_quantize_w2_fp8", "dspark_strerror",
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
     "dspark_check_logf", "dspark_check_tanhf", "dspark_noise_bound_tables",
 )
@@ -102,6 +102,7 @@ def load(build_if_missing: bool = False):
         "dspark_fill_uniforms": (ctypes.c_int, [P, i64, ctypes.c_uint64, ctypes.c_uint64, P]),
         "dspark_probabilistic_accept": (ctypes.c_int, [P, P, P, P, P, P, P, i32, i32, i32, i32, P]),
         "dspark_logits_to_probs": (ctypes.c_int, [P, P, i32, i32, ctypes.c_float, i32, ctypes.c_float, P]),
+        "dspark_quantize_w2_fp8": (ctypes.c_int, [P, P, P, i64, i32, P]),
         "dspark_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "dspark_check_noise_range": (ctypes.c_int, [ctypes.c_uint32, P, i64, P]),
         "dspark_check_hash": (ctypes.c_int, [i64, i32, i64, ctypes.c_uint32, P, P, i64, P]),
@@ -267,6 +268,11 @@ def dspark_probabilistic_accept(target_probs, draft_probs, draft, proposal_len, 
 def dspark_logits_to_probs(logits, probs, rows, vocab, temperature, top_k, top_p, stream=None):
     _check(load().dspark_logits_to_probs(_ptr(logits), _ptr(probs), rows, vocab, temperature, top_k, top_p,
                                          _stream(stream)), "dspark_logits_to_probs")
+
+
+def dspark_quantize_w2_fp8(w2_bf16, w2_fp8, scale_f16, vocab, rank, stream=None):
+    _check(load().dspark_quantize_w2_fp8(_ptr(w2_bf16), _ptr(w2_fp8), _ptr(scale_f16), vocab, rank, _stream(stream)),
+           "dspark_quantize_w2_fp8")
 
 
 def dspark_noise_bound_tables(n: int = 512):

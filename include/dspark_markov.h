@@ -320,6 +320,21 @@ DSPARK_API int dspark_probabilistic_accept(const float *target_probs, const floa
 DSPARK_API int dspark_logits_to_probs(const float *logits, float *probs, int32_t rows, int32_t vocab,
                                       float temperature, int32_t top_k, float top_p, cudaStream_t stream);
 
+/*
+ * dspark_quantize_w2_fp8 -- [P1] dsparkQuantizeMarkovW2Fp8: markov_w2 as
+ * E4M3 bytes with one FP16 scale per row.  Device pointers: w2_bf16
+ * [vocab, rank] BF16 bits (16-byte aligned), w2_fp8 out [vocab, rank] E4M3
+ * bytes (8-byte aligned), scale_f16 out [vocab] FP16 bits (2-byte aligned).
+ * Per row: rowAbsMax over the non-NaN values, scale = RN(rowAbsMax / 448)
+ * in FP32, then to FP16 nearest even, saturating at 65504 (the pages give
+ * rowAbsMax / 448 only); q = E4M3(RN(w / scale)), nearest even, saturating
+ * to +-448, NaN to 0x7F; a row whose scale is 0 stores zeros.
+ * rank a multiple of 8 (>= 8), vocab >= 0.  DSPARK_ERR_MISALIGNED for a
+ * pointer off its alignment.  Allocates nothing; one kernel on `stream`.
+ */
+DSPARK_API int dspark_quantize_w2_fp8(const uint16_t *w2_bf16, uint8_t *w2_fp8, uint16_t *scale_f16,
+                                      int64_t vocab, int32_t rank, cudaStream_t stream);
+
 /* A short English description of a DSPARK_* code (static storage). */
 DSPARK_API const char *dspark_strerror(int code);
 
