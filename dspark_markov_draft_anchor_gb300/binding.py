@@ -29,7 +29,8 @@ NOALLOC_MAX_VERIFY_ROWS = 8192  # DSPARK_NOALLOC_MAX_VERIFY_ROWS
 
 EXPORTED = (
     "dspark_markov_init", "dspark_markov_loop", "dspark_markov_anchor", "dspark_markov_step",
-    "dspark_markov_partial_count", "dspark_markov_bias_path", "dspark_markov_loop_kernels", "dspark_markov_get_status",
+    "dspark_markov_partial_count", "dspark_markov_bias_path", "dspark_markov_set_w2_fp8", "dspark_markov_loop_kernels",
+    "dspark_markov_get_status",
     "dspark_markov_get_status_detail",
     "dspark_markov_destroy", "dspark_build_verify_tokens", "dspark_greedy_accept_scratch_bytes",
     "dspark_greedy_accept", "dspark_greedy_accept_noalloc", "dspark_fill_uniforms",
@@ -91,6 +92,7 @@ def load(build_if_missing: bool = False):
         "dspark_markov_step": (ctypes.c_int, [P, ctypes.POINTER(LoopArgs), i32, P]),
         "dspark_markov_partial_count": (i32, [P]),
         "dspark_markov_bias_path": (i32, [P, i32]),
+        "dspark_markov_set_w2_fp8": (ctypes.c_int, [P, P, P]),
         "dspark_markov_loop_kernels": (i32, [P, ctypes.POINTER(LoopArgs)]),
         "dspark_markov_get_status": (ctypes.c_int, [P, P, ctypes.POINTER(i32)]),
         "dspark_markov_get_status_detail": (ctypes.c_int, [P, P, ctypes.POINTER(i32)]),
@@ -182,6 +184,10 @@ def dspark_markov_partial_count(ctx) -> int:
 
 def dspark_markov_bias_path(ctx, rows: int) -> int:
     return int(load().dspark_markov_bias_path(ctx, rows))
+
+
+def dspark_markov_set_w2_fp8(ctx, w2_fp8, w2_scale_f16):
+    _check(load().dspark_markov_set_w2_fp8(ctx, _ptr(w2_fp8), _ptr(w2_scale_f16)), "dspark_markov_set_w2_fp8")
 
 
 def dspark_markov_loop_kernels(ctx, args: LoopArgs) -> int:
@@ -337,6 +343,12 @@ class MarkovContext:
 
     def loop_kernels(self, args: LoopArgs) -> int:
         return dspark_markov_loop_kernels(self.ctx, args)
+
+    def set_w2_fp8(self, w2_fp8, w2_scale_f16) -> None:
+        """Attach E4M3 w2 and FP16 row scales (device tensors the caller keeps
+        alive); None, None detaches."""
+        dspark_markov_set_w2_fp8(self.ctx, w2_fp8, w2_scale_f16)
+        self._fp8 = (w2_fp8, w2_scale_f16)
 
     def status(self, stream=None) -> int:
         return dspark_markov_get_status(self.ctx, stream)

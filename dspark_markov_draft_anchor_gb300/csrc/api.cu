@@ -26,6 +26,8 @@ struct dspark_markov_ctx {
   bool fused_ok;              // the tensor-core kernel may run several steps in one cooperative launch
   CUtensorMap w2_map;         // TMA map over w2: boxes of 32 rows x 64 K, 128-byte swizzle
   CUtensorMap w2_tile_map;    // the same with boxes of 128 rows (whole vocabulary tiles)
+  const uint8_t* w2_fp8;      // E4M3 w2 [V, 256] (caller-owned) or null: when set, every step takes
+  const uint16_t* w2_scale;   // its bias from it and these FP16 row scales [V]
 };
 
 namespace {
@@ -145,7 +147,7 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   if (major != 10 || minor != 3) return DSPARK_ERR_UNSUPPORTED_DEVICE;
-  if (dspark::setup_step_simple() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (dspark::setup_step_simple() != cudaSuccess || dspark::setup_step_fp8() != cudaSuccess) return DSPARK_ERR_CUDA;
   const bool tc_setup = dspark::setup_step_tc() == cudaSuccess;
   (void)cudaGetLastError();
 
@@ -198,6 +200,7 @@ void dspark_markov_destroy(dspark_markov_ctx* ctx) {
 }
 
 int32_t dspark_markov_bias_path(const dspark_markov_ctx* ctx, int32_t rows) {
+  if (ctx && ctx->w2_fp8) return 2;
   if (!ctx || !ctx->tc_ok || (ctx->cfg.flags & DSPARK_FLAG_FORCE_FMA)) return 0;
   if (ctx->cfg.flags & DSPARK_FLAG_FORCE_MMA) return 1;
   return rows > kFmaMaxRows ? 1 : 0;
@@ -205,7 +208,16 @@ int32_t dspark_markov_bias_path(const dspark_markov_ctx* ctx, int32_t rows) {
 
 int32_t dspark_markov_partial_count(const dspark_markov_ctx* ctx) {
   if (!ctx) return 0;
-  return dspark_markov_bias_path(ctx, ctx->cfg.max_rows) ? ctx->grid_tc : ctx->grid_simple;
+  return dspark_markov_bias_path(ctx, ctx->cfg.max_rows) == 1 ? ctx->grid_tc : ctx->grid_simple;
+}
+
+int dspark_markov_set_w2_fp8(dspark_markov_ctx* ctx, const void* w2_fp8, const void* w2_scale_f16) {
+  if (!ctx || (!w2_fp8) != (!w2_scale_f16)) return DSPARK_ERR_INVALID_ARG;
+  if (w2_fp8 && (!aligned16(w2_fp8) || (reinterpret_cast<uintptr_t>(w2_scale_f16) & 1u)))
+    return DSPARK_ERR_MISALIGNED;
+  ctx->w2_fp8 = static_cast<const uint8_t*>(w2_fp8);
+  ctx->w2_scale = static_cast<const uint16_t*>(w2_scale_f16);
+  return DSPARK_OK;
 }
 
 int dspark_markov_anchor(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
@@ -234,7 +246,10 @@ int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_
   if (select) p.partials = ctx->partials;
   cudaError_t e;
   int grid;
-  if (dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a)) {
+  if (ctx->w2_fp8) {
+    grid = ctx->grid_simple;
+    e = dspark::launch_step_fp8(p, ctx->w2_fp8, ctx->w2_scale, a->cap != 0.0f, pdl, stream);
+  } else if (dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a)) {
     if (select) {
       p.finish = 0;
     } else if (in_loop) {

@@ -28,6 +28,12 @@ int simple_step_grid(int64_t vocab);
 cudaError_t setup_step_simple();
 cudaError_t launch_step_simple(const StepParams& p, bool has_cap, bool pdl, cudaStream_t stream);
 
+// The same step with w2 as E4M3 bytes [V, 256] and FP16 row scales [V]
+// (CUDA-core FMA bias, the scale applied to each row's sum).
+cudaError_t setup_step_fp8();
+cudaError_t launch_step_fp8(const StepParams& p, const uint8_t* w2q, const uint16_t* w2s, bool has_cap, bool pdl,
+                            cudaStream_t stream);
+
 // Tensor-core fused step: persistent CTAs over vocabulary ranges, TMA-fed w2
 // and base, tcgen05 bias into TMEM.
 cudaError_t setup_step_tc();

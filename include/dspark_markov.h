@@ -165,8 +165,24 @@ DSPARK_API int dspark_markov_step(dspark_markov_ctx *ctx, const dspark_markov_lo
  * kernel partitions the vocabulary into (its grid size). */
 DSPARK_API int32_t dspark_markov_partial_count(const dspark_markov_ctx *ctx);
 
-/* Which bias path a call with `rows` rows takes: 0 = FMA, 1 = tcgen05. */
+/* Which bias path a call with `rows` rows takes: 0 = FMA, 1 = tcgen05,
+ * 2 = FMA over the FP8 w2 attached by dspark_markov_set_w2_fp8. */
 DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t rows);
+
+/*
+ * dspark_markov_set_w2_fp8 -- attach (or, with two NULLs, detach) an FP8 w2
+ * ([P1] dsparkMarkovGreedyFusedStepFp8): w2_fp8 [vocab, 256] E4M3 bytes
+ * (16-byte aligned) and w2_scale_f16 [vocab] FP16 row scales, device
+ * pointers owned by the caller (e.g. from dspark_quantize_w2_fp8) and read by
+ * every later step.  While attached, every step takes its bias as
+ * RN_bf16(RN(scale * sum_j e_j * decode(q_j))) with the sum in FP32 (any
+ * order; within 1 BF16 ulp of the exactly rounded s * sum(e * decode(q))
+ * outside the FP32 accumulation bound), one CUDA-core launch per step; the
+ * rest of the step is unchanged.  Enqueues nothing.  DSPARK_ERR_INVALID_ARG
+ * for one NULL and one non-NULL pointer, DSPARK_ERR_MISALIGNED for a pointer
+ * off its alignment.
+ */
+DSPARK_API int dspark_markov_set_w2_fp8(dspark_markov_ctx *ctx, const void *w2_fp8, const void *w2_scale_f16);
 
 /* The number of kernels dspark_markov_loop enqueues for `args` (2 when one
  * launch runs every step, 1 + 2 steps with DSPARK_FLAG_SELECT_2LAUNCH, else
