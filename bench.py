@@ -89,8 +89,10 @@ def rank_seed_salt(rank: int) -> int:
     return 1000 + rank
 
 
-def algorithmic_bytes_per_step(vocab: int, rows: int, rank: int = 256) -> int:
-    return vocab * rank * 2 + 2 * rows * vocab * 2
+def algorithmic_bytes_per_step(vocab: int, rows: int, rank: int = 256, w2: str = "bf16") -> int:
+    """w2 read (BF16, or E4M3 bytes plus FP16 row scales) + base read + cache write."""
+    w2_bytes = vocab * rank * 2 if w2 == "bf16" else vocab * rank + vocab * 2
+    return w2_bytes + 2 * rows * vocab * 2
 
 
 LOOP_SOURCES = ("api.cu", "step_tc.cu", "step_simple.cu", "step_common.cuh", "markov_math.cuh", "ptx.cuh",
@@ -277,6 +279,12 @@ def run_native(args, d: Dist):
     tokens = torch.zeros((R, K), dtype=torch.int64, device=dev)
     flags = binding.FLAG_PDL | {"auto": 0, "fma": binding.FLAG_FORCE_FMA, "mma": binding.FLAG_FORCE_MMA}[args.bias_path]
     ctx = binding.MarkovContext(w1, w2, max_rows=R, max_steps=K, flags=flags)
+    if args.w2 == "fp8":  # E4M3 w2 with FP16 row scales, quantised once outside the timed region
+        w2q = torch.empty((V, 256), dtype=torch.uint8, device=dev)
+        w2s = torch.empty(V, dtype=torch.int16, device=dev)
+        binding.dspark_quantize_w2_fp8(w2, w2q, w2s, V, 256)
+        torch.cuda.synchronize()
+        ctx.set_w2_fp8(w2q, w2s)
     a = binding.loop_args(base=base, cache=cache, input_ids=ids, anchor_idx=anc, sample_pos=pos, seeds=seeds,
                           temperature=temp, tokens=tokens, req_idx=req, mult=wl.mult, cap=wl.cap, salt=wl.salt)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -393,7 +401,7 @@ def run_native(args, d: Dist):
     result = None
     if d.rank == 0:
         peak, peak_kind = measured_peaks()
-        algo = algorithmic_bytes_per_step(V, R)
+        algo = algorithmic_bytes_per_step(V, R, w2=args.w2)
         algo_launch = algo * launch_steps
         achieved = algo_launch / (kernel_us * 1e-6) / 1e9
         cpu_us, cpu_s = (None, None)
@@ -409,13 +417,14 @@ def run_native(args, d: Dist):
                        "model": "DSpark Markov head (random-init w1/w2 BF16)", "global_batch": R * d.world,
                        "seq_len": K, "parallelism": f"replicas x{d.world} (rows sharded, no collective)",
                        "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed loop",
-                       "graph": True, "pdl": True, "bias_path": ["fma", "tcgen05"][ctx.bias_path(R)]},
+                       "graph": True, "pdl": True, "bias_path": ["fma", "tcgen05", "fp8 fma"][ctx.bias_path(R)], "w2": args.w2},
             "loop_us": {"mean": mean_us, "p10": qs[0], "p50": qs[1], "p90": qs[2], "anchor": anchor_us,
                         "eager_with_events": eager_loop_us},
             "gbs_loop": algo * K / (mean_us * 1e-6) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": recorded_traffic(wl.name), "peak_kind": f"{peak_kind} hbm_gbs",
-                         "kernel": "step_tc_kernel, all k steps in one launch" if fused else "markov step",
+                         "frac": achieved / peak, "traffic": recorded_traffic(wl.name) if args.w2 == "bf16" else None, "peak_kind": f"{peak_kind} hbm_gbs",
+                         "kernel": ("step_tc_kernel, all k steps in one launch" if fused else
+                                    "step_fp8_kernel, one launch per step" if args.w2 == "fp8" else "markov step"),
                          "kernel_us": kernel_us, "step_us": step_us, "step_us_eager_per_step_launch": eager_step_us,
                          "kernel_us_from": "graphed loop - graphed anchor (per launch), CUDA events, L2 flushed",
                          "algorithmic_bytes": algo_launch, "algorithmic_bytes_per_step": algo,
@@ -612,6 +621,8 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     p.add_argument("--bias-path", choices=["auto", "fma", "mma"], default="auto",
                    help="bias contraction: the library's choice by row count, or forced")
+    p.add_argument("--w2", choices=["bf16", "fp8"], default="bf16",
+                   help="markov_w2 as BF16 (headline) or E4M3 with FP16 row scales")
     p.add_argument("--path", choices=["draft_loop", "prob_verify"], default="draft_loop",
                    help="the draft loop (headline) or the probabilistic verify of a 256 x 5 x 129280 batch")
     args = p.parse_args(argv)
