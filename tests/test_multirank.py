@@ -99,3 +99,8 @@ def test_prob_verify_path_reference_arm_is_declared_unavailable(capsys):
 def test_prob_verify_traffic_lookup_is_keyed_by_its_own_sources():
     assert bench.PV_WORKLOAD == "prob_verify_256x5x129280"
     assert bench.source_digest(bench.PV_SOURCES) != bench.source_digest()
+
+
+def test_algorithmic_bytes_per_step_with_fp8_w2():
+    # E4M3 w2 (1 byte an entry) + FP16 row scales + base read + cache write
+    assert bench.algorithmic_bytes_per_step(163840, 16, w2="fp8") == 163840 * 256 + 163840 * 2 + 2 * 16 * 163840 * 2
