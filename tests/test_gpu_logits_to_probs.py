@@ -86,6 +86,18 @@ def test_in_place_and_errors():
     binding.dspark_logits_to_probs(None, None, 0, 5, 1.0, 0, 1.0)  # no rows: nothing to do
 
 
+@pytest.mark.parametrize("rows,V,T,K,P", [(400, 300, 1.0, 20, 0.9), (333, 1001, 0.8, 0, 0.95), (200, 100, 0.0, 0, 1.0),
+                                          (320, 4096, 1.2, 5000, 0.7), (310, 700, 1.0, 0, 1.0)])
+def test_more_rows_than_ctas(rows, V, T, K, P):
+    """More rows than the persistent grid (one CTA per SM): each CTA takes
+    several rows in turn, with every shared decision reset between them."""
+    rng = np.random.default_rng(rows + V)
+    l = _logits(rng, rows, V)
+    l[::7, ::3] = np.round(l[::7, ::3])  # ties in some rows
+    l[5, :] = np.nan                     # an all-NaN row among them
+    _check(l, T, K, P)
+
+
 def test_full_vocabulary_rows():
     """64 rows of V = 129280 (the verify shape's vocabulary)."""
     rng = np.random.default_rng(17)

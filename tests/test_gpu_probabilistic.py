@@ -12,7 +12,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("n,seed,offset", [(1, 0, 0), (1_000_003, 0x1234_5678_9ABC_DEF0, 77),
-                                           (4097, 2**64 - 1, 2**64 - 3), (7, 5, 2**40)])
+                                           (4097, 2**64 - 1, 2**64 - 3), (7, 5, 2**40),
+                                           (6_000_001, 99, 2**32 - 5)])  # grid-stride: more blocks than threads
 def test_fill_uniforms_bit_exact(n, seed, offset):
     u = torch.empty(n, dtype=torch.float32, device="cuda")
     binding.dspark_fill_uniforms(u, n, seed, offset)
