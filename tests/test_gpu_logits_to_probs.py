@@ -74,6 +74,18 @@ def test_degenerate_rows_and_settings():
     _check(l, 1.0, 10, 0.2)
 
 
+def test_top_p_exact_boundaries():
+    """p W exactly on a prefix sum, and one float above or below, on both the
+    compact (top-k) and the full-row cut."""
+    l = np.float32([[2.0, 2.0, 2.0, 2.0, -50.0]] * 3)
+    l2 = np.float32([[1.0] * 8 + [-60.0] * 9])
+    for P in (0.25, 0.5, 0.75, float(np.nextafter(np.float32(0.5), np.float32(1))),
+              float(np.nextafter(np.float32(0.5), np.float32(0)))):
+        for K in (0, 4, 8):
+            _check(l, 1.0, K, P)
+            _check(l2, 1.0, K, P)
+
+
 def test_in_place_and_errors():
     rng = np.random.default_rng(4)
     l = _logits(rng, 5, 4096)

@@ -144,3 +144,20 @@ def test_monotone_and_normalised_under_both_filters():
         # everything dropped is no larger than the smallest kept logit
         dropped = np.setdiff1d(np.arange(l.shape[1]), kept)
         assert l[r][dropped].max() <= l[r][kept].min()
+
+
+def test_top_p_threshold_is_reached_not_exceeded():
+    """Four equal logits weigh exactly 2^40 each (W = 2^42): p = 1/4 and 1/2
+    put p W exactly on a prefix sum, which is then enough (sum >= ceil(p W));
+    a p just above moves the cut by one id (the ceiling), one just below
+    does not."""
+    l = np.float32([[2.0, 2.0, 2.0, 2.0, -50.0]])
+    def kept(p):
+        return int(np.count_nonzero(oracle.logits_to_probs(l, 1.0, 4, p)[0]))
+    assert kept(0.25) == 1 and kept(0.5) == 2 and kept(0.75) == 3
+    up = np.nextafter(np.float32(0.5), np.float32(1))
+    down = np.nextafter(np.float32(0.5), np.float32(0))
+    assert kept(up) == 3 and kept(down) == 2
+    assert kept(np.nextafter(np.float32(0.25), np.float32(0))) == 1
+    p = oracle.logits_to_probs(l, 1.0, 4, 0.5)[0]
+    assert p[0] == p[1] == np.float32(0.5) and p[2] == 0 and p[3] == 0
