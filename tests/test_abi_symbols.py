@@ -86,3 +86,18 @@ def test_verify_side_rejects_bad_arguments_before_touching_the_device(lib):
     assert l2p(fake, fake, 3, 0, 1.0, 0, 1.0, None) == -1
     assert l2p(None, fake, 3, 10, 1.0, 0, 1.0, None) == -1
     assert l2p(None, None, 0, 10, 1.0, 0, 1.0, None) == 0
+
+
+def test_fp8_calls_reject_bad_arguments_before_touching_the_device(lib):
+    P = ctypes.c_void_p
+    lib.dspark_quantize_w2_fp8.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int32, P]
+    lib.dspark_markov_set_w2_fp8.argtypes = [P, P, P]
+    q = lib.dspark_quantize_w2_fp8
+    a16, a8, a2 = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 8), ctypes.c_void_p((1 << 20) + 2)
+    assert q(a16, a16, a16, 4, 12, None) == -1     # rank not a multiple of 8
+    assert q(a16, a16, a16, -1, 256, None) == -1   # negative vocab
+    assert q(None, None, None, 0, 256, None) == 0  # nothing to do
+    assert q(None, a16, a16, 4, 256, None) == -1   # null table
+    assert q(a8, a16, a16, 4, 256, None) == -3     # w2 off its 16-byte alignment
+    assert q(a16, a2, a16, 4, 256, None) == -3     # codes off their 8-byte alignment
+    assert lib.dspark_markov_set_w2_fp8(None, a16, a16) == -1  # no context
