@@ -116,3 +116,15 @@ def test_full_vocabulary_rows():
     l = _logits(rng, 64, 129280, 2.5)
     _check(l, 1.0, 0, 1.0)
     _check(l, 0.8, 50, 0.95)
+
+
+@pytest.mark.parametrize("T", [0.7, 3.0])
+def test_scaled_logit_ties_decide_top_k_like_the_oracle(T):
+    """Rows whose two scaled logits tie under the correctly rounded quotient
+    but not under a reciprocal multiply (and the other way round): with top-k
+    1 the kept id shows which quotient the kernel formed."""
+    from tests.test_oracle_logits_to_probs import tie_revealing_rows
+    rows, kept = tie_revealing_rows(T, 150, int(T * 1000))
+    got = _gpu(rows, T, 1, 1.0)
+    assert np.array_equal(np.argmax(got, axis=1), kept)
+    _check(rows, T, 1, 1.0)

@@ -76,3 +76,62 @@ def test_noise_bound_tables_reject_short_arrays():
     L = binding.load()
     a = (ctypes.c_float * 100)()
     assert L.dspark_noise_bound_tables(a, a, 100) == -1
+
+
+def _bucket_ranges():
+    """Every bucket as contiguous hash ranges: the bucket is a non-decreasing
+    function of h (h | 1 and its leading-one position and next 4 bits never
+    fall as h grows), so a range whose two ends share a bucket lies in it.
+    Below 2^16 every hash is listed; above, bucket 16 k + m is the range
+    [2^k + m 2^(k-4), 2^k + (m + 1) 2^(k-4))."""
+    small = np.arange(1 << 16, dtype=np.uint32)
+    ranges = []
+    for k in range(16, 32):
+        for m in range(16):
+            lo = (1 << k) + (m << (k - 4))
+            ranges.append((16 * k + m, lo, lo + (1 << (k - 4))))
+    # the ranges tile [2^16, 2^32) in order, each inside one bucket
+    ends = [(lo, hi) for _, lo, hi in ranges]
+    assert ends[0][0] == 1 << 16 and ends[-1][1] == 1 << 32
+    assert all(a[1] == b[0] for a, b in zip(ends, ends[1:]))
+    e = np.array([[lo, hi - 1] for _, lo, hi in ranges], np.uint64)
+    bk = _bucket(e)
+    assert np.array_equal(bk[:, 0], bk[:, 1]) and np.array_equal(bk[:, 0], [b for b, _, _ in ranges])
+    assert np.all(np.diff(_bucket(small)) >= 0)
+    return small, ranges
+
+
+def test_noise_bounds_hold_for_every_hash():
+    """Exhaustive: for all 2^32 hashes h, lb[b(h)] <= -L(h) <= ub[b(h)] with
+    the oracle's noise L, so pruning by these bounds never drops the argmax.
+    The work is split in 2^22-hash chunks over the host's cores (the oracle's
+    C routine runs outside the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
+    ub, lb = binding.dspark_noise_bound_tables()
+    ub, lb = np.asarray(ub, np.float64), np.asarray(lb, np.float64)
+    small, ranges = _bucket_ranges()
+    noise = -oracle.noise_L(small).astype(np.float64)
+    b = _bucket(small)
+    assert np.all(noise <= ub[b]) and np.all(noise >= lb[b])
+
+    step = 1 << 22
+    jobs = []
+    for bk, lo, hi in ranges:
+        for c in range(lo, hi, step):
+            jobs.append((bk, c, min(hi, c + step)))
+
+    def extremes(job):
+        bk, lo, hi = job
+        L = oracle.noise_L(np.arange(lo, hi, dtype=np.uint64).astype(np.uint32))
+        return bk, float(L.min()), float(L.max()), bool(np.isfinite(L).all())
+
+    with ThreadPoolExecutor(os.cpu_count() or 1) as ex:
+        results = list(ex.map(extremes, jobs))
+    assert len(results) == len(jobs) and sum(hi - lo for _, lo, hi in jobs) == (1 << 32) - (1 << 16)
+    for bk, lmin, lmax, finite in results:
+        assert finite, bk
+        # -L is largest at the smallest L and smallest at the largest L
+        assert -lmin <= ub[bk], (bk, -lmin, ub[bk])
+        assert -lmax >= lb[bk], (bk, -lmax, lb[bk])

@@ -161,3 +161,35 @@ def test_top_p_threshold_is_reached_not_exceeded():
     assert kept(np.nextafter(np.float32(0.25), np.float32(0))) == 1
     p = oracle.logits_to_probs(l, 1.0, 4, 0.5)[0]
     assert p[0] == p[1] == np.float32(0.5) and p[2] == 0 and p[3] == 0
+
+
+def tie_revealing_rows(T, n, seed):
+    """Rows [a, b] with a < b adjacent floats whose scaled logits tie under
+    the correctly rounded quotient RN(l / T) but not under l * RN(1 / T), and
+    rows where it is the other way round.  Returns (rows, kept id with top-k
+    1 under the quotient: the lower id on a tie, else the larger z)."""
+    rng = np.random.default_rng(seed)
+    tf = np.float32(T)
+    a = (rng.random(50 * n) * 8 + 0.5).astype(np.float32)
+    b = np.nextafter(a, np.float32(np.inf))
+    qa, qb = a / tf, b / tf
+    ra, rb = a * (np.float32(1.0) / tf), b * (np.float32(1.0) / tf)
+    tie_q = np.nonzero((qa == qb) & (ra != rb))[0][:n]
+    tie_r = np.nonzero((qa != qb) & (ra == rb))[0][:n]
+    assert tie_q.size == n and tie_r.size == n
+    idx = np.concatenate([tie_q, tie_r])
+    rows = np.stack([a[idx], b[idx]], axis=1)
+    kept = np.concatenate([np.zeros(n, np.int64), np.ones(n, np.int64)])
+    return rows, kept
+
+
+@pytest.mark.parametrize("T", [0.7, 0.8, 3.0, 1.7])
+def test_scaled_logit_is_the_correctly_rounded_quotient(T):
+    """The scaled logit z = RN(l / T) decides top-k ties bit for bit: with
+    K = 1 a tie keeps the lower id, so each row shows whether its two z are
+    equal.  A quotient formed any other way (a reciprocal multiply, or a
+    quotient off by one ulp) flips these rows."""
+    rows, kept = tie_revealing_rows(T, 150, int(T * 1000))
+    p = oracle.logits_to_probs(rows, T, 1, 1.0)
+    assert np.array_equal(np.argmax(p, axis=1), kept)
+    assert np.all(p.max(axis=1) == 1.0) and np.all(np.count_nonzero(p, axis=1) == 1)

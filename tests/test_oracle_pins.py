@@ -244,6 +244,35 @@ def test_key_temperature_zero_and_nan():
     assert np.array_equal(k1, want.astype(np.float32))
 
 
+@pytest.mark.parametrize("t", [0.7, 0.8, 3.0, 1e-30, -1.5, 0.1, 7.0])
+def test_key_divides_by_the_temperature_exactly(t):
+    """[P2] _gumbel_key: the logit is divided by the temperature, one
+    correctly rounded quotient (numpy's float32 division is IEEE), then the
+    noise is subtracted with one rounding.  At these temperatures 1/t is not
+    a power of two, so a key formed as l * RN(1/t) differs on a share of the
+    inputs; the pin checks that share is there and that the oracle is not it."""
+    rng = np.random.default_rng(int(abs(t) * 1e6) % 2**31 + 17)
+    n = 6000
+    l = np.concatenate([
+        rng.standard_normal(n).astype(np.float32) * np.float32(4.0),
+        # BF16-valued logits, as the loop's keys are formed from
+        ((rng.integers(0, 2**16, n // 2, dtype=np.int64).astype(np.uint32) & 0x7F7F) << 16).view(np.float32)
+        * np.float32(1.0),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.0, 1e30, -1e-30, np.inf, -np.inf], np.float32),
+    ]).astype(np.float32)
+    h = rng.integers(0, 2**32, l.size, dtype=np.uint64).astype(np.uint32)
+    tf = np.float32(t)
+    with np.errstate(over="ignore", invalid="ignore"):
+        q = (l / tf).astype(np.float32)
+        want = (q - oracle.noise_L(h)).astype(np.float32)
+        recip = (l * (np.float32(1.0) / tf)).astype(np.float32)
+    got = oracle.key(l, float(tf), h)
+    same_bits = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    assert same_bits.all(), (l[~same_bits][:4], got[~same_bits][:4], want[~same_bits][:4])
+    # the pin has teeth: the reciprocal form gives other quotients here
+    assert np.count_nonzero(q[np.isfinite(q)] != recip[np.isfinite(q)]) > 50
+
+
 # --------------------------------------------------------------------------
 # Output transform: BF16 add, multiplier, soft cap
 # --------------------------------------------------------------------------
