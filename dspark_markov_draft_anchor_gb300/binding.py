@@ -17,7 +17,7 @@ DSPARK_OK = 0
 ERRORS = {
     -1: "DSPARK_ERR_INVALID_ARG", -2: "DSPARK_ERR_UNSUPPORTED_RANK", -3: "DSPARK_ERR_MISALIGNED",
     -4: "DSPARK_ERR_TOO_MANY_ROWS", -5: "DSPARK_ERR_CAPTURING", -6: "DSPARK_ERR_CUDA",
-    -7: "DSPARK_ERR_DEVICE_TIMEOUT", -8: "DSPARK_ERR_UNSUPPORTED_DEVICE",
+    -7: "DSPARK_ERR_DEVICE_TIMEOUT", -8: "DSPARK_ERR_UNSUPPORTED_DEVICE", -9: "DSPARK_ERR_HOST_ALLOC",
 }
 FLAG_PDL = 0x1
 FLAG_FORCE_FMA = 0x2

@@ -110,6 +110,40 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
 
 }  // namespace
 
+namespace dspark {
+
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  struct Fns {
+    GetCurrentFn get_current = nullptr;
+    GetIdFn get_id = nullptr;
+  };
+  // looked up once (a function-local static is initialised by one thread)
+  static const Fns fns = [] {
+    Fns f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<GetIdFn>(p);
+    (void)cudaGetLastError();
+    return f;
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!fns.get_current || !fns.get_id || fns.get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      fns.get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+}  // namespace dspark
+
 extern "C" {
 
 const char* dspark_strerror(int code) {
@@ -123,6 +157,7 @@ const char* dspark_strerror(int code) {
     case DSPARK_ERR_CUDA: return "CUDA error";
     case DSPARK_ERR_DEVICE_TIMEOUT: return "a bounded device wait gave up";
     case DSPARK_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (GB300)";
+    case DSPARK_ERR_HOST_ALLOC: return "host memory allocation failed";
     default: return "unknown error";
   }
 }
@@ -152,7 +187,7 @@ int dspark_markov_init(dspark_markov_ctx** out, const dspark_markov_config* cfg,
   (void)cudaGetLastError();
 
   dspark_markov_ctx* ctx = static_cast<dspark_markov_ctx*>(calloc(1, sizeof(dspark_markov_ctx)));
-  if (!ctx) return DSPARK_ERR_INVALID_ARG;
+  if (!ctx) return DSPARK_ERR_HOST_ALLOC;
   ctx->device = dev;
   ctx->sm_count = sms;
   ctx->cfg = *cfg;

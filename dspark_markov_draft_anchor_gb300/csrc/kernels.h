@@ -50,6 +50,13 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
 // The grid's CTAs can all be resident at once (a cooperative launch is possible).
 bool tc_cooperative_ok(int grid);
 
+// The unique id of the calling thread's current CUDA context (a driver
+// context id, never reused within a process), or 0 when no context is
+// current or the driver cannot say.  One-time set-up that lives in a context
+// (a kernel attribute, a looked-up symbol address) is keyed on it, so that a
+// device reset or a new context makes the next call redo it.
+unsigned long long current_context_id();
+
 // Bounds of the Gumbel noise -L(h) used to skip elements that cannot win:
 // bucket 16 k + m of g = h | 1 (k: the position of g's leading one, m: the
 // 4 bits after it); ub[b] >= -L(h) >= lb[b] for every h of bucket b (host

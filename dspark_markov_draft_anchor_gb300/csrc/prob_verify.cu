@@ -11,7 +11,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dspark_markov.h"
+#include "kernels.h"
 #include "ptx.cuh"
 
 namespace dspark {
@@ -494,6 +497,29 @@ __global__ void __launch_bounds__(kAcceptThreads, 2)
 
 int done() { return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA; }
 
+// The accept kernel's dynamic shared-memory limit, raised once per context
+// of each device (a kernel attribute lives in the context: a device reset or
+// another context needs it set again).  The context the attribute was set in
+// is kept per device ordinal; setting it twice is harmless, so two threads
+// racing here only repeat the call.
+constexpr int kAttrMaxDevices = 64;
+std::atomic<unsigned long long> g_accept_attr_ctx[kAttrMaxDevices];
+
+bool accept_attr_ready() {
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kAttrMaxDevices) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && g_accept_attr_ctx[device].load(std::memory_order_acquire) == ctx) return true;
+  if (cudaFuncSetAttribute(prob_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kStageBytes)) != cudaSuccess)
+    return false;
+  g_accept_attr_ctx[device].store(current_context_id(), std::memory_order_release);
+  return true;
+}
+
 }  // namespace
 }  // namespace dspark
 
@@ -518,13 +544,7 @@ int dspark_probabilistic_accept(const float* target_probs, const float* draft_pr
   if (!target_probs || !uniforms || !accepted || !accept_len || !proposal_len ||
       (P > 0 && (!draft_probs || !draft)))
     return DSPARK_ERR_INVALID_ARG;
-  static bool attr_set = false;  // the attribute is idempotent; a race only repeats it
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(dspark::prob_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(dspark::kStageBytes)) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!dspark::accept_attr_ready()) return DSPARK_ERR_CUDA;
   dspark::prob_accept_kernel<<<batch, dspark::kAcceptThreads, dspark::kStageBytes, stream>>>(
       target_probs, draft_probs, draft, proposal_len, uniforms, accepted, accept_len, draft_stride, P, vocab);
   return dspark::done();

@@ -1060,23 +1060,51 @@ int tc_step_grid(int64_t vocab, int sm_count) {
   return static_cast<int>(units < sm_count ? units : sm_count);
 }
 
+namespace {
+
+// Resident CTAs per SM of one build of the kernel at its launch shape.
+template <bool C, bool M, bool T = false, int RW = kHalfRows>
+int tc_blocks_per_sm() {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_tc_kernel<C, M, T, RW>, kThreads, max_tc_smem()) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return per_sm;
+}
+
+}  // namespace
+
 bool tc_cooperative_ok(int grid) {
-  int dev = 0, coop = 0, sms = 0, per_sm = 0;
+  int dev = 0, coop = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_tc_kernel<false, true>, kThreads,
-                                                    max_tc_smem()) != cudaSuccess) {
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     (void)cudaGetLastError();
     return false;
   }
+  // every build a loop may launch (their register counts may differ)
+  const int counts[] = {tc_blocks_per_sm<false, false>(), tc_blocks_per_sm<false, true>(),
+                        tc_blocks_per_sm<true, false>(), tc_blocks_per_sm<true, true>(),
+                        tc_blocks_per_sm<false, true, true>(), tc_blocks_per_sm<false, true, false, 1>(),
+                        tc_blocks_per_sm<false, true, false, 4>()};
+  int per_sm = counts[0];
+  for (int c : counts) per_sm = c < per_sm ? c : per_sm;
   return coop != 0 && per_sm >= 1 && grid <= per_sm * sms;
 }
 
 namespace {
 // Whether a cooperative launch may also carry programmatic stream
-// serialisation: unknown until the first such launch (1 yes, 0 no, -1 unknown).
-std::atomic<int> g_coop_pdl{-1};
+// serialisation, per device: unknown until the first such launch on it (1
+// yes, 0 no, -1 unknown).
+constexpr int kCoopMaxDevices = 64;
+std::atomic<int> g_coop_pdl[kCoopMaxDevices];
+struct CoopPdlInit {
+  CoopPdlInit() {
+    for (auto& v : g_coop_pdl) v.store(-1, std::memory_order_relaxed);
+  }
+} g_coop_pdl_init;
 }  // namespace
 
 cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
@@ -1134,15 +1162,21 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
     return cudaLaunchKernelEx(&cfg, kernel, w2_map, w2_tile_map, base_map, tp);
   };
   if (!cooperative || !pdl) return launch(pdl);
-  if (g_coop_pdl.load(std::memory_order_relaxed) != 0) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kCoopMaxDevices) {
+    (void)cudaGetLastError();
+    return launch(false);
+  }
+  std::atomic<int>& known = g_coop_pdl[dev];
+  if (known.load(std::memory_order_relaxed) != 0) {
     const cudaError_t e = launch(true);
     if (e == cudaSuccess) {
-      g_coop_pdl.store(1, std::memory_order_relaxed);
+      known.store(1, std::memory_order_relaxed);
       return e;
     }
-    if (g_coop_pdl.load(std::memory_order_relaxed) == 1) return e;
+    if (known.load(std::memory_order_relaxed) == 1) return e;
     (void)cudaGetLastError();
-    g_coop_pdl.store(0, std::memory_order_relaxed);
+    known.store(0, std::memory_order_relaxed);
   }
   return launch(false);
 }

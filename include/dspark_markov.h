@@ -50,6 +50,7 @@ extern "C" {
 #define DSPARK_ERR_CUDA (-6)             /* a CUDA runtime call or launch failed */
 #define DSPARK_ERR_DEVICE_TIMEOUT (-7)   /* a bounded device wait gave up (status word) */
 #define DSPARK_ERR_UNSUPPORTED_DEVICE (-8) /* not a compute capability 10.3 device */
+#define DSPARK_ERR_HOST_ALLOC (-9)       /* a host memory allocation failed */
 
 /* ---- config flags ------------------------------------------------------ */
 #define DSPARK_FLAG_PDL 0x1        /* launch steps with programmatic dependent launch */
@@ -70,7 +71,11 @@ extern "C" {
 /* Opaque context: the Markov tables, the tensor maps over them and the
  * scratch of one loop (per-step argmax slots and arrival counters), sized
  * once for max_rows x max_steps so that captured graphs keep its addresses
- * ([P2] FusedMarkov: "scratch sized for its largest batch, allocated once"). */
+ * ([P2] FusedMarkov: "scratch sized for its largest batch, allocated once").
+ * A context serves one loop at a time: its slots, counters, status word and
+ * soft-cap table belong to the call in flight, so calls on one context must
+ * be ordered (one stream, or streams ordered by events).  Loops that should
+ * run concurrently need one context each. */
 typedef struct dspark_markov_ctx dspark_markov_ctx;
 
 typedef struct {
@@ -90,7 +95,9 @@ typedef struct {
  * The tables are not copied: they must stay valid and unchanged while the
  * context is used.  Allocates with cudaMalloc, so it must not run while
  * `stream` is being captured (DSPARK_ERR_CAPTURING).  On success *out owns
- * the context; free it with dspark_markov_destroy.
+ * the context; free it with dspark_markov_destroy.  DSPARK_ERR_HOST_ALLOC if
+ * the context's host structure cannot be allocated, DSPARK_ERR_CUDA if a
+ * device allocation or set-up call fails.
  */
 DSPARK_API int dspark_markov_init(dspark_markov_ctx **out, const dspark_markov_config *cfg, const void *w1_bf16,
                        const void *w2_bf16, cudaStream_t stream);
@@ -224,7 +231,10 @@ DSPARK_API int dspark_build_verify_tokens(const int64_t *last, const int64_t *dr
  *   accepted: out [batch, P + 1] int64: a_0 .. a_n, then -1.
  *   accept_len: out [batch] int32 = n + 1 (drafts accepted plus the bonus).
  *   scratch: device, >= dspark_greedy_accept_scratch_bytes(batch, P, vocab)
- *            bytes, 16-byte aligned; its contents on entry do not matter.
+ *            bytes (8 per verify row + 16), 16-byte aligned; its contents
+ *            on entry do not matter.
+ * Three kernels on `stream` (clear the slots, scan, walk the acceptance),
+ * chained with programmatic dependent launch.
  * Positions after the last one the acceptance can reach are not scanned.
  */
 DSPARK_API size_t dspark_greedy_accept_scratch_bytes(int32_t batch, int32_t P, int32_t vocab);
@@ -254,12 +264,16 @@ DSPARK_API int dspark_greedy_accept(const void *logits, const int64_t *draft, co
  *     DSPARK_ERR_TOO_MANY_ROWS before anything is launched; use
  *     dspark_greedy_accept with caller scratch for larger batches.
  *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and keeps it; make that
- *     first call before any stream capture.  If the lookup fails the call
- *     returns DSPARK_ERR_CUDA and the next call tries again.
+ *     array's device address (cudaGetSymbolAddress) and keeps it for the
+ *     device's current context; make that first call before any stream
+ *     capture.  A device reset (cudaDeviceReset) or another context made
+ *     current starts a new context, and the next call looks the address up
+ *     again, so after a reset make one call before capturing again.  If the
+ *     lookup fails the call returns DSPARK_ERR_CUDA and the next call tries
+ *     again.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - Every call shares the one array, which keeps the last call's contents.
- *     The slots and the arrival counter, which must start at zero, are
+ *     The slots, which must start at zero, are
  *     cleared by the call's first kernel, so stale contents do no harm.  Two
  *     calls whose kernels overlap on the GPU (different streams without an
  *     ordering between them) race on the array and may give wrong results:

@@ -66,6 +66,32 @@ class GpuLoop:
         }
 
 
+def graph_run(g, wl):
+    """One loop launched as the benchmark launches it: PDL on, warmed up
+    outside capture, captured in a CUDA graph and replayed; returns the
+    tokens, the cache and the bias the kernels wrote."""
+    cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
+    tokens = torch.full((wl.rows, wl.steps), -9, dtype=torch.int64, device="cuda")
+    bias = torch.empty((wl.rows, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
+    a = g.args(cache, tokens, bias)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g.ctx.loop(a, s)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.ctx.loop(a)
+    tokens.fill_(-9)
+    cache.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert g.ctx.status() == 0
+    return {"tokens": tokens.cpu().numpy(), "cache": cache.cpu().numpy().view(np.uint16),
+            "bias": bias.cpu().numpy().view(np.uint16)}
+
+
 def oracle_run(wl, *, fed_bias=None, want_keys=False, rows=None, cache_fill=0):
     cache = np.full((wl.num_req, wl.steps, wl.vocab), cache_fill, np.uint16)
     out = oracle.markov_loop(w1=wl.w1, w2=wl.w2, base=wl.base, input_ids=wl.input_ids, anchor_idx=wl.anchor_idx,

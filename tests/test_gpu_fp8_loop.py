@@ -15,7 +15,8 @@ import torch
 
 import oracle
 from dspark_markov_draft_anchor_gb300 import binding, workloads
-from tests.gpu_util import (NTHREADS, GpuLoop, assert_bf16_equal, bf16_ordinal, check_end_to_end, oracle_run,
+from tests.gpu_util import (NTHREADS, GpuLoop, assert_bf16_equal, bf16_ordinal, check_end_to_end, graph_run,
+                            oracle_run,
                             prev_tokens)
 
 pytestmark = pytest.mark.gpu
@@ -117,3 +118,29 @@ def test_attach_detach_launch_counts_and_errors():
     with pytest.raises(binding.DsparkError) as e:
         g.ctx.set_w2_fp8(q.view(-1)[1:], s)  # one byte off: misaligned
     assert e.value.code == -3
+
+
+def test_full_size_large16_fp8_loop():
+    """The FP8 option on the benchmark workload (V = 163840, 16 rows, 5
+    steps, E4M3 w2 quantised on the GPU), launched as the benchmark launches
+    it (PDL, CUDA graph): codes and scales equal the oracle's, tokens and the
+    whole cache bit-exact in fed mode, 50000 sampled bias entries against the
+    exact FP8 dot, end-to-end tokens for 2 rows against the oracle's FP8 loop."""
+    wl = workloads.make("large16")
+    g, qn, sn = _fp8_loop(wl)
+    q_o, s_o = oracle.quantize_w2_fp8(wl.w2)
+    assert np.array_equal(qn, q_o) and np.array_equal(sn, s_o)
+    gpu = graph_run(g, wl)
+    orc = oracle_run(wl, fed_bias=gpu["bias"])
+    assert np.array_equal(gpu["tokens"], orc["tokens"]), np.argwhere(gpu["tokens"] != orc["tokens"])[:5]
+    assert_bf16_equal(gpu["cache"], orc["cache"], "cache")
+    _check_fp8_bias(wl, gpu, qn, sn, sample=50_000)
+    n = 2
+    sub = workloads.make("large16")
+    o2 = oracle.markov_loop(w1=sub.w1, w2=None, w2_fp8=qn, w2_scale=sn, base=sub.base, input_ids=sub.input_ids,
+                            anchor_idx=sub.anchor_idx, sample_pos=sub.sample_pos, seeds=sub.seeds,
+                            temperature=sub.temperature, req_idx=sub.req_idx, mult=sub.mult, cap=sub.cap,
+                            salt=sub.salt, want_bias=True, want_keys=True, rows=n, nthreads=NTHREADS)
+    sub.rows = n
+    compared, tolerated = check_end_to_end(sub, {k: v[:n] for k, v in gpu.items() if k != "cache"}, o2)
+    assert compared >= n and tolerated <= 1

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from dspark_markov_draft_anchor_gb300 import binding, workloads
-from tests.gpu_util import (GpuLoop, assert_bf16_equal, check_bias, check_end_to_end, oracle_run)
+from tests.gpu_util import (GpuLoop, assert_bf16_equal, check_bias, check_end_to_end, graph_run, oracle_run)
 
 pytestmark = pytest.mark.gpu
 
@@ -86,6 +86,14 @@ def test_loop_end_to_end_margin(name, V, R, K):
     assert compared >= R and tolerated <= max(1, R // 8)
 
 
+def _end_to_end_rows(name, gpu, n):
+    """End-to-end tokens of the first n rows on the oracle's own bias."""
+    sub = workloads.make(name)
+    orc = oracle_run(sub, want_keys=True, rows=n)
+    sub.rows = n
+    return check_end_to_end(sub, {k: v[:n] for k, v in gpu.items() if k != "cache"}, orc)
+
+
 def test_full_size_large16_fed_parity_and_sampled_bias():
     """The bench workload (V = 163840, 16 rows, 5 steps), launched as the
     benchmark launches it (PDL, captured in a CUDA graph): tokens and the
@@ -93,31 +101,28 @@ def test_full_size_large16_fed_parity_and_sampled_bias():
     exact dot; end-to-end tokens on the oracle's own bias for 4 rows."""
     wl = workloads.make("large16")
     g = GpuLoop(wl)
-    cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
-    tokens = torch.full((wl.rows, wl.steps), -9, dtype=torch.int64, device="cuda")
-    bias = torch.empty((wl.rows, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
-    a = g.args(cache, tokens, bias)
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        g.ctx.loop(a, s)  # warm-up outside capture
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        g.ctx.loop(a)
-    tokens.fill_(-9)
-    graph.replay()
-    torch.cuda.synchronize()
-    gpu = {"tokens": tokens.cpu().numpy(), "cache": cache.cpu().numpy().view(np.uint16),
-           "bias": bias.cpu().numpy().view(np.uint16)}
+    gpu = graph_run(g, wl)
     _fed_parity(wl, gpu)
     check_bias(wl, gpu, sample=50_000, rng=np.random.default_rng(9))
-    orc = oracle_run(wl, want_keys=True, rows=4)
-    sub = workloads.make("large16")
-    sub.rows = 4
-    compared, tolerated = check_end_to_end(sub, {k: v[:4] for k, v in gpu.items() if k != "cache"}, orc)
+    compared, tolerated = _end_to_end_rows("large16", gpu, 4)
     assert compared >= 4 and tolerated <= 1
+
+
+def test_full_size_tc64_fed_parity_and_sampled_bias():
+    """The tensor-core regime workload (V = 163840, 64 rows, 7 steps,
+    multiplier 1.5, soft cap 30, temperature 0.7) as the benchmark launches
+    it: one cooperative launch for all 7 steps (more than five steps through
+    the grid waits), the soft-cap table built for the call; tokens and the
+    whole cache bit-exact in fed mode, 50000 sampled bias entries against the
+    exact dot, end-to-end tokens for 2 rows."""
+    wl = workloads.make("tc64")
+    assert (wl.vocab, wl.rows, wl.steps, wl.mult, wl.cap) == (163840, 64, 7, 1.5, 30.0)
+    g = GpuLoop(wl)
+    gpu = graph_run(g, wl)
+    _fed_parity(wl, gpu)
+    check_bias(wl, gpu, sample=50_000, rng=np.random.default_rng(10))
+    compared, tolerated = _end_to_end_rows("tc64", gpu, 2)
+    assert compared >= 2 and tolerated <= 1
 
 
 def _plant_hash_ties(wl, rows, rng):

@@ -74,3 +74,22 @@ def test_no_alloc_accept_rejects_rows_beyond_its_array():
     B = binding.NOALLOC_MAX_VERIFY_ROWS // 4
     ins = _inputs(B, P, V, 5)
     assert all(np.array_equal(a, b) for a, b in zip(_no_alloc(*ins, B, P, V), _with_caller_scratch(*ins, B, P, V)))
+
+
+def test_no_alloc_accept_allocates_no_device_memory():
+    """The property the entry point exists for: after a first call (which
+    looks up the array's address), further calls leave both torch's
+    allocator and the device's free memory exactly where they were."""
+    B, P, V = 256, 5, 20000 + 8
+    logits, draft, plen = _inputs(B, P, V, 6)
+    acc, alen = _outputs(B, P)
+    binding.dspark_greedy_accept_noalloc(logits, draft, plen, acc, alen, B, P, P, V)
+    torch.cuda.synchronize()
+    before_torch = torch.cuda.memory_allocated()
+    before_free, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        binding.dspark_greedy_accept_noalloc(logits, draft, plen, acc, alen, B, P, P, V)
+    torch.cuda.synchronize()
+    after_free, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == before_torch
+    assert after_free == before_free
