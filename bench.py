@@ -469,7 +469,7 @@ def run_native(args, d: Dist):
                        "model": "DSpark Markov head (random-init w1/w2 BF16)", "global_batch": R * d.world,
                        "seq_len": K, "parallelism": f"replicas x{d.world} (rows sharded, no collective)",
                        "l2": L2_NOTE + " loop",
-                       "graph": True, "pdl": True, "bias_path": ["fma", "tcgen05", "fp8 fma"][ctx.bias_path(R)], "w2": args.w2},
+                       "graph": True, "pdl": True, "bias_path": ["fma", "tcgen05", "fp8 fma", "fp8 tcgen05"][ctx.bias_path(R)], "w2": args.w2},
             "loop_us": {"mean": mean_us, "p10": qs[0], "p50": qs[1], "p90": qs[2], "anchor": anchor_us,
                         "eager_with_events": eager_loop_us},
             "gbs_loop": algo * K / (mean_us * 1e-6) / 1e9,
@@ -477,8 +477,11 @@ def run_native(args, d: Dist):
             # 70 % target is stated at
             "frac_vs_8tbs_whole_loop": algo * K / (mean_us * 1e-6) / 8e12,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": recorded_traffic(wl.name) if args.w2 == "bf16" else None, "peak_kind": f"{peak_kind} hbm_gbs",
-                         "kernel": ("step_tc_kernel, all k steps in one launch" if fused else
+                         "frac": achieved / peak,
+                         "traffic": recorded_traffic(wl.name if args.w2 == "bf16" else wl.name + "_fp8"),
+                         "peak_kind": f"{peak_kind} hbm_gbs",
+                         "kernel": (("step_tc_kernel (E4M3 w2)" if args.w2 == "fp8" else "step_tc_kernel") +
+                                    ", all k steps in one launch" if fused else
                                     "step_fp8_kernel, one launch per step" if args.w2 == "fp8" else "markov step"),
                          "kernel_us": kernel_us, "step_us": step_us, "step_us_eager_per_step_launch": eager_step_us,
                          "kernel_us_from": "graphed loop - graphed anchor (per launch), CUDA events, L2 flushed",

@@ -28,6 +28,9 @@ struct dspark_markov_ctx {
   CUtensorMap w2_tile_map;    // the same with boxes of 128 rows (whole vocabulary tiles)
   const uint8_t* w2_fp8;      // E4M3 w2 [V, 256] (caller-owned) or null: when set, every step takes
   const uint16_t* w2_scale;   // its bias from it and these FP16 row scales [V]
+  bool tc8_ok;                // TMA maps over the E4M3 w2 encoded: the tensor-core step can read it
+  CUtensorMap w2f8_map;       // boxes of 32 rows x 128 K bytes, 128-byte swizzle
+  CUtensorMap w2f8_tile_map;  // the same with boxes of 128 rows
 };
 
 namespace {
@@ -105,6 +108,7 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.partials = nullptr;
   p.test_stall = (ctx->cfg.flags & DSPARK_FLAG_TEST_STALL) != 0;
   p.xform_lut = ctx->xform_lut;
+  p.w2_scale = nullptr;
   return p;
 }
 
@@ -235,7 +239,8 @@ void dspark_markov_destroy(dspark_markov_ctx* ctx) {
 }
 
 int32_t dspark_markov_bias_path(const dspark_markov_ctx* ctx, int32_t rows) {
-  if (ctx && ctx->w2_fp8) return 2;
+  if (ctx && ctx->w2_fp8)
+    return ctx->tc8_ok && !(ctx->cfg.flags & DSPARK_FLAG_FORCE_FMA) && rows <= dspark::tc_fp8_max_rows() ? 3 : 2;
   if (!ctx || !ctx->tc_ok || (ctx->cfg.flags & DSPARK_FLAG_FORCE_FMA)) return 0;
   if (ctx->cfg.flags & DSPARK_FLAG_FORCE_MMA) return 1;
   return rows > kFmaMaxRows ? 1 : 0;
@@ -243,7 +248,8 @@ int32_t dspark_markov_bias_path(const dspark_markov_ctx* ctx, int32_t rows) {
 
 int32_t dspark_markov_partial_count(const dspark_markov_ctx* ctx) {
   if (!ctx) return 0;
-  return dspark_markov_bias_path(ctx, ctx->cfg.max_rows) == 1 ? ctx->grid_tc : ctx->grid_simple;
+  const int32_t path = dspark_markov_bias_path(ctx, ctx->cfg.max_rows);
+  return path == 1 || path == 3 ? ctx->grid_tc : ctx->grid_simple;
 }
 
 int dspark_markov_set_w2_fp8(dspark_markov_ctx* ctx, const void* w2_fp8, const void* w2_scale_f16) {
@@ -252,6 +258,10 @@ int dspark_markov_set_w2_fp8(dspark_markov_ctx* ctx, const void* w2_fp8, const v
     return DSPARK_ERR_MISALIGNED;
   ctx->w2_fp8 = static_cast<const uint8_t*>(w2_fp8);
   ctx->w2_scale = static_cast<const uint16_t*>(w2_scale_f16);
+  // the tensor-core step reads E4M3 stages by TMA; without the maps the
+  // CUDA-core FP8 step serves every call
+  ctx->tc8_ok = w2_fp8 && ctx->tc_ok && dspark::encode_w2_fp8_map(&ctx->w2f8_map, w2_fp8, ctx->cfg.vocab, 32) &&
+                dspark::encode_w2_fp8_map(&ctx->w2f8_tile_map, w2_fp8, ctx->cfg.vocab, 128);
   return DSPARK_OK;
 }
 
@@ -281,10 +291,8 @@ int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_
   if (select) p.partials = ctx->partials;
   cudaError_t e;
   int grid;
-  if (ctx->w2_fp8) {
-    grid = ctx->grid_simple;
-    e = dspark::launch_step_fp8(p, ctx->w2_fp8, ctx->w2_scale, a->cap != 0.0f, pdl, stream);
-  } else if (dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a)) {
+  const int32_t path = dspark_markov_bias_path(ctx, a->rows);
+  if ((path == 1 || path == 3) && tma_base_ok(a)) {
     if (select) {
       p.finish = 0;
     } else if (in_loop) {
@@ -292,7 +300,15 @@ int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_
       p.write_prev = step > 0;
     }
     grid = ctx->grid_tc;
-    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, grid, pdl, false, stream);
+    if (path == 3) {
+      p.w2_scale = ctx->w2_scale;
+      e = dspark::launch_step_tc(p, ctx->w2f8_map, ctx->w2f8_tile_map, grid, pdl, false, stream, true);
+    } else {
+      e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, grid, pdl, false, stream);
+    }
+  } else if (ctx->w2_fp8) {
+    grid = ctx->grid_simple;
+    e = dspark::launch_step_fp8(p, ctx->w2_fp8, ctx->w2_scale, a->cap != 0.0f, pdl, stream);
   } else {
     grid = ctx->grid_simple;
     e = dspark::launch_step_simple(p, a->cap != 0.0f, pdl, stream);
@@ -305,8 +321,9 @@ int launch_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_
 // The loop runs as one multi-step launch: tensor-core path, TMA-readable base,
 // several steps, a cooperative launch possible and not switched off.
 bool loop_fused(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
+  const int32_t path = dspark_markov_bias_path(ctx, a->rows);
   return ctx->fused_ok && !(ctx->cfg.flags & (DSPARK_FLAG_PER_STEP | DSPARK_FLAG_SELECT_2LAUNCH)) && a->steps > 1 &&
-         dspark_markov_bias_path(ctx, a->rows) == 1 && tma_base_ok(a);
+         (path == 1 || path == 3) && tma_base_ok(a);
 }
 
 }  // namespace
@@ -334,7 +351,12 @@ int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
     dspark::StepParams p = make_params(ctx, a, 0);
     p.step_end = a->steps;
     const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
-    const cudaError_t e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, true, stream);
+    const bool fp8 = dspark_markov_bias_path(ctx, a->rows) == 3;
+    if (fp8) p.w2_scale = ctx->w2_scale;
+    const cudaError_t e = fp8 ? dspark::launch_step_tc(p, ctx->w2f8_map, ctx->w2f8_tile_map, ctx->grid_tc, pdl,
+                                                       true, stream, true)
+                              : dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, true,
+                                                       stream);
     if (e == cudaSuccess) return DSPARK_OK;
     if (e != cudaErrorInvalidValue) return DSPARK_ERR_CUDA;
     // the base strides do not form the multi-step tensor map: step by step

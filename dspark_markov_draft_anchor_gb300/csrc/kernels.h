@@ -41,12 +41,18 @@ int tc_step_grid(int64_t vocab, int sm_count);
 int tc_smem_bytes(int rows);
 // box_rows: 32 (any tile) or 128 (whole tiles, one copy per stage).
 bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab, int box_rows);
+// The same over E4M3 w2 [V, 256] bytes: boxes of 128 K bytes x box_rows.
+bool encode_w2_fp8_map(CUtensorMap* map, const void* w2_fp8, int64_t vocab, int box_rows);
+// The most rows the tensor-core step takes with E4M3 w2 (its shared memory
+// holds the FP16 operand stages beside the E4M3 ones).
+int tc_fp8_max_rows();
 // Steps p.step .. p.step_end - 1 in one launch; more than one step needs a
-// cooperative launch (its CTAs wait for one another between steps).  Returns
-// cudaErrorInvalidValue, launching nothing, when the base logits' strides
-// cannot form the kernel's tensor map.
+// cooperative launch (its CTAs wait for one another between steps).  With
+// fp8 the maps are E4M3 maps (encode_w2_fp8_map) and p.w2_scale is set.
+// Returns cudaErrorInvalidValue, launching nothing, when the base logits'
+// strides cannot form the kernel's tensor map or the rows do not fit.
 cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
-                           bool pdl, bool cooperative, cudaStream_t stream);
+                           bool pdl, bool cooperative, cudaStream_t stream, bool fp8 = false);
 // The grid's CTAs can all be resident at once (a cooperative launch is possible).
 bool tc_cooperative_ok(int grid);
 

@@ -289,7 +289,13 @@ __device__ __forceinline__ void stream_sums(const Row& r, int64_t chunk_len, uin
     }
     uint64_t part = wflush(hi, lo);
     __syncwarp();
-    if (lane == 0 && piece + kAcceptWarps < n_pieces) issue(piece + kAcceptWarps);
+    // the stage's next fill is an async-proxy write: the proxy fence orders
+    // it after the warp's generic reads of the stage (synchronised by the
+    // warp barrier above)
+    if (lane == 0 && piece + kAcceptWarps < n_pieces) {
+      ptx::fence_proxy_async_smem();
+      issue(piece + kAcceptWarps);
+    }
     part = warp_sum_u64(part);
     if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&chunk[v0 / chunk_len]), part);
   }

@@ -178,6 +178,35 @@ __device__ __forceinline__ void mma_bf16_c(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T: the A operand read from tensor memory
+// (M = 128 rows = lanes, K along columns: a K step of 16 16-bit values is 8
+// columns), kind::f16 (operand types in idesc); issued by one thread.
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_tmem_a_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(kAccumulate ? 1 : 0)
+      : "memory");
+}
+
+// Copy a 128-row x 256-bit block (one K step of 16 16-bit values per row) of
+// a shared-memory matrix, given by its descriptor, into tensor memory: row r
+// to lane r, its 32 bytes to 8 consecutive columns from taddr.  Issued by one
+// thread; it and the thread's later tcgen05.mma run in issue order, and a
+// later tcgen05.commit covers it.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// kind::f16 with FP16 operands: the same instruction (the operand type is in
+// the instruction descriptor, idesc_f16_f32).
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_f16_c(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  mma_bf16_c<kAccumulate>(d_tmem, a_desc, b_desc, idesc);
+}
+
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -253,6 +282,27 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
          | (1u << 10)         // B: BF16
          | ((n >> 3) << 17)   // N / 8
          | ((m >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor of kind::f16: FP16 A and B, FP32 D, both K-major,
+// shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n) {
+  return (1u << 4)            // D: F32
+         | (0u << 7)          // A: F16
+         | (0u << 10)         // B: F16
+         | ((n >> 3) << 17)   // N / 8
+         | ((m >> 4) << 24);  // M / 16
+}
+
+// 16-byte shared-memory load and store at a shared-space address.
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 // Packed BF16 arithmetic: two FP32 values rounded to nearest into one BF16x2

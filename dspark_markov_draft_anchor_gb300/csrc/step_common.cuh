@@ -64,6 +64,8 @@ struct StepParams {
   // With a soft cap: the cached BF16 of every BF16 sum x (x's bits index it),
   // built by the anchor for this call's multiplier and cap.
   const uint16_t* xform_lut;
+  // E4M3 w2 on the tensor-core step: the FP16 row scales [V] (else null).
+  const uint16_t* w2_scale;
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this

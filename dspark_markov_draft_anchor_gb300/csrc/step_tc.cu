@@ -49,6 +49,7 @@
 #include <atomic>
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -84,11 +85,14 @@ constexpr int kNoiseT = kNoiseBuckets;
 struct TcLayout {
   int n;         // MMA N: rows padded to 16
   int nacc;      // TMEM accumulators (tiles the MMA may run ahead)
-  int stages;    // w2 ring stages
+  int stages;    // w2 ring stages (E4M3 w2: stages of 128 rows x 128 K bytes)
+  int stages16;  // E4M3 w2 only: FP16 operand stages (128 rows x 64 K), two rings, one per MMA warp
   int nbase;     // base ring slots (two rings, one per tile parity)
   int tmem_cols;
-  int smem;      // dynamic shared memory bytes
-  int emb_off, w2_off, base_off, bar_off, row_off, queue_off;
+  int res_tiles; // w2 tiles kept in tensor memory as the MMA's A operand after the first step
+  int res_col;   // their first column (128 columns a tile)
+  int smem;      // dynamic shared memory bytes (0: the layout does not fit)
+  int emb_off, w2_off, f16_off, base_off, bar_off, row_off, queue_off;
 };
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -109,33 +113,56 @@ constexpr int kRowThr = kRowTemp + 4 * kMaxRows;       // f32 pruning threshold
 constexpr int kRowGmask = kRowThr + 4 * kMaxRows;      // u32 per 16-row chunk: store bits 0..15, live bits 16..31
 constexpr int kRowGtab = kRowGmask + 4 * (kMaxRows / kChunkRows);  // f32 noise upper bound by clz
 constexpr int kRowLtab = kRowGtab + 4 * kNoiseT;                   // f32 noise lower bound by bucket
-constexpr int kRowBytes = kRowLtab + 4 * kNoiseT;
+constexpr int kRowKs = kRowLtab + 4 * kNoiseT;                      // f32 E4M3 w2: 2^-k of the row's B scaling
+constexpr int kRowBytes = kRowKs + 4 * kMaxRows;
 
 constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared variables
 
-TcLayout tc_layout(int rows) {
+// Shared memory of one CTA.  BF16 w2: the rest of the budget goes to the w2
+// ring (at most 12 stages).  E4M3 w2: four FP16 operand stages (two per MMA
+// warp) and the rest to the E4M3 ring (at most 8 stages); smem = 0 when the
+// ring would have fewer than two stages (E4M3 w2 above 128 rows).
+TcLayout tc_layout(int rows, bool fp8 = false) {
   TcLayout L;
   L.n = ((rows + 15) / 16) * 16;
   // even: each accumulator belongs to one tile parity
   L.nacc = 8 * L.n <= 512 ? 8 : (4 * L.n <= 512 ? 4 : 2);
   L.tmem_cols = pow2_at_least(L.nacc * L.n);
+  // the columns the accumulators leave hold whole w2 tiles (128 rows x 256 K
+  // of 16-bit values: 128 columns): the whole tensor memory is then allocated
+  L.res_col = (L.nacc * L.n + 127) / 128 * 128;
+  L.res_tiles = (512 - L.res_col) / 128;
+  if (L.res_tiles > 0) L.tmem_cols = 512;
   // 4 KB chunks, half per parity's ring; more slots where a tile has several
   // chunks, or three per parity at 16 rows, where the w2 ring can spare them
   L.nbase = (L.n > kChunkRows && L.n < 128) ? 8 : (L.n == kChunkRows ? 6 : 4);
-  const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + 8 * (2 * 12 + 2 * L.nbase + 2 * 8 + 3) + 16 +
-                    kRowBytes + kEpiWarps * kQCap * 8 + 1024 + 64;
-  L.stages = (kSmemBudget - fixed) / kW2StageBytes;
-  if (L.stages > 12) L.stages = 12;
-  L.stages &= ~1;  // two w2 rings of stages / 2, one per MMA warp
+  const int bars_max = 8 * (2 * 12 + 4 + 2 * L.nbase + 2 * 8 + 3);
+  const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + bars_max + 16 + kRowBytes + kEpiWarps * kQCap * 8 +
+                    1024 + 64;
+  const int avail = (kSmemBudget - fixed) / kW2StageBytes;  // 16 KB stages that fit
+  L.smem = 0;
+  if (!fp8) {
+    L.stages16 = 0;
+    L.stages = avail > 12 ? 12 : avail;
+    L.stages &= ~1;  // two w2 rings of stages / 2, one per MMA warp
+    if (L.stages < 2) return L;
+  } else {
+    L.stages16 = 4;  // two per MMA warp: one is filled while the other's MMAs run
+    L.stages = avail - L.stages16 > 8 ? 8 : avail - L.stages16;
+    L.stages &= ~1;  // two E4M3 rings, one per tile parity
+    if (L.stages < 2) return L;
+  }
   int off = 0;
   L.emb_off = off;
   off += L.n * kRank * 2;
   L.w2_off = off;
   off += L.stages * kW2StageBytes;
+  L.f16_off = off;
+  off += L.stages16 * kW2StageBytes;
   L.base_off = off;
   off += L.nbase * kChunkBytes;
   L.bar_off = off;
-  off += 8 * (2 * L.stages + 2 * L.nbase + 2 * L.nacc + 3);
+  off += 8 * (2 * L.stages + L.stages16 + 2 * L.nbase + 2 * L.nacc + 3);
   off = (off + 15) & ~15;
   L.row_off = off;
   off += kRowBytes;
@@ -151,9 +178,12 @@ struct TcParams {
   int32_t n;
   int32_t nacc;
   int32_t stages;
+  int32_t stages16;
   int32_t nbase;
   int32_t tmem_cols;
-  int32_t emb_off, w2_off, base_off, bar_off, row_off, queue_off;
+  int32_t res_tiles;  // the CTA's last res_tiles tiles stay in tensor memory from the second step on
+  int32_t res_col;
+  int32_t emb_off, w2_off, f16_off, base_off, bar_off, row_off, queue_off;
   int32_t num_units;  // ceil(V / 32)
   int32_t base_steps_mid;  // base tensor map dims are (vocab, step, row), else (vocab, row, step)
 };
@@ -197,6 +227,8 @@ struct Shared {
   uint64_t* tmem_empty;  // [nacc]
   uint64_t* emb_ready;
   uint64_t* spare;       // [2], one per MMA warp
+  uint64_t* empty_f16;   // E4M3 w2: [stages16], FP16 operand stage free (its MMAs completed)
+  unsigned char* f16;    // E4M3 w2: FP16 operand stages
   unsigned long long* best;
   int64_t* cache_off;  // per row: the address of its cache row (an int64)
   uint32_t* prefix;
@@ -207,6 +239,7 @@ struct Shared {
   uint32_t* gmask;  // per 16-row chunk: rows that store (bits 0..15), rows that exist (16..31)
   float* gtab;      // the computed noise never exceeds gtab[noise_index(h)]
   float* ltab;      // the computed noise is never below ltab[noise_index(h)]
+  float* kscale;    // E4M3 w2: per row, 2^-k undoing the FP16 embedding's power-of-two scaling
   Cand* queues;
 };
 
@@ -263,6 +296,11 @@ __device__ __forceinline__ long long lds_i64(const void* ptr) {
   asm volatile("ld.shared.s64 %0, [%1];" : "=l"(r) : "r"(ptx::smem_addr(ptr)));
   return r;
 }
+__device__ __forceinline__ float ld_shared_f32(const float* ptr) {
+  float r;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(ptx::smem_addr(ptr)));
+  return r;
+}
 __device__ __forceinline__ float ld_volatile_f32(const float* ptr) {
   float r;
   asm volatile("ld.volatile.shared.f32 %0, [%1];" : "=f"(r) : "r"(ptx::smem_addr(ptr)));
@@ -298,10 +336,125 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
   __syncwarp();
 }
 
+// Four E4M3 values (bytes of w, lowest first) as two FP16 pairs: lo holds
+// values 0 and 1, hi values 2 and 3 (the hardware conversion, exact).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  // each cvt takes an E4M3 pair (lower byte = lower half of the result)
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// E4M3 w2: one embedding row (eight BF16 values a lane, the warp holding
+// the whole row) as FP16 values of e * 2^k, the power of two k chosen per row
+// so that the largest finite |e| lands in [2^14, 2^15): then every entry
+// within 2^32 of the row's largest converts exactly (smaller ones, whose
+// products are below 2^-32 of the row's largest, round to the FP16 grid), and
+// infinities and NaN stay what they are.  Lane 0 stores 2^-k for the
+// epilogue.  k is clamped to [-112, 126] so that 2^k and 2^-k are normal floats.
+__device__ __forceinline__ uint4 embedding_to_f16(uint4 v, float* kscale, int lane) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t emax = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t e0 = (w[i] >> 7) & 0xFFu, e1 = (w[i] >> 23) & 0xFFu;
+    emax = max(emax, max(e0 == 0xFFu ? 0u : e0, e1 == 0xFFu ? 0u : e1));
+  }
+  emax = __reduce_max_sync(0xFFFFFFFFu, emax);
+  int k = 14 - (static_cast<int>(emax < 1u ? 1u : emax) - 127);
+  k = k < -112 ? -112 : (k > 126 ? 126 : k);
+  const float up = __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+  if (lane == 0) *kscale = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half lo = __float2half_rn(__fmul_rn(__uint_as_float(w[i] << 16), up));
+    const __half hi = __float2half_rn(__fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), up));
+    o[i] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The kernel's bounded mbarrier wait as a value that out-of-line helpers can
+// take (the same polls, limits and give-up record as the kernel's own).
+struct BoundedWait {
+  volatile int* abort_flag;
+  unsigned int* abort_word;
+  int* status;
+  __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity, int site, int detail) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+      if (ptx::mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+      if ((it & 15) == 15 && (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitNs)) break;
+    }
+    if (*abort_flag) return false;
+    *abort_flag = 1;
+    atomicExch(abort_word, 1u);
+    if (atomicCAS(status, 0, kStatusTimeout) == 0) {
+      status[1] = site;
+      status[2] = static_cast<int>(blockIdx.x);
+      status[3] = detail;
+    }
+    return false;
+  }
+};
+
+// A resident tile in the first step of a launch: each w2 stage is taken from
+// the ring as usual, copied into tensor memory (from column `at`, 32 columns
+// a stage) and multiplied from shared memory; the stage's commit covers the
+// copy too.  Returns false if a wait gave up.
+__device__ __noinline__ bool resident_first_step(uint64_t* full_w2, uint64_t* empty_w2, int g, int SG, uint32_t d,
+                                                 uint32_t at, uint64_t a0, uint64_t b0, uint64_t b_kstep,
+                                                 uint32_t idesc, int k, BoundedWait wait, int detail) {
+  for (int kb = 0; kb < kKBlocks; ++kb, ++k) {
+    const int s = g * SG + k % SG;
+    if (!wait(&full_w2[s], (k / SG) & 1, 5, detail | (k & 0xFFF))) return false;
+    ptx::tc_fence_after();
+    const uint64_t a = a0 + static_cast<uint64_t>(s * (kW2StageBytes >> 4));
+    const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
+    const uint32_t ak = at + static_cast<uint32_t>(kb * 32);
+    ptx::tmem_cp_128x256b(ak, a);
+    ptx::tmem_cp_128x256b(ak + 8, a + 2);
+    ptx::tmem_cp_128x256b(ak + 16, a + 4);
+    ptx::tmem_cp_128x256b(ak + 24, a + 6);
+    if (kb == 0)
+      ptx::mma_bf16_c<false>(d, a, bd, idesc);
+    else
+      ptx::mma_bf16_c<true>(d, a, bd, idesc);
+    ptx::mma_bf16_c<true>(d, a + 2, bd + 2, idesc);
+    ptx::mma_bf16_c<true>(d, a + 4, bd + 4, idesc);
+    ptx::mma_bf16_c<true>(d, a + 6, bd + 6, idesc);
+    ptx::mma_commit(&empty_w2[s]);
+  }
+  return true;
+}
+
+// The MMAs of one tile whose A operand (w2, 128 rows x 256 K of 16-bit
+// values) sits in tensor memory from column `at` (8 columns a K step).
+__device__ __noinline__ void resident_step(uint32_t d, uint32_t at, uint64_t b0, uint64_t b_kstep, uint32_t idesc) {
+  for (int kb = 0; kb < kKBlocks; ++kb) {
+    const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
+    const uint32_t ak = at + static_cast<uint32_t>(kb * 32);
+    if (kb == 0)
+      ptx::mma_tmem_a_c<false>(d, ak, bd, idesc);
+    else
+      ptx::mma_tmem_a_c<true>(d, ak, bd, idesc);
+    ptx::mma_tmem_a_c<true>(d, ak + 8, bd + 2, idesc);
+    ptx::mma_tmem_a_c<true>(d, ak + 16, bd + 4, idesc);
+    ptx::mma_tmem_a_c<true>(d, ak + 24, bd + 6, idesc);
+  }
+}
+
 // kRW: rows of a chunk each epilogue warp takes -- kHalfRows, or 1 or 4 for
 // loops of at most that many rows (the second half's warps then only keep
 // the barriers).
-template <bool kHasCap, bool kMultOne, bool kTestStall = false, int kRW = kHalfRows>
+// kFp8: w2 as E4M3 bytes with FP16 row scales (the w2 tensor maps then
+// describe the E4M3 table: boxes of 128 K bytes).
+template <bool kHasCap, bool kMultOne, bool kTestStall = false, int kRW = kHalfRows, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_w2_tile,
                const __grid_constant__ CUtensorMap tmap_base, const TcParams tp) {
@@ -340,6 +493,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.tmem_empty = sh.tmem_full + NACC;
   sh.emb_ready = sh.tmem_full + 2 * NACC;
   sh.spare = sh.emb_ready + 1;
+  sh.empty_f16 = sh.spare + 2;
+  sh.f16 = smem + tp.f16_off;
   unsigned char* rowreg = smem + tp.row_off;
   sh.best = reinterpret_cast<unsigned long long*>(rowreg + kRowBest);
   sh.cache_off = reinterpret_cast<int64_t*>(rowreg + kRowCoff);
@@ -351,6 +506,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.gmask = reinterpret_cast<uint32_t*>(rowreg + kRowGmask);
   sh.gtab = reinterpret_cast<float*>(rowreg + kRowGtab);
   sh.ltab = reinterpret_cast<float*>(rowreg + kRowLtab);
+  sh.kscale = reinterpret_cast<float*>(rowreg + kRowKs);
   sh.queues = reinterpret_cast<Cand*>(smem + tp.queue_off);
 
   // This CTA's vocabulary range.
@@ -361,6 +517,9 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   const int64_t v_end = min(u1 * kUnit, p.vocab);
   const int n_tiles = static_cast<int>((v_end - v_begin + kTileV - 1) / kTileV);
   const int chunks = (p.rows + kChunkRows - 1) / kChunkRows;
+  // tiles res0 .. n_tiles - 1 are copied into tensor memory in the first step
+  // and read from there afterwards (their w2 is streamed once per launch)
+  const int res0 = n_tiles - tp.res_tiles > 0 ? n_tiles - tp.res_tiles : 0;
 
   pdl_launch_dependents();
 
@@ -380,6 +539,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     ptx::mbar_init(sh.emb_ready, 1);
     ptx::mbar_init(sh.spare, 1);
     ptx::mbar_init(sh.spare + 1, 1);
+    for (int i = 0; i < tp.stages16; ++i) ptx::mbar_init(&sh.empty_f16[i], 1);
     s_abort = 0;
     ptx::fence_mbar_init();
   }
@@ -448,21 +608,26 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           const int64_t t0 = v_begin + static_cast<int64_t>(i) * kTileV;
           const int rows_i = static_cast<int>(v_end - t0 < kTileV ? v_end - t0 : kTileV);
           const int boxes = (rows_i + kUnit - 1) / kUnit;
-          for (int kb = 0; kb < kKBlocks; ++kb) {
+          // a stage holds 128 bytes of each of the tile's rows: 64 K of BF16
+          // (four stages a tile) or 128 K of E4M3 (two)
+          constexpr int kStagesPerTile = kFp8 ? 2 : kKBlocks;
+          constexpr int kStageK = kFp8 ? 128 : kKBlock;
+          const bool w2_resident = st > 0 && i >= res0;  // in tensor memory since the first step
+          for (int kb = 0; kb < kStagesPerTile && !w2_resident; ++kb) {
             const int k = issued;
             const int s = g * SG + k % SG;
             if (!wait(&sh.empty_w2[s], ((k / SG) & 1) ^ 1, 1, (st << 24) | (i << 12) | (k & 0xFFF))) {
               stop = true;
               break;
             }
-            ptx::mbar_arrive_expect_tx(&sh.full_w2[s], static_cast<uint32_t>(boxes * kUnit * kKBlock * 2));
+            ptx::mbar_arrive_expect_tx(&sh.full_w2[s], static_cast<uint32_t>(boxes * kUnit * 128));
             if (boxes == kTileV / kUnit) {  // a whole tile: one 128-row copy
-              ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes, &tmap_w2_tile, &sh.full_w2[s], kb * kKBlock,
+              ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes, &tmap_w2_tile, &sh.full_w2[s], kb * kStageK,
                                     static_cast<int32_t>(t0), keep);
             } else {
               for (int bx = 0; bx < boxes; ++bx)
                 ptx::tma_load_2d_hint(sh.w2 + s * kW2StageBytes + bx * kUnit * 128, &tmap_w2, &sh.full_w2[s],
-                                      kb * kKBlock, static_cast<int32_t>(t0 + bx * kUnit), keep);
+                                      kb * kStageK, static_cast<int32_t>(t0 + bx * kUnit), keep);
             }
             issued = k + 1;
           }
@@ -473,6 +638,10 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
               stop = true;
               break;
             }
+            // the epilogue read this slot with generic loads (released to
+            // this thread through the barrier); the refill is an async-proxy
+            // write, which the proxy fence orders after them
+            ptx::fence_proxy_async_smem();
             ptx::mbar_arrive_expect_tx(&sh.full_base[s], kChunkBytes);
             if (tp.base_steps_mid)  // dims (vocab, step, row)
               ptx::tma_load_3d_hint(sh.base + s * kChunkBytes, &tmap_base, &sh.full_base[s],
@@ -506,7 +675,132 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
     // (its j-th tile uses accumulator g + 2 (j % NA)).  A step's MMAs start
     // once the epilogue has written that step's embeddings.
     const int g = warp == 1 ? 0 : 1;
-    if (lane == 0 && n_tiles > g) {
+    if constexpr (kFp8) {
+      // E4M3 w2: the whole warp turns each E4M3 stage (128 rows x 128 K) into
+      // two FP16 operand stages (128 rows x 64 K each, the MMA's 128-byte
+      // swizzle layout) of this warp's ring, one hardware conversion per pair
+      // (exact: every E4M3 value is an FP16 value), releases the E4M3 stage,
+      // and lane 0 issues the two K-blocks' MMAs (FP16 x FP16 into FP32) with
+      // one commit per FP16 stage.
+      if (n_tiles > g) {
+        const int SG = S / 2;                 // E4M3 slots of this parity's ring
+        const int SG16 = tp.stages16 / 2;     // FP16 slots of this warp's ring
+        const uint32_t idesc = ptx::idesc_f16_f32(kTileV, static_cast<uint32_t>(N));
+        const uint64_t a0 = ptx::sw128_desc(ptx::smem_addr(sh.f16), 1024);
+        const uint64_t b0 = ptx::sw128_desc(ptx::smem_addr(sh.emb), 1024);
+        const uint64_t b_kstep = static_cast<uint64_t>((N * 128) >> 4);
+        // a lane converts rows 8 q + (lane & 7) of 16-byte chunk (lane >> 3) +
+        // 4 h of each E4M3 row: the eight lanes of a shared-memory phase take
+        // eight rows of one chunk, so neither the reads nor the writes of a
+        // phase share a bank
+        const int rl = lane & 7, cq = lane >> 3;
+        bool ok = true;
+        int k = 0;   // E4M3 stages taken from this parity's ring
+        int k16 = 0; // FP16 stages used
+        int j = 0;   // tiles issued
+        for (int st = 0; st < n_steps && ok; ++st) {
+          if (!(ok = __all_sync(0xFFFFFFFFu, wait(sh.emb_ready, st & 1, 3, st << 24)))) break;
+          ptx::tc_fence_after();
+          for (int i = g; i < n_tiles && ok; i += 2, ++j) {
+            const int b = g + 2 * (j % NA);
+            if (!(ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_empty[b], ((j / NA) & 1) ^ 1, 4, (st << 24) | (i << 12)))))
+              break;
+            ptx::tc_fence_after();
+            const uint32_t d = tmem_base + static_cast<uint32_t>(b * N);
+            const bool res = i >= res0;
+            const uint32_t at = tmem_base + static_cast<uint32_t>(tp.res_col + (i - res0) * 128);
+            if (res && st > 0) {  // converted in the first step and kept in tensor memory
+              if (lane == 0) {
+                for (int kb = 0; kb < kKBlocks; ++kb) {
+                  const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
+                  const uint32_t ak = at + static_cast<uint32_t>(kb * 32);
+                  if (kb == 0)
+                    ptx::mma_tmem_a_c<false>(d, ak, bd, idesc);
+                  else
+                    ptx::mma_tmem_a_c<true>(d, ak, bd, idesc);
+                  ptx::mma_tmem_a_c<true>(d, ak + 8, bd + 2, idesc);
+                  ptx::mma_tmem_a_c<true>(d, ak + 16, bd + 4, idesc);
+                  ptx::mma_tmem_a_c<true>(d, ak + 24, bd + 6, idesc);
+                }
+                ptx::mma_commit(&sh.tmem_full[b]);
+              }
+              __syncwarp();
+              continue;
+            }
+            for (int h = 0; h < 2 && ok; ++h, ++k, k16 += 2) {
+              const int s8 = g * SG + k % SG;
+              const int sa = g * SG16 + k16 % SG16, sb = g * SG16 + (k16 + 1) % SG16;
+              ok = __all_sync(0xFFFFFFFFu,
+                              wait(&sh.full_w2[s8], (k / SG) & 1, 5, (st << 24) | (i << 12) | (k & 0xFFF)) &&
+                                  wait(&sh.empty_f16[sa], ((k16 / SG16) & 1) ^ 1, 10, (st << 24) | (i << 12)) &&
+                                  wait(&sh.empty_f16[sb], (((k16 + 1) / SG16) & 1) ^ 1, 10, (st << 24) | (i << 12)));
+              if (!ok) break;
+              const uint32_t src = ptx::smem_addr(sh.w2 + s8 * kW2StageBytes) + rl * 128;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int c = cq + 4 * hh;  // logical 16-byte chunk: K 16 c .. 16 c + 15 of this stage
+                const uint32_t dst =
+                    ptx::smem_addr(sh.f16 + (hh ? sb : sa) * kW2StageBytes) + rl * 128;
+                const uint32_t rd = src + ((c ^ rl) << 4);
+                const uint32_t w0 = dst + (((2 * cq) ^ rl) << 4), w1 = dst + (((2 * cq + 1) ^ rl) << 4);
+                // eight 16-byte loads in flight, then their conversions
+#pragma unroll
+                for (int q0 = 0; q0 < kTileV / 8; q0 += 8) {
+                  uint4 v8[8];
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) v8[q] = ptx::lds_v4(rd + (q0 + q) * 1024);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) {
+                    uint4 lo, hi;
+                    e4m3x4_to_f16(v8[q].x, lo.x, lo.y);
+                    e4m3x4_to_f16(v8[q].y, lo.z, lo.w);
+                    e4m3x4_to_f16(v8[q].z, hi.x, hi.y);
+                    e4m3x4_to_f16(v8[q].w, hi.z, hi.w);
+                    ptx::sts_v4(w0 + (q0 + q) * 1024, lo);
+                    ptx::sts_v4(w1 + (q0 + q) * 1024, hi);
+                  }
+                }
+              }
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::mbar_arrive(&sh.empty_w2[s8]);
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  const int s16 = hh ? sb : sa;
+                  const uint64_t a = a0 + static_cast<uint64_t>(s16 * (kW2StageBytes >> 4));
+                  const uint64_t bd = b0 + static_cast<uint64_t>(2 * h + hh) * b_kstep;
+                  if (res) {  // first step: keep the FP16 stage in tensor memory for the later steps
+                    const uint32_t ak = at + static_cast<uint32_t>((2 * h + hh) * 32);
+                    ptx::tmem_cp_128x256b(ak, a);
+                    ptx::tmem_cp_128x256b(ak + 8, a + 2);
+                    ptx::tmem_cp_128x256b(ak + 16, a + 4);
+                    ptx::tmem_cp_128x256b(ak + 24, a + 6);
+                  }
+                  if (h == 0 && hh == 0)
+                    ptx::mma_f16_c<false>(d, a, bd, idesc);
+                  else
+                    ptx::mma_f16_c<true>(d, a, bd, idesc);
+                  ptx::mma_f16_c<true>(d, a + 2, bd + 2, idesc);
+                  ptx::mma_f16_c<true>(d, a + 4, bd + 4, idesc);
+                  ptx::mma_f16_c<true>(d, a + 6, bd + 6, idesc);
+                  ptx::mma_commit(&sh.empty_f16[s16]);
+                }
+              }
+              __syncwarp();
+            }
+            if (ok && lane == 0) ptx::mma_commit(&sh.tmem_full[b]);
+          }
+        }
+        // every MMA lane 0 issued has completed before TMEM is freed
+        if (lane == 0) {
+          ptx::mma_commit(sh.spare + g);
+          ptx::mbar_wait(sh.spare + g, 0, kWaitLimit);
+        }
+        __syncwarp();
+      }
+    } else if (lane == 0 && n_tiles > g) {
       const int SG = S / 2;
       const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, static_cast<uint32_t>(N));
       // descriptors of stage 0 / K-block 0; a stage is 16 KB (1024 in the
@@ -526,20 +820,29 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           if (!(ok = wait(&sh.tmem_empty[b], ((j / NA) & 1) ^ 1, 4, (st << 24) | (i << 12)))) break;
           ptx::tc_fence_after();
           const uint32_t d = tmem_base + static_cast<uint32_t>(b * N);
-          for (int kb = 0; kb < kKBlocks && ok; ++kb, ++k) {
-            const int s = g * SG + k % SG;
-            if (!(ok = wait(&sh.full_w2[s], (k / SG) & 1, 5, (st << 24) | (i << 12) | (k & 0xFFF)))) break;
-            ptx::tc_fence_after();
-            const uint64_t a = a0 + static_cast<uint64_t>(s * (kW2StageBytes >> 4));
-            const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
-            if (kb == 0)
-              ptx::mma_bf16_c<false>(d, a, bd, idesc);
-            else
-              ptx::mma_bf16_c<true>(d, a, bd, idesc);
-            ptx::mma_bf16_c<true>(d, a + 2, bd + 2, idesc);
-            ptx::mma_bf16_c<true>(d, a + 4, bd + 4, idesc);
-            ptx::mma_bf16_c<true>(d, a + 6, bd + 6, idesc);
-            ptx::mma_commit(&sh.empty_w2[s]);
+          if (i < res0) {  // w2 streamed through the ring
+            for (int kb = 0; kb < kKBlocks && ok; ++kb, ++k) {
+              const int s = g * SG + k % SG;
+              if (!(ok = wait(&sh.full_w2[s], (k / SG) & 1, 5, (st << 24) | (i << 12) | (k & 0xFFF)))) break;
+              ptx::tc_fence_after();
+              const uint64_t a = a0 + static_cast<uint64_t>(s * (kW2StageBytes >> 4));
+              const uint64_t bd = b0 + static_cast<uint64_t>(kb) * b_kstep;
+              if (kb == 0)
+                ptx::mma_bf16_c<false>(d, a, bd, idesc);
+              else
+                ptx::mma_bf16_c<true>(d, a, bd, idesc);
+              ptx::mma_bf16_c<true>(d, a + 2, bd + 2, idesc);
+              ptx::mma_bf16_c<true>(d, a + 4, bd + 4, idesc);
+              ptx::mma_bf16_c<true>(d, a + 6, bd + 6, idesc);
+              ptx::mma_commit(&sh.empty_w2[s]);
+            }
+          } else if (st == 0) {  // a resident tile's first step: streamed, and copied into tensor memory
+            ok = resident_first_step(sh.full_w2, sh.empty_w2, g, SG, d,
+                                     tmem_base + static_cast<uint32_t>(tp.res_col + (i - res0) * 128), a0, b0, b_kstep,
+                                     idesc, k, BoundedWait{abort_flag, p.abort_word, p.status}, (st << 24) | (i << 12));
+            k += kKBlocks;
+          } else {  // a resident tile: A read from tensor memory
+            resident_step(d, tmem_base + static_cast<uint32_t>(tp.res_col + (i - res0) * 128), b0, b_kstep, idesc);
           }
           if (ok) ptx::mma_commit(&sh.tmem_full[b]);
         }
@@ -599,7 +902,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       const bool write_prev = blockIdx.x == 0 && (st > 0 || p.write_prev);
       const int64_t prev_step = static_cast<int64_t>(p.step) + st - 1;
       for (int idx = et; idx < N * 32; idx += kEpiThreads) {
-        const int r = idx >> 5, ch = idx & 31;
+        const int r = idx >> 5, ch = idx & 31;  // a warp takes one row
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (r < p.rows) {
           const int64_t tok = slot_token(__ldcg(prev + r));
@@ -607,6 +910,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           val = ldg_nc_v4(p.w1 + row * kRank + ch * 8);
           if (write_prev && ch == 0) p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + prev_step] = tok;
         }
+        if constexpr (kFp8) val = embedding_to_f16(val, sh.kscale + r, ch);
         const int kb = ch >> 3, c = ch & 7;
         *reinterpret_cast<uint4*>(sh.emb + kb * N * 128 + r * 128 + ((c ^ (r & 7)) << 4)) = val;
       }
@@ -652,12 +956,14 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       bool ok = true;
       for (int i = wg; i < n_tiles && ok; i += 2, ++j) {
         const int b = wg + 2 * (j % NA);
-        ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (j / NA) & 1, 6, (st << 24) | (i << 12)));
-        if (!ok) break;
-        ptx::tc_fence_after();
         const int64_t v = v_begin + static_cast<int64_t>(i) * kTileV + vr;
         const bool in = v < v_end;
         const uint32_t kv = murmur_kmix(static_cast<uint32_t>(v));
+        float w2s = 0.0f;  // E4M3 w2: this vocabulary row's FP16 scale (read while the tile's MMAs run)
+        if constexpr (kFp8) w2s = in ? __half2float(__ushort_as_half(__ldg(p.w2_scale + v))) : 0.0f;
+        ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (j / NA) & 1, 6, (st << 24) | (i << 12)));
+        if (!ok) break;
+        ptx::tc_fence_after();
         const bool first = i == wg;
         for (int c = 0; c < chunks && ok; ++c) {
           const int k = taken++;
@@ -704,6 +1010,16 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           // call's lookup table with a soft cap, else the multiplier
           uint32_t cb[R], biasb[R];
           float lv[R];
+          if constexpr (kFp8) {
+            // E4M3 w2: the dot of e 2^k with decode(q), back to e's scale
+            // (exact) and times the FP16 row scale, rounded once to FP32
+            // ([P1] dsparkMarkovGreedyFusedStepFp8: the scale meets the FP32
+            // sum); then the BF16 rounding below
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr)
+              acc[rr] = __float_as_uint(
+                  __fmul_rn(__fmul_rn(__uint_as_float(acc[rr]), ld_shared_f32(sh.kscale + r0 + rr)), w2s));
+          }
           if constexpr (R == 1) {
             const uint32_t bias1 = ptx::cvt_bf16x2(__uint_as_float(acc[0]), 0.0f);
             biasb[0] = bias1 & 0xFFFFu;
@@ -933,13 +1249,16 @@ EncodeTiledFn encode_fn() {
 
 int max_tc_smem() {
   int m = 0;
-  for (int r = 1; r <= kMaxRows; ++r) m = tc_layout(r).smem > m ? tc_layout(r).smem : m;
+  for (int r = 1; r <= kMaxRows; ++r) {
+    m = tc_layout(r).smem > m ? tc_layout(r).smem : m;
+    m = tc_layout(r, true).smem > m ? tc_layout(r, true).smem : m;
+  }
   return m;
 }
 
-template <bool C, bool M, bool T = false, int RW = kHalfRows>
+template <bool C, bool M, bool T = false, int RW = kHalfRows, bool F = false>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(step_tc_kernel<C, M, T, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(step_tc_kernel<C, M, T, RW, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               max_tc_smem());
 }
 
@@ -1012,10 +1331,36 @@ cudaError_t setup_step_tc() {
   if ((e = set_attrs<false, true, true>()) != cudaSuccess) return e;
   if ((e = set_attrs<false, true, false, 1>()) != cudaSuccess) return e;
   if ((e = set_attrs<false, true, false, 4>()) != cudaSuccess) return e;
-  return set_attrs<true, true>();
+  if ((e = set_attrs<true, true>()) != cudaSuccess) return e;
+  // E4M3 w2
+  if ((e = set_attrs<false, false, false, kHalfRows, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<false, true, false, kHalfRows, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<true, false, false, kHalfRows, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<true, true, false, kHalfRows, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<false, true, false, 1, true>()) != cudaSuccess) return e;
+  return set_attrs<false, true, false, 4, true>();
+}
+
+int tc_fp8_max_rows() {
+  int m = 0;
+  for (int r = 1; r <= kMaxRows; ++r)
+    if (tc_layout(r, true).smem > 0) m = r;
+  return m;
 }
 
 int tc_smem_bytes(int rows) { return tc_layout(rows).smem; }
+
+bool encode_w2_fp8_map(CUtensorMap* map, const void* w2_fp8, int64_t vocab, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRank), static_cast<cuuint64_t>(vocab)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRank)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};  // 128 K bytes: one swizzle row
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w2_fp8), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool encode_w2_map(CUtensorMap* map, const void* w2, int64_t vocab, int box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -1063,10 +1408,10 @@ int tc_step_grid(int64_t vocab, int sm_count) {
 namespace {
 
 // Resident CTAs per SM of one build of the kernel at its launch shape.
-template <bool C, bool M, bool T = false, int RW = kHalfRows>
+template <bool C, bool M, bool T = false, int RW = kHalfRows, bool F = false>
 int tc_blocks_per_sm() {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_tc_kernel<C, M, T, RW>, kThreads, max_tc_smem()) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_tc_kernel<C, M, T, RW, F>, kThreads, max_tc_smem()) !=
       cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
@@ -1085,10 +1430,19 @@ bool tc_cooperative_ok(int grid) {
     return false;
   }
   // every build a loop may launch (their register counts may differ)
-  const int counts[] = {tc_blocks_per_sm<false, false>(), tc_blocks_per_sm<false, true>(),
-                        tc_blocks_per_sm<true, false>(), tc_blocks_per_sm<true, true>(),
-                        tc_blocks_per_sm<false, true, true>(), tc_blocks_per_sm<false, true, false, 1>(),
-                        tc_blocks_per_sm<false, true, false, 4>()};
+  const int counts[] = {tc_blocks_per_sm<false, false>(),
+                        tc_blocks_per_sm<false, true>(),
+                        tc_blocks_per_sm<true, false>(),
+                        tc_blocks_per_sm<true, true>(),
+                        tc_blocks_per_sm<false, true, true>(),
+                        tc_blocks_per_sm<false, true, false, 1>(),
+                        tc_blocks_per_sm<false, true, false, 4>(),
+                        tc_blocks_per_sm<false, false, false, kHalfRows, true>(),
+                        tc_blocks_per_sm<false, true, false, kHalfRows, true>(),
+                        tc_blocks_per_sm<true, false, false, kHalfRows, true>(),
+                        tc_blocks_per_sm<true, true, false, kHalfRows, true>(),
+                        tc_blocks_per_sm<false, true, false, 1, true>(),
+                        tc_blocks_per_sm<false, true, false, 4, true>()};
   int per_sm = counts[0];
   for (int c : counts) per_sm = c < per_sm ? c : per_sm;
   return coop != 0 && per_sm >= 1 && grid <= per_sm * sms;
@@ -1108,20 +1462,25 @@ struct CoopPdlInit {
 }  // namespace
 
 cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const CUtensorMap& w2_tile_map, int grid,
-                           bool pdl, bool cooperative, cudaStream_t stream) {
+                           bool pdl, bool cooperative, cudaStream_t stream, bool fp8) {
   CUtensorMap base_map;
   bool steps_mid = false;
   if (!encode_base_map(&base_map, p, &steps_mid)) return cudaErrorInvalidValue;
-  const TcLayout L = tc_layout(p.rows);
+  const TcLayout L = tc_layout(p.rows, fp8);
+  if (L.smem == 0 || (fp8 && !p.w2_scale)) return cudaErrorInvalidValue;
   TcParams tp;
   tp.p = p;
   tp.n = L.n;
   tp.nacc = L.nacc;
   tp.stages = L.stages;
+  tp.stages16 = L.stages16;
   tp.nbase = L.nbase;
   tp.tmem_cols = L.tmem_cols;
+  tp.res_tiles = L.res_tiles;
+  tp.res_col = L.res_col;
   tp.emb_off = L.emb_off;
   tp.w2_off = L.w2_off;
+  tp.f16_off = L.f16_off;
   tp.base_off = L.base_off;
   tp.bar_off = L.bar_off;
   tp.row_off = L.row_off;
@@ -1133,7 +1492,15 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
   const bool one = p.mult == 1.0f;
   auto kernel = cap ? (one ? step_tc_kernel<true, true> : step_tc_kernel<true, false>)
                     : (one ? step_tc_kernel<false, true> : step_tc_kernel<false, false>);
-  if (p.test_stall) {  // the checking aid is built for multiplier 1 without a cap only
+  if (fp8) {
+    if (p.test_stall) return cudaErrorNotSupported;
+    kernel = cap ? (one ? step_tc_kernel<true, true, false, kHalfRows, true>
+                        : step_tc_kernel<true, false, false, kHalfRows, true>)
+                 : (one ? step_tc_kernel<false, true, false, kHalfRows, true>
+                        : step_tc_kernel<false, false, false, kHalfRows, true>);
+    if (p.rows <= 4 && !cap && one)
+      kernel = p.rows == 1 ? step_tc_kernel<false, true, false, 1, true> : step_tc_kernel<false, true, false, 4, true>;
+  } else if (p.test_stall) {  // the checking aid is built for multiplier 1 without a cap only
     if (cap || !one) return cudaErrorNotSupported;
     kernel = step_tc_kernel<false, true, true>;
   } else if (p.rows <= 4 && !cap && one) {  // few rows: the few-row epilogue

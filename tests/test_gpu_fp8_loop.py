@@ -1,5 +1,7 @@
 """Parity of the Markov loop over FP8 w2 ([P1] dsparkQuantizeMarkovW2Fp8 +
-dsparkMarkovGreedyFusedStepFp8) with the oracle (GPU, through the C ABI):
+dsparkMarkovGreedyFusedStepFp8) with the oracle (GPU, through the C ABI), on
+the tensor-core step (E4M3 stages turned into FP16 operands in shared memory)
+and on the CUDA-core step (forced, or above 128 rows):
   * the bias within 1 BF16 ulp of the exactly rounded s * sum(e * decode(q))
     (outside that, within the FP32 accumulation bound and the scale's one
     rounding);
@@ -62,8 +64,15 @@ def _check_fp8_bias(wl, gpu, qn, sn, sample=None):
     return int(far.sum())
 
 
-CASES = [("tiny", 4096 + 37, 4, 5), ("tiny", 1000, 1, 3), ("tc64", 3000 + 5, 64, 3), ("large16", 8192 + 8, 17, 2)]
-FLAGS = {"pdl": binding.FLAG_PDL, "nopdl": 0, "select": binding.FLAG_PDL | binding.FLAG_SELECT_2LAUNCH}
+CASES = [("tiny", 4096 + 37, 4, 5), ("tiny", 1000, 1, 3), ("tc64", 3000 + 5, 64, 3), ("large16", 8192 + 8, 17, 2),
+         ("tc64", 40000 + 16, 128, 2), ("large16", 60000, 24, 3), ("stress256", 2048 + 8, 200, 2)]
+FLAGS = {"pdl": binding.FLAG_PDL, "nopdl": 0, "select": binding.FLAG_PDL | binding.FLAG_SELECT_2LAUNCH,
+         "fma": binding.FLAG_PDL | binding.FLAG_FORCE_FMA, "per_step": binding.FLAG_PDL | binding.FLAG_PER_STEP}
+
+
+def _want_path(R, flags):
+    """The tensor-core FP8 step (3) up to 128 rows, else the CUDA-core one (2)."""
+    return 2 if (flags & binding.FLAG_FORCE_FMA) or R > 128 else 3
 
 
 @pytest.mark.parametrize("flags", list(FLAGS))
@@ -77,7 +86,7 @@ def test_fp8_loop_fed_parity_and_bias(name, V, R, K, flags):
     g, qn, sn = _fp8_loop(wl, FLAGS[flags])
     q_o, s_o = oracle.quantize_w2_fp8(wl.w2)
     assert np.array_equal(qn, q_o) and np.array_equal(sn, s_o)
-    assert g.ctx.bias_path(R) == 2
+    assert g.ctx.bias_path(R) == _want_path(R, FLAGS[flags])
     gpu = g.run(cache_fill=0x2468)
     orc = oracle_run(wl, fed_bias=gpu["bias"], cache_fill=0x2468)
     assert np.array_equal(gpu["tokens"], orc["tokens"]), np.argwhere(gpu["tokens"] != orc["tokens"])[:5]
@@ -98,11 +107,17 @@ def test_fp8_loop_end_to_end_against_the_oracle_fp8_loop():
 
 
 def test_attach_detach_launch_counts_and_errors():
-    wl = workloads.make("tiny", vocab=2048 + 3, rows=3, steps=4, seed_salt=5)
+    wl = workloads.make("tiny", vocab=2048 + 8, rows=3, steps=4, seed_salt=5)
     g, qn, sn = _fp8_loop(wl)
     cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
     tokens = torch.zeros((wl.rows, wl.steps), dtype=torch.int64, device="cuda")
-    assert g.ctx.loop_kernels(g.args(cache, tokens)) == 1 + wl.steps
+    assert g.ctx.bias_path(wl.rows) == 3
+    assert g.ctx.loop_kernels(g.args(cache, tokens)) == 2  # one launch runs every step
+    # a base row stride off the 16-byte grid: the CUDA-core FP8 step, one launch per step
+    odd = workloads.make("tiny", vocab=2048 + 3, rows=3, steps=4, seed_salt=5)
+    g_odd, _, _ = _fp8_loop(odd)
+    c_odd = torch.zeros((odd.num_req, odd.steps, odd.vocab), dtype=torch.int16, device="cuda")
+    assert g_odd.ctx.loop_kernels(g_odd.args(c_odd, tokens)) == 1 + odd.steps
     fp8 = g.run()
     g.ctx.set_w2_fp8(None, None)  # back to BF16 w2
     assert g.ctx.bias_path(wl.rows) != 2
@@ -130,6 +145,7 @@ def test_full_size_large16_fp8_loop():
     g, qn, sn = _fp8_loop(wl)
     q_o, s_o = oracle.quantize_w2_fp8(wl.w2)
     assert np.array_equal(qn, q_o) and np.array_equal(sn, s_o)
+    assert g.ctx.bias_path(wl.rows) == 3
     gpu = graph_run(g, wl)
     orc = oracle_run(wl, fed_bias=gpu["bias"])
     assert np.array_equal(gpu["tokens"], orc["tokens"]), np.argwhere(gpu["tokens"] != orc["tokens"])[:5]
