@@ -80,6 +80,7 @@ class LoopArgs(ctypes.Structure):
         ("nthreads", ctypes.c_int),
         ("w2_fp8", ctypes.c_void_p),
         ("w2_scale", ctypes.c_void_p),
+        ("logits_out", ctypes.c_void_p),
     ]
 
 
@@ -132,6 +133,9 @@ def lib():
             "oracle_expf_nonpos": (f32, [f32]),
             "oracle_expf_nonpos_array": (None, [P, P, i64]),
             "oracle_logits_to_probs": (ctypes.c_int, [P, P, i32, i64, f32, i32, f32]),
+            "oracle_shard_packet": (None, [P, i64, i64, P]),
+            "oracle_pick": (None, [P, i32, i32, P]),
+            "oracle_cache_fill": (None, [P, i64, P, i64, i64, P, i64, i64, i32, i32, i32, i32, i64]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -256,7 +260,7 @@ def murmur_fmix(h):
 def markov_loop(*, w1, w2, base, input_ids, anchor_idx, sample_pos, seeds, temperature,
                 req_idx=None, num_req=None, mult=1.0, cap=0.0, salt=1 << 30, fed_bias=None,
                 cache=None, want_bias=False, want_keys=False, rows=None, nthreads=None,
-                w2_fp8=None, w2_scale=None):
+                w2_fp8=None, w2_scale=None, want_logits=False):
     """Run the oracle loop.
 
     ``base`` is a BF16 bit array ``[rows, steps, V]`` (any strides with last
@@ -293,6 +297,7 @@ def markov_loop(*, w1, w2, base, input_ids, anchor_idx, sample_pos, seeds, tempe
     tokens = np.full((R, K), -7, np.int64)
     bias_out = np.empty((R, K, V), np.uint16) if want_bias else None
     keys_out = np.empty((R, K, V), np.float32) if want_keys else None
+    logits_out = np.empty((R, K, V), np.uint16) if want_logits else None
     if fed_bias is not None:
         fed_bias = _c(fed_bias, np.uint16)
         assert fed_bias.shape[0] >= R and fed_bias.shape[1:] == (K, V)
@@ -317,10 +322,11 @@ def markov_loop(*, w1, w2, base, input_ids, anchor_idx, sample_pos, seeds, tempe
     a.bias_out, a.keys_out = _ptr(bias_out), _ptr(keys_out)
     a.nthreads = int(nthreads or os.cpu_count() or 1)
     a.w2_fp8, a.w2_scale = _ptr(w2_fp8), _ptr(w2_scale)
+    a.logits_out = _ptr(logits_out)
     rc = lib().oracle_markov_loop(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_markov_loop failed: {rc}")
-    return {"tokens": tokens, "bias": bias_out, "keys": keys_out}
+    return {"tokens": tokens, "bias": bias_out, "keys": keys_out, "logits": logits_out}
 
 
 def build_verify_tokens(last, draft, P):
@@ -473,3 +479,40 @@ def dot_fp8(e, q, scale):
     out = np.empty(n, np.uint16)
     lib().oracle_dot_fp8_rows(_ptr(e), _ptr(q), _ptr(scale), _ptr(out), n, R)
     return out
+
+
+# --------------------------------------------------------------------------
+# The vocabulary-sharded loop ([P3] _finish packets, markov_pick, cache_fill)
+# --------------------------------------------------------------------------
+
+def shard_packet(keys, vocab_offset):
+    """The packet [key bits, global id, 0, 0] (uint32) of one rank's winner
+    over its slice of keys (local ids 0 .. len - 1)."""
+    keys = _c(keys, np.float32)
+    out = np.zeros(4, np.uint32)
+    lib().oracle_shard_packet(_ptr(keys), keys.size, int(vocab_offset), _ptr(out))
+    return out
+
+
+def pick(packets):
+    """Winners of the gathered packets ``[tp, rows, 4]`` uint32: int64 [rows]."""
+    packets = _c(packets, np.uint32)
+    tp, rows, _ = packets.shape
+    out = np.empty(rows, np.int64)
+    lib().oracle_pick(_ptr(packets), tp, rows, _ptr(out))
+    return out
+
+
+def cache_fill(src, cache, req_idx, num_req, vocab):
+    """Place the gathered rank-local caches ``src`` [tp, rows, steps, shard]
+    (uint16) into ``cache`` [num_req, steps, >= vocab] (updated in place) for
+    the rows whose request ``req_idx`` [rows, steps] (None: the row) is valid."""
+    src = _c(src, np.uint16)
+    tp, rows, steps, shard = src.shape
+    assert cache.dtype == np.uint16 and cache.strides[-1] == 2
+    if req_idx is not None:
+        req_idx = np.ascontiguousarray(req_idx, dtype=np.int64)
+    lib().oracle_cache_fill(_ptr(src), rows * steps * shard, cache.ctypes.data, cache.strides[0] // 2,
+                            cache.strides[1] // 2, _ptr(req_idx), steps, int(num_req), rows, steps, shard, tp,
+                            int(vocab))
+    return cache

@@ -696,6 +696,7 @@ static void *row_step_range(void *arg) {
     float l;
     uint16_t c = oracle_logit(base_row[v], b, a->mult, j->has_cap, j->inv_cap, a->cap, &l);
     if (j->valid && a->cache) a->cache[j->req * a->cache_s0 + (int64_t)j->s * a->cache_s1 + v] = c;
+    if (a->logits_out) a->logits_out[((int64_t)j->r * a->steps + j->s) * V + v] = c;
     uint32_t h = oracle_noise_hash(j->seed, j->s, j->pos, a->salt, (uint32_t)v);
     j->keys[v] = oracle_key(l, j->temp, h);
   }
@@ -1108,4 +1109,69 @@ void oracle_f32_to_bf16_array(const float *x, uint16_t *out, int64_t n) {
 }
 void oracle_key_array(const float *l, float temp, const uint32_t *h, float *out, int64_t n) {
   for (int64_t i = 0; i < n; i++) out[i] = oracle_key(l[i], temp, h[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Vocabulary-sharded loop ([P3] module docstring: with a vocab-parallel w2  */
+/* each rank works on its vocab range, its last block writes a packet       */
+/* instead of the token, markov_pick picks the winner from the gathered     */
+/* per-rank packets, cache_fill scatters the gathered draft-logits shards). */
+/* ------------------------------------------------------------------------ */
+
+/* [P3] _finish, sharded: the packet of one rank's winner over its slice,
+ * keys[0 .. width) being the keys of global ids vocab_offset + local:
+ * [bits of the key, global id, 0, 0], the winner by the total order. */
+void oracle_shard_packet(const float *keys, int64_t width, int64_t vocab_offset, uint32_t packet[4]) {
+  int64_t local = oracle_argmax(keys, width);
+  float v = keys[local];
+  uint32_t bits;
+  memcpy(&bits, &v, 4);
+  packet[0] = bits;
+  packet[1] = (uint32_t)(int32_t)(vocab_offset + local);
+  packet[2] = 0;
+  packet[3] = 0;
+}
+
+/* [P3] markov_pick: per row, the winner over the ranks' packets
+ * packets[(k * rows + r) * 4 + ...], k = 0 .. tp - 1, by the total order on
+ * (value, global id): the first NaN, else the largest value, ties to the
+ * lower id (which, with rank k holding the ids above rank k - 1's, is the
+ * unsharded argmax).  Written as a left-to-right pass with _combine. */
+void oracle_pick(const uint32_t *packets, int32_t tp, int32_t rows, int64_t *tokens) {
+  for (int32_t r = 0; r < rows; r++) {
+    float best = 0.0f;
+    int64_t best_id = -1;
+    for (int32_t k = 0; k < tp; k++) {
+      const uint32_t *pk = packets + ((int64_t)k * rows + r) * 4;
+      float v;
+      memcpy(&v, &pk[0], 4);
+      int64_t id = (int64_t)(int32_t)pk[1];
+      if (best_id < 0 || oracle_combine_first_wins(v, id, best, best_id)) {
+        best = v;
+        best_id = id;
+      }
+    }
+    tokens[r] = best_id;
+  }
+}
+
+/* [P3] cache_fill: the gathered rank-local caches src[k * src_s0 + (r *
+ * steps + i) * shard + local] (rank k, row r, step i, local id) go to
+ * cache[req * cache_s0 + i * cache_s1 + v] for v = k * shard + local < vocab,
+ * for every (r, i) whose request req = req_idx[r * req_s0 + i] (r without
+ * req_idx) is valid: 0 <= req < num_req.  Other rows are left as they are. */
+void oracle_cache_fill(const uint16_t *src, int64_t src_s0, uint16_t *cache, int64_t cache_s0, int64_t cache_s1,
+                       const int64_t *req_idx, int64_t req_s0, int64_t num_req, int32_t rows, int32_t steps,
+                       int32_t shard, int32_t tp, int64_t vocab) {
+  for (int32_t r = 0; r < rows; r++)
+    for (int32_t i = 0; i < steps; i++) {
+      int64_t req = req_idx ? req_idx[(int64_t)r * req_s0 + i] : r;
+      if (req < 0 || req >= num_req) continue;
+      for (int64_t v = 0; v < vocab; v++) {
+        int64_t k = v / shard, local = v - k * shard;
+        if (k >= tp) break;
+        cache[req * cache_s0 + (int64_t)i * cache_s1 + v] =
+            src[k * src_s0 + ((int64_t)r * steps + i) * shard + local];
+      }
+    }
 }

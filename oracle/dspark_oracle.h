@@ -63,6 +63,8 @@ typedef struct {
   int nthreads;
   const uint8_t *w2_fp8;   /* optional [vocab, rank] E4M3: the bias from it (and w2_scale) instead of w2 */
   const uint16_t *w2_scale; /* [vocab] FP16 row scales, with w2_fp8 */
+  uint16_t *logits_out;     /* optional [rows, steps, vocab]: the cached BF16 logit c of every row,
+                               valid or not (the rank-local cache of a vocabulary shard holds them all) */
 } oracle_loop_args;
 
 int oracle_markov_loop(const oracle_loop_args *a);
@@ -97,6 +99,13 @@ float oracle_expf_nonpos(float x);
 void oracle_expf_nonpos_array(const float *x, float *out, int64_t n);
 int oracle_logits_to_probs(const float *logits, float *probs, int32_t rows, int64_t vocab, float temperature,
                            int32_t top_k, float top_p);
+
+/* Vocabulary-sharded loop ([P3] module docstring, _finish, markov_pick, cache_fill). */
+void oracle_shard_packet(const float *keys, int64_t width, int64_t vocab_offset, uint32_t packet[4]);
+void oracle_pick(const uint32_t *packets, int32_t tp, int32_t rows, int64_t *tokens);
+void oracle_cache_fill(const uint16_t *src, int64_t src_s0, uint16_t *cache, int64_t cache_s0, int64_t cache_s1,
+                       const int64_t *req_idx, int64_t req_s0, int64_t num_req, int32_t rows, int32_t steps,
+                       int32_t shard, int32_t tp, int64_t vocab);
 
 #ifdef __cplusplus
 }
