@@ -37,6 +37,7 @@ EXPORTED = (
     "dspark_probabilistic_accept", "dspark_logits_to_probs", "dspark_quantize_w2_fp8", "dspark_strerror",
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
     "dspark_check_logf", "dspark_check_tanhf", "dspark_noise_bound_tables",
+    "dspark_markov_shard_step", "dspark_markov_pick", "dspark_cache_fill",
 )
 
 
@@ -113,6 +114,9 @@ def load(build_if_missing: bool = False):
         "dspark_check_logf": (ctypes.c_int, [P, P, i64, P]),
         "dspark_check_tanhf": (ctypes.c_int, [P, P, i64, P]),
         "dspark_noise_bound_tables": (ctypes.c_int, [P, P, i32]),
+        "dspark_markov_shard_step": (ctypes.c_int, [P, ctypes.POINTER(LoopArgs), i32, i64, P, P]),
+        "dspark_markov_pick": (ctypes.c_int, [P, P, i32, i32, P, i64, i32, P]),
+        "dspark_cache_fill": (ctypes.c_int, [P, i64, P, i64, i64, P, i64, i64, i32, i32, i32, i32, i32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -176,6 +180,24 @@ def dspark_markov_anchor(ctx, args: LoopArgs, stream=None):
 
 def dspark_markov_step(ctx, args: LoopArgs, step: int, stream=None):
     _check(load().dspark_markov_step(ctx, ctypes.byref(args), step, _stream(stream)), "dspark_markov_step")
+
+
+def dspark_markov_shard_step(ctx, args: LoopArgs, step: int, vocab_offset: int, packets, stream=None):
+    """One step on a vocabulary shard; packets: int32 [rows, 4] (device)."""
+    _check(load().dspark_markov_shard_step(ctx, ctypes.byref(args), step, vocab_offset, _ptr(packets),
+                                           _stream(stream)), "dspark_markov_shard_step")
+
+
+def dspark_markov_pick(ctx, packets, tp: int, rows: int, tokens, tokens_s0: int, step: int, stream=None):
+    """The winners of the gathered packets int32 [tp, rows, 4] into tokens[:, step]."""
+    _check(load().dspark_markov_pick(ctx, _ptr(packets), tp, rows, _ptr(tokens), tokens_s0, step, _stream(stream)),
+           "dspark_markov_pick")
+
+
+def dspark_cache_fill(src, src_s0: int, cache, cache_s0: int, cache_s1: int, req_idx, req_s0: int, num_req: int,
+                      rows: int, steps: int, shard: int, tp: int, vocab: int, stream=None):
+    _check(load().dspark_cache_fill(_ptr(src), src_s0, _ptr(cache), cache_s0, cache_s1, _ptr(req_idx), req_s0,
+                                    num_req, rows, steps, shard, tp, vocab, _stream(stream)), "dspark_cache_fill")
 
 
 def dspark_markov_partial_count(ctx) -> int:
@@ -334,6 +356,12 @@ class MarkovContext:
 
     def step(self, args: LoopArgs, step: int, stream=None):
         dspark_markov_step(self.ctx, args, step, stream)
+
+    def shard_step(self, args: LoopArgs, step: int, vocab_offset: int, packets, stream=None):
+        dspark_markov_shard_step(self.ctx, args, step, vocab_offset, packets, stream)
+
+    def pick(self, packets, tp: int, rows: int, tokens, step: int, stream=None):
+        dspark_markov_pick(self.ctx, packets, tp, rows, tokens, tokens.stride(0), step, stream)
 
     def partial_count(self) -> int:
         return dspark_markov_partial_count(self.ctx)

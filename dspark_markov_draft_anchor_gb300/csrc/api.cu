@@ -109,6 +109,9 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.test_stall = (ctx->cfg.flags & DSPARK_FLAG_TEST_STALL) != 0;
   p.xform_lut = ctx->xform_lut;
   p.w2_scale = nullptr;
+  p.sharded = 0;
+  p.vocab_offset = 0;
+  p.packets = nullptr;
   return p;
 }
 
@@ -334,6 +337,45 @@ int dspark_markov_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
   if (rc != DSPARK_OK) return rc;
   if (step < 0 || step >= a->steps) return DSPARK_ERR_INVALID_ARG;
   return launch_step(ctx, a, step, false, stream);
+}
+
+int dspark_markov_shard_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, int32_t step,
+                             int64_t vocab_offset, int32_t* packets, cudaStream_t stream) {
+  int rc = check_args(ctx, a);
+  if (rc != DSPARK_OK) return rc;
+  if (step < 0 || step >= a->steps || vocab_offset < 0 || !packets) return DSPARK_ERR_INVALID_ARG;
+  if (vocab_offset + ctx->cfg.vocab > (int64_t{1} << 31)) return DSPARK_ERR_INVALID_ARG;  // global ids are int32
+  if (reinterpret_cast<uintptr_t>(packets) & 15u) return DSPARK_ERR_MISALIGNED;
+  const int32_t path = dspark_markov_bias_path(ctx, a->rows);
+  if (path != 1 && path != 3) return DSPARK_ERR_INVALID_ARG;  // the tensor-core step only
+  if (!tma_base_ok(a)) return DSPARK_ERR_MISALIGNED;
+  dspark::StepParams p = make_params(ctx, a, step);
+  p.sharded = 1;
+  p.vocab_offset = vocab_offset;
+  p.packets = packets;
+  p.finish = 1;
+  p.write_prev = 0;
+  const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
+  cudaError_t e;
+  if (path == 3) {
+    p.w2_scale = ctx->w2_scale;
+    e = dspark::launch_step_tc(p, ctx->w2f8_map, ctx->w2f8_tile_map, ctx->grid_tc, pdl, false, stream, true);
+  } else {
+    e = dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, false, stream);
+  }
+  return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+int dspark_markov_pick(dspark_markov_ctx* ctx, const int32_t* packets, int32_t tp, int32_t rows, int64_t* tokens,
+                       int64_t tokens_s0, int32_t step, cudaStream_t stream) {
+  if (!ctx || !packets || !tokens || tp < 1 || tp > 32 || rows < 1 || step < 0) return DSPARK_ERR_INVALID_ARG;
+  if (rows > ctx->cfg.max_rows || step >= ctx->cfg.max_steps) return DSPARK_ERR_TOO_MANY_ROWS;
+  if (tokens_s0 <= step) return DSPARK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(packets) & 15u) return DSPARK_ERR_MISALIGNED;
+  unsigned long long* slot_next = ctx->slots + static_cast<int64_t>(step + 1) * ctx->cfg.max_rows;
+  return dspark::launch_pick(packets, tp, rows, tokens, tokens_s0, step, slot_next, stream) == cudaSuccess
+             ? DSPARK_OK
+             : DSPARK_ERR_CUDA;
 }
 
 int32_t dspark_markov_loop_kernels(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {

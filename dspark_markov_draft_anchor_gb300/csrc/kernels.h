@@ -23,6 +23,11 @@ cudaError_t launch_xform_lut(uint16_t* lut, float mult, float cap, cudaStream_t 
 cudaError_t launch_select(const unsigned long long* partials, int nparts, unsigned long long* slots_out,
                           int64_t* tokens, int64_t tokens_s0, int step, int rows, bool pdl, cudaStream_t stream);
 
+// Sharded loop: the winner of the gathered packets [tp, rows, 4] per row
+// (one warp a row) into tokens[:, step] and slot_next.
+cudaError_t launch_pick(const int32_t* packets, int tp, int rows, int64_t* tokens, int64_t tokens_s0, int step,
+                        unsigned long long* slot_next, cudaStream_t stream);
+
 // Simple fused step: one CTA per 128-entry vocabulary tile, FP32 FMA bias.
 int simple_step_grid(int64_t vocab);
 cudaError_t setup_step_simple();

@@ -223,6 +223,12 @@ __device__ __forceinline__ unsigned long long pack_key(float v, uint32_t id) {
   return (static_cast<unsigned long long>(orderable(v)) << 32) | static_cast<uint32_t>(~id);
 }
 
+// The float bits of an orderable key (NaN comes back as the canonical NaN).
+__device__ __forceinline__ uint32_t key_bits(uint32_t o) {
+  if (o == 0xFFFFFFFFu) return 0x7FFFFFFFu;
+  return (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+}
+
 __device__ __forceinline__ int64_t slot_token(unsigned long long slot) {
   return static_cast<int64_t>(static_cast<int32_t>(~static_cast<uint32_t>(slot)));
 }

@@ -66,6 +66,15 @@ struct StepParams {
   const uint16_t* xform_lut;
   // E4M3 w2 on the tensor-core step: the FP16 row scales [V] (else null).
   const uint16_t* w2_scale;
+  // One rank of a vocabulary-sharded loop ([P3] markov_step with a
+  // vocab-parallel w2): the step covers global ids vocab_offset .. +vocab-1
+  // (the noise hashes the global id), the cache is rank-local [rows, steps,
+  // shard] indexed by row and written for every row, and the launch's last
+  // CTA writes packets[r * 4 .. +3] = (key bits, global id, 0, 0) instead of
+  // the token (tensor-core step, one step per launch).
+  int32_t sharded;
+  int64_t vocab_offset;
+  int32_t* packets;
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this
@@ -102,9 +111,14 @@ __device__ __forceinline__ RowInfo row_info(const StepParams& p, int r, int step
   const int64_t pos = p.sample_pos[static_cast<int64_t>(r) * p.pos_s0 + step];
   ri.prefix = murmur_prefix(seed, step, pos, p.salt);
   ri.temp = temp;
-  ri.valid = valid && p.cache != nullptr;
+  if (p.sharded) {  // a rank-local cache row per request row, written whatever the row's request
+    ri.valid = p.cache != nullptr;
+    ri.cache_off = static_cast<int64_t>(r) * p.cache_s0;
+  } else {
+    ri.valid = valid && p.cache != nullptr;
+    ri.cache_off = valid ? req * p.cache_s0 : 0;
+  }
   ri.pad = 0;
-  ri.cache_off = valid ? req * p.cache_s0 : 0;
   return ri;
 }
 

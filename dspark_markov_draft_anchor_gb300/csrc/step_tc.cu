@@ -241,6 +241,7 @@ struct Shared {
   float* ltab;      // the computed noise is never below ltab[noise_index(h)]
   float* kscale;    // E4M3 w2: per row, 2^-k undoing the FP16 embedding's power-of-two scaling
   Cand* queues;
+  uint32_t id_offset;  // the global id of local vocabulary id 0 (a vocabulary shard's offset; else 0)
 };
 
 // Bounds of the noise -L(h) by bucket of the hash h: with g = h | 1, the
@@ -325,7 +326,8 @@ __device__ __forceinline__ void WarpQueue::flush(uint32_t min_count, const Share
       const Cand e = q[(head + lane) & (kQCap - 1)];
       const uint32_t r = e.vr >> 24, v = e.vr & 0xFFFFFFu;
       const float t = sh.temp[r];
-      const float key = t != 0.0f ? eval_key(e.l, t, murmur_finish_mixed(sh.prefix[r], murmur_kmix(v))) : e.l;
+      const float key =
+          t != 0.0f ? eval_key(e.l, t, murmur_finish_mixed(sh.prefix[r], murmur_kmix(v + sh.id_offset))) : e.l;
       const unsigned long long cand = pack_key(key, v);
       const unsigned long long old = atomicMax(sh.best + r, cand);
       if (cand > old) sh.thr[r] = key != key ? INFINITY : key;
@@ -508,6 +510,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.ltab = reinterpret_cast<float*>(rowreg + kRowLtab);
   sh.kscale = reinterpret_cast<float*>(rowreg + kRowKs);
   sh.queues = reinterpret_cast<Cand*>(smem + tp.queue_off);
+  sh.id_offset = static_cast<uint32_t>(p.vocab_offset);
 
   // This CTA's vocabulary range.
   const int G = gridDim.x;
@@ -958,7 +961,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         const int b = wg + 2 * (j % NA);
         const int64_t v = v_begin + static_cast<int64_t>(i) * kTileV + vr;
         const bool in = v < v_end;
-        const uint32_t kv = murmur_kmix(static_cast<uint32_t>(v));
+        const uint32_t kv = murmur_kmix(static_cast<uint32_t>(v) + sh.id_offset);  // the global id
         float w2s = 0.0f;  // E4M3 w2: this vocabulary row's FP16 scale (read while the tile's MMAs run)
         if constexpr (kFp8) w2s = in ? __half2float(__ushort_as_half(__ldg(p.w2_scale + v))) : 0.0f;
         ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (j / NA) & 1, 6, (st << 24) | (i << 12)));
@@ -1204,7 +1207,13 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
           __threadfence();
           for (int r = et; r < p.rows; r += kEpiThreads) {
             const unsigned long long sv = atomicAdd(out + r, 0ull);
-            p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + step] = slot_token(sv);
+            if (p.packets) {  // a rank of a sharded loop: its winner's packet ([P3] _finish)
+              const int4 pk = make_int4(static_cast<int>(key_bits(static_cast<uint32_t>(sv >> 32))),
+                                        static_cast<int>(static_cast<int64_t>(p.vocab_offset) + slot_token(sv)), 0, 0);
+              *reinterpret_cast<int4*>(p.packets + 4 * r) = pk;
+            } else {
+              p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + step] = slot_token(sv);
+            }
           }
         }
         break;

@@ -196,6 +196,56 @@ DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t
  */
 DSPARK_API int dspark_markov_set_w2_fp8(dspark_markov_ctx *ctx, const void *w2_fp8, const void *w2_scale_f16);
 
+/*
+ * Vocabulary-sharded loop ([P3] "muse_spark cutedsl draft markov": module
+ * docstring -- with a vocab-parallel w2 each rank works on its vocab range,
+ * its last block writes a packet instead of the token, markov_pick picks the
+ * winner from the gathered per-rank packets, cache_fill scatters the gathered
+ * draft-logits shards after the loop; _finish, markov_pick, cache_fill).
+ * A rank's context is initialised over its w2 shard (cfg.vocab = the shard's
+ * width, w2 = its [width, 256] rows) and the whole w1.  Per call: the anchor
+ * (dspark_markov_anchor), then for each step s: dspark_markov_shard_step on
+ * every rank, an all-gather of the ranks' packets into [tp, rows, 4] (rank
+ * k's rows at offset k * rows * 4; the caller's collective, into local
+ * memory), dspark_markov_pick on every rank; after the last step the
+ * all-gather of the rank-local caches and dspark_cache_fill.  The tokens equal
+ * the unsharded loop's (the total order makes the pick shard-invariant).
+ *
+ * dspark_markov_shard_step -- step `step` of this rank's shard: global ids
+ *   vocab_offset .. vocab_offset + width - 1 (the noise hashes the global id;
+ *   vocab_offset + width <= 2^31).  args->base is the rank's base shard
+ *   [rows, steps, width] (TMA-readable: 16-byte aligned, strides multiples of
+ *   8); args->cache, if not NULL, the rank-local cache [rows, steps, >= width]
+ *   written at [r, step, v] for every row r whatever its request (the fill
+ *   places the valid ones); the previous token comes from the anchor (step
+ *   0) or the pick of step - 1.  Writes packets [rows, 4] int32 (device,
+ *   16-byte aligned): (bits of the winner's noised key, its global id, 0, 0)
+ *   -- args->tokens is not written.  The tensor-core step only (bias path 1 or
+ *   3, else DSPARK_ERR_INVALID_ARG); one launch.
+ */
+DSPARK_API int dspark_markov_shard_step(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args, int32_t step,
+                                        int64_t vocab_offset, int32_t *packets, cudaStream_t stream);
+
+/* dspark_markov_pick -- [P3] markov_pick: per row the winner over the
+ * gathered packets [tp, rows, 4] int32 (device, 16-byte aligned; 1 <= tp <= 32)
+ * under the total order (the first NaN, else the largest value, ties to the
+ * lower global id); writes tokens[r * tokens_s0 + step] (int64) and makes it
+ * the previous token of the context's next step.  One launch. */
+DSPARK_API int dspark_markov_pick(dspark_markov_ctx *ctx, const int32_t *packets, int32_t tp, int32_t rows,
+                                  int64_t *tokens, int64_t tokens_s0, int32_t step, cudaStream_t stream);
+
+/* dspark_cache_fill -- [P3] cache_fill: src = the gathered rank-local caches,
+ * BF16 [tp, rows, steps, shard] (rank stride src_s0 elements, >= rows * steps
+ * * shard); for every (row r, step i) whose request req = req_idx[r * req_s0 +
+ * i] (r when req_idx is NULL) lies in [0, num_req), cache[req * cache_s0 + i *
+ * cache_s1 + v] = src[k * src_s0 + (r * steps + i) * shard + v - k * shard],
+ * k = v / shard, for v < vocab (shard * tp >= vocab); other cache rows are
+ * left alone.  16-byte copies when pointers, strides, shard and vocab allow.
+ * One launch, nothing allocated. */
+DSPARK_API int dspark_cache_fill(const void *src, int64_t src_s0, void *cache, int64_t cache_s0, int64_t cache_s1,
+                                 const int64_t *req_idx, int64_t req_s0, int64_t num_req, int32_t rows,
+                                 int32_t steps, int32_t shard, int32_t tp, int32_t vocab, cudaStream_t stream);
+
 /* The number of kernels dspark_markov_loop enqueues for `args` (2 when one
  * launch runs every step, 1 + 2 steps with DSPARK_FLAG_SELECT_2LAUNCH, else
  * 1 + steps); 0 if the arguments are invalid.
