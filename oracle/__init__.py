@@ -134,6 +134,11 @@ def lib():
             "oracle_expf_nonpos_array": (None, [P, P, i64]),
             "oracle_logits_to_probs": (ctypes.c_int, [P, P, i32, i64, f32, i32, f32]),
             "oracle_shard_packet": (None, [P, i64, i64, P]),
+            "oracle_dot_bf16_f32": (f32, [P, P, ctypes.c_int]),
+            "oracle_sigmoid": (f32, [f32]),
+            "oracle_confidence": (None, [P, i64, i64, P, i64, i32, P, f32, P, P, i64, i32, i32, i32, i32, P, P, P]),
+            "oracle_threshold_length": (i32, [P, i32, f32, i32, i32]),
+            "oracle_sps_length": (i32, [P, i32, f32, i32, i32, P]),
             "oracle_pick": (None, [P, i32, i32, P]),
             "oracle_cache_fill": (None, [P, i64, P, i64, i64, P, i64, i64, i32, i32, i32, i32, i64]),
         }
@@ -516,3 +521,51 @@ def cache_fill(src, cache, req_idx, num_req, vocab):
                             cache.strides[1] // 2, _ptr(req_idx), steps, int(num_req), rows, steps, shard, tp,
                             int(vocab))
     return cache
+
+
+# --------------------------------------------------------------------------
+# Confidence-scored proposal lengths ([P1] dsparkComputeConfidenceScores,
+# dsparkComputeConfidenceAndProposalLengths, ...SPSProposalLengths)
+# --------------------------------------------------------------------------
+
+def dot_bf16_f32(a, b):
+    a, b = _c(a, np.uint16), _c(b, np.uint16)
+    return float(lib().oracle_dot_bf16_f32(_ptr(a), _ptr(b), a.size))
+
+
+def sigmoid(z):
+    return np.array([lib().oracle_sigmoid(float(x)) for x in np.asarray(z, np.float32).ravel()],
+                    np.float32).reshape(np.shape(z))
+
+
+def confidence(*, hidden, w1, weight, bias, first_prev, draft, with_markov=True, fed_logits=None,
+               hidden_stride=0, hidden_offset=0, P=None, hidden_size=None):
+    """Scores [B, P] (and the logits z) of the confidence head.  ``hidden``
+    BF16 bits laid out as (b, j, k) at hidden_offset + (b P + j) stride + k."""
+    hidden, w1, weight = _c(hidden, np.uint16), _c(w1, np.uint16), _c(weight, np.uint16)
+    first_prev = _c(first_prev, np.int64)
+    draft = np.ascontiguousarray(draft, dtype=np.int64)
+    B = first_prev.shape[0]
+    P = draft.shape[1] if P is None else P
+    H = hidden_size if hidden_size is not None else (hidden.shape[-1] if hidden_stride == 0 else hidden_stride)
+    rank = w1.shape[1]
+    logits = np.empty((B, P), np.float32)
+    scores = np.empty((B, P), np.float32)
+    if fed_logits is not None:
+        fed_logits = _c(fed_logits, np.float32)
+    lib().oracle_confidence(_ptr(hidden), int(hidden_stride), int(hidden_offset), _ptr(w1), w1.shape[0], rank,
+                            _ptr(weight), float(bias), _ptr(first_prev), _ptr(draft), draft.shape[1], B, P, H,
+                            int(bool(with_markov)), _ptr(fed_logits), _ptr(logits), _ptr(scores))
+    return scores, logits
+
+
+def threshold_length(scores, threshold, min_len, max_len):
+    scores = _c(scores, np.float32)
+    return int(lib().oracle_threshold_length(_ptr(scores), scores.size, float(threshold), int(min_len), int(max_len)))
+
+
+def sps_length(scores, survival_floor, min_len, max_len, cost):
+    scores, cost = _c(scores, np.float32), _c(cost, np.float32)
+    assert cost.size >= scores.size + 1
+    return int(lib().oracle_sps_length(_ptr(scores), scores.size, float(survival_floor), int(min_len), int(max_len),
+                                       _ptr(cost)))

@@ -1175,3 +1175,167 @@ void oracle_cache_fill(const uint16_t *src, int64_t src_s0, uint16_t *cache, int
       }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Confidence-scored proposal lengths ([P1] "Dspark Kernels":               */
+/* dsparkComputeConfidenceScores, dsparkComputeConfidenceAndProposalLengths, */
+/* dsparkComputeConfidenceAndSPSProposalLengths).  The page gives the       */
+/* inputs and one-line contracts; the readings taken:                       */
+/*   - the confidence that draft position j is accepted is a logistic head: */
+/*     z = RN_f32(exact dot(weight, feature)) + bias (one FP32 add), with   */
+/*     feature = the draft hidden state of (b, j), followed (with the       */
+/*     Markov term) by the Markov embedding w1[prev] of the token before    */
+/*     position j (firstPrevTokens[b] for j = 0, draft[b, j - 1] after;     */
+/*     clamped to the last w1 row as in the loop); score = sigmoid(z) by    */
+/*     the library's own exp: E = exp(-|z|), RN(1 / RN(1 + E)) for z >= 0,  */
+/*     RN(E / RN(1 + E)) below;                                             */
+/*   - threshold scheduling proposes while the running product of scores   */
+/*     (the chance that every draft so far is accepted) stays >= threshold, */
+/*     clamped to [minProposalLen, maxProposalLen];                         */
+/*   - SPS scheduling takes the length L in [min, max] whose expected       */
+/*     output, 1 + the sum of the first L running products, per verify cost */
+/*     cost[L] is largest (ties to the shorter), considering L > min only   */
+/*     while the running product at L - 1 is >= the survival floor; the     */
+/*     verify-bucket costs are the caller's (the page names a B100 cost     */
+/*     model without giving it).                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Round sign * mag * 2^-ACC_OFFSET to FP32, nearest even. */
+static float wide_to_f32(const wide_t *mag, int negative) {
+  int t = wide_top(mag);
+  if (t < 0) return negative ? -0.0f : 0.0f;
+  int q = t - 23; /* 24 significant bits, never below the quantum 2^-149 */
+  if (q < ACC_OFFSET - 149) q = ACC_OFFSET - 149;
+  uint32_t kept = 0;
+  for (int b = t; b >= q; b--) kept = (kept << 1) | (uint32_t)wide_bit(mag, b);
+  int rbit = wide_bit(mag, q - 1);
+  int sticky = wide_any_below(mag, q - 1);
+  if (rbit && (sticky || (kept & 1u))) kept += 1u;
+  float v = ldexpf((float)kept, q - ACC_OFFSET); /* exact: kept <= 2^24 */
+  return negative ? -v : v;
+}
+
+float oracle_dot_bf16_f32(const uint16_t *a, const uint16_t *b, int n) {
+  int has_nan = 0, has_pinf = 0, has_ninf = 0, all_negzero = 1;
+  wide_t pos, neg;
+  memset(&pos, 0, sizeof(pos));
+  memset(&neg, 0, sizeof(neg));
+  for (int j = 0; j < n; j++) {
+    uint16_t x = a[j], y = b[j];
+    int x_nan = ((x & 0x7F80) == 0x7F80) && (x & 0x7F);
+    int y_nan = ((y & 0x7F80) == 0x7F80) && (y & 0x7F);
+    int x_inf = (x & 0x7FFF) == 0x7F80, y_inf = (y & 0x7FFF) == 0x7F80;
+    int x_zero = (x & 0x7FFF) == 0, y_zero = (y & 0x7FFF) == 0;
+    int negative = ((x ^ y) & 0x8000) != 0;
+    if (x_nan || y_nan) {
+      has_nan = 1;
+      continue;
+    }
+    if (x_inf || y_inf) {
+      if (x_zero || y_zero) has_nan = 1;
+      else if (negative) has_ninf = 1;
+      else has_pinf = 1;
+      continue;
+    }
+    if (x_zero || y_zero) {
+      if (!negative) all_negzero = 0;
+      continue;
+    }
+    all_negzero = 0;
+    uint32_t sx, sy;
+    int ex, ey;
+    bf16_parts(x, &sx, &ex);
+    bf16_parts(y, &sy, &ey);
+    wide_add_shifted(negative ? &neg : &pos, (uint64_t)sx * (uint64_t)sy, ex + ey + ACC_OFFSET);
+  }
+  if (has_nan || (has_pinf && has_ninf)) return NAN;
+  if (has_pinf) return INFINITY;
+  if (has_ninf) return -INFINITY;
+  int c = wide_cmp(&pos, &neg);
+  if (c == 0) return (n > 0 && all_negzero) ? -0.0f : 0.0f;
+  wide_t mag;
+  if (c > 0) wide_sub(&mag, &pos, &neg);
+  else wide_sub(&mag, &neg, &pos);
+  return wide_to_f32(&mag, c < 0);
+}
+
+float oracle_sigmoid(float z) {
+  if (isnan(z)) return z;
+  float a = z < 0.0f ? -z : z;
+  float E = oracle_expf_nonpos(-a);
+  float d = 1.0f + E;
+  return z >= 0.0f ? 1.0f / d : E / d;
+}
+
+void oracle_confidence(const uint16_t *hidden, int64_t hidden_stride, int64_t hidden_offset, const uint16_t *w1,
+                       int64_t w1_rows, int32_t rank, const uint16_t *weight, float bias, const int64_t *first_prev,
+                       const int64_t *draft, int64_t draft_stride, int32_t batch, int32_t P, int32_t hidden_size,
+                       int32_t with_markov, const float *fed_logits, float *logits_out, float *scores) {
+  uint16_t *feat = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(hidden_size + rank));
+  int64_t hs = hidden_stride > 0 ? hidden_stride : hidden_size;
+  for (int32_t b = 0; b < batch; b++)
+    for (int32_t j = 0; j < P; j++) {
+      float z;
+      if (fed_logits) {
+        z = fed_logits[(int64_t)b * P + j];
+      } else {
+        const uint16_t *h = hidden + hidden_offset + ((int64_t)b * P + j) * hs;
+        int n = hidden_size;
+        memcpy(feat, h, sizeof(uint16_t) * (size_t)hidden_size);
+        if (with_markov) {
+          int64_t prev = j == 0 ? first_prev[b] : draft[(int64_t)b * draft_stride + j - 1];
+          uint64_t last = (uint64_t)(w1_rows - 1);
+          uint64_t row = (uint64_t)prev < last ? (uint64_t)prev : last;
+          memcpy(feat + hidden_size, w1 + row * (uint64_t)rank, sizeof(uint16_t) * (size_t)rank);
+          n += rank;
+        }
+        z = oracle_dot_bf16_f32(weight, feat, n) + bias;
+      }
+      if (logits_out) logits_out[(int64_t)b * P + j] = z;
+      scores[(int64_t)b * P + j] = oracle_sigmoid(z);
+    }
+  free(feat);
+}
+
+static int32_t clamp_len(int32_t L, int32_t min_len, int32_t max_len, int32_t P) {
+  if (max_len > P) max_len = P;
+  if (min_len < 0) min_len = 0;
+  if (min_len > max_len) min_len = max_len;
+  return L < min_len ? min_len : (L > max_len ? max_len : L);
+}
+
+int32_t oracle_threshold_length(const float *scores, int32_t P, float threshold, int32_t min_len, int32_t max_len) {
+  float S = 1.0f;
+  int32_t L = 0;
+  for (int32_t j = 0; j < P; j++) {
+    S = S * scores[j];
+    if (!(S >= threshold)) break;
+    L = j + 1;
+  }
+  return clamp_len(L, min_len, max_len, P);
+}
+
+int32_t oracle_sps_length(const float *scores, int32_t P, float survival_floor, int32_t min_len, int32_t max_len,
+                          const float *cost) {
+  int32_t lo = clamp_len(min_len, min_len, max_len, P), hi = clamp_len(max_len, min_len, max_len, P);
+  float S = 1.0f, T = 1.0f; /* running product before position L; expected output of length L */
+  int32_t best = lo;
+  float best_ratio = 0.0f;
+  int have = 0;
+  for (int32_t L = 0; L <= hi; L++) {
+    if (L > 0) {
+      S = S * scores[L - 1];
+      T = T + S;
+      if (L > lo && !(S >= survival_floor)) break;
+    }
+    if (L < lo) continue;
+    if (!(cost[L] > 0.0f)) continue;
+    float ratio = T / cost[L];
+    if (!have || ratio > best_ratio) {
+      best = L;
+      best_ratio = ratio;
+      have = 1;
+    }
+  }
+  return best;
+}

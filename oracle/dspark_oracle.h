@@ -103,6 +103,15 @@ int oracle_logits_to_probs(const float *logits, float *probs, int32_t rows, int6
 /* Vocabulary-sharded loop ([P3] module docstring, _finish, markov_pick, cache_fill). */
 void oracle_shard_packet(const float *keys, int64_t width, int64_t vocab_offset, uint32_t packet[4]);
 void oracle_pick(const uint32_t *packets, int32_t tp, int32_t rows, int64_t *tokens);
+float oracle_dot_bf16_f32(const uint16_t *a, const uint16_t *b, int n);
+float oracle_sigmoid(float z);
+void oracle_confidence(const uint16_t *hidden, int64_t hidden_stride, int64_t hidden_offset, const uint16_t *w1,
+                       int64_t w1_rows, int32_t rank, const uint16_t *weight, float bias, const int64_t *first_prev,
+                       const int64_t *draft, int64_t draft_stride, int32_t batch, int32_t P, int32_t hidden_size,
+                       int32_t with_markov, const float *fed_logits, float *logits_out, float *scores);
+int32_t oracle_threshold_length(const float *scores, int32_t P, float threshold, int32_t min_len, int32_t max_len);
+int32_t oracle_sps_length(const float *scores, int32_t P, float survival_floor, int32_t min_len, int32_t max_len,
+                          const float *cost);
 void oracle_cache_fill(const uint16_t *src, int64_t src_s0, uint16_t *cache, int64_t cache_s0, int64_t cache_s1,
                        const int64_t *req_idx, int64_t req_s0, int64_t num_req, int32_t rows, int32_t steps,
                        int32_t shard, int32_t tp, int64_t vocab);
