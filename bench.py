@@ -783,16 +783,16 @@ def run_greedy_accept(args, d: Dist):
                        "l2": L2_NOTE + " step"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(GA_WORKLOAD, GA_SOURCES),
-                         "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "accept_scan_kernel (+ accept_clear_kernel)",
+                         "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "accept_scan_kernel (+ clear and walk kernels)",
                          "kernel_us": step_us, "algorithmic_bytes": algo,
-                         "kernel_us_from": "CUDA events around the two launches of one call, L2 flushed"},
+                         "kernel_us_from": "CUDA events around the three launches of one call, L2 flushed"},
             "proposal_mix": {"proposal_len": "uniform in [1, 5]", "us": mix_us, "algorithmic_bytes": mix_bytes,
                              "achieved_gbs": mix_bytes / (mix_us * 1e-6) / 1e9,
                              "frac": mix_bytes / (mix_us * 1e-6) / 1e9 / peak},
             "full_proposals_all_rows_accepted_len_ge_1": full_ok,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * 2,
+            "gpu_launches": args.steps * 3,
             "clocks": clock_info,
             "wall_timed_s": t_wall,
         }
@@ -800,6 +800,163 @@ def run_greedy_accept(args, d: Dist):
     if result is not None:
         print(json.dumps(result), flush=True)
     return 0
+
+
+CF_B, CF_P = 256, 5  # confidence head: the stress batch's 256 requests x 5 drafts
+CF_SOURCES = ("confidence.cu", "markov_math.cuh")
+CF_WORKLOAD = f"confidence_{CF_B}x{CF_P}x7168"
+CF_THRESHOLD, CF_FLOOR = 0.45, 0.12
+
+
+def run_confidence(args, d: Dist):
+    """One step = dspark_confidence_and_proposal_lengths (threshold 0.45, min
+    1, max 5) over 256 requests x 5 draft positions: hidden states [256, 5,
+    7168] BF16, the Markov embedding of each position's previous token from w1
+    [129280, 256], a synthetic logistic weight (workloads.confidence_workload),
+    inputs resident in HBM, L2 flushed before each.  The SPS form (survival
+    floor 0.12, the synthetic bucketed verify cost) is timed beside it."""
+    import torch
+    from dspark_markov_draft_anchor_gb300 import binding, workloads
+
+    torch.cuda.set_device(d.local_rank)
+    dev = torch.device("cuda", d.local_rank)
+    d.init("nccl")
+    B, P = CF_B, CF_P
+    w = workloads.confidence_workload(B, P, seed_salt=d.rank)
+    H, r = w["hidden_size"], w["rank"]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    hidden = t(w["hidden"].view(np.int16))
+    w1 = t(w["w1"].view(np.int16))
+    weight = t(w["weight"].view(np.int16))
+    bias = torch.tensor([w["bias"]], dtype=torch.float32, device=dev)
+    first_prev, draft, cost = t(w["first_prev"]), t(w["draft"]), t(w["cost"])
+    scores = torch.empty(B, P, dtype=torch.float32, device=dev)
+    lengths = torch.empty(B, dtype=torch.int32, device=dev)
+    a = binding.confidence_args(hidden=hidden, w1=w1, weight=weight, bias=bias, first_prev=first_prev, draft=draft,
+                                scores=scores, batch=B, proposal_len=P, hidden_size=H, rank=r,
+                                w1_rows=w["w1"].shape[0], draft_s0=P)
+    flush = L2Flush(dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def thr():
+        binding.dspark_confidence_and_proposal_lengths(a, CF_THRESHOLD, 1, P, lengths, stream)
+
+    def sps():
+        binding.dspark_confidence_and_sps_proposal_lengths(a, CF_FLOOR, 1, P, cost, lengths, stream)
+
+    def timed(n, fn):
+        ev = []
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                ev.append((e0, e1))
+        return ev
+
+    def mean_us(ev):
+        torch.cuda.synchronize()
+        return statistics.mean([e0.elapsed_time(e1) for e0, e1 in ev]) * 1e3
+
+    # the floor of this timing method: a one-element torch kernel timed the
+    # same way (launch, cold instruction and TLB state after the flush)
+    one = torch.zeros(1, device=dev)
+    timed(3, lambda: one.add_(1))
+    floor_us = mean_us(timed(50, lambda: one.add_(1)))
+    timed(max(args.warmup, 3), thr)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(d.local_rank)
+    if d.rank == 0:
+        clocks.start()
+    d.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    ev = timed(args.steps, thr)
+    torch.cuda.synchronize()
+    d.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clock_info = clocks.stop() if d.rank == 0 else None
+    step_us = d.max(mean_us(ev), dev)
+    len_thr = lengths.cpu().numpy().copy()
+    timed(3, sps)
+    sps_us = mean_us(timed(max(10, min(args.steps, 200)), sps))
+    len_sps = lengths.cpu().numpy().copy()
+
+    # end to end through the C ABI from pinned host buffers: the hidden
+    # states and ids in, the scores and lengths out
+    h_hidden, h_prev, h_draft = hidden.cpu().pin_memory(), first_prev.cpu().pin_memory(), draft.cpu().pin_memory()
+    h_scores = torch.empty_like(scores, device="cpu").pin_memory()
+    h_len = torch.empty_like(lengths, device="cpu").pin_memory()
+    h2d = h_hidden.numel() * 2 + h_prev.numel() * 8 + h_draft.numel() * 8
+    d2h = h_scores.numel() * 4 + h_len.numel() * 4
+
+    def e2e():
+        hidden.copy_(h_hidden, non_blocking=True)
+        first_prev.copy_(h_prev, non_blocking=True)
+        draft.copy_(h_draft, non_blocking=True)
+        thr()
+        h_scores.copy_(scores, non_blocking=True)
+        h_len.copy_(lengths, non_blocking=True)
+
+    timed(2, e2e)
+    e2e_us = d.max(mean_us(timed(max(5, min(args.steps, 50)), e2e)), dev)
+    torch.cuda.synchronize()
+
+    result = None
+    if d.rank == 0:
+        peak, peak_kind = measured_peaks()
+        # hidden rows, gathered w1 rows, the weight, ids, bias, scores, lengths
+        algo = B * P * (H + r) * 2 + (H + r) * 2 + B * 8 + B * (P - 1) * 8 + 4 + B * P * 4 + B * 4
+        achieved = algo / (step_us * 1e-6) / 1e9
+        cpu = None
+        if args.cpu_baseline and d.world == 1:
+            import oracle
+            t0 = time.perf_counter()
+            s_o, _ = oracle.confidence(hidden=w["hidden"], w1=w["w1"], weight=w["weight"], bias=w["bias"],
+                                       first_prev=w["first_prev"], draft=w["draft"], hidden_size=H)
+            l_o = np.array([oracle.threshold_length(s_o[b], CF_THRESHOLD, 1, P) for b in range(B)])
+            dt = time.perf_counter() - t0
+            cpu = {"value": dt * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+                   "sample": f"the whole batch of {B} requests x {P} positions, threshold lengths, one call "
+                             f"({dt:.2f} s wall)",
+                   "cpu_model": cpu_model(),
+                   "lengths_equal_gpu": int((l_o == len_thr).sum()), "of": B}
+        result = {
+            "metric": "µs per confidence-scored proposal-length call (256 requests x 5 drafts, hidden 7168, "
+                      "rank 256) and achieved HBM GB/s",
+            "value": step_us, "unit": "us", "n_gpus": d.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_us / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 features, f32 logit and scores", "data": "synthetic (seeded; no trained weights)",
+            "config": {"workload": f"confidence head: {B} requests x {P} positions, hidden {H} + Markov rank {r}, "
+                                   f"threshold {CF_THRESHOLD}, lengths in [1, {P}]",
+                       "parallelism": f"replicas x{d.world} (requests sharded, no collective)",
+                       "l2": L2_NOTE + " step"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": recorded_traffic(CF_WORKLOAD, CF_SOURCES),
+                         "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "confidence_kernel",
+                         "kernel_us": step_us, "algorithmic_bytes": algo,
+                         "kernel_us_from": "CUDA events around the one launch of a call, L2 flushed",
+                         "event_floor_us": floor_us,
+                         "event_floor_from": "a one-element torch kernel timed the same way: launch, cold code and "
+                                             "TLB after the flush"},
+            "sps": {"survival_floor": CF_FLOOR, "us": sps_us, "achieved_gbs": algo / (sps_us * 1e-6) / 1e9,
+                    "frac": algo / (sps_us * 1e-6) / 1e9 / peak,
+                    "length_histogram": np.bincount(len_sps, minlength=P + 1).tolist()},
+            "threshold_length_histogram": np.bincount(len_thr, minlength=P + 1).tolist(),
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clock_info,
+            "wall_timed_s": t_wall,
+        }
+    d.close()
+    if result is not None:
+        print(json.dumps(result), flush=True)
+    return 0
+
 
 
 def main(argv=None):
@@ -816,15 +973,19 @@ def main(argv=None):
                    help="bias contraction: the library's choice by row count, or forced")
     p.add_argument("--w2", choices=["bf16", "fp8"], default="bf16",
                    help="markov_w2 as BF16 (headline) or E4M3 with FP16 row scales")
-    p.add_argument("--path", choices=["draft_loop", "prob_verify", "greedy_accept"], default="draft_loop",
-                   help="the draft loop (headline), the probabilistic verify of a 256 x 5 x 129280 batch, or the "
-                        "greedy accept of a 256 x 6 x 129280 batch")
+    p.add_argument("--path", choices=["draft_loop", "prob_verify", "greedy_accept", "confidence"],
+                   default="draft_loop",
+                   help="the draft loop (headline), the probabilistic verify of a 256 x 5 x 129280 batch, the "
+                        "greedy accept of a 256 x 6 x 129280 batch, or the confidence-scored proposal lengths of "
+                        "256 requests x 5 drafts")
     args = p.parse_args(argv)
     d = Dist()
-    if args.path in ("prob_verify", "greedy_accept"):
+    if args.path in ("prob_verify", "greedy_accept", "confidence"):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the draft loop only"}))
             return 0
+        if args.path == "confidence":
+            return run_confidence(args, d)
         return run_prob_verify(args, d) if args.path == "prob_verify" else run_greedy_accept(args, d)
     if args.impl == "reference":
         return run_reference(args, d)

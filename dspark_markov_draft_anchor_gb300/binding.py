@@ -38,7 +38,10 @@ EXPORTED = (
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
     "dspark_check_logf", "dspark_check_tanhf", "dspark_noise_bound_tables",
     "dspark_markov_shard_step", "dspark_markov_pick", "dspark_cache_fill",
+    "dspark_confidence_scores", "dspark_confidence_and_proposal_lengths",
+    "dspark_confidence_and_sps_proposal_lengths",
 )
+CONFIDENCE_MAX_P = 256  # DSPARK_CONFIDENCE_MAX_P
 
 
 class DsparkError(RuntimeError):
@@ -50,6 +53,18 @@ class DsparkError(RuntimeError):
 class MarkovConfig(ctypes.Structure):
     _fields_ = [("vocab", ctypes.c_int32), ("rank", ctypes.c_int32), ("w1_rows", ctypes.c_int32),
                 ("max_rows", ctypes.c_int32), ("max_steps", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class ConfidenceArgs(ctypes.Structure):
+    _fields_ = [
+        ("hidden", ctypes.c_void_p), ("hidden_stride", ctypes.c_int64), ("hidden_offset", ctypes.c_int64),
+        ("hidden_size", ctypes.c_int32), ("with_markov", ctypes.c_int32),
+        ("w1", ctypes.c_void_p), ("w1_rows", ctypes.c_int64), ("rank", ctypes.c_int32),
+        ("batch", ctypes.c_int32), ("proposal_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("first_prev", ctypes.c_void_p),
+        ("draft", ctypes.c_void_p), ("draft_s0", ctypes.c_int64),
+        ("scores", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+    ]
 
 
 class LoopArgs(ctypes.Structure):
@@ -117,6 +132,11 @@ def load(build_if_missing: bool = False):
         "dspark_markov_shard_step": (ctypes.c_int, [P, ctypes.POINTER(LoopArgs), i32, i64, P, P]),
         "dspark_markov_pick": (ctypes.c_int, [P, P, i32, i32, P, i64, i32, P]),
         "dspark_cache_fill": (ctypes.c_int, [P, i64, P, i64, i64, P, i64, i64, i32, i32, i32, i32, i32, P]),
+        "dspark_confidence_scores": (ctypes.c_int, [ctypes.POINTER(ConfidenceArgs), P]),
+        "dspark_confidence_and_proposal_lengths": (
+            ctypes.c_int, [ctypes.POINTER(ConfidenceArgs), ctypes.c_float, i32, i32, P, P]),
+        "dspark_confidence_and_sps_proposal_lengths": (
+            ctypes.c_int, [ctypes.POINTER(ConfidenceArgs), ctypes.c_float, i32, i32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -226,6 +246,37 @@ def dspark_markov_get_status_detail(ctx, stream=None) -> list:
     d = (ctypes.c_int32 * 4)()
     _check(load().dspark_markov_get_status_detail(ctx, _stream(stream), d), "dspark_markov_get_status_detail")
     return list(d)
+
+
+def confidence_args(*, hidden, w1, weight, bias, first_prev, draft, scores, batch, proposal_len, hidden_size,
+                    rank, w1_rows, with_markov=True, hidden_stride=0, hidden_offset=0, draft_s0=None,
+                    logits=None) -> ConfidenceArgs:
+    """Marshal device tensors (or raw addresses) into dspark_confidence_args."""
+    if draft_s0 is None:
+        draft_s0 = draft.stride(0) if hasattr(draft, "stride") else proposal_len
+    return ConfidenceArgs(_ptr(hidden), hidden_stride, hidden_offset, hidden_size, int(bool(with_markov)),
+                          _ptr(w1), w1_rows, rank, batch, proposal_len, 0, _ptr(weight), _ptr(bias),
+                          _ptr(first_prev), _ptr(draft), draft_s0, _ptr(scores), _ptr(logits))
+
+
+def dspark_confidence_scores(args: ConfidenceArgs, stream=None):
+    _check(load().dspark_confidence_scores(ctypes.byref(args), _stream(stream)), "dspark_confidence_scores")
+
+
+def dspark_confidence_and_proposal_lengths(args: ConfidenceArgs, threshold: float, min_proposal_len: int,
+                                           max_proposal_len: int, proposal_lengths, stream=None):
+    _check(load().dspark_confidence_and_proposal_lengths(ctypes.byref(args), threshold, min_proposal_len,
+                                                         max_proposal_len, _ptr(proposal_lengths),
+                                                         _stream(stream)),
+           "dspark_confidence_and_proposal_lengths")
+
+
+def dspark_confidence_and_sps_proposal_lengths(args: ConfidenceArgs, survival_floor: float, min_proposal_len: int,
+                                               max_proposal_len: int, verify_cost, proposal_lengths, stream=None):
+    _check(load().dspark_confidence_and_sps_proposal_lengths(ctypes.byref(args), survival_floor, min_proposal_len,
+                                                             max_proposal_len, _ptr(verify_cost),
+                                                             _ptr(proposal_lengths), _stream(stream)),
+           "dspark_confidence_and_sps_proposal_lengths")
 
 
 def dspark_build_verify_tokens(last, draft, verify, batch, draft_stride, P, stream=None):

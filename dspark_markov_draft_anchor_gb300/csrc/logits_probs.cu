@@ -10,7 +10,7 @@
 //     infinite one over an infinite temperature) weighs nothing; top-k
 //     (0 < K < count of the others) keeps the first K ids in the order
 //     (z descending, id ascending);
-//   - e = exp(x) by this file's own exp, x = z - m (m the largest z; x = 0
+//   - e = exp(x) by the library's own exp, x = z - m (m the largest z; x = 0
 //     where z == m), w = floor(e 2^40);
 //   - top-p (p < 1) keeps the shortest prefix in the order (w descending, id
 //     ascending) whose weight reaches max(1, ceil(p W)), W the kept total;
@@ -27,46 +27,13 @@
 #include <stdint.h>
 
 #include "dspark_markov.h"
+#include "markov_math.cuh"
 
 namespace dspark {
 namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-
-// Cody-Waite reduction by ln 2 (its high part with the last 8 significand
-// bits cleared, so k * hi is exact for |k| < 2^8) and the Taylor series of
-// exp to degree 7 on |r| <= ln2/2.
-constexpr double kLn2 = 0.69314718055994530941723212145818;
-constexpr float kInvLn2 = static_cast<float>(1.0 / kLn2);
-constexpr float kLn2Hi = 0.693145751953125f;
-constexpr float kLn2Lo = static_cast<float>(kLn2 - 0.693145751953125);
-constexpr float kC2 = static_cast<float>(1.0 / 2.0);
-constexpr float kC3 = static_cast<float>(1.0 / 6.0);
-constexpr float kC4 = static_cast<float>(1.0 / 24.0);
-constexpr float kC5 = static_cast<float>(1.0 / 120.0);
-constexpr float kC6 = static_cast<float>(1.0 / 720.0);
-constexpr float kC7 = static_cast<float>(1.0 / 5040.0);
-
-// exp(x) for x <= 0: NaN propagates, below -104 gives 0, and 2^k scales the
-// polynomial exactly (k >= -125) or with one rounding into the subnormals.
-__device__ __forceinline__ float exp_nonpos(float x) {
-  if (isnan(x)) return x;
-  if (x < -104.0f) return 0.0f;
-  const float kf = rintf(__fmul_rn(x, kInvLn2));
-  float r = __fmaf_rn(-kf, kLn2Hi, x);
-  r = __fmaf_rn(-kf, kLn2Lo, r);
-  float p = __fmaf_rn(r, kC7, kC6);
-  p = __fmaf_rn(r, p, kC5);
-  p = __fmaf_rn(r, p, kC4);
-  p = __fmaf_rn(r, p, kC3);
-  p = __fmaf_rn(r, p, kC2);
-  p = __fmaf_rn(r, p, 1.0f);
-  p = __fmaf_rn(r, p, 1.0f);
-  const int k = static_cast<int>(kf);  // in [-150, 0]
-  if (k >= -125) return __fmul_rn(p, __int_as_float((k + 127) << 23));
-  return __fmul_rn(__fmul_rn(p, __int_as_float((k + 64 + 127) << 23)), 0x1p-64f);
-}
 
 // floor(e 2^40) for e in [0, 1], in integer instructions (significand
 // shifted by the exponent).
@@ -302,7 +269,7 @@ __device__ __noinline__ void compact_finish(float* out, int64_t vocab, bool vec,
   for (int i = threadIdx.x; i < (topp ? P2 : K); i += kThreads) {
     if (i < K) {
       const float z = cs.e[i];
-      const float e = exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
+      const float e = own_exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
       const uint64_t w = weight(e);
       cs.e[i] = e;
       cs.w[i] = w;
@@ -524,7 +491,7 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
       const uint32_t key = order_key(z);
       if (!(key > k_key || (key == k_key && v <= k_id))) return -1.0f;
     }
-    const float e = exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
+    const float e = own_exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
     part += weight(e);
     return e;
   });

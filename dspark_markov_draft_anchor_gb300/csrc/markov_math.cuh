@@ -1,6 +1,6 @@
 // markov_math.cuh -- per-element arithmetic of the DSpark Markov step on the
-// GPU: the output transform, the MurmurHash3 noise, the library's own log and
-// tanh, and the packed total-order key.
+// GPU: the output transform, the MurmurHash3 noise, the library's own log,
+// tanh and exp, and the packed total-order key.
 //
 // Every floating-point operation is an explicit round-to-nearest intrinsic
 // (__fadd_rn, __fmul_rn, __fmaf_rn, __fdiv_rn), which nvcc never contracts or
@@ -98,6 +98,41 @@ __device__ __forceinline__ float own_tanhf(float z) {
     t = __fdiv_rn(E, __fadd_rn(E, 2.0f));
   }
   return copysignf(t, z);
+}
+
+// ---------------------------------------------------------------------------
+// Own exp(x) for x <= 0 (the pages' expf is a vendor library's): Cody-Waite
+// reduction by ln 2 (its high part with the last 8 significand bits cleared,
+// so k * hi is exact for |k| < 2^8) and the Taylor series of exp to degree 7
+// on |r| <= ln2/2.  NaN propagates, below -104 gives 0, and 2^k scales the
+// polynomial exactly (k >= -125) or with one rounding into the subnormals.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float own_exp_nonpos(float x) {
+  constexpr double kLn2 = 0.69314718055994530941723212145818;
+  constexpr float kInvLn2 = static_cast<float>(1.0 / kLn2);
+  constexpr float kLn2Hi = 0.693145751953125f;
+  constexpr float kLn2Lo = static_cast<float>(kLn2 - 0.693145751953125);
+  constexpr float kC2 = static_cast<float>(1.0 / 2.0);
+  constexpr float kC3 = static_cast<float>(1.0 / 6.0);
+  constexpr float kC4 = static_cast<float>(1.0 / 24.0);
+  constexpr float kC5 = static_cast<float>(1.0 / 120.0);
+  constexpr float kC6 = static_cast<float>(1.0 / 720.0);
+  constexpr float kC7 = static_cast<float>(1.0 / 5040.0);
+  if (isnan(x)) return x;
+  if (x < -104.0f) return 0.0f;
+  const float kf = rintf(__fmul_rn(x, kInvLn2));
+  float r = __fmaf_rn(-kf, kLn2Hi, x);
+  r = __fmaf_rn(-kf, kLn2Lo, r);
+  float p = __fmaf_rn(r, kC7, kC6);
+  p = __fmaf_rn(r, p, kC5);
+  p = __fmaf_rn(r, p, kC4);
+  p = __fmaf_rn(r, p, kC3);
+  p = __fmaf_rn(r, p, kC2);
+  p = __fmaf_rn(r, p, 1.0f);
+  p = __fmaf_rn(r, p, 1.0f);
+  const int k = static_cast<int>(kf);  // in [-150, 0]
+  if (k >= -125) return __fmul_rn(p, __int_as_float((k + 127) << 23));
+  return __fmul_rn(__fmul_rn(p, __int_as_float((k + 64 + 127) << 23)), 0x1p-64f);
 }
 
 // ---------------------------------------------------------------------------

@@ -128,13 +128,6 @@ struct Stage {
   bool failed;
 };
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   ptx::smem_addr(dst)),
-               "l"(src), "r"(bytes), "r"(ptx::smem_addr(bar))
-               : "memory");
-}
-
 // The weights of ids v .. v+3 (ids past the end weigh 0): max(0, RN(t - q))
 // for a residual, else t, each through weight().
 __device__ __forceinline__ void weights4(const Row& r, int64_t v, uint64_t w[4]) {
@@ -263,8 +256,8 @@ __device__ __forceinline__ void stream_sums(const Row& r, int64_t chunk_len, uin
     const int64_t v0 = piece * kPiece;
     const uint32_t bytes = static_cast<uint32_t>((r.vocab - v0 < kPiece ? r.vocab - v0 : kPiece) * sizeof(float));
     ptx::mbar_arrive_expect_tx(st.full, kRes ? 2 * bytes : bytes);
-    bulk_load(st_t, r.t + v0, bytes, st.full);
-    if (kRes) bulk_load(st_q, r.q + v0, bytes, st.full);
+    ptx::bulk_load(st_t, r.t + v0, bytes, st.full);
+    if (kRes) ptx::bulk_load(st_q, r.q + v0, bytes, st.full);
   };
   int64_t piece = warp;
   if (lane == 0 && piece < n_pieces) issue(piece);

@@ -197,3 +197,46 @@ def verify_workload(draft: np.ndarray, vocab: int, P: int, seed_salt: int = 7, a
     proposal_len = rng.integers(1, P + 1, size=B).astype(np.int32)
     last = rng.integers(0, vocab, size=B).astype(np.int64)
     return logits, proposal_len, last
+
+
+# Confidence head: the draft hidden size of the pages' models (7168 for the
+# DeepSeek / Kimi families) and the loop's rank.  Trained confidence weights
+# are not available.
+CONF_HIDDEN = 7168
+
+
+def confidence_workload(batch: int, P: int, *, hidden_size: int = CONF_HIDDEN, vocab: int = 129280,
+                        rank: int = RANK, hidden_stride: int = 0, hidden_offset: int = 0, seed_salt: int = 0,
+                        bad_ids: bool = True) -> dict:
+    """Inputs of the confidence head: draft hidden states ~ N(0, 1) (post-norm
+    scale) laid out at ``hidden_offset + (b P + j) hidden_stride``; w1 ~
+    N(0, 0.02); a weight whose hidden part is N(0, 1/sqrt(H)) and Markov part
+    N(0, 1/(0.02 sqrt(rank))), so both parts give logits of unit spread; bias
+    1.5 (scores around 0.8, so running products fall over a few positions);
+    uniform previous and draft ids with a few out of range; and a verify cost
+    table that is flat inside power-of-two buckets of verified tokens."""
+    rng = rng_for("confidence", seed_salt)
+    hs = hidden_stride or hidden_size
+    n_hidden = hidden_offset + max(batch * P - 1, 0) * hs + hidden_size if batch * P else hidden_offset
+    hidden = normal_bf16(rng, (max(n_hidden, 1),), 1.0)
+    w1 = normal_bf16(rng, (vocab, rank), 0.02)
+    wh = normal_bf16(rng, (hidden_size,), 1.0 / np.sqrt(max(hidden_size, 1)))
+    wm = normal_bf16(rng, (rank,), 1.0 / (0.02 * np.sqrt(rank)))
+    first_prev = rng.integers(0, vocab, size=batch, dtype=np.int64)
+    draft = rng.integers(0, vocab, size=(batch, max(P, 1)), dtype=np.int64)[:, :P].copy()
+    if bad_ids and batch * P:
+        n_bad = max(1, batch * P // 50)
+        flat = draft.reshape(-1)
+        idx = rng.choice(flat.size, size=min(n_bad, flat.size), replace=False)
+        flat[idx] = np.array([-1, vocab, vocab + 1000, -(2**40)], np.int64)[np.arange(idx.size) % 4]
+        if batch:
+            first_prev[0] = vocab + 5
+    return dict(hidden=hidden, w1=w1, weight=np.concatenate([wh, wm]), weight_hidden_only=wh, bias=1.5,
+                first_prev=first_prev, draft=draft, hidden_size=hidden_size, hidden_stride=hidden_stride,
+                hidden_offset=hidden_offset, rank=rank, vocab=vocab, cost=verify_cost(P))
+
+
+def verify_cost(P: int) -> np.ndarray:
+    """A synthetic verify cost for L = 0..P drafts (L + 1 verified tokens):
+    1 + 0.08 per power-of-two bucket step."""
+    return np.array([1.0 + 0.08 * int(np.ceil(np.log2(L + 1))) for L in range(P + 1)], np.float32)

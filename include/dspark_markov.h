@@ -340,6 +340,97 @@ DSPARK_API int dspark_greedy_accept_noalloc(const void *logits, const int64_t *d
                                  int32_t draft_stride, int32_t P, int32_t vocab, cudaStream_t stream);
 
 /*
+ * Confidence-scored proposal lengths -- [P1] "Dspark Kernels":
+ * dsparkComputeConfidenceScores, dsparkComputeConfidenceAndProposalLengths and
+ * dsparkComputeConfidenceAndSPSProposalLengths.  The pages give the inputs
+ * and one-line contracts; what follows is this library's reading of them.
+ *
+ * The confidence that draft position j of request b (0 <= j < P) is accepted
+ * is a logistic head over the feature that produced that draft:
+ *   feature = hidden[b, j, 0 .. H)  ++  w1[prev_j, 0 .. rank)  (the second
+ *             part only with with_markov), prev_0 = first_prev[b],
+ *             prev_j = draft[b, j - 1]; an id outside [0, w1_rows) takes the
+ *             last w1 row, as in the loop;
+ *   z      = (weight . feature) + bias  -- products exact in FP32, summed in
+ *            FP32 in a fixed order (within (H + rank + 2) 2^-24 of the sum of
+ *            |products| and |bias| of the exactly rounded value), one FP32
+ *            bias add;
+ *   score  = sigmoid(z) = RN(1 / RN(1 + E)) for z >= 0, RN(E / RN(1 + E))
+ *            below, E = exp(-|z|) by the library's own exp; NaN stays NaN.
+ * Device pointers; BF16 values are raw 16-bit patterns.
+ *   hidden: BF16; the feature of (b, j) starts at element
+ *           hidden_offset + (b * P + j) * hidden_stride (hidden_stride 0 means
+ *           hidden_size; otherwise >= hidden_size).
+ *   w1 [w1_rows, rank] BF16 row-major (read only with with_markov).
+ *   weight [hidden_size + rank] BF16 (rank counted only with with_markov);
+ *   bias [1] FP32.
+ *   first_prev [batch] int64; draft [batch, draft_s0] int64 (draft_s0 >= P;
+ *   both read only with with_markov).
+ *   scores: out [batch, P] FP32 contiguous; logits: optional out [batch, P]
+ *   FP32 (z), NULL to skip.
+ * When hidden (plus offset), w1 and weight start on 16 bytes, hidden_size,
+ * rank and hidden_stride are multiples of 8 and (P + 1) (hidden_size + rank)
+ * 2 bytes fit in 200 KB, a request's rows are bulk-copied into shared memory
+ * (one mbarrier, bounded wait; a request whose wait gave up -- never in
+ * correct operation -- gets NaN scores and length -1); otherwise the rows
+ * load into registers (16-byte loads where aligned, else 2-byte loads).
+ * batch >= 0, 0 <= P <= DSPARK_CONFIDENCE_MAX_P.  One kernel on `stream`,
+ * one CTA per request; allocates nothing.
+ */
+#define DSPARK_CONFIDENCE_MAX_P 256
+typedef struct dspark_confidence_args {
+  const void *hidden;
+  int64_t hidden_stride;
+  int64_t hidden_offset;
+  int32_t hidden_size;
+  int32_t with_markov;
+  const void *w1;
+  int64_t w1_rows;
+  int32_t rank;
+  int32_t batch;
+  int32_t proposal_len;     /* P */
+  int32_t reserved;         /* 0 */
+  const void *weight;
+  const float *bias;
+  const int64_t *first_prev;
+  const int64_t *draft;
+  int64_t draft_s0;
+  float *scores;
+  float *logits;
+} dspark_confidence_args;
+
+/* The scores alone (the pages keep this form for chain-side analysis). */
+DSPARK_API int dspark_confidence_scores(const dspark_confidence_args *args, cudaStream_t stream);
+
+/*
+ * Scores and threshold-scheduled lengths: with S_j = RN(S_{j-1} * score_j)
+ * (S_{-1} = 1, the chance that drafts 0..j are all accepted),
+ * L = the number of leading positions whose S_j >= threshold, clamped to
+ * [lo, hi]: hi = clamp(max_proposal_len, 0, P), lo = clamp(min_proposal_len,
+ * 0, hi).  proposal_lengths: out [batch] int32.
+ */
+DSPARK_API int dspark_confidence_and_proposal_lengths(const dspark_confidence_args *args, float threshold,
+                                                      int32_t min_proposal_len, int32_t max_proposal_len,
+                                                      int32_t *proposal_lengths, cudaStream_t stream);
+
+/*
+ * Scores and SPS-scheduled lengths (draft-side confidence only): the length
+ * L in [lo, hi] (as above) with the largest RN(T_L / verify_cost[L]),
+ * T_L = 1 + S_0 + ... + S_{L-1} summed in that order in FP32 (the expected
+ * tokens out of a verify of L drafts), ties to the shorter; a length L > lo
+ * is considered only while S_{L-1} >= survival_floor (the scan stops at the
+ * first that is below), and a cost that is not > 0 (or NaN) rules its
+ * length out (lo if every one is ruled out).  verify_cost: [P + 1] FP32
+ * device array, the caller's estimate of a verify of L + 1 tokens (the pages
+ * use a B100 verify-bucket cost model that they do not give).
+ * proposal_lengths: out [batch] int32.
+ */
+DSPARK_API int dspark_confidence_and_sps_proposal_lengths(const dspark_confidence_args *args,
+                                                          float survival_floor, int32_t min_proposal_len,
+                                                          int32_t max_proposal_len, const float *verify_cost,
+                                                          int32_t *proposal_lengths, cudaStream_t stream);
+
+/*
  * dspark_fill_uniforms -- [P1] dsparkFillUniforms: n deterministic uniforms
  * in [0, 1) into `uniforms` (device, float32).  Element i is word i % 4 of
  * Philox4x32-10 (Salmon et al., SC 2011) at counter offset + i / 4 (a 64-bit

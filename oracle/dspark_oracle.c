@@ -1299,6 +1299,7 @@ void oracle_confidence(const uint16_t *hidden, int64_t hidden_stride, int64_t hi
 
 static int32_t clamp_len(int32_t L, int32_t min_len, int32_t max_len, int32_t P) {
   if (max_len > P) max_len = P;
+  if (max_len < 0) max_len = 0;
   if (min_len < 0) min_len = 0;
   if (min_len > max_len) min_len = max_len;
   return L < min_len ? min_len : (L > max_len ? max_len : L);

@@ -101,3 +101,30 @@ def test_fp8_calls_reject_bad_arguments_before_touching_the_device(lib):
     assert q(a8, a16, a16, 4, 256, None) == -3     # w2 off its 16-byte alignment
     assert q(a16, a2, a16, 4, 256, None) == -3     # codes off their 8-byte alignment
     assert lib.dspark_markov_set_w2_fp8(None, a16, a16) == -1  # no context
+
+
+def test_confidence_rejects_bad_arguments_before_touching_the_device(lib):
+    """The confidence entry points check sizes before any CUDA call; an empty
+    batch returns at once (no device needed)."""
+    fn = lib.dspark_confidence_and_proposal_lengths
+    fn.argtypes = [ctypes.POINTER(binding.ConfidenceArgs), ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    sps = lib.dspark_confidence_and_sps_proposal_lengths
+    sps.argtypes = [ctypes.POINTER(binding.ConfidenceArgs), ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
+                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    fake = 16
+    def args(**kw):
+        base = dict(hidden=fake, hidden_stride=0, hidden_offset=0, hidden_size=64, with_markov=1, w1=fake,
+                    w1_rows=100, rank=256, batch=4, proposal_len=5, reserved=0, weight=fake, bias=fake,
+                    first_prev=fake, draft=fake, draft_s0=5, scores=fake, logits=None)
+        base.update(kw)
+        return binding.ConfidenceArgs(**base)
+    assert fn(None, 0.5, 0, 5, fake, None) == -1
+    for bad in (dict(batch=-1), dict(proposal_len=-1), dict(proposal_len=binding.CONFIDENCE_MAX_P + 1),
+                dict(hidden_size=-1), dict(hidden_stride=10), dict(hidden_offset=-2), dict(rank=0),
+                dict(w1_rows=0), dict(draft_s0=4)):
+        assert fn(ctypes.byref(args(**bad)), 0.5, 0, 5, fake, None) == -1, bad
+    assert fn(ctypes.byref(args(batch=0)), 0.5, 0, 5, None, None) == 0
+    assert fn(ctypes.byref(args(scores=None)), 0.5, 0, 5, fake, None) == -1
+    assert fn(ctypes.byref(args()), 0.5, 0, 5, None, None) == -1      # no lengths
+    assert sps(ctypes.byref(args()), 0.5, 0, 5, None, fake, None) == -1  # no cost table

@@ -173,7 +173,7 @@ def survival(scores):
 
 
 def clamp_bounds(mn, mx, P):
-    mx = min(mx, P)
+    mx = max(min(mx, P), 0)
     mn = max(mn, 0)
     mn = min(mn, mx)
     return mn, mx
