@@ -665,6 +665,129 @@ def run_prob_verify(args, d: Dist):
     return 0
 
 
+L2P_ROWS, L2P_V = PV_B * (PV_P + 1), PV_V  # the verify's target shape [256, 6, 129280] as rows
+L2P_SOURCES = ("logits_probs.cu", "markov_math.cuh")
+L2P_SETTINGS = {"plain": (1.0, 0, 1.0), "filtered": (0.8, 50, 0.95)}
+
+
+def run_logits_to_probs(args, d: Dist):
+    """One step = dspark_logits_to_probs over rows x 129280 FP32 logits ~
+    N(0, 2.5^2) (the verify's target shape, 256 x 6 rows, by default): the
+    plain setting (T = 1, no top-k, no top-p) is the line's value, T = 0.8
+    with top-k 50 and top-p 0.95 is timed beside it; inputs resident in HBM,
+    L2 flushed before each."""
+    import torch
+    from dspark_markov_draft_anchor_gb300 import binding
+
+    torch.cuda.set_device(d.local_rank)
+    dev = torch.device("cuda", d.local_rank)
+    d.init("nccl")
+    rows, V = args.l2p_rows, L2P_V
+    lg = torch.randn(rows, V, device=dev, generator=torch.Generator(device=dev).manual_seed(77 + d.rank)) * 2.5
+    pr = torch.empty_like(lg)
+    flush = L2Flush(dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def timed(n, fn):
+        ev = []
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                ev.append((e0, e1))
+        return ev
+
+    def mean_us(ev):
+        torch.cuda.synchronize()
+        return statistics.mean([e0.elapsed_time(e1) for e0, e1 in ev]) * 1e3
+
+    def l2p(name):
+        T, K, Pp = L2P_SETTINGS[name]
+        return lambda: binding.dspark_logits_to_probs(lg, pr, rows, V, T, K, Pp, stream)
+
+    plain = l2p("plain")
+    timed(max(args.warmup, 3), plain)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(d.local_rank)
+    if d.rank == 0:
+        clocks.start()
+    d.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    ev = timed(args.steps, plain)
+    torch.cuda.synchronize()
+    d.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clock_info = clocks.stop() if d.rank == 0 else None
+    step_us = d.max(mean_us(ev), dev)
+    algo = 8 * V * rows  # one read and one write of every row
+    filt = l2p("filtered")
+    timed(2, filt)
+    filt_us = mean_us(timed(max(5, min(args.steps, 20)), filt))
+
+    # end to end through the C ABI from pinned host buffers: logits in,
+    # probabilities out
+    h_lg = lg.cpu().pin_memory()
+    h_pr = torch.empty_like(h_lg).pin_memory()
+
+    def e2e():
+        lg.copy_(h_lg, non_blocking=True)
+        plain()
+        h_pr.copy_(pr, non_blocking=True)
+
+    timed(2, e2e)
+    e2e_us = d.max(mean_us(timed(max(3, min(args.steps, 10)), e2e)), dev)
+    torch.cuda.synchronize()
+
+    result = None
+    if d.rank == 0:
+        peak, peak_kind = measured_peaks()
+        achieved = algo / (step_us * 1e-6) / 1e9
+        cpu = None
+        if args.cpu_baseline and d.world == 1:
+            import oracle
+            rs = 16
+            x = lg[:rs].cpu().numpy()
+            t0 = time.perf_counter()
+            got = oracle.logits_to_probs(x, *L2P_SETTINGS["plain"])
+            dt = time.perf_counter() - t0
+            same = bool(np.array_equal(got.view(np.uint32), pr[:rs].cpu().numpy().view(np.uint32)))
+            cpu = {"value": dt / rs * rows * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+                   "sample": f"{rs} of the {rows} rows, plain setting, scaled x{rows / rs:g} ({dt:.2f} s wall)",
+                   "cpu_model": cpu_model(), "same_result_as_gpu": same}
+        result = {
+            "metric": f"µs per logits-to-probabilities pass over {rows} x {V} FP32 rows and achieved HBM GB/s",
+            "value": step_us, "unit": "us", "n_gpus": d.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_us / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 logits and probabilities, u64 fixed-point sums", "data": "synthetic (seeded)",
+            "config": {"workload": f"logits to probabilities: {rows} rows x vocab {V}, T = 1, no top-k, no top-p",
+                       "parallelism": f"replicas x{d.world} (rows sharded, no collective)",
+                       "l2": L2_NOTE + " step"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": recorded_traffic(f"logits_probs_{rows}x{V}_plain", L2P_SOURCES),
+                         "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "logits_probs_kernel",
+                         "kernel_us": step_us, "algorithmic_bytes": algo,
+                         "kernel_us_from": "CUDA events around the one launch of a call, L2 flushed"},
+            "filtered": {"temperature": L2P_SETTINGS["filtered"][0], "top_k": L2P_SETTINGS["filtered"][1],
+                         "top_p": L2P_SETTINGS["filtered"][2], "us": filt_us,
+                         "achieved_gbs": algo / (filt_us * 1e-6) / 1e9, "frac": algo / (filt_us * 1e-6) / 1e9 / peak},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": rows * V * 4,
+                    "d2h_bytes_per_step": rows * V * 4},
+            "gpu_launches": args.steps,
+            "clocks": clock_info,
+            "wall_timed_s": t_wall,
+        }
+    d.close()
+    if result is not None:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
 GA_B, GA_P, GA_V = 256, 5, 129280  # greedy accept: the stress workload's verify shape [256, 6, 129280]
 GA_SOURCES = ("verify.cu", "markov_math.cuh", "step_common.cuh")
 GA_WORKLOAD = f"greedy_accept_{GA_B}x{GA_P + 1}x{GA_V}"
@@ -973,19 +1096,23 @@ def main(argv=None):
                    help="bias contraction: the library's choice by row count, or forced")
     p.add_argument("--w2", choices=["bf16", "fp8"], default="bf16",
                    help="markov_w2 as BF16 (headline) or E4M3 with FP16 row scales")
-    p.add_argument("--path", choices=["draft_loop", "prob_verify", "greedy_accept", "confidence"],
+    p.add_argument("--path", choices=["draft_loop", "prob_verify", "greedy_accept", "confidence", "logits_to_probs"],
                    default="draft_loop",
                    help="the draft loop (headline), the probabilistic verify of a 256 x 5 x 129280 batch, the "
-                        "greedy accept of a 256 x 6 x 129280 batch, or the confidence-scored proposal lengths of "
-                        "256 requests x 5 drafts")
+                        "greedy accept of a 256 x 6 x 129280 batch, the confidence-scored proposal lengths of "
+                        "256 requests x 5 drafts, or logits to probabilities over 1536 x 129280 rows")
+    p.add_argument("--l2p-rows", type=int, default=L2P_ROWS,
+                   help="rows of the logits-to-probabilities path (smaller for profiles)")
     args = p.parse_args(argv)
     d = Dist()
-    if args.path in ("prob_verify", "greedy_accept", "confidence"):
+    if args.path in ("prob_verify", "greedy_accept", "confidence", "logits_to_probs"):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the draft loop only"}))
             return 0
         if args.path == "confidence":
             return run_confidence(args, d)
+        if args.path == "logits_to_probs":
+            return run_logits_to_probs(args, d)
         return run_prob_verify(args, d) if args.path == "prob_verify" else run_greedy_accept(args, d)
     if args.impl == "reference":
         return run_reference(args, d)

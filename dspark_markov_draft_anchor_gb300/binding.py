@@ -36,7 +36,8 @@ EXPORTED = (
     "dspark_greedy_accept", "dspark_greedy_accept_noalloc", "dspark_fill_uniforms",
     "dspark_probabilistic_accept", "dspark_logits_to_probs", "dspark_quantize_w2_fp8", "dspark_strerror",
     "dspark_check_noise_range", "dspark_check_hash", "dspark_check_logit", "dspark_check_key",
-    "dspark_check_logf", "dspark_check_tanhf", "dspark_noise_bound_tables",
+    "dspark_check_logf", "dspark_check_tanhf", "dspark_check_expf", "dspark_check_div",
+    "dspark_check_div_sweep", "dspark_noise_bound_tables",
     "dspark_markov_shard_step", "dspark_markov_pick", "dspark_cache_fill",
     "dspark_confidence_scores", "dspark_confidence_and_proposal_lengths",
     "dspark_confidence_and_sps_proposal_lengths",
@@ -128,6 +129,9 @@ def load(build_if_missing: bool = False):
         "dspark_check_key": (ctypes.c_int, [P, ctypes.c_float, P, P, i64, P]),
         "dspark_check_logf": (ctypes.c_int, [P, P, i64, P]),
         "dspark_check_tanhf": (ctypes.c_int, [P, P, i64, P]),
+        "dspark_check_expf": (ctypes.c_int, [P, P, i64, P]),
+        "dspark_check_div": (ctypes.c_int, [P, ctypes.c_float, P, i64, P]),
+        "dspark_check_div_sweep": (ctypes.c_int, [ctypes.c_float, ctypes.c_uint32, i64, P, P]),
         "dspark_noise_bound_tables": (ctypes.c_int, [P, P, i32]),
         "dspark_markov_shard_step": (ctypes.c_int, [P, ctypes.POINTER(LoopArgs), i32, i64, P, P]),
         "dspark_markov_pick": (ctypes.c_int, [P, P, i32, i32, P, i64, i32, P]),
@@ -329,6 +333,18 @@ def dspark_check_logf(x, y, n, stream=None):
 
 def dspark_check_tanhf(x, y, n, stream=None):
     _check(load().dspark_check_tanhf(_ptr(x), _ptr(y), n, _stream(stream)), "dspark_check_tanhf")
+
+
+def dspark_check_expf(x, y, n, stream=None):
+    _check(load().dspark_check_expf(_ptr(x), _ptr(y), n, _stream(stream)), "dspark_check_expf")
+
+
+def dspark_check_div(x, d, y, n, stream=None):
+    _check(load().dspark_check_div(_ptr(x), d, _ptr(y), n, _stream(stream)), "dspark_check_div")
+
+
+def dspark_check_div_sweep(d, lo, n, out, stream=None):
+    _check(load().dspark_check_div_sweep(d, lo, n, _ptr(out), _stream(stream)), "dspark_check_div_sweep")
 
 
 def dspark_fill_uniforms(uniforms, n, seed, offset, stream=None):

@@ -54,6 +54,37 @@ __global__ void tanhf_kernel(const float* x, float* y, int64_t n) {
   GRID_STRIDE(i, n) { y[i] = own_tanhf(x[i]); }
 }
 
+__global__ void expf_kernel(const float* x, float* y, int64_t n) {
+  GRID_STRIDE(i, n) { y[i] = own_exp_nonpos(x[i]); }
+}
+
+__global__ void div_kernel(const float* x, float d, float* y, int64_t n) {
+  const Divider D = make_divider(d);
+  GRID_STRIDE(i, n) { y[i] = div_rn(x[i], D); }
+}
+
+// Every float x with bits in [lo, lo + n): count the x whose div_rn(x, d)
+// differs in its bits from the IEEE quotient (two NaNs count as equal) and
+// keep the smallest such bit pattern.
+__global__ void div_sweep_kernel(float d, uint32_t lo, int64_t n, unsigned long long* out) {
+  const Divider D = make_divider(d);
+  unsigned long long bad = 0;
+  uint32_t first = 0xFFFFFFFFu;
+  GRID_STRIDE(i, n) {
+    const uint32_t b = lo + static_cast<uint32_t>(i);
+    const float x = __uint_as_float(b);
+    const float got = div_rn(x, D), want = __fdiv_rn(x, d);
+    if (__float_as_uint(got) != __float_as_uint(want) && !(got != got && want != want)) {
+      ++bad;
+      first = b < first ? b : first;
+    }
+  }
+  if (bad) {
+    atomicAdd(out, bad);
+    atomicMin(out + 1, static_cast<unsigned long long>(first));
+  }
+}
+
 int done() { return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA; }
 
 }  // namespace
@@ -109,6 +140,27 @@ int dspark_check_tanhf(const float* x, float* y, int64_t n, cudaStream_t stream)
   if (n < 0 || (n > 0 && (!x || !y))) return DSPARK_ERR_INVALID_ARG;
   if (n == 0) return DSPARK_OK;
   dspark::tanhf_kernel<<<dspark::grid_for(n), dspark::kThreads, 0, stream>>>(x, y, n);
+  return dspark::done();
+}
+
+int dspark_check_expf(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return DSPARK_ERR_INVALID_ARG;
+  if (n == 0) return DSPARK_OK;
+  dspark::expf_kernel<<<dspark::grid_for(n), dspark::kThreads, 0, stream>>>(x, y, n);
+  return dspark::done();
+}
+
+int dspark_check_div(const float* x, float d, float* y, int64_t n, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return DSPARK_ERR_INVALID_ARG;
+  if (n == 0) return DSPARK_OK;
+  dspark::div_kernel<<<dspark::grid_for(n), dspark::kThreads, 0, stream>>>(x, d, y, n);
+  return dspark::done();
+}
+
+int dspark_check_div_sweep(float d, uint32_t lo, int64_t n, unsigned long long* out, cudaStream_t stream) {
+  if (n < 0 || n > (int64_t{1} << 32) || !out) return DSPARK_ERR_INVALID_ARG;
+  if (n == 0) return DSPARK_OK;
+  dspark::div_sweep_kernel<<<dspark::grid_for(n), dspark::kThreads, 0, stream>>>(d, lo, n, out);
   return dspark::done();
 }
 

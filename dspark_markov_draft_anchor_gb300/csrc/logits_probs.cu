@@ -26,8 +26,12 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dspark_markov.h"
+#include "kernels.h"
 #include "markov_math.cuh"
+#include "ptx.cuh"
 
 namespace dspark {
 namespace {
@@ -35,17 +39,9 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
-// floor(e 2^40) for e in [0, 1], in integer instructions (significand
-// shifted by the exponent).
-__device__ __forceinline__ uint64_t weight(float e) {
-  if (!(e > 0.0f)) return 0ull;
-  if (e >= 1.0f) return 1ull << 40;
-  const uint32_t b = __float_as_uint(e);
-  const uint32_t ex = b >> 23;
-  const uint32_t m = (b & 0x7FFFFFu) | (ex ? 0x800000u : 0u);
-  const int sh = static_cast<int>(ex ? ex : 1u) - 110;
-  return sh >= 0 ? static_cast<uint64_t>(m) << sh : static_cast<uint64_t>(m >> (-sh < 31 ? -sh : 31));
-}
+// floor(e 2^40) for e in [0, 1]: the scaling by 2^40 is exact (subnormal e
+// included), and the conversion rounds toward zero.
+__device__ __forceinline__ uint64_t weight(float e) { return __float2ull_rz(__fmul_rn(e, 0x1p40f)); }
 
 // An order-preserving 32-bit key of a non-NaN float (+0 and -0 equal).
 __device__ __forceinline__ uint32_t order_key(float z) {
@@ -147,17 +143,19 @@ __device__ int64_t nth_in_order(int64_t vocab, int64_t r, Pred pred, RowSmem& sm
 // reads and then writes each id, so src may equal dst).
 template <int kBatch = 1, class F>
 __device__ __forceinline__ void row_each(const float* src, int64_t vocab, bool vec, F&& f) {
+  const int n = static_cast<int>(vocab);  // < 2^31 (the C ABI's vocab is an int32)
+  const int t = static_cast<int>(threadIdx.x);
   if (vec) {
     const float4* s4 = reinterpret_cast<const float4*>(src);
-    const int64_t n4 = vocab >> 2;
-    for (int64_t g0 = threadIdx.x; g0 < n4; g0 += kBatch * kThreads) {
+    const int n4 = n >> 2;
+    for (int g0 = t; g0 < n4; g0 += kBatch * kThreads) {
       float4 x[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
         if (g0 + k * kThreads < n4) x[k] = s4[g0 + k * kThreads];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int64_t g = g0 + k * kThreads;
+        const int g = g0 + k * kThreads;
         if (g < n4) {
           f(4 * g, x[k].x);
           f(4 * g + 1, x[k].y);
@@ -167,34 +165,36 @@ __device__ __forceinline__ void row_each(const float* src, int64_t vocab, bool v
       }
     }
   } else {
-    for (int64_t v0 = threadIdx.x; v0 < vocab; v0 += kBatch * kThreads) {
+    for (int v0 = t; v0 < n; v0 += kBatch * kThreads) {
       float x[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
-        if (v0 + k * kThreads < vocab) x[k] = src[v0 + k * kThreads];
+        if (v0 + k * kThreads < n) x[k] = src[v0 + k * kThreads];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
-        if (v0 + k * kThreads < vocab) f(v0 + k * kThreads, x[k]);
+        if (v0 + k * kThreads < n) f(v0 + k * kThreads, x[k]);
     }
   }
 }
 
 template <bool kStreamIn, bool kStreamOut, int kBatch = 1, class F>
 __device__ __forceinline__ void row_map(const float* src, float* dst, int64_t vocab, bool vec, F&& f) {
+  const int n = static_cast<int>(vocab);
+  const int t = static_cast<int>(threadIdx.x);
   if (vec) {
     const float4* s4 = reinterpret_cast<const float4*>(src);
     float4* d4 = reinterpret_cast<float4*>(dst);
-    const int64_t n4 = vocab >> 2;
-    for (int64_t g0 = threadIdx.x; g0 < n4; g0 += kBatch * kThreads) {
+    const int n4 = n >> 2;
+    for (int g0 = t; g0 < n4; g0 += kBatch * kThreads) {
       float4 x[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int64_t g = g0 + k * kThreads;
+        const int g = g0 + k * kThreads;
         if (g < n4) x[k] = kStreamIn ? __ldcs(s4 + g) : s4[g];
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int64_t g = g0 + k * kThreads;
+        const int g = g0 + k * kThreads;
         if (g < n4) {
           const float4 y =
               make_float4(f(4 * g, x[k].x), f(4 * g + 1, x[k].y), f(4 * g + 2, x[k].z), f(4 * g + 3, x[k].w));
@@ -206,17 +206,17 @@ __device__ __forceinline__ void row_map(const float* src, float* dst, int64_t vo
       }
     }
   } else {
-    for (int64_t v0 = threadIdx.x; v0 < vocab; v0 += kBatch * kThreads) {
+    for (int v0 = t; v0 < n; v0 += kBatch * kThreads) {
       float x[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int64_t v = v0 + k * kThreads;
-        if (v < vocab) x[k] = kStreamIn ? __ldcs(src + v) : src[v];
+        const int v = v0 + k * kThreads;
+        if (v < n) x[k] = kStreamIn ? __ldcs(src + v) : src[v];
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int64_t v = v0 + k * kThreads;
-        if (v < vocab) {
+        const int v = v0 + k * kThreads;
+        if (v < n) {
           const float y = f(v, x[k]);
           if (kStreamOut)
             __stcs(dst + v, y);
@@ -348,6 +348,277 @@ __device__ __noinline__ void compact_finish(float* out, int64_t vocab, bool vec,
   for (int i = threadIdx.x; i < n_final; i += kThreads) out[cs.id[i]] = __fdiv_rn(cs.e[i], Sf);
 }
 
+// ---------------------------------------------------------------------------
+// The plain setting -- T > 0, no top-k, no top-p -- on a 16-byte-aligned
+// row, four ids at a time.  Each group of four takes one range check that
+// keeps the reciprocal division (div_rn's fast form) and the exp's fast form
+// exact, with the general forms behind it, so the common path is a few
+// instructions an id.  Same passes and values as logits_probs_row.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// z = RN(x / T), -0 as +0
+__device__ __forceinline__ float4 scaled4(float4 x, const Divider& D) {
+  const float lo = fminf(fminf(fabsf(x.x), fabsf(x.y)), fminf(fabsf(x.z), fabsf(x.w)));
+  const float hi = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  float4 z;
+  if (D.fast && lo >= 0x1p-60f && hi < 0x1p60f) {  // a NaN id is NaN either way
+    const auto q = [&](float v) { const float a = __fmul_rn(v, D.y); return __fmaf_rn(__fmaf_rn(-a, D.d, v), D.y, a); };
+    z = make_float4(q(x.x), q(x.y), q(x.z), q(x.w));
+  } else {
+    z = make_float4(__fdiv_rn(x.x, D.d), __fdiv_rn(x.y, D.d), __fdiv_rn(x.z, D.d), __fdiv_rn(x.w, D.d));
+  }
+  return make_float4(__fadd_rn(z.x, 0.0f), __fadd_rn(z.y, 0.0f), __fadd_rn(z.z, 0.0f), __fadd_rn(z.w, 0.0f));
+}
+
+// exp(x) for -86.5 <= x <= 0: own_exp_nonpos with k >= -125 (one scaling),
+// no zero clamp and no NaN
+__device__ __forceinline__ float exp_mid(float x) {
+  constexpr double kLn2 = 0.69314718055994530941723212145818;
+  constexpr float kInvLn2 = static_cast<float>(1.0 / kLn2);
+  constexpr float kLn2Hi = 0.693145751953125f;
+  constexpr float kLn2Lo = static_cast<float>(kLn2 - 0.693145751953125);
+  constexpr float kRound = 0x1.8p23f;
+  const float t = __fadd_rn(__fmul_rn(x, kInvLn2), kRound);
+  const float kf = __fsub_rn(t, kRound);
+  float r = __fmaf_rn(-kf, kLn2Hi, x);
+  r = __fmaf_rn(-kf, kLn2Lo, r);
+  float p = __fmaf_rn(r, static_cast<float>(1.0 / 5040.0), static_cast<float>(1.0 / 720.0));
+  p = __fmaf_rn(r, p, static_cast<float>(1.0 / 120.0));
+  p = __fmaf_rn(r, p, static_cast<float>(1.0 / 24.0));
+  p = __fmaf_rn(r, p, static_cast<float>(1.0 / 6.0));
+  p = __fmaf_rn(r, p, 0.5f);
+  p = __fmaf_rn(r, p, 1.0f);
+  p = __fmaf_rn(r, p, 1.0f);
+  // 2^k: k + 127 in the exponent field, k the low bits of t
+  return __fmul_rn(p, __uint_as_float((__float_as_uint(t) - (0x4B400000u - 127u)) << 23));
+}
+
+// e = exp(z - m) (1 where z == m), -1 for a NaN z
+__device__ __forceinline__ float weight_e(float z, float m) {
+  if (z != z) return -1.0f;
+  return own_exp_nonpos(z == m ? 0.0f : __fsub_rn(z, m));
+}
+
+// ---------------------------------------------------------------------------
+// The plain setting on clusters: a row's ids are split over the C CTAs of a
+// cluster, CTA c keeping ids [c S, c S + S) (S = slice) in its shared memory,
+// so the row is read from HBM once, written once, and its three passes run
+// over shared memory -- the passes of the one-CTA-per-row kernels go through
+// L2, whose traffic, not HBM, bounds them.  The row's largest z and its
+// weight total are combined across the cluster through distributed shared
+// memory.  CTAs are small (256 threads, one slice buffer) so that two or
+// three of them, from different clusters, share an SM and one's copies and
+// barriers overlap another's arithmetic.  The slice travels in two halves,
+// each on its own mbarrier: pass 1 starts on the first half while the second
+// lands, and the next row's first half is copied while pass 3 finishes the
+// second.  Each cluster takes rows cid, cid + clusters, ...; its CTAs take
+// the same rows and the same branches, so every cluster barrier is reached
+// by all of them.
+// ---------------------------------------------------------------------------
+constexpr int kCThreads = 256;
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kCSliceBytesMax = 100 * 1024;
+constexpr uint32_t kCopyWaitLimit = 1u << 24;  // polls of a slice copy's mbarrier
+
+__global__ void __launch_bounds__(kCThreads, 3)
+    probs_plain_cluster_kernel(const float* __restrict__ logits, float* __restrict__ probs, int rows, int vocab,
+                               float temperature, int slice) {
+  extern __shared__ __align__(128) float sbuf[];  // [slice]: halves [0, h) and [h, cnt)
+  __shared__ uint64_t bar[2];                     // one per half
+  __shared__ float2 s_mm[2];  // (largest z, smallest z or NaN if any z is NaN)
+  __shared__ int s_any[2];
+  __shared__ unsigned long long s_sum[2];
+  __shared__ float2 red_f[kCWarps];
+  __shared__ unsigned long long red_u[kCWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t csize = ptx::cluster_nctarank();
+  const int cid = static_cast<int>(ptx::clusterid_x()), ncl = static_cast<int>(ptx::nclusterid_x());
+  const int v0 = static_cast<int>(ptx::cluster_ctarank()) * slice;
+  const int cnt = vocab - v0 < slice ? (vocab - v0 > 0 ? vocab - v0 : 0) : slice;  // a multiple of 4
+  const int n4 = cnt >> 2;
+  const int h4 = n4 >> 1;  // float4 groups of the first half
+  float4* b4 = reinterpret_cast<float4*>(sbuf);
+  if (tid == 0) {
+    ptx::mbar_init(&bar[0], 1);
+    ptx::mbar_init(&bar[1], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  // thread 0: half hf of row r's slice into the buffer (the half's last
+  // generic reads, ordered before this thread by a CTA barrier, before the
+  // async write)
+  auto issue = [&](int r, int hf) {
+    ptx::fence_proxy_async_smem();
+    const int g0 = hf ? h4 : 0, g1 = hf ? n4 : h4;
+    if (g1 > g0) {
+      const uint32_t bytes = static_cast<uint32_t>(g1 - g0) * 16u;
+      ptx::mbar_arrive_expect_tx(&bar[hf], bytes);
+      ptx::bulk_load(b4 + g0, logits + static_cast<int64_t>(r) * vocab + v0 + 4 * g0, bytes, &bar[hf]);
+    } else {
+      ptx::mbar_arrive(&bar[hf]);
+    }
+  };
+  if (tid == 0 && cid < rows) {
+    issue(cid, 0);
+    issue(cid, 1);
+  }
+  // wait for half hf of the i-th row (every half completes one phase a row);
+  // a wait that gives up (never in correct operation) lets the copy land
+  // (bounded) and marks the half by NaN results, keeping to the protocol
+  auto land = [&](int i, int hf) {
+    const bool ok = ptx::mbar_wait(&bar[hf], i & 1, kCopyWaitLimit);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0) ptx::mbar_wait(&bar[hf], i & 1, kCopyWaitLimit);
+      for (int g = (hf ? h4 : 0) + tid; g < (hf ? n4 : h4); g += kCThreads) b4[g] = make_float4(NAN, NAN, NAN, NAN);
+      __syncthreads();
+    }
+  };
+  const Divider by_t = make_divider(temperature);
+  int i = 0;
+  for (int r = cid; r < rows; r += ncl, ++i) {
+    const int b = i & 1;  // the exchange slots alternate between rows
+    const bool next = r + ncl < rows;
+    float4* o4 = reinterpret_cast<float4*>(probs + static_cast<int64_t>(r) * vocab + v0);
+
+    // pass 1: z in place; the cluster's largest z, and its smallest (NaN if
+    // any z is NaN), which decides whether the later passes need the range
+    // checks of their fast forms
+    float m = -INFINITY, lo = INFINITY;
+    for (int hf = 0; hf < 2; ++hf) {
+      land(i, hf);
+      for (int g = (hf ? h4 : 0) + tid; g < (hf ? n4 : h4); g += kCThreads) {
+        const float4 z = scaled4(b4[g], by_t);
+        m = fmaxf(m, fmaxf(fmaxf(z.x, z.y), fmaxf(z.z, z.w)));
+        lo = min_nan(lo, min_nan(min_nan(z.x, z.y), min_nan(z.z, z.w)));
+        b4[g] = z;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+      lo = min_nan(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+    }
+    if (lane == 0) red_f[warp] = make_float2(m, lo);
+    __syncthreads();
+    if (tid == 0) {
+      float2 t = make_float2(-INFINITY, INFINITY);
+#pragma unroll
+      for (int w = 0; w < kCWarps; ++w) t = make_float2(fmaxf(t.x, red_f[w].x), min_nan(t.y, red_f[w].y));
+      s_mm[b] = t;
+    }
+    ptx::cluster_sync();
+    // lane q reads CTA q's values: the cluster's loads go out together
+    m = -INFINITY;
+    lo = INFINITY;
+    if (static_cast<uint32_t>(lane) < csize) {
+      const uint32_t a = ptx::dsmem_addr(&s_mm[b], lane);
+      m = ptx::ld_dsmem_f32(a);
+      lo = ptx::ld_dsmem_f32(a + 4);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+      lo = min_nan(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+    }
+    if (m == -INFINITY) {  // every z of the row is NaN or -inf: is any -inf?
+      int any = 0;
+      for (int g = tid; g < n4; g += kCThreads) {
+        const float4 z = b4[g];
+        any |= (z.x == z.x) | (z.y == z.y) | (z.z == z.z) | (z.w == z.w);
+      }
+      any = __syncthreads_or(any);
+      if (tid == 0) s_any[b] = any;
+      ptx::cluster_sync();
+      any = static_cast<uint32_t>(lane) < csize ? static_cast<int>(ptx::ld_dsmem_u32(ptx::dsmem_addr(&s_any[b], lane)))
+                                                 : 0;
+      if (!__any_sync(0xFFFFFFFFu, any)) {  // all NaN: a row of zeros
+        for (int g = tid; g < n4; g += kCThreads) __stcs(o4 + g, make_float4(0.f, 0.f, 0.f, 0.f));
+        __syncthreads();
+        if (tid == 0 && next) {
+          issue(r + ncl, 0);
+          issue(r + ncl, 1);
+        }
+        continue;
+      }
+    }
+
+    // pass 2: e in place (-1 for a NaN z); the cluster's weight total.  When
+    // every z is a number within 86.5 of m (and m is finite), every id takes
+    // exp's fast form with no check: RN(z - m) >= RN(lo - m) >= -86.5.
+    uint64_t part = 0;
+    const bool m_finite = fabsf(m) <= 3.4028235e38f;
+    const float spread = __fsub_rn(lo, m);  // NaN if any z is NaN
+    if (m_finite && spread >= -86.5f) {
+      for (int g = tid; g < n4; g += kCThreads) {
+        const float4 z = b4[g];
+        const float4 e = make_float4(exp_mid(__fsub_rn(z.x, m)), exp_mid(__fsub_rn(z.y, m)),
+                                     exp_mid(__fsub_rn(z.z, m)), exp_mid(__fsub_rn(z.w, m)));
+        part += weight(e.x) + weight(e.y) + weight(e.z) + weight(e.w);
+        b4[g] = e;
+      }
+    } else {
+      for (int g = tid; g < n4; g += kCThreads) {
+        const float4 z = b4[g];
+        float4 e;
+        const float4 x = make_float4(__fsub_rn(z.x, m), __fsub_rn(z.y, m), __fsub_rn(z.z, m), __fsub_rn(z.w, m));
+        if (m_finite && min_nan(min_nan(x.x, x.y), min_nan(x.z, x.w)) >= -86.5f) {
+          e = make_float4(exp_mid(x.x), exp_mid(x.y), exp_mid(x.z), exp_mid(x.w));
+          part += weight(e.x) + weight(e.y) + weight(e.z) + weight(e.w);
+        } else {
+          e = make_float4(weight_e(z.x, m), weight_e(z.y, m), weight_e(z.z, m), weight_e(z.w, m));
+          part += (e.x >= 0.0f ? weight(e.x) : 0ull) + (e.y >= 0.0f ? weight(e.y) : 0ull) +
+                  (e.z >= 0.0f ? weight(e.z) : 0ull) + (e.w >= 0.0f ? weight(e.w) : 0ull);
+        }
+        b4[g] = e;
+      }
+    }
+    part = warp_sum_u64(part);
+    if (lane == 0) red_u[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long t = 0;
+#pragma unroll
+      for (int w = 0; w < kCWarps; ++w) t += red_u[w];
+      s_sum[b] = t;
+    }
+    ptx::cluster_sync();
+    uint64_t S = static_cast<uint32_t>(lane) < csize ? ptx::ld_dsmem_u64(ptx::dsmem_addr(&s_sum[b], lane)) : 0ull;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, off);
+
+    // pass 3: the probabilities of this slice, a half at a time, each half
+    // then taking the next row's
+    // (every e >= exp(-41) > 2^-60 when the spread is within 41: no checks)
+    const Divider by_s = make_divider(__fmul_rn(__ull2float_rn(S), 0x1p-40f));
+    const bool all_fast = by_s.fast && m_finite && spread >= -41.0f;
+    for (int hf = 0; hf < 2; ++hf) {
+      for (int g = (hf ? h4 : 0) + tid; g < (hf ? n4 : h4); g += kCThreads) {
+        const float4 e = b4[g];
+        float4 p;
+        if (all_fast || (by_s.fast && fminf(fminf(e.x, e.y), fminf(e.z, e.w)) >= 0x1p-60f)) {
+          const auto q = [&](float v) {
+            const float a = __fmul_rn(v, by_s.y);
+            return __fmaf_rn(__fmaf_rn(-a, by_s.d, v), by_s.y, a);
+          };
+          p = make_float4(q(e.x), q(e.y), q(e.z), q(e.w));
+        } else {
+          const auto q = [&](float v) { return v >= 0.0f ? div_rn(v, by_s) : 0.0f; };
+          p = make_float4(q(e.x), q(e.y), q(e.z), q(e.w));
+        }
+        __stcs(o4 + g, p);
+      }
+      __syncthreads();  // the half is free
+      if (tid == 0 && next) issue(r + ncl, hf);
+    }
+  }
+  ptx::cluster_sync();  // no CTA leaves while another may still read its slots
+}
+
 // One row.  The output row doubles as scratch: pass 1 stores z there, the
 // weight pass replaces it by e (or -1 for an id that top-k or a NaN z
 // dropped), and the last pass by the probability, so later passes read a
@@ -400,13 +671,11 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
   // pass 1: z into the output row; non-NaN count and the largest z
   int n_local = 0;
   float m = -INFINITY;
+  const Divider by_t = make_divider(temperature);
   row_map<true, false, 4>(l, out, vocab, vec, [&](int64_t, float x) {
-    float z = __fdiv_rn(x, temperature);
-    if (!isnan(z)) {
-      ++n_local;
-      if (z == 0.0f) z = 0.0f;
-      m = fmaxf(m, z);
-    }
+    const float z = __fadd_rn(div_rn(x, by_t), 0.0f);  // -0 becomes +0
+    n_local += z == z;
+    m = fmaxf(m, z);  // a NaN z leaves m as it is
     return z;
   });
 #pragma unroll
@@ -551,13 +820,14 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
   }
 
   const float Sf = __fmul_rn(__ull2float_rn(S), 0x1p-40f);
+  const Divider by_s = make_divider(Sf);
   row_map<false, true>(out, out, vocab, vec, [&](int64_t v, float e) {
     bool keep = e >= 0.0f;
     if (keep && topp) {
       const uint64_t w = weight(e);
       keep = w > p_w || (w == p_w && v <= p_id);
     }
-    return keep ? __fdiv_rn(e, Sf) : 0.0f;
+    return keep ? div_rn(e, by_s) : 0.0f;
   });
 }
 
@@ -574,6 +844,57 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+constexpr int kAttrMaxDevices = 64;
+std::atomic<unsigned long long> g_cluster_attr_ctx[kAttrMaxDevices];
+
+// The cluster kernel's shared-memory limit, set once per device context.
+bool cluster_attr_ready(int device) {
+  if (device < 0 || device >= kAttrMaxDevices) return false;
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && g_cluster_attr_ctx[device].load(std::memory_order_acquire) == ctx) return true;
+  if (cudaFuncSetAttribute(probs_plain_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kCSliceBytesMax) != cudaSuccess)
+    return false;
+  g_cluster_attr_ctx[device].store(ctx, std::memory_order_release);
+  return true;
+}
+
+// The plain setting on clusters; false when that does not apply (a
+// vocabulary of more than 8 slices, or no cluster fits), and the caller
+// takes the one-CTA-per-row kernel.
+bool launch_plain_cluster(const float* logits, float* probs, int rows, int vocab, float temperature, int device,
+                          cudaStream_t stream, int* rc) {
+  int C = 1, slice = 0;
+  for (; C <= 8; C *= 2) {
+    slice = ((vocab + C - 1) / C + 3) & ~3;
+    if (slice * 4 <= kCSliceBytesMax) break;
+  }
+  if (C > 8 || !cluster_attr_ready(device)) return false;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kCThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(slice) * 4;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(C);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, probs_plain_cluster_kernel, &cfg) != cudaSuccess || clusters < 1) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  cfg.gridDim = dim3((rows < clusters ? rows : clusters) * C);
+  *rc = cudaLaunchKernelEx(&cfg, probs_plain_cluster_kernel, logits, probs, rows, vocab, temperature, slice) ==
+                cudaSuccess
+            ? DSPARK_OK
+            : DSPARK_ERR_CUDA;
+  return true;
+}
+
 }  // namespace
 }  // namespace dspark
 
@@ -586,6 +907,11 @@ extern "C" int dspark_logits_to_probs(const float* logits, float* probs, int32_t
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   const int grid = rows < sms ? rows : sms;
+  const bool vec = (vocab & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs)) & 15u) == 0;
+  if (vec && temperature > 0.0f && !(top_k > 0 && top_k < vocab) && !(top_p < 1.0f)) {
+    int rc = DSPARK_OK;
+    if (dspark::launch_plain_cluster(logits, probs, rows, vocab, temperature, dev, stream, &rc)) return rc;
+  }
   dspark::logits_probs_kernel<<<grid, dspark::kThreads, 0, stream>>>(logits, probs, rows, vocab, temperature, top_k,
                                                                      top_p);
   return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;

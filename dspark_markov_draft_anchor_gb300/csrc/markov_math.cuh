@@ -106,6 +106,9 @@ __device__ __forceinline__ float own_tanhf(float z) {
 // so k * hi is exact for |k| < 2^8) and the Taylor series of exp to degree 7
 // on |r| <= ln2/2.  NaN propagates, below -104 gives 0, and 2^k scales the
 // polynomial exactly (k >= -125) or with one rounding into the subnormals.
+// k = rint(RN(x / ln2)) comes from adding and removing 1.5 2^23, which
+// rounds to an integer with ties to even as rint does (|x / ln2| < 2^22),
+// and leaves k in the low bits of the sum.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float own_exp_nonpos(float x) {
   constexpr double kLn2 = 0.69314718055994530941723212145818;
@@ -118,9 +121,11 @@ __device__ __forceinline__ float own_exp_nonpos(float x) {
   constexpr float kC5 = static_cast<float>(1.0 / 120.0);
   constexpr float kC6 = static_cast<float>(1.0 / 720.0);
   constexpr float kC7 = static_cast<float>(1.0 / 5040.0);
+  constexpr float kRound = 0x1.8p23f;
   if (isnan(x)) return x;
   if (x < -104.0f) return 0.0f;
-  const float kf = rintf(__fmul_rn(x, kInvLn2));
+  const float t = __fadd_rn(__fmul_rn(x, kInvLn2), kRound);
+  const float kf = __fsub_rn(t, kRound);
   float r = __fmaf_rn(-kf, kLn2Hi, x);
   r = __fmaf_rn(-kf, kLn2Lo, r);
   float p = __fmaf_rn(r, kC7, kC6);
@@ -130,9 +135,41 @@ __device__ __forceinline__ float own_exp_nonpos(float x) {
   p = __fmaf_rn(r, p, kC2);
   p = __fmaf_rn(r, p, 1.0f);
   p = __fmaf_rn(r, p, 1.0f);
-  const int k = static_cast<int>(kf);  // in [-150, 0]
+  const int k = static_cast<int>(__float_as_uint(t) - 0x4B400000u);  // in [-150, 0]
   if (k >= -125) return __fmul_rn(p, __int_as_float((k + 127) << 23));
   return __fmul_rn(__fmul_rn(p, __int_as_float((k + 64 + 127) << 23)), 0x1p-64f);
+}
+
+// ---------------------------------------------------------------------------
+// Correctly rounded division by one divisor d, many dividends: with
+// y = RN(1/d), q = RN(x y) is a faithful quotient, the remainder x - q d is
+// exact (one fma) and RN(q + (x - q d) y) is RN(x / d) -- P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990 -- provided nothing overflows or
+// underflows.  `fast` holds for 2^-20 <= |d| < 2^40; the quotient is taken
+// that way for 2^-60 <= |x| < 2^60 (remainders stay multiples of 2^-146,
+// quotients normal), by the IEEE division otherwise.
+// ---------------------------------------------------------------------------
+struct Divider {
+  float d, y;
+  bool fast;
+};
+
+__device__ __forceinline__ Divider make_divider(float d) {
+  const uint32_t a = __float_as_uint(d) & 0x7FFFFFFFu;
+  // 2^-20 has exponent field 107, 2^40 has 167
+  return Divider{d, __frcp_rn(d), a >= (107u << 23) && a < (167u << 23)};
+}
+
+__device__ __forceinline__ float div_rn(float x, const Divider& D) {
+  const uint32_t a = __float_as_uint(x) & 0x7FFFFFFFu;
+  // 2^-60 has exponent field 67, 2^60 has 187
+  if (D.fast && a - (67u << 23) < (120u << 23)) {
+    const float q = __fmul_rn(x, D.y);
+    const float r = __fmaf_rn(-q, D.d, x);
+    return __fmaf_rn(r, D.y, q);
+  }
+  return __fdiv_rn(x, D.d);
 }
 
 // ---------------------------------------------------------------------------

@@ -491,7 +491,9 @@ DSPARK_API int dspark_probabilistic_accept(const float *target_probs, const floa
  *     0 elsewhere.
  * Every decision is an exact comparison (readings: the pages name the three
  * filters only).  rows >= 0, vocab >= 1.  Allocates nothing; one kernel on
- * `stream` (one CTA per row).
+ * `stream`: without top-k and top-p (temperature > 0), with 16-byte-aligned
+ * rows and vocab a multiple of 4 up to 8 x 25600, a cluster of CTAs holds
+ * each row in shared memory; otherwise one CTA per row.
  */
 DSPARK_API int dspark_logits_to_probs(const float *logits, float *probs, int32_t rows, int32_t vocab,
                                       float temperature, int32_t top_k, float top_p, cudaStream_t stream);

@@ -41,6 +41,22 @@ DSPARK_API int dspark_check_key(const float *l, float temp, const uint32_t *h, f
 DSPARK_API int dspark_check_logf(const float *x, float *y, int64_t n, cudaStream_t stream);
 DSPARK_API int dspark_check_tanhf(const float *x, float *y, int64_t n, cudaStream_t stream);
 
+/* own exp of the library for x <= 0 (the logits-to-probabilities weights and
+ * the confidence logistic), elementwise. */
+DSPARK_API int dspark_check_expf(const float *x, float *y, int64_t n, cudaStream_t stream);
+
+/* The library's division by one divisor (a correctly rounded reciprocal, the
+ * quotient and one remainder correction -- Markstein's method -- in the range
+ * where that is exact, the IEEE division elsewhere): y[i] = x[i] / d. */
+DSPARK_API int dspark_check_div(const float *x, float d, float *y, int64_t n, cudaStream_t stream);
+
+/* The same division against the IEEE quotient for every float whose bits lie
+ * in [lo, lo + n) (n <= 2^32, wrapping): adds to out[0] the number whose bits
+ * differ (two NaNs agree) and lowers out[1] to the smallest such bit
+ * pattern.  out: two device words the caller sets to 0 and ~0 first. */
+DSPARK_API int dspark_check_div_sweep(float d, uint32_t lo, int64_t n, unsigned long long *out,
+                                      cudaStream_t stream);
+
 /* The step kernel's bounds of the Gumbel noise -L(h), which let it skip
  * elements that cannot be the argmax (no counterpart in the pages: the pages
  * evaluate every key).  Host code only, no GPU and no stream: fills HOST

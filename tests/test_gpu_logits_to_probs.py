@@ -128,3 +128,27 @@ def test_scaled_logit_ties_decide_top_k_like_the_oracle(T):
     got = _gpu(rows, T, 1, 1.0)
     assert np.array_equal(np.argmax(got, axis=1), kept)
     _check(rows, T, 1, 1.0)
+
+
+@pytest.mark.parametrize("rows,V,T", [(1, 100, 1.0), (200, 32768, 0.7), (500, 1000, 1.3), (24, 163840, 1.0),
+                                      (9, 100004, 0.9), (5, 51204, 1e-30), (4, 250000, 1.0), (3, 129281, 1.0)])
+def test_plain_setting_on_clusters(rows, V, T):
+    """The plain setting (no top-k, no top-p) runs on clusters of CTAs that
+    split each row across their shared memory (one to eight slices, the next
+    row prefetched while this one is processed); a vocabulary too large for
+    that, or not a multiple of 4, takes the one-CTA-per-row kernel."""
+    rng = np.random.default_rng(rows + V)
+    l = _logits(rng, rows, V, 2.5)
+    if rows > 3:
+        l[0, V // 2:] = np.nan                   # the maximum in an early slice
+        l[1, :] = -np.inf                        # all -inf: uniform over the row
+        l[2, :] = np.nan                         # all NaN: zeros
+        l[3, [V - 1, 5]] = np.inf                # infinite logits at both ends
+    _check(l, T, 0, 1.0)
+    _check(l, T, V + 1, float("nan"))            # settings that mean "no filter"
+
+
+def test_plain_setting_in_place_on_clusters():
+    rng = np.random.default_rng(23)
+    l = _logits(rng, 40, 129280, 2.5)
+    _check(l, 0.8, 0, 1.0, in_place=True)

@@ -105,3 +105,61 @@ def test_own_log_and_tanh_match_oracle_bitwise():
     got, want = t_d.cpu().numpy(), oracle.tanhf(z)
     same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
     assert same.all()
+
+
+def test_own_exp_matches_oracle_bitwise():
+    """The library's exp of x <= 0 (probability weights, the confidence
+    logistic) equals the oracle's: every float in [-2^-20, 0] stepping
+    through the bit patterns, a dense sweep of [-104, -2^-20], the
+    subnormal-result range and the special values."""
+    rng = np.random.default_rng(5)
+    neg = lambda lo, hi, step: (np.arange(lo, hi, step, dtype=np.uint64).astype(np.uint32)).view(np.float32)
+    x = np.concatenate([
+        neg(0x80000000, 0xB5800000, 4093),        # -0 .. -2^-20
+        neg(0xB5800000, 0xC2D00001, 7),           # -2^-20 .. -104
+        -rng.uniform(86.0, 104.0, 1 << 20).astype(np.float32),  # results subnormal or zero
+        np.float32([0.0, -0.0, -np.inf, -104.0, -103.99999, -104.00001, -87.33654, -1e-45, np.nan]),
+    ])
+    x_d = torch.from_numpy(x).cuda()
+    y_d = torch.empty_like(x_d)
+    binding.dspark_check_expf(x_d, y_d, x.size)
+    got = y_d.cpu().numpy()
+    want = _par(oracle.expf_nonpos, x)
+    same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), x[~same][:5]
+
+
+# Divisors for the division check: temperatures, ones whose significand is
+# all ones or has a single low bit, powers of two, the fast range's ends,
+# probability-sum scales, and seeded random ones.
+DIVISORS = [0.7, 0.8, 3.0, 1.0, 0.1, 0.3, 1.5, 7.0, 1e-3, 2.5, 1 - 2.0**-24, 1 + 2.0**-23, 2 - 2.0**-23,
+            1.75 - 2.0**-22, 2.0**-20, 2.0**-20 * (1 + 2.0**-23), 2.0**40 * (1 - 2.0**-24), 2.0**-21, 2.0**41,
+            12345.678, 129279.98, 3.3e9, 1e-7, 65536.0]
+
+
+def test_division_matches_numpy_ieee_quotient():
+    """div_rn over random dividends (and the special ones) against numpy's
+    float32 quotient, which IEEE 754 fixes."""
+    rng = np.random.default_rng(6)
+    x = np.concatenate([(rng.standard_normal(1 << 18) * 2.5).astype(np.float32),
+                        rng.integers(0, 2**32, 1 << 18, dtype=np.uint64).astype(np.uint32).view(np.float32),
+                        np.float32([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, 3.4e38, 2.0**-60, 2.0**60])])
+    x_d = torch.from_numpy(x).cuda()
+    y_d = torch.empty_like(x_d)
+    with np.errstate(all="ignore"):
+        for d in DIVISORS:
+            d32 = np.float32(d)
+            binding.dspark_check_div(x_d, float(d32), y_d, x.size)
+            got, want = y_d.cpu().numpy(), x / d32
+            same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+            assert same.all(), (d, x[~same][:5])
+
+
+@pytest.mark.parametrize("d", DIVISORS + list(np.random.default_rng(7).uniform(0.05, 20.0, 24)))
+def test_division_exhaustive_against_ieee(d):
+    """Every one of the 2^32 dividends: the division with the reciprocal
+    and one remainder correction gives the IEEE quotient's bits."""
+    out = torch.tensor([0, -1], dtype=torch.int64, device="cuda")
+    binding.dspark_check_div_sweep(float(np.float32(d)), 0, 1 << 32, out)
+    bad, first = out.cpu().numpy().view(np.uint64)
+    assert bad == 0, (d, int(bad), hex(int(first)))
