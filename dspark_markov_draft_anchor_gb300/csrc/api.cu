@@ -31,6 +31,10 @@ struct dspark_markov_ctx {
   bool tc8_ok;                // TMA maps over the E4M3 w2 encoded: the tensor-core step can read it
   CUtensorMap w2f8_map;       // boxes of 32 rows x 128 K bytes, 128-byte swizzle
   CUtensorMap w2f8_tile_map;  // the same with boxes of 128 rows
+  // The slots, counters and abort word are as the anchor leaves them (zero):
+  // a one-launch loop then needs no anchor launch, and leaves them so again.
+  // Any other launch on them, or a reported device error, clears this.
+  bool state_clean;
 };
 
 namespace {
@@ -112,6 +116,9 @@ dspark::StepParams make_params(const dspark_markov_ctx* ctx, const dspark_markov
   p.sharded = 0;
   p.vocab_offset = 0;
   p.packets = nullptr;
+  p.self_reset = 0;
+  p.input_ids = a->input_ids;
+  p.anchor_idx = a->anchor_idx;
   return p;
 }
 
@@ -277,6 +284,7 @@ int dspark_markov_anchor(dspark_markov_ctx* ctx, const dspark_markov_loop_args* 
                             ctx->counters + ctx->cfg.max_steps, a->rows, a->steps, ctx->cfg.max_rows,
                             stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
+  ctx->state_clean = true;
   return DSPARK_OK;
 }
 
@@ -336,6 +344,7 @@ int dspark_markov_step(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
   int rc = check_args(ctx, a);
   if (rc != DSPARK_OK) return rc;
   if (step < 0 || step >= a->steps) return DSPARK_ERR_INVALID_ARG;
+  ctx->state_clean = false;
   return launch_step(ctx, a, step, false, stream);
 }
 
@@ -349,6 +358,7 @@ int dspark_markov_shard_step(dspark_markov_ctx* ctx, const dspark_markov_loop_ar
   const int32_t path = dspark_markov_bias_path(ctx, a->rows);
   if (path != 1 && path != 3) return DSPARK_ERR_INVALID_ARG;  // the tensor-core step only
   if (!tma_base_ok(a)) return DSPARK_ERR_MISALIGNED;
+  ctx->state_clean = false;
   dspark::StepParams p = make_params(ctx, a, step);
   p.sharded = 1;
   p.vocab_offset = vocab_offset;
@@ -373,6 +383,7 @@ int dspark_markov_pick(dspark_markov_ctx* ctx, const int32_t* packets, int32_t t
   if (tokens_s0 <= step) return DSPARK_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(packets) & 15u) return DSPARK_ERR_MISALIGNED;
   unsigned long long* slot_next = ctx->slots + static_cast<int64_t>(step + 1) * ctx->cfg.max_rows;
+  ctx->state_clean = false;
   return dspark::launch_pick(packets, tp, rows, tokens, tokens_s0, step, slot_next, stream) == cudaSuccess
              ? DSPARK_OK
              : DSPARK_ERR_CUDA;
@@ -380,18 +391,29 @@ int dspark_markov_pick(dspark_markov_ctx* ctx, const int32_t* packets, int32_t t
 
 int32_t dspark_markov_loop_kernels(const dspark_markov_ctx* ctx, const dspark_markov_loop_args* a) {
   if (check_args(ctx, a) != DSPARK_OK) return 0;
-  if (loop_fused(ctx, a)) return 2;
-  return 1 + a->steps * ((ctx->cfg.flags & DSPARK_FLAG_SELECT_2LAUNCH) ? 2 : 1);
+  const int32_t lut = a->cap != 0.0f ? 1 : 0;
+  if (loop_fused(ctx, a)) return (ctx->state_clean ? 1 : 2) + lut;
+  return 1 + lut + a->steps * ((ctx->cfg.flags & DSPARK_FLAG_SELECT_2LAUNCH) ? 2 : 1);
 }
 
 int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a, cudaStream_t stream) {
-  int rc = dspark_markov_anchor(ctx, a, stream);
+  int rc = check_args(ctx, a);
   if (rc != DSPARK_OK) return rc;
-  if (loop_fused(ctx, a)) {
+  const bool fused = loop_fused(ctx, a);
+  if (fused && ctx->state_clean) {
+    // the loop state is zero: no anchor launch (the soft cap's table only)
+    if (a->cap != 0.0f && dspark::launch_xform_lut(ctx->xform_lut, a->mult, a->cap, stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  } else {
+    rc = dspark_markov_anchor(ctx, a, stream);
+    if (rc != DSPARK_OK) return rc;
+  }
+  if (fused) {
     // every step in one cooperative launch; the last CTA to arrive at the
-    // last step writes its tokens
+    // last step writes its tokens and leaves the loop state zero
     dspark::StepParams p = make_params(ctx, a, 0);
     p.step_end = a->steps;
+    p.self_reset = 1;
     const bool pdl = (ctx->cfg.flags & DSPARK_FLAG_PDL) != 0;
     const bool fp8 = dspark_markov_bias_path(ctx, a->rows) == 3;
     if (fp8) p.w2_scale = ctx->w2_scale;
@@ -399,10 +421,18 @@ int dspark_markov_loop(dspark_markov_ctx* ctx, const dspark_markov_loop_args* a,
                                                        true, stream, true)
                               : dspark::launch_step_tc(p, ctx->w2_map, ctx->w2_tile_map, ctx->grid_tc, pdl, true,
                                                        stream);
-    if (e == cudaSuccess) return DSPARK_OK;
+    if (e == cudaSuccess) {
+      ctx->state_clean = true;
+      return DSPARK_OK;
+    }
+    ctx->state_clean = false;
     if (e != cudaErrorInvalidValue) return DSPARK_ERR_CUDA;
-    // the base strides do not form the multi-step tensor map: step by step
+    // the base strides do not form the multi-step tensor map: step by step,
+    // from the anchor's previous tokens
+    rc = dspark_markov_anchor(ctx, a, stream);
+    if (rc != DSPARK_OK) return rc;
   }
+  ctx->state_clean = false;
   for (int s = 0; s < a->steps; ++s) {
     rc = launch_step(ctx, a, s, true, stream);
     if (rc != DSPARK_OK) return rc;
@@ -416,6 +446,9 @@ int dspark_markov_get_status_detail(dspark_markov_ctx* ctx, cudaStream_t stream,
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   if (cudaMemcpy(v, ctx->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DSPARK_ERR_CUDA;
   if (cudaMemset(ctx->status, 0, sizeof(v)) != cudaSuccess) return DSPARK_ERR_CUDA;
+  // a loop that gave up left its slots, counters and abort word set: the
+  // next loop starts from the anchor
+  if (v[0] != 0) ctx->state_clean = false;
   for (int i = 0; i < 4; ++i) detail[i] = v[i];
   return DSPARK_OK;
 }

@@ -55,7 +55,7 @@ struct StepParams {
   int64_t base_s1;
   int64_t cache_s1;
   int64_t slots_s;            // elements between consecutive steps' argmax slots
-  unsigned int* abort_word;   // set by a CTA whose bounded wait gave up; cleared by the anchor
+  unsigned int* abort_word;   // set by a CTA whose bounded wait gave up; cleared by the anchor kernel
   // Two-launch select: each CTA writes its row maxima to partials[r * grid +
   // block] and a separate select launch reduces them (null: one atomicMax per
   // row into slots_out).
@@ -75,6 +75,14 @@ struct StepParams {
   int32_t sharded;
   int64_t vocab_offset;
   int32_t* packets;
+  // One-launch loop without the anchor launch: step 0's previous tokens are
+  // read from input_ids[anchor_idx[r]], and the loop leaves its slots and
+  // counters zero for the next call (the last CTA to arrive at step j >= 1
+  // clears step j - 1's counter and the slots step j read; at the last step
+  // it clears the rest after writing the tokens).
+  int32_t self_reset;
+  const int32_t* input_ids;
+  const int64_t* anchor_idx;
 };
 
 // PTX griddepcontrol (programmatic dependent launch): wait for the grids this

@@ -92,7 +92,7 @@ struct TcLayout {
   int res_tiles; // w2 tiles kept in tensor memory as the MMA's A operand after the first step
   int res_col;   // their first column (128 columns a tile)
   int smem;      // dynamic shared memory bytes (0: the layout does not fit)
-  int emb_off, w2_off, f16_off, base_off, bar_off, row_off, queue_off;
+  int emb_off, w2_off, f16_off, base_off, bar_off, row_off, queue_off, scale_off;
 };
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -117,6 +117,9 @@ constexpr int kRowKs = kRowLtab + 4 * kNoiseT;                      // f32 E4M3 
 constexpr int kRowBytes = kRowKs + 4 * kMaxRows;
 
 constexpr int kSmemBudget = 232448 - 64;  // 227 KB less the static shared variables
+// E4M3 w2: the FP16 row scales of a CTA's vocabulary range are kept in shared
+// memory when the range has at most this many rows (every step reads them)
+constexpr int kScaleRowsMax = 2048;
 
 // Shared memory of one CTA.  BF16 w2: the rest of the budget goes to the w2
 // ring (at most 12 stages).  E4M3 w2: four FP16 operand stages (two per MMA
@@ -138,7 +141,7 @@ TcLayout tc_layout(int rows, bool fp8 = false) {
   L.nbase = (L.n > kChunkRows && L.n < 128) ? 8 : (L.n == kChunkRows ? 6 : 4);
   const int bars_max = 8 * (2 * 12 + 4 + 2 * L.nbase + 2 * 8 + 3);
   const int fixed = L.n * kRank * 2 + L.nbase * kChunkBytes + bars_max + 16 + kRowBytes + kEpiWarps * kQCap * 8 +
-                    1024 + 64;
+                    (fp8 ? kScaleRowsMax * 2 : 0) + 1024 + 64;
   const int avail = (kSmemBudget - fixed) / kW2StageBytes;  // 16 KB stages that fit
   L.smem = 0;
   if (!fp8) {
@@ -169,6 +172,8 @@ TcLayout tc_layout(int rows, bool fp8 = false) {
   off = (off + 15) & ~15;
   L.queue_off = off;
   off += kEpiWarps * kQCap * 8;
+  L.scale_off = off;
+  if (fp8) off += kScaleRowsMax * 2;
   L.smem = off + 1024;  // room to align the base to 1024 bytes
   return L;
 }
@@ -183,7 +188,7 @@ struct TcParams {
   int32_t tmem_cols;
   int32_t res_tiles;  // the CTA's last res_tiles tiles stay in tensor memory from the second step on
   int32_t res_col;
-  int32_t emb_off, w2_off, f16_off, base_off, bar_off, row_off, queue_off;
+  int32_t emb_off, w2_off, f16_off, base_off, bar_off, row_off, queue_off, scale_off;
   int32_t num_units;  // ceil(V / 32)
   int32_t base_steps_mid;  // base tensor map dims are (vocab, step, row), else (vocab, row, step)
 };
@@ -241,6 +246,7 @@ struct Shared {
   float* ltab;      // the computed noise is never below ltab[noise_index(h)]
   float* kscale;    // E4M3 w2: per row, 2^-k undoing the FP16 embedding's power-of-two scaling
   Cand* queues;
+  uint16_t* w2s;       // E4M3 w2: the FP16 scales of the CTA's rows (range of at most kScaleRowsMax rows)
   uint32_t id_offset;  // the global id of local vocabulary id 0 (a vocabulary shard's offset; else 0)
 };
 
@@ -510,6 +516,7 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
   sh.ltab = reinterpret_cast<float*>(rowreg + kRowLtab);
   sh.kscale = reinterpret_cast<float*>(rowreg + kRowKs);
   sh.queues = reinterpret_cast<Cand*>(smem + tp.queue_off);
+  sh.w2s = reinterpret_cast<uint16_t*>(smem + tp.scale_off);
   sh.id_offset = static_cast<uint32_t>(p.vocab_offset);
 
   // This CTA's vocabulary range.
@@ -908,7 +915,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         const int r = idx >> 5, ch = idx & 31;  // a warp takes one row
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (r < p.rows) {
-          const int64_t tok = slot_token(__ldcg(prev + r));
+          const int64_t tok = st == 0 && p.self_reset ? static_cast<int64_t>(__ldg(p.input_ids + __ldg(p.anchor_idx + r)))
+                                                      : slot_token(__ldcg(prev + r));
           const uint64_t row = static_cast<uint64_t>(tok) < last_row ? static_cast<uint64_t>(tok) : last_row;
           val = ldg_nc_v4(p.w1 + row * kRank + ch * 8);
           if (write_prev && ch == 0) p.tokens[static_cast<int64_t>(r) * p.tokens_s0 + prev_step] = tok;
@@ -946,6 +954,11 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       sh.gtab[t] = c_noise_ub[t];
       sh.ltab[t] = c_noise_lb[t];
     }
+    // E4M3 w2: the range's row scales, read by every step (a weight table:
+    // no wait on the previous launch); published by gather's barrier
+    const bool w2s_local = kFp8 && v_end - v_begin <= kScaleRowsMax;
+    if (w2s_local)
+      for (int t = et; t < v_end - v_begin; t += kEpiThreads) sh.w2s[t] = __ldg(p.w2_scale + v_begin + t);
     pdl_wait();
     gather(0);
 
@@ -963,7 +976,8 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
         const bool in = v < v_end;
         const uint32_t kv = murmur_kmix(static_cast<uint32_t>(v) + sh.id_offset);  // the global id
         float w2s = 0.0f;  // E4M3 w2: this vocabulary row's FP16 scale (read while the tile's MMAs run)
-        if constexpr (kFp8) w2s = in ? __half2float(__ushort_as_half(__ldg(p.w2_scale + v))) : 0.0f;
+        if constexpr (kFp8)
+          w2s = in ? __half2float(__ushort_as_half(w2s_local ? sh.w2s[v - v_begin] : __ldg(p.w2_scale + v))) : 0.0f;
         ok = __all_sync(0xFFFFFFFFu, wait(&sh.tmem_full[b], (j / NA) & 1, 6, (st << 24) | (i << 12)));
         if (!ok) break;
         ptx::tc_fence_after();
@@ -1200,13 +1214,22 @@ step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constan
       if (et == 0) {
         __threadfence();
         s_last = atomicAdd(p.counter + st, 1u) == static_cast<unsigned int>(G - 1);
+        if (p.self_reset && s_last && st > 0) {
+          // every CTA is past step st - 1's grid wait and has read the slots
+          // of step st's previous tokens: clear both for the next call
+          p.counter[st - 1] = 0u;
+          unsigned long long* used = p.slots_out + static_cast<int64_t>(st - 1) * p.slots_s;
+          for (int r = 0; r < p.rows; ++r) used[r] = 0ull;
+        }
       }
       if (last) {
         ptx::named_bar_sync(1, kEpiThreads);
         if (s_last) {
           __threadfence();
+          if (p.self_reset && et == 0) p.counter[st] = 0u;
           for (int r = et; r < p.rows; r += kEpiThreads) {
             const unsigned long long sv = atomicAdd(out + r, 0ull);
+            if (p.self_reset) out[r] = 0ull;
             if (p.packets) {  // a rank of a sharded loop: its winner's packet ([P3] _finish)
               const int4 pk = make_int4(static_cast<int>(key_bits(static_cast<uint32_t>(sv >> 32))),
                                         static_cast<int>(static_cast<int64_t>(p.vocab_offset) + slot_token(sv)), 0, 0);
@@ -1494,6 +1517,7 @@ cudaError_t launch_step_tc(const StepParams& p, const CUtensorMap& w2_map, const
   tp.bar_off = L.bar_off;
   tp.row_off = L.row_off;
   tp.queue_off = L.queue_off;
+  tp.scale_off = L.scale_off;
   tp.num_units = static_cast<int32_t>((p.vocab + kUnit - 1) / kUnit);
   tp.base_steps_mid = steps_mid ? 1 : 0;
 

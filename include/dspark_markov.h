@@ -149,11 +149,18 @@ typedef struct {
  * MurmurHash3 noise of (seed, step, position + salt, vocab id), and a
  * total-order argmax (first NaN, else lowest id of the maximum).  The
  * winner is tokens[r, s] and the next step's previous token.
- * Enqueues the anchor kernel, then either one launch for all steps (tensor-
- * core path, steps > 1, TMA-readable base, a cooperative launch possible and
- * DSPARK_FLAG_PER_STEP not set: its CTAs, all resident at once, wait for one
- * another between steps with bounded waits) or one launch per step; see
- * dspark_markov_loop_kernels.  No host synchronisation.
+ * Enqueues either one launch for all steps (tensor-core path, steps > 1,
+ * TMA-readable base, a cooperative launch possible and DSPARK_FLAG_PER_STEP
+ * not set: its CTAs, all resident at once, wait for one another between
+ * steps with bounded waits) or the anchor kernel and one launch per step;
+ * with a soft cap, the cap's table kernel first.  The one-launch loop reads
+ * step 0's previous tokens itself and leaves the context's argmax slots and
+ * step counters zero, so it needs the anchor kernel only when something
+ * else used them last (the context's first call, a per-step, sharded or
+ * select launch, or a device error read by dspark_markov_get_status*); see
+ * dspark_markov_loop_kernels.  After a device error that nobody has read,
+ * later loops on the context give up at once (the error stays recorded).
+ * No host synchronisation.
  */
 DSPARK_API int dspark_markov_loop(dspark_markov_ctx *ctx, const dspark_markov_loop_args *args,
                        cudaStream_t stream);
@@ -246,10 +253,12 @@ DSPARK_API int dspark_cache_fill(const void *src, int64_t src_s0, void *cache, i
                                  const int64_t *req_idx, int64_t req_s0, int64_t num_req, int32_t rows,
                                  int32_t steps, int32_t shard, int32_t tp, int32_t vocab, cudaStream_t stream);
 
-/* The number of kernels dspark_markov_loop enqueues for `args` (2 when one
- * launch runs every step, 1 + 2 steps with DSPARK_FLAG_SELECT_2LAUNCH, else
- * 1 + steps); 0 if the arguments are invalid.
- * No counterpart in the pages: it tells a caller what a captured loop holds. */
+/* The number of kernels dspark_markov_loop would enqueue now for `args`:
+ * when one launch runs every step, 1 (2 if the anchor is needed first, see
+ * dspark_markov_loop); else 1 + 2 steps with DSPARK_FLAG_SELECT_2LAUNCH, else
+ * 1 + steps; plus 1 with a soft cap (its table); 0 if the arguments are
+ * invalid.  No counterpart in the pages: it tells a caller what a captured
+ * loop holds. */
 DSPARK_API int32_t dspark_markov_loop_kernels(const dspark_markov_ctx *ctx, const dspark_markov_loop_args *args);
 
 /* Synchronise `stream`, then read and clear the device status word: 0, or a

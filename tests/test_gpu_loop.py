@@ -8,13 +8,16 @@ only the summation order of the bias differs):
     (outside that, within the FP32 accumulation bound), and end to end the
     tokens must agree wherever the oracle's top-2 noised margin exceeds 1e-2.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from dspark_markov_draft_anchor_gb300 import binding, workloads
-from tests.gpu_util import (GpuLoop, assert_bf16_equal, check_bias, check_end_to_end, graph_run, oracle_run)
+from tests.gpu_util import (GpuLoop, assert_bf16_equal, bf16_dev, check_bias, check_end_to_end, dev, graph_run,
+                            oracle_run)
 
 pytestmark = pytest.mark.gpu
 
@@ -263,3 +266,69 @@ def test_argument_errors_are_reported_not_launched():
             binding.MarkovContext(g.w1, g.w2, max_rows=4, max_steps=3)
     assert e.value.code == -5
     assert g.ctx.status() == 0
+
+
+def test_fused_loop_leaves_its_state_zero_for_the_next_call():
+    """After the first call (anchor + loop) the one-launch loop runs without
+    the anchor launch: it reads step 0's previous tokens itself and leaves its
+    slots and counters zero.  Repeated calls, graph replays with new inputs
+    between them, and a per-step launch in between (which brings the anchor
+    back for one call) all stay bit-exact in fed mode."""
+    wl = _small("large16", 8192 + 8, 16, 4, salt=41)
+    g = GpuLoop(wl)
+    cache = torch.zeros((wl.num_req, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
+    tokens = torch.full((wl.rows, wl.steps), -9, dtype=torch.int64, device="cuda")
+    bias = torch.empty((wl.rows, wl.steps, wl.vocab), dtype=torch.int16, device="cuda")
+    a = g.args(cache, tokens, bias)
+    assert g.ctx.loop_kernels(a) == 2  # a fresh context: the anchor first
+
+    def check(w):
+        torch.cuda.synchronize()
+        assert g.ctx.status() == 0
+        gpu = {"tokens": tokens.cpu().numpy(), "cache": cache.cpu().numpy().view(np.uint16),
+               "bias": bias.cpu().numpy().view(np.uint16)}
+        _fed_parity(w, gpu)
+
+    g.ctx.loop(a)
+    check(wl)
+    assert g.ctx.loop_kernels(a) == 1  # the state is zero: one launch
+    def renewed(salt):  # the same tables and shapes, new base logits, seeds and previous tokens
+        o = _small("large16", 8192 + 8, 16, 4, salt=salt)
+        return dataclasses.replace(wl, base=o.base, seeds=o.seeds, input_ids=o.input_ids % wl.vocab)
+
+    for salt in (42, 43):
+        w = renewed(salt)
+        g.base.copy_(bf16_dev(w.base))
+        g.seeds.copy_(dev(w.seeds))
+        g.input_ids.copy_(dev(w.input_ids))
+        g.wl = w
+        tokens.fill_(-9)
+        g.ctx.loop(a)
+        check(w)
+
+    # captured once, replayed with new inputs each time
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.ctx.loop(a, s)
+    torch.cuda.synchronize()
+    for salt in (44, 45, 46):
+        w = renewed(salt)
+        g.base.copy_(bf16_dev(w.base))
+        g.seeds.copy_(dev(w.seeds))
+        g.input_ids.copy_(dev(w.input_ids))
+        g.wl = w
+        tokens.fill_(-9)
+        graph.replay()
+        check(w)
+
+    # a per-step launch leaves counters behind: the next loop runs the anchor
+    g.ctx.step(a, 0)
+    torch.cuda.synchronize()
+    assert g.ctx.loop_kernels(a) == 2
+    tokens.fill_(-9)
+    g.ctx.loop(a)
+    check(g.wl)
+    assert g.ctx.loop_kernels(a) == 1
