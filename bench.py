@@ -677,7 +677,7 @@ def run_prob_verify(args, d: Dist):
 
 
 L2P_ROWS, L2P_V = PV_B * (PV_P + 1), PV_V  # the verify's target shape [256, 6, 129280] as rows
-L2P_SOURCES = ("logits_probs.cu", "markov_math.cuh")
+L2P_SOURCES = ("logits_probs.cu", "markov_math.cuh", "ptx.cuh", "kernels.h")
 L2P_SETTINGS = {"plain": (1.0, 0, 1.0), "filtered": (0.8, 50, 0.95)}
 
 
@@ -937,7 +937,7 @@ def run_greedy_accept(args, d: Dist):
 
 
 CF_B, CF_P = 256, 5  # confidence head: the stress batch's 256 requests x 5 drafts
-CF_SOURCES = ("confidence.cu", "markov_math.cuh")
+CF_SOURCES = ("confidence.cu", "markov_math.cuh", "ptx.cuh")
 CF_WORKLOAD = f"confidence_{CF_B}x{CF_P}x7168"
 CF_THRESHOLD, CF_FLOOR = 0.45, 0.12
 
