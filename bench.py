@@ -662,7 +662,8 @@ def run_prob_verify(args, d: Dist):
                          "algorithmic_bytes": algo, "rows_rejected": rejected,
                          "kernel_us_from": "CUDA events around the accept launch alone, L2 flushed"},
             "cpu_baseline": cpu,
-            "logits_to_probs": {"rows": rows_l, "vocab": V, "kernel": "logits_probs_kernel",
+            "logits_to_probs": {"rows": rows_l, "vocab": V,
+                                "kernel": "probs_plain_cluster_kernel (plain), logits_probs_kernel (filtered)",
                                 "bytes_note": "algorithmic: one read and one write of every row",
                                 "peak_gbs": peak, **l2p},
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -780,7 +781,7 @@ def run_logits_to_probs(args, d: Dist):
                        "l2": L2_NOTE + " step"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": recorded_traffic(f"logits_probs_{rows}x{V}_plain", L2P_SOURCES),
-                         "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "logits_probs_kernel",
+                         "peak_kind": f"{peak_kind} hbm_gbs", "kernel": "probs_plain_cluster_kernel",
                          "kernel_us": step_us, "algorithmic_bytes": algo,
                          "kernel_us_from": "CUDA events around the one launch of a call, L2 flushed"},
             "filtered": {"temperature": L2P_SETTINGS["filtered"][0], "top_k": L2P_SETTINGS["filtered"][1],

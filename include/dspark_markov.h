@@ -181,7 +181,7 @@ DSPARK_API int32_t dspark_markov_partial_count(const dspark_markov_ctx *ctx);
 
 /* Which bias path a call with `rows` rows takes: 0 = FMA, 1 = tcgen05,
  * 2 = FMA over the FP8 w2 attached by dspark_markov_set_w2_fp8 (forced, or
- * above 128 rows), 3 = tcgen05 over that FP8 w2.  (A base whose pointer or
+ * above 160 rows), 3 = tcgen05 over that FP8 w2.  (A base whose pointer or
  * strides a TMA cannot address takes the FMA form of the same path.) */
 DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t rows);
 
@@ -194,7 +194,7 @@ DSPARK_API int32_t dspark_markov_bias_path(const dspark_markov_ctx *ctx, int32_t
  * RN_bf16(RN(scale * sum_j e_j * decode(q_j))) with the sum in FP32 (any
  * order; within 1 BF16 ulp of the exactly rounded s * sum(e * decode(q))
  * outside the FP32 accumulation bound); the rest of the step is unchanged.
- * Up to 128 rows the tensor-core loop serves it (E4M3 stages by TMA, turned
+ * Up to 160 rows the tensor-core loop serves it (E4M3 stages by TMA, turned
  * into FP16 operands in shared memory; the embeddings enter as FP16 of
  * e * 2^k per row, exact for every entry within 2^32 of the row's largest),
  * else one CUDA-core launch per step.  Enqueues nothing.  DSPARK_ERR_INVALID_ARG

@@ -65,14 +65,15 @@ def _check_fp8_bias(wl, gpu, qn, sn, sample=None):
 
 
 CASES = [("tiny", 4096 + 37, 4, 5), ("tiny", 1000, 1, 3), ("tc64", 3000 + 5, 64, 3), ("large16", 8192 + 8, 17, 2),
-         ("tc64", 40000 + 16, 128, 2), ("large16", 60000, 24, 3), ("stress256", 2048 + 8, 200, 2)]
+         ("tc64", 40000 + 16, 128, 2), ("large16", 60000, 24, 3), ("stress256", 2048 + 8, 200, 2),
+         ("stress256", 3000 + 5, 160, 2)]
 FLAGS = {"pdl": binding.FLAG_PDL, "nopdl": 0, "select": binding.FLAG_PDL | binding.FLAG_SELECT_2LAUNCH,
          "fma": binding.FLAG_PDL | binding.FLAG_FORCE_FMA, "per_step": binding.FLAG_PDL | binding.FLAG_PER_STEP}
 
 
 def _want_path(R, flags):
-    """The tensor-core FP8 step (3) up to 128 rows, else the CUDA-core one (2)."""
-    return 2 if (flags & binding.FLAG_FORCE_FMA) or R > 128 else 3
+    """The tensor-core FP8 step (3) up to 160 rows, else the CUDA-core one (2)."""
+    return 2 if (flags & binding.FLAG_FORCE_FMA) or R > 160 else 3
 
 
 @pytest.mark.parametrize("flags", list(FLAGS))
