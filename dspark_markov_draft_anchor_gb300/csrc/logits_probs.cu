@@ -39,9 +39,36 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
-// floor(e 2^40) for e in [0, 1]: the scaling by 2^40 is exact (subnormal e
-// included), and the conversion rounds toward zero.
-__device__ __forceinline__ uint64_t weight(float e) { return __float2ull_rz(__fmul_rn(e, 0x1p40f)); }
+// floor(e 2^40) for e in [0, 1], in two halves and FP32/INT32 instructions
+// only (a float-to-64-bit conversion runs on this part's small FP64 pipe):
+// with y = e 2^20 (exact, subnormal e included) the weight is
+// floor(y) 2^20 + floor(frac(y) 2^20).  Each floor is the low mantissa bits of
+// a round-toward-zero add of 2^23 (exact for values below 2^23; both are at
+// most 2^20), and frac(y) = y - floor(y) is exact.
+struct WeightHalves {
+  uint32_t hi, lo;
+};
+__device__ __forceinline__ WeightHalves weight_halves(float e) {
+  const float y = __fmul_rn(e, 0x1p20f);
+  const float hm = __fadd_rz(y, 0x1p23f);
+  const float lm = __fmaf_rz(__fsub_rn(y, __fsub_rn(hm, 0x1p23f)), 0x1p20f, 0x1p23f);
+  return {__float_as_uint(hm) - 0x4B000000u, __float_as_uint(lm) - 0x4B000000u};
+}
+__device__ __forceinline__ uint64_t weight(float e) {
+  const WeightHalves h = weight_halves(e);
+  return (static_cast<uint64_t>(h.hi) << 20) | h.lo;
+}
+// A thread's total of up to 4095 weights: each half is at most 2^20, so
+// their 32-bit sums are exact.
+struct WeightSum {
+  uint32_t hi = 0, lo = 0;
+  __device__ __forceinline__ void add(float e) {
+    const WeightHalves h = weight_halves(e);
+    hi += h.hi;
+    lo += h.lo;
+  }
+  __device__ __forceinline__ uint64_t total() const { return (static_cast<uint64_t>(hi) << 20) + lo; }
+};
 
 // An order-preserving 32-bit key of a non-NaN float (+0 and -0 equal).
 __device__ __forceinline__ uint32_t order_key(float z) {
@@ -423,6 +450,7 @@ __device__ __forceinline__ float weight_e(float z, float m) {
 constexpr int kCThreads = 256;
 constexpr int kCWarps = kCThreads / 32;
 constexpr int kCSliceBytesMax = 100 * 1024;
+static_assert(kCSliceBytesMax / 4 / kCThreads <= 4095, "a thread's weights must sum exactly in WeightSum");
 constexpr uint32_t kCopyWaitLimit = 1u << 24;  // polls of a slice copy's mbarrier
 
 __global__ void __launch_bounds__(kCThreads, 3)
@@ -550,7 +578,7 @@ __global__ void __launch_bounds__(kCThreads, 3)
     // pass 2: e in place (-1 for a NaN z); the cluster's weight total.  When
     // every z is a number within 86.5 of m (and m is finite), every id takes
     // exp's fast form with no check: RN(z - m) >= RN(lo - m) >= -86.5.
-    uint64_t part = 0;
+    WeightSum ws;  // at most kCSliceBytesMax / (16 kCThreads) groups of four a thread
     const bool m_finite = fabsf(m) <= 3.4028235e38f;
     const float spread = __fsub_rn(lo, m);  // NaN if any z is NaN
     if (m_finite && spread >= -86.5f) {
@@ -558,7 +586,10 @@ __global__ void __launch_bounds__(kCThreads, 3)
         const float4 z = b4[g];
         const float4 e = make_float4(exp_mid(__fsub_rn(z.x, m)), exp_mid(__fsub_rn(z.y, m)),
                                      exp_mid(__fsub_rn(z.z, m)), exp_mid(__fsub_rn(z.w, m)));
-        part += weight(e.x) + weight(e.y) + weight(e.z) + weight(e.w);
+        ws.add(e.x);
+        ws.add(e.y);
+        ws.add(e.z);
+        ws.add(e.w);
         b4[g] = e;
       }
     } else {
@@ -566,18 +597,18 @@ __global__ void __launch_bounds__(kCThreads, 3)
         const float4 z = b4[g];
         float4 e;
         const float4 x = make_float4(__fsub_rn(z.x, m), __fsub_rn(z.y, m), __fsub_rn(z.z, m), __fsub_rn(z.w, m));
-        if (m_finite && min_nan(min_nan(x.x, x.y), min_nan(x.z, x.w)) >= -86.5f) {
+        if (m_finite && min_nan(min_nan(x.x, x.y), min_nan(x.z, x.w)) >= -86.5f)
           e = make_float4(exp_mid(x.x), exp_mid(x.y), exp_mid(x.z), exp_mid(x.w));
-          part += weight(e.x) + weight(e.y) + weight(e.z) + weight(e.w);
-        } else {
+        else
           e = make_float4(weight_e(z.x, m), weight_e(z.y, m), weight_e(z.z, m), weight_e(z.w, m));
-          part += (e.x >= 0.0f ? weight(e.x) : 0ull) + (e.y >= 0.0f ? weight(e.y) : 0ull) +
-                  (e.z >= 0.0f ? weight(e.z) : 0ull) + (e.w >= 0.0f ? weight(e.w) : 0ull);
-        }
+        ws.add(fmaxf(e.x, 0.0f));  // -1 (a NaN z) weighs nothing
+        ws.add(fmaxf(e.y, 0.0f));
+        ws.add(fmaxf(e.z, 0.0f));
+        ws.add(fmaxf(e.w, 0.0f));
         b4[g] = e;
       }
     }
-    part = warp_sum_u64(part);
+    uint64_t part = warp_sum_u64(ws.total());
     if (lane == 0) red_u[warp] = part;
     __syncthreads();
     if (tid == 0) {

@@ -131,12 +131,15 @@ def test_scaled_logit_ties_decide_top_k_like_the_oracle(T):
 
 
 @pytest.mark.parametrize("rows,V,T", [(1, 100, 1.0), (200, 32768, 0.7), (500, 1000, 1.3), (24, 163840, 1.0),
-                                      (9, 100004, 0.9), (5, 51204, 1e-30), (4, 250000, 1.0), (3, 129281, 1.0)])
+                                      (9, 100004, 0.9), (5, 51204, 1e-30), (4, 250000, 1.0), (3, 129281, 1.0),
+                                      (200, 129280, 1.0), (90, 163840, 0.8), (2000, 4096, 1.0)])
 def test_plain_setting_on_clusters(rows, V, T):
     """The plain setting (no top-k, no top-p) runs on clusters of CTAs that
-    split each row across their shared memory (one to eight slices, the next
-    row prefetched while this one is processed); a vocabulary too large for
-    that, or not a multiple of 4, takes the one-CTA-per-row kernel."""
+    split each row (one to sixteen slices, each held in registers through
+    the passes, the next row's slice copied while this one is processed; the
+    larger row counts take each CTA through many rows); a vocabulary too
+    large for that, or not a multiple of 4, takes the one-CTA-per-row
+    kernel."""
     rng = np.random.default_rng(rows + V)
     l = _logits(rng, rows, V, 2.5)
     if rows > 3:
