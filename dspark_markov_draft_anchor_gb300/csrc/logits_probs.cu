@@ -108,6 +108,8 @@ struct RowSmem {
   uint32_t k_prefix, k_mask;
   int64_t k_rem;
   uint64_t p_prefix, p_mask, p_above, p_thr;
+  uint32_t tkey[kThreads];  // per thread: the order key of its largest z (0 if it has none)
+  int cand_n;
 };
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t x) {
@@ -265,6 +267,76 @@ struct CompactSmem {
   int n;
 };
 
+// Sort a[0, n) descending, n a power of two: a bitonic network, one
+// compare-exchange per pair and stage, kThreads threads.
+template <class T>
+__device__ void bitonic_desc(T* a, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const T x = a[i], y = a[ixj];
+          if ((i & k) == 0 ? x < y : x > y) {
+            a[i] = y;
+            a[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// The top-k cut (k_key, k_id) without radix passes over the row, for K <=
+// kThreads.  Each thread's largest z (from pass 1, sm.tkey) is an element of
+// the row, so the K-th largest of the kThreads thread maxima, tau, is at most
+// the K-th largest key: every id the cut keeps has a key >= tau (a thread
+// without a number counts as key 0, and if one of those is among the K
+// largest, tau is 0 and every number passes).  The ids passing tau -- about
+// K for a row of independent logits -- are gathered into shared memory and
+// sorted by (key descending, id ascending); the K-th entry is the cut, as
+// the radix passes and the ordered tie scan would find it, and the first K
+// entries are the ids it keeps: they go to cs.id / cs.e (z from its key) as
+// compact_finish's gather would leave them.  False, nothing decided, when
+// more than kCompactMax ids pass.
+__device__ __noinline__ bool prefilter_cut(const float* out, int64_t vocab, bool vec, int K, uint32_t& k_key,
+                                           int64_t& k_id, RowSmem& sm, CompactSmem& cs) {
+  bitonic_desc(sm.tkey, kThreads);
+  const uint32_t tau = sm.tkey[K - 1];
+  if (threadIdx.x == 0) sm.cand_n = 0;
+  __syncthreads();
+  row_each(out, vocab, vec, [&](int64_t v, float z) {
+    if (isnan(z)) return;
+    const uint32_t key = order_key(z);
+    if (key >= tau) {
+      const int slot = atomicAdd(&sm.cand_n, 1);
+      if (slot < kCompactMax)  // (key, ~id): larger first is key descending, id ascending
+        cs.w[slot] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(v));
+    }
+  });
+  __syncthreads();
+  const int n = sm.cand_n;
+  if (n > kCompactMax) return false;  // the same in every thread
+  int P2 = 1;
+  while (P2 < n) P2 <<= 1;
+  for (int i = n + static_cast<int>(threadIdx.x); i < P2; i += kThreads) cs.w[i] = 0ull;  // below every key
+  __syncthreads();
+  bitonic_desc(cs.w, P2);
+  const unsigned long long c = cs.w[K - 1];
+  k_key = static_cast<uint32_t>(c >> 32);
+  k_id = static_cast<int64_t>(0xFFFFFFFFu - static_cast<uint32_t>(c));
+  for (int i = threadIdx.x; i < K; i += kThreads) {
+    const unsigned long long ci = cs.w[i];
+    const uint32_t key = static_cast<uint32_t>(ci >> 32);  // order_key inverted (no NaN here)
+    cs.id[i] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(ci));
+    cs.e[i] = __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+  }
+  if (threadIdx.x == 0) cs.n = K;
+  __syncthreads();
+  return true;
+}
+
 // After a top-k cut of K <= kCompactMax ids: gather them (and their z) into
 // shared memory, take e and w there, cut top-p on the K entries sorted by
 // (w descending, id ascending) (a bitonic sort, then a block scan for the
@@ -272,22 +344,24 @@ struct CompactSmem {
 // the probabilities.  Equal to the full-row passes: the same sets, sums and
 // roundings.
 __device__ __noinline__ void compact_finish(float* out, int64_t vocab, bool vec, int K, uint32_t k_key, int64_t k_id,
-                                            float m, float top_p, RowSmem& sm, CompactSmem& cs) {
+                                            float m, float top_p, bool gathered, RowSmem& sm, CompactSmem& cs) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) cs.n = 0;
-  __syncthreads();
-  row_each(out, vocab, vec, [&](int64_t v, float z) {
-    if (isnan(z)) return;
-    const uint32_t key = order_key(z);
-    if (key > k_key || (key == k_key && v <= k_id)) {
-      const int slot = atomicAdd(&cs.n, 1);
-      if (slot < kCompactMax) {  // exactly K ids pass the cut
-        cs.id[slot] = static_cast<int32_t>(v);
-        cs.e[slot] = z;
+  if (!gathered) {  // (else prefilter_cut left the kept ids there)
+    if (threadIdx.x == 0) cs.n = 0;
+    __syncthreads();
+    row_each(out, vocab, vec, [&](int64_t v, float z) {
+      if (isnan(z)) return;
+      const uint32_t key = order_key(z);
+      if (key > k_key || (key == k_key && v <= k_id)) {
+        const int slot = atomicAdd(&cs.n, 1);
+        if (slot < kCompactMax) {  // exactly K ids pass the cut
+          cs.id[slot] = static_cast<int32_t>(v);
+          cs.e[slot] = z;
+        }
       }
-    }
-  });
-  __syncthreads();
+    });
+    __syncthreads();
+  }
   K = cs.n < K ? cs.n : K;  // equal in correct operation; never past what was gathered
   const bool topp = top_p < 1.0f;
   int P2 = 1;
@@ -709,6 +783,7 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
     m = fmaxf(m, z);  // a NaN z leaves m as it is
     return z;
   });
+  sm.tkey[threadIdx.x] = n_local > 0 ? order_key(m) : 0u;  // read after the barriers below
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     n_local += __shfl_xor_sync(0xFFFFFFFFu, n_local, off);
@@ -735,7 +810,8 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
   const bool topk = top_k > 0 && top_k < n_valid;
   uint32_t k_key = 0;
   int64_t k_id = vocab;
-  if (topk) {
+  const bool gathered = topk && top_k <= kThreads && prefilter_cut(out, vocab, vec, top_k, k_key, k_id, sm, cs);
+  if (topk && !gathered) {
     if (threadIdx.x == 0) {
       sm.k_prefix = 0;
       sm.k_mask = 0;
@@ -777,10 +853,10 @@ __device__ void logits_probs_row(const float* l, float* out, int64_t vocab, floa
             return !isnan(z) && order_key(z) == k_key;
           },
           sm);
-    if (top_k <= kCompactMax) {
-      compact_finish(out, vocab, vec, top_k, k_key, k_id, m, top_p, sm, cs);
-      return;
-    }
+  }
+  if (topk && top_k <= kCompactMax) {
+    compact_finish(out, vocab, vec, top_k, k_key, k_id, m, top_p, gathered, sm, cs);
+    return;
   }
 
   // weight pass: e (or -1 for a dropped id) into the output row; the kept total

@@ -155,3 +155,23 @@ def test_plain_setting_in_place_on_clusters():
     rng = np.random.default_rng(23)
     l = _logits(rng, 40, 129280, 2.5)
     _check(l, 0.8, 0, 1.0, in_place=True)
+
+
+@pytest.mark.parametrize("K", [1, 10, 1024, 1025])
+def test_top_k_prefilter_and_its_fallback(K):
+    """Top-k up to 1024 is cut from the ids at or above the K-th largest of
+    the CTA's per-thread maxima; a row where more than 2048 ids pass that
+    bound (mostly equal logits, or few finite ones) takes the radix passes
+    instead, as does K above 1024.  Every route gives the oracle's cut."""
+    rng = np.random.default_rng(K)
+    V = 129280
+    l = _logits(rng, 6, V, 2.5)
+    l[1, :] = 0.0
+    l[1, rng.choice(V, 20, replace=False)] = 3.0   # 20 winners over a sea of ties
+    l[2, :] = 1.0                                  # all equal
+    l[3, ::2] = np.nan                             # half NaN
+    l[4, :] = np.round(l[4, :])                    # coarse grid: long ties at the cut
+    l[5, :] = -np.inf
+    l[5, :3000] = rng.standard_normal(3000)        # few finite ids
+    _check(l, 0.8, K, 0.95)
+    _check(l, 1.0, K, 1.0)
