@@ -521,9 +521,24 @@ __device__ __forceinline__ float weight_e(float z, float m) {
 // the same rows and the same branches, so every cluster barrier is reached
 // by all of them.
 // ---------------------------------------------------------------------------
+// Cluster pushes: a store into a peer CTA's shared memory (a shared::cluster
+// address from mapa) that completes its bytes on the peer's mbarrier (in the
+// same CTA as the destination), so the peer waits on its own barrier.
+__device__ __forceinline__ void push_f32x2(uint32_t dst, float a, float b, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(dst),
+               "f"(a), "f"(b), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void push_u64(uint32_t dst, unsigned long long v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(dst), "l"(v),
+               "r"(bar)
+               : "memory");
+}
+
 constexpr int kCThreads = 256;
 constexpr int kCWarps = kCThreads / 32;
 constexpr int kCSliceBytesMax = 100 * 1024;
+constexpr int kCMaxCluster = 8;
 static_assert(kCSliceBytesMax / 4 / kCThreads <= 4095, "a thread's weights must sum exactly in WeightSum");
 constexpr uint32_t kCopyWaitLimit = 1u << 24;  // polls of a slice copy's mbarrier
 
@@ -532,13 +547,19 @@ __global__ void __launch_bounds__(kCThreads, 3)
                                float temperature, int slice) {
   extern __shared__ __align__(128) float sbuf[];  // [slice]: halves [0, h) and [h, cnt)
   __shared__ uint64_t bar[2];                     // one per half
-  __shared__ float2 s_mm[2];  // (largest z, smallest z or NaN if any z is NaN)
-  __shared__ int s_any[2];
-  __shared__ unsigned long long s_sum[2];
+  // The row's exchanges, pushed by every CTA into every CTA's slots: per row
+  // parity, each CTA's (largest z, smallest z or NaN if any z is NaN), its
+  // "some z is -inf" flag (rows of only NaN and -inf), its weight total;
+  // xbar[exchange][parity] completes when all of the cluster's have landed.
+  __shared__ float2 x_mm[2][kCMaxCluster];
+  __shared__ unsigned long long x_any[2][kCMaxCluster];
+  __shared__ unsigned long long x_sum[2][kCMaxCluster];
+  __shared__ uint64_t xbar[3][2];
   __shared__ float2 red_f[kCWarps];
   __shared__ unsigned long long red_u[kCWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t csize = ptx::cluster_nctarank();
+  const uint32_t rank = ptx::cluster_ctarank();
   const int cid = static_cast<int>(ptx::clusterid_x()), ncl = static_cast<int>(ptx::nclusterid_x());
   const int v0 = static_cast<int>(ptx::cluster_ctarank()) * slice;
   const int cnt = vocab - v0 < slice ? (vocab - v0 > 0 ? vocab - v0 : 0) : slice;  // a multiple of 4
@@ -548,9 +569,33 @@ __global__ void __launch_bounds__(kCThreads, 3)
   if (tid == 0) {
     ptx::mbar_init(&bar[0], 1);
     ptx::mbar_init(&bar[1], 1);
+    for (int e = 0; e < 3; ++e) {
+      ptx::mbar_init(&xbar[e][0], 1);
+      ptx::mbar_init(&xbar[e][1], 1);
+    }
     ptx::fence_mbar_init();
   }
   __syncthreads();
+  ptx::cluster_sync();  // every CTA's exchange barriers exist before any push
+  // warp 0: push this CTA's value of exchange e (parity p) to every CTA of
+  // the cluster (lane q to CTA q); lane 0 arms the local barrier for the
+  // cluster's values (a push may land before it: the transaction count may
+  // go below zero until then)
+  auto push2 = [&](int e, int p, float2* slots, float a, float c) {
+    if (lane == 0) ptx::mbar_arrive_expect_tx(&xbar[e][p], csize * 8u);
+    if (static_cast<uint32_t>(lane) < csize)
+      push_f32x2(ptx::dsmem_addr(&slots[rank], lane), a, c, ptx::dsmem_addr(&xbar[e][p], lane));
+  };
+  auto push8 = [&](int e, int p, unsigned long long* slots, unsigned long long v) {
+    if (lane == 0) ptx::mbar_arrive_expect_tx(&xbar[e][p], csize * 8u);
+    if (static_cast<uint32_t>(lane) < csize)
+      push_u64(ptx::dsmem_addr(&slots[rank], lane), v, ptx::dsmem_addr(&xbar[e][p], lane));
+  };
+  // every thread: the k-th phase of exchange e's barrier p landed (bounded;
+  // the answer is made the same in the whole CTA)
+  auto landed = [&](int e, int p, int k) {
+    return __syncthreads_and(ptx::mbar_wait(&xbar[e][p], static_cast<uint32_t>(k) & 1u, kCopyWaitLimit));
+  };
   // thread 0: half hf of row r's slice into the buffer (the half's last
   // generic reads, ordered before this thread by a CTA barrier, before the
   // async write)
@@ -581,9 +626,9 @@ __global__ void __launch_bounds__(kCThreads, 3)
     }
   };
   const Divider by_t = make_divider(temperature);
-  int i = 0;
+  int i = 0, n_any = 0, n_sum = 0;  // exchanges of each kind so far (a row of zeros takes no sum)
   for (int r = cid; r < rows; r += ncl, ++i) {
-    const int b = i & 1;  // the exchange slots alternate between rows
+    const int b = i & 1;  // the (largest, smallest) exchange's slots and barrier alternate between rows
     const bool next = r + ncl < rows;
     float4* o4 = reinterpret_cast<float4*>(probs + static_cast<int64_t>(r) * vocab + v0);
 
@@ -607,26 +652,28 @@ __global__ void __launch_bounds__(kCThreads, 3)
     }
     if (lane == 0) red_f[warp] = make_float2(m, lo);
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
       float2 t = make_float2(-INFINITY, INFINITY);
 #pragma unroll
       for (int w = 0; w < kCWarps; ++w) t = make_float2(fmaxf(t.x, red_f[w].x), min_nan(t.y, red_f[w].y));
-      s_mm[b] = t;
+      push2(0, b, x_mm[b], t.x, t.y);
     }
-    ptx::cluster_sync();
-    // lane q reads CTA q's values: the cluster's loads go out together
+    // lane q takes CTA q's values (NaN, never in correct operation, if the
+    // cluster's did not all land)
+    const bool ok_mm = landed(0, b, i >> 1);
     m = -INFINITY;
     lo = INFINITY;
     if (static_cast<uint32_t>(lane) < csize) {
-      const uint32_t a = ptx::dsmem_addr(&s_mm[b], lane);
-      m = ptx::ld_dsmem_f32(a);
-      lo = ptx::ld_dsmem_f32(a + 4);
+      const float2 v = x_mm[b][lane];
+      m = v.x;
+      lo = v.y;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
       lo = min_nan(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
     }
+    if (!ok_mm) m = NAN;
     if (m == -INFINITY) {  // every z of the row is NaN or -inf: is any -inf?
       int any = 0;
       for (int g = tid; g < n4; g += kCThreads) {
@@ -634,10 +681,11 @@ __global__ void __launch_bounds__(kCThreads, 3)
         any |= (z.x == z.x) | (z.y == z.y) | (z.z == z.z) | (z.w == z.w);
       }
       any = __syncthreads_or(any);
-      if (tid == 0) s_any[b] = any;
-      ptx::cluster_sync();
-      any = static_cast<uint32_t>(lane) < csize ? static_cast<int>(ptx::ld_dsmem_u32(ptx::dsmem_addr(&s_any[b], lane)))
-                                                 : 0;
+      const int xa = n_any & 1;
+      if (warp == 0) push8(1, xa, x_any[xa], static_cast<unsigned long long>(any));
+      const bool ok_any = landed(1, xa, n_any >> 1);
+      ++n_any;
+      any = ok_any && static_cast<uint32_t>(lane) < csize ? static_cast<int>(x_any[xa][lane]) : 0;
       if (!__any_sync(0xFFFFFFFFu, any)) {  // all NaN: a row of zeros
         for (int g = tid; g < n4; g += kCThreads) __stcs(o4 + g, make_float4(0.f, 0.f, 0.f, 0.f));
         __syncthreads();
@@ -685,14 +733,15 @@ __global__ void __launch_bounds__(kCThreads, 3)
     uint64_t part = warp_sum_u64(ws.total());
     if (lane == 0) red_u[warp] = part;
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
       unsigned long long t = 0;
 #pragma unroll
       for (int w = 0; w < kCWarps; ++w) t += red_u[w];
-      s_sum[b] = t;
+      push8(2, n_sum & 1, x_sum[n_sum & 1], t);
     }
-    ptx::cluster_sync();
-    uint64_t S = static_cast<uint32_t>(lane) < csize ? ptx::ld_dsmem_u64(ptx::dsmem_addr(&s_sum[b], lane)) : 0ull;
+    const bool ok_sum = landed(2, n_sum & 1, n_sum >> 1);
+    uint64_t S = ok_sum && static_cast<uint32_t>(lane) < csize ? x_sum[n_sum & 1][lane] : 0ull;
+    ++n_sum;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, off);
 
@@ -972,11 +1021,11 @@ bool cluster_attr_ready(int device) {
 bool launch_plain_cluster(const float* logits, float* probs, int rows, int vocab, float temperature, int device,
                           cudaStream_t stream, int* rc) {
   int C = 1, slice = 0;
-  for (; C <= 8; C *= 2) {
+  for (; C <= kCMaxCluster; C *= 2) {
     slice = ((vocab + C - 1) / C + 3) & ~3;
     if (slice * 4 <= kCSliceBytesMax) break;
   }
-  if (C > 8 || !cluster_attr_ready(device)) return false;
+  if (C > kCMaxCluster || !cluster_attr_ready(device)) return false;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
