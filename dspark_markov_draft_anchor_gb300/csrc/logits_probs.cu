@@ -306,7 +306,7 @@ __device__ __noinline__ bool prefilter_cut(const float* out, int64_t vocab, bool
   const uint32_t tau = sm.tkey[K - 1];
   if (threadIdx.x == 0) sm.cand_n = 0;
   __syncthreads();
-  row_each(out, vocab, vec, [&](int64_t v, float z) {
+  row_each<4>(out, vocab, vec, [&](int64_t v, float z) {  // four loads in flight a thread: an L2 pass
     if (isnan(z)) return;
     const uint32_t key = order_key(z);
     if (key >= tau) {
