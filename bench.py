@@ -331,6 +331,20 @@ def run_native(args, d: Dist):
     w1, w2 = bf16(wl.w1), bf16(wl.w2)
     base, ids, anc, pos, req = bf16(wl.base), t(wl.input_ids), t(wl.anchor_idx), t(wl.sample_pos), t(wl.req_idx)
     seeds, temp = t(wl.seeds), t(wl.temperature)
+    # the per-row inputs as views of one buffer (16-byte aligned slices), so
+    # that the end-to-end leg moves them in one copy
+    small = [ids, anc, pos, req, seeds, temp]
+    offs, nbytes = [], 0
+    for x in small:
+        offs.append(nbytes)
+        nbytes += (x.numel() * x.element_size() + 15) // 16 * 16
+    small_blob = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    views = []
+    for x, o in zip(small, offs):
+        v = small_blob[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+        v.copy_(x)
+        views.append(v)
+    ids, anc, pos, req, seeds, temp = views
     cache = torch.zeros((wl.num_req, K, V), dtype=torch.int16, device=dev)
     tokens = torch.zeros((R, K), dtype=torch.int64, device=dev)
     flags = binding.FLAG_PDL | {"auto": 0, "fma": binding.FLAG_FORCE_FMA, "mma": binding.FLAG_FORCE_MMA}[args.bias_path]
@@ -432,12 +446,12 @@ def run_native(args, d: Dist):
     eager_loop_us = statistics.mean([m[0].elapsed_time(m[K + 1]) for m in evk]) * 1e3
 
     # end to end through the C ABI from pinned host buffers
-    hb = {k: v.cpu().pin_memory() for k, v in dict(base=base, ids=ids, anc=anc, pos=pos, req=req, seeds=seeds,
-                                                   temp=temp).items()}
+    # (the base logits, then the per-row inputs' one buffer)
+    hb = {k: v.cpu().pin_memory() for k, v in dict(base=base, small=small_blob).items()}
     h_tokens = torch.empty_like(tokens, device="cpu").pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in hb.values())
     d2h = h_tokens.numel() * h_tokens.element_size()
-    dev_bufs = dict(base=base, ids=ids, anc=anc, pos=pos, req=req, seeds=seeds, temp=temp)
+    dev_bufs = dict(base=base, small=small_blob)
 
     def e2e_loops(n):
         out = []
