@@ -16,11 +16,16 @@
 //     ascending) whose weight reaches max(1, ceil(p W)), W the kept total;
 //   - probability = RN(e / S), S = RN(sum of the final w) 2^-40; 0 elsewhere.
 //
-// One CTA of 1024 threads per row.  The k-th largest key and the top-p cut
-// are radix selects over the row (8 bits a pass: four passes of counts over
-// the 32-bit logit keys, six passes of weight sums over the 48-bit weights),
-// ties at a cut are resolved by one ordered scan, and a last pass writes the
-// row.  The output row holds z, then e, between passes (see
+// The plain setting (no top-k, no top-p, T > 0) on aligned rows runs on
+// clusters that hold each row in shared memory (probs_plain_cluster_kernel).
+// Otherwise one CTA of 1024 threads per row: top-k with K <= 1024 is cut
+// from the few ids at or above the K-th largest per-thread maximum
+// (prefilter_tau), else the k-th largest key is a radix select over the row
+// (8 bits a pass: four passes of counts over the 32-bit logit keys) with an
+// ordered scan for ties; with K <= 2048 the rest happens on the kept ids in
+// shared memory (compact_finish), else the top-p cut is a radix select of
+// weight sums over the 48-bit weights (six passes), and a last pass writes
+// the row.  The output row holds z, then e, between passes (see
 // logits_probs_row).
 #include <cuda_runtime.h>
 #include <math.h>
@@ -166,8 +171,9 @@ __device__ int64_t nth_in_order(int64_t vocab, int64_t r, Pred pred, RowSmem& sm
 // Row iteration: every id of a row, four at a time (float4) where the row
 // allows it.  Each thread issues the loads of kBatch groups (or ids) before
 // it uses any: the passes that stream from or to HBM batch 4 so that one CTA
-// per SM keeps enough requests in flight; the passes over L2 take 1 (more
-// would spill the inlined per-id work).
+// per SM keeps enough requests in flight, as does the top-k prefilter's
+// light pass over L2; the other passes over L2 take 1 (more would spill
+// their inlined per-id work).
 // row_map writes f's value back in place of what it read (the same thread
 // reads and then writes each id, so src may equal dst).
 template <int kBatch = 1, class F>
