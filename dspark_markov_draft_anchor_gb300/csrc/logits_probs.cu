@@ -304,9 +304,10 @@ __device__ void bitonic_desc(T* a, int n) {
 // sorted by (key descending, id ascending); the K-th entry is the cut, as
 // the radix passes and the ordered tie scan would find it, and the first K
 // entries are the ids it keeps: they go to cs.id / cs.e (z from its key) as
-// compact_finish's gather would leave them.  False, nothing decided, when
-// more than kCompactMax ids pass.
-__device__ __noinline__ bool prefilter_cut(const float* out, int64_t vocab, bool vec, int K, uint32_t& k_key,
+// compact_finish's gather would leave them; the row's zeros are written
+// here (nothing reads the row after the gather).  False, nothing decided and
+// nothing written, when more than kCompactMax ids pass.
+__device__ __noinline__ bool prefilter_cut(float* out, int64_t vocab, bool vec, int K, uint32_t& k_key,
                                            int64_t& k_id, RowSmem& sm, CompactSmem& cs) {
   bitonic_desc(sm.tkey, kThreads);
   const uint32_t tau = sm.tkey[K - 1];
@@ -324,6 +325,14 @@ __device__ __noinline__ bool prefilter_cut(const float* out, int64_t vocab, bool
   __syncthreads();
   const int n = sm.cand_n;
   if (n > kCompactMax) return false;  // the same in every thread
+  // The row is not read again: its zeros go out now, under the sorts below
+  // and compact_finish's work on the kept ids (which then only scatters).
+  if (vec) {
+    float4* d4 = reinterpret_cast<float4*>(out);
+    for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) __stcs(d4 + g, make_float4(0.f, 0.f, 0.f, 0.f));
+  } else {
+    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) __stcs(out + v, 0.0f);
+  }
   int P2 = 1;
   while (P2 < n) P2 <<= 1;
   for (int i = n + static_cast<int>(threadIdx.x); i < P2; i += kThreads) cs.w[i] = 0ull;  // below every key
@@ -445,11 +454,13 @@ __device__ __noinline__ void compact_finish(float* out, int64_t vocab, bool vec,
     __syncthreads();
   }
   const float Sf = __fmul_rn(__ull2float_rn(S), 0x1p-40f);
-  if (vec) {
-    float4* d4 = reinterpret_cast<float4*>(out);
-    for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) __stcs(d4 + g, make_float4(0.f, 0.f, 0.f, 0.f));
-  } else {
-    for (int64_t v = threadIdx.x; v < vocab; v += kThreads) __stcs(out + v, 0.0f);
+  if (!gathered) {  // (else prefilter_cut wrote the zeros)
+    if (vec) {
+      float4* d4 = reinterpret_cast<float4*>(out);
+      for (int64_t g = threadIdx.x; g < (vocab >> 2); g += kThreads) __stcs(d4 + g, make_float4(0.f, 0.f, 0.f, 0.f));
+    } else {
+      for (int64_t v = threadIdx.x; v < vocab; v += kThreads) __stcs(out + v, 0.0f);
+    }
   }
   __syncthreads();  // the zeros are ordered before the scattered values
   for (int i = threadIdx.x; i < n_final; i += kThreads) out[cs.id[i]] = __fdiv_rn(cs.e[i], Sf);
