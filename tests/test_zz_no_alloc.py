@@ -10,6 +10,8 @@ point that takes caller scratch.  The file is named to be collected last; it
 passes alone in a fresh process (the first call then does the one-time
 address lookup) and after the other tests.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -85,6 +87,7 @@ def test_no_alloc_accept_allocates_no_device_memory():
     acc, alen = _outputs(B, P)
     binding.dspark_greedy_accept_noalloc(logits, draft, plen, acc, alen, B, P, P, V)
     torch.cuda.synchronize()
+    gc.collect()  # tensors of earlier tests freed now, not during the calls measured
     before_torch = torch.cuda.memory_allocated()
     before_free, _ = torch.cuda.mem_get_info()
     for _ in range(3):
